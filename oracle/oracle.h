@@ -1,0 +1,81 @@
+/* oracle.h -- plain CPU oracle for continuity-aware draft-tree construction.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the package smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code with
+ * the CUDA path.  Everything is double precision, every ordering is a full
+ * sort, the n-gram model is a sorted array searched with bsearch.
+ *
+ * Sources (page titles and sections):
+ *  - "DART: Diffusion-Inspired Speculative Decoding for Fast LLM Inference",
+ *    Figure 3 caption: d logits from one forward pass, the first from the last
+ *    prefix position; candidates per position taken from that position's
+ *    logits; an N-gram model keeps expanded tokens continuous; the pruned tree
+ *    is verified with tree attention.
+ *  - "DARTree: Speculative Diffusion Decoding with Autoregressive Draft Trees",
+ *    Method / Tree Construction: a tree of fixed width; all nodes of the
+ *    previous depth are expanded and scored together, and after each depth
+ *    only the W best-scoring nodes of the full frontier survive.
+ *  - The two pages made precise (the readings are listed in oracle.c):
+ *    p_j = log_softmax(z_j / T), C_j = top-k of p_j, child score = parent
+ *    score + p_j[c] + lambda * ngram(last n-1 path tokens, c), a missing
+ *    n-gram costing beta, ties broken by lower parent index then lower token
+ *    id; outputs are tokens, parents, depths and a bit-packed ancestor mask.
+ */
+#ifndef DART_ORACLE_H
+#define DART_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* dtype codes of the stored logits: 0 = f32, 1 = f16, 2 = bf16 (bit patterns). */
+
+/* Per row r < rows of logits[rows][V]: lse[r], the k best token ids (value
+ * descending, lower id first on equal values) and their log-probabilities. */
+int oracle_rows(const void* logits, int dtype, int64_t rows, int V, double T, int k,
+                int32_t* ids, double* logp, double* lse, int threads);
+
+/* Decode one stored logit to double (exact for all three dtypes). */
+double oracle_decode(const void* logits, int dtype, int64_t index);
+
+typedef struct oracle_ngram oracle_ngram;
+/* keys[M][n] (oldest context token first, predicted token last), vals[M].
+ * A repeated key keeps its first value. */
+oracle_ngram* oracle_ngram_new(int n, const int32_t* keys, const float* vals, int64_t M);
+void oracle_ngram_free(oracle_ngram* t);
+/* found[q] = 1 and vals[q] = value when keys[q][0..n) is in the model, else 0. */
+void oracle_ngram_lookup(const oracle_ngram* t, const int32_t* keys, int64_t Q,
+                         float* vals, int32_t* found);
+
+/* Tree construction from per-depth candidate lists ids/logp [B][d][k].
+ * tab == NULL means no continuity term.  Outputs [B][N] (mask [B][N][MW]);
+ * min_pos_gap[B][d] (may be NULL) is, per depth, the smallest positive score
+ * gap between neighbours in the sorted candidate list among the pairs that
+ * decide a kept node's rank or the cut (1e300 when there is none). */
+int oracle_tree_from_lists(int B, int d, int k, int W,
+                           const int32_t* ids, const double* logp,
+                           double lam, double beta, const oracle_ngram* tab, int n,
+                           const int32_t* ctx,
+                           int32_t* tokens, int32_t* parents, int32_t* pos,
+                           uint32_t* mask, double* scores, double* min_pos_gap,
+                           int threads);
+
+/* Rows, then the tree, as one call.  row_ids/row_logp/row_lse may be NULL. */
+int oracle_tree_build(const void* logits, int dtype, int B, int d, int V, double T,
+                      int k, int W, double lam, double beta,
+                      const oracle_ngram* tab, int n, const int32_t* ctx,
+                      int32_t* tokens, int32_t* parents, int32_t* pos, uint32_t* mask,
+                      double* scores, double* min_pos_gap,
+                      int32_t* row_ids, double* row_logp, double* row_lse, int threads);
+
+/* N = sum over depths j = 1..d of min(W, k^j); -1 when the arguments are invalid. */
+int oracle_num_nodes(int d, int k, int W);
+
+/* Ancestor-or-self mask rows from a parent array (parents[i] < i, -1 for depth 1). */
+int oracle_mask_from_parents(int B, int N, const int32_t* parents, uint32_t* mask);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

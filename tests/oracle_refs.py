@@ -1,0 +1,129 @@
+"""Independent references used to pin the oracle (not the oracle itself).
+
+Each helper here is written from a definition that does not go through
+oracle.c: exhaustive enumeration of all k^d paths, Python dictionaries for the
+n-gram model, numpy / scipy library routines for sorting and log-softmax,
+Python sets for ancestor masks, and closed forms from the worked examples.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def decode_np(logits: np.ndarray, dtype: str) -> np.ndarray:
+    """Stored logits -> float64 through numpy's own conversions."""
+    if dtype == "f32":
+        return logits.astype(np.float64)
+    if dtype == "f16":
+        return logits.astype(np.float16).astype(np.float64)
+    if dtype == "bf16":
+        return (logits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    raise ValueError(dtype)
+
+
+def topk_lexsort(z: np.ndarray, k: int) -> np.ndarray:
+    """k best ids of a 1-D row: value descending, lower id first (numpy lexsort)."""
+    ids = np.arange(z.shape[0])
+    order = np.lexsort((ids, -z))
+    return order[:k]
+
+
+def load_worked_example(name: str):
+    with open(os.path.join(GOLDEN, name)) as f:
+        ex = json.load(f)
+    V, d = ex["V"], ex["d"]
+    probs = np.zeros((d, V), dtype=np.float64)
+    for j, row in enumerate(ex["probs"]):
+        probs[j, :] = ex_default(row)
+        for tok, p in row["set"].items():
+            probs[j, int(tok)] = p
+    logits = np.log(probs).astype(np.float32)[None]   # [1, d, V] f32
+    keys = np.array([t for t, _ in ex["table"]], dtype=np.int32).reshape(-1, ex["n"])
+    vals = np.array([v for _, v in ex["table"]], dtype=np.float32)
+    return ex, logits, keys, vals
+
+
+def ex_default(row) -> float:
+    num, den = row["default_num"].split("/")
+    return float(num) / float(den)
+
+
+def eval_closed_form(expr: str) -> float:
+    return float(eval(expr, {"__builtins__": {}}, {"log": math.log}))
+
+
+def dict_ngram(keys: np.ndarray, vals: np.ndarray) -> dict:
+    """First value wins for a repeated key."""
+    out = {}
+    for key, v in zip(map(tuple, keys.tolist()), vals.tolist()):
+        if key not in out:
+            out[key] = float(np.float32(v))
+    return out
+
+
+def brute_force_paths(ids, logp, *, lam, beta, table: dict | None, n: int, ctx):
+    """Every root-to-depth-j path for one tree, scored from its own token sequence.
+
+    ids/logp: [d][k].  Returns {path tuple (of candidate ranks): score} over all
+    depths 1..d (paths of every length), computed by direct enumeration.
+    """
+    d, k = len(ids), len(ids[0])
+    out = {}
+    for depth in range(1, d + 1):
+        for ranks in itertools.product(range(k), repeat=depth):
+            toks = [ids[j][ranks[j]] for j in range(depth)]
+            seq = list(ctx) + toks
+            s = 0.0
+            for j in range(depth):
+                s = s + logp[j][ranks[j]]
+                if table is not None:
+                    pos_in_seq = len(ctx) + j                  # index of token j in seq
+                    context = tuple(seq[pos_in_seq - (n - 1):pos_in_seq])
+                    g = table.get(context + (toks[j],))
+                    s = s + lam * (g if g is not None else beta)
+            out[ranks] = s
+    return out
+
+
+def node_paths(tokens, parents, ids):
+    """For one tree: node -> tuple of candidate ranks from the root (via parents)."""
+    N = len(tokens)
+    paths = []
+    for x in range(N):
+        seq = []
+        a = x
+        while a >= 0:
+            seq.append(tokens[a])
+            a = parents[a]
+        seq.reverse()
+        ranks = tuple(list(ids[j]).index(t) for j, t in enumerate(seq))
+        paths.append(ranks)
+    return paths
+
+
+def masks_from_sets(parents_row) -> list[set]:
+    out = []
+    for x in range(len(parents_row)):
+        s = set()
+        a = x
+        while a >= 0:
+            s.add(a)
+            a = parents_row[a]
+        out.append(s)
+    return out
+
+
+def mask_row_to_set(words) -> set:
+    s = set()
+    for w, word in enumerate(words):
+        for b in range(32):
+            if (int(word) >> b) & 1:
+                s.add(w * 32 + b)
+    return s

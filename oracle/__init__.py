@@ -51,7 +51,7 @@ def _declare(lib):
     lib.oracle_ngram_free.restype = None
     lib.oracle_ngram_lookup.argtypes = [P, P, i64, P, P]
     lib.oracle_ngram_lookup.restype = None
-    lib.oracle_tree_from_lists.argtypes = [i32, i32, i32, i32, P, P, dbl, dbl, P, i32, P,
+    lib.oracle_tree_from_lists.argtypes = [i32, i32, i32, i32, P, P, dbl, P, dbl, dbl, P, i32, P,
                                            P, P, P, P, P, P, i32]
     lib.oracle_tree_from_lists.restype = i32
     lib.oracle_tree_build.argtypes = [P, i32, i32, i32, i32, dbl, i32, i32, dbl, dbl, P, i32, P,
@@ -127,16 +127,19 @@ def rows(logits: np.ndarray, dtype: str, V: int, T: float, k: int, threads: int 
     return ids, logp, lse
 
 
-def tree_from_lists(ids, logp, *, B, d, k, W, lam, beta, ngram: NGram | None, ctx,
-                    threads: int = 0, lib=None):
-    """The tree stage alone, from candidate lists ids/logp [B, d, k]."""
+def tree_from_lists(ids, base, *, B, d, k, W, lam, beta, ngram: NGram | None, ctx,
+                    invT: float = 1.0, off=None, threads: int = 0, lib=None):
+    """The tree stage alone, from candidate lists ids/base [B, d, k].
+
+    With the defaults (invT = 1, off = None) base holds log-probabilities."""
     lib = lib or load()
     N = lib.oracle_num_nodes(d, k, W)
     if N < 0:
         raise ValueError("invalid d/k/W")
     MW = (N + 31) // 32
     ids = np.ascontiguousarray(ids, dtype=np.int32)
-    logp = np.ascontiguousarray(logp, dtype=np.float64)
+    base = np.ascontiguousarray(base, dtype=np.float64)
+    offa = None if off is None else np.ascontiguousarray(off, dtype=np.float64)
     tok = np.zeros((B, N), dtype=np.int32)
     par = np.zeros((B, N), dtype=np.int32)
     pos = np.zeros((B, N), dtype=np.int32)
@@ -145,8 +148,8 @@ def tree_from_lists(ids, logp, *, B, d, k, W, lam, beta, ngram: NGram | None, ct
     gap = np.zeros((B, d), dtype=np.float64)
     n = ngram.n if ngram is not None else 0
     c = None if ctx is None else np.ascontiguousarray(ctx, dtype=np.int32)
-    rc = lib.oracle_tree_from_lists(B, d, k, W, _p(ids), _p(logp), float(lam), float(beta),
-                                    ngram.h if ngram is not None else None, n, _p(c),
+    rc = lib.oracle_tree_from_lists(B, d, k, W, _p(ids), _p(base), float(invT), _p(offa), float(lam),
+                                    float(beta), ngram.h if ngram is not None else None, n, _p(c),
                                     _p(tok), _p(par), _p(pos), _p(mask), _p(sc), _p(gap), threads)
     if rc:
         raise ValueError(f"oracle_tree_from_lists failed ({rc})")

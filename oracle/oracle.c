@@ -200,13 +200,13 @@ int oracle_num_nodes(int d, int k, int W) {
     return (int)total;
 }
 
-typedef struct { double s; int32_t i; int32_t tok; } cand_t;
+typedef struct { double key, Z, G; int32_t i; int32_t tok; } cand_t;
 
 static int cmp_cand(const void* pa, const void* pb) {
     const cand_t* a = (const cand_t*)pa;
     const cand_t* b = (const cand_t*)pb;
-    if (a->s > b->s) return -1;           /* higher score first */
-    if (a->s < b->s) return 1;
+    if (a->key > b->key) return -1;       /* higher score first */
+    if (a->key < b->key) return 1;
     if (a->i != b->i) return a->i < b->i ? -1 : 1;       /* then lower parent */
     return (a->tok > b->tok) - (a->tok < b->tok);        /* then lower token id */
 }
@@ -232,49 +232,63 @@ int oracle_mask_from_parents(int B, int N, const int32_t* parents, uint32_t* mas
     return 0;
 }
 
-/* one tree: frontier entries carry their whole token sequence (context ++ path) */
+/* One tree.  A node's path score is sum_j p_j[c_j] + lam * sum_j g_j with
+ * p_j[c] = base_j[c] * invT - off_j.  Every node of one depth carries the same
+ * sum of off_j, so children are ranked by key = Z * invT + lam * G, where Z is
+ * the sum of the base values along the path and G the sum of n-gram terms,
+ * each accumulated in double from the root in path order; the reported score
+ * is key minus that common sum.  Ranking on the key keeps every tie that the
+ * inputs hold exactly (equal sums of logits along two paths) an exact tie,
+ * whatever the rounding of the log-partition terms. */
 static int one_tree(int b, int d, int k, int W, int N,
-                    const int32_t* ids, const double* logp,
+                    const int32_t* ids, const double* base, double invT, const double* off,
                     double lam, double beta, const oracle_ngram* tab, int n,
                     const int32_t* ctx,
                     int32_t* tokens, int32_t* parents, int32_t* pos, double* scores,
                     double* min_pos_gap) {
     int L = (n > 1 ? n - 1 : 0) + d;             /* longest sequence */
     int Wmax = W;
-    double* fs = (double*)malloc(sizeof(double) * Wmax);
+    double* fZ = (double*)malloc(sizeof(double) * Wmax);
+    double* fG = (double*)malloc(sizeof(double) * Wmax);
     int* fnode = (int*)malloc(sizeof(int) * Wmax);
     int32_t* fseq = (int32_t*)malloc(sizeof(int32_t) * (size_t)Wmax * (L > 0 ? L : 1));
-    double* ns = (double*)malloc(sizeof(double) * Wmax);
+    double* nZ = (double*)malloc(sizeof(double) * Wmax);
+    double* nG = (double*)malloc(sizeof(double) * Wmax);
     int* nnode = (int*)malloc(sizeof(int) * Wmax);
     int32_t* nseq = (int32_t*)malloc(sizeof(int32_t) * (size_t)Wmax * (L > 0 ? L : 1));
     cand_t* cand = (cand_t*)malloc(sizeof(cand_t) * (size_t)Wmax * k);
-    if (!fs || !fnode || !fseq || !ns || !nnode || !nseq || !cand) {
-        free(fs); free(fnode); free(fseq); free(ns); free(nnode); free(nseq); free(cand);
-        return 1;
-    }
+    int rc = 0;
+    if (!fZ || !fG || !fnode || !fseq || !nZ || !nG || !nnode || !nseq || !cand) rc = 1;
     int nc = n > 1 ? n - 1 : 0;                  /* committed context length */
     int F = 1, len = nc, next = 0;
-    fs[0] = 0.0;
-    fnode[0] = -1;
-    for (int c = 0; c < nc; ++c) fseq[c] = ctx[(size_t)b * nc + c];
-
-    for (int j = 0; j < d; ++j) {
+    double Lsum = 0.0;
+    if (!rc) {
+        fZ[0] = 0.0;
+        fG[0] = 0.0;
+        fnode[0] = -1;
+        for (int c = 0; c < nc; ++c) fseq[c] = ctx[(size_t)b * nc + c];
+    }
+    for (int j = 0; j < d && !rc; ++j) {
         const int32_t* C = ids + ((size_t)b * d + j) * k;
-        const double* P = logp + ((size_t)b * d + j) * k;
+        const double* P = base + ((size_t)b * d + j) * k;
+        if (off) Lsum = Lsum + off[(size_t)b * d + j];
         int m = 0;
         for (int i = 0; i < F; ++i) {
             const int32_t* seq = fseq + (size_t)i * L;
             for (int c = 0; c < k; ++c) {
-                double s = fs[i] + P[c];
+                double Z = fZ[i] + P[c];
+                double G = fG[i];
                 if (tab) {
                     int32_t key[4];
                     for (int q = 0; q < n - 1; ++q) key[q] = seq[len - (n - 1) + q];
                     key[n - 1] = C[c];
                     float g = 0.0f;
                     double gg = ngram_get(tab, key, &g) ? (double)g : beta;
-                    s = s + lam * gg;
+                    G = G + gg;
                 }
-                cand[m].s = s;
+                cand[m].Z = Z;
+                cand[m].G = G;
+                cand[m].key = Z * invT + lam * G;
                 cand[m].i = i;
                 cand[m].tok = C[c];
                 ++m;
@@ -285,20 +299,21 @@ static int one_tree(int b, int d, int k, int W, int N,
         if (min_pos_gap) {
             double g = 1e300;
             for (int r = 0; r < keep && r + 1 < m; ++r) {
-                double gap = cand[r].s - cand[r + 1].s;
+                double gap = cand[r].key - cand[r + 1].key;
                 if (gap > 0.0 && gap < g) g = gap;
             }
             min_pos_gap[(size_t)b * d + j] = g;
         }
         for (int r = 0; r < keep; ++r) {
             int node = next + r;
-            if (node >= N) return 2;
+            if (node >= N) { rc = 2; break; }
             const cand_t* e = &cand[r];
             tokens[(size_t)b * N + node] = e->tok;
             parents[(size_t)b * N + node] = fnode[e->i];
             pos[(size_t)b * N + node] = j + 1;
-            if (scores) scores[(size_t)b * N + node] = e->s;
-            ns[r] = e->s;
+            if (scores) scores[(size_t)b * N + node] = e->key - Lsum;
+            nZ[r] = e->Z;
+            nG[r] = e->G;
             nnode[r] = node;
             memcpy(nseq + (size_t)r * L, fseq + (size_t)e->i * L, sizeof(int32_t) * (size_t)len);
             nseq[(size_t)r * L + len] = e->tok;
@@ -306,23 +321,27 @@ static int one_tree(int b, int d, int k, int W, int N,
         next += keep;
         F = keep;
         len += 1;
-        memcpy(fs, ns, sizeof(double) * F);
-        memcpy(fnode, nnode, sizeof(int) * F);
-        memcpy(fseq, nseq, sizeof(int32_t) * (size_t)F * L);
+        if (!rc) {
+            memcpy(fZ, nZ, sizeof(double) * F);
+            memcpy(fG, nG, sizeof(double) * F);
+            memcpy(fnode, nnode, sizeof(int) * F);
+            memcpy(fseq, nseq, sizeof(int32_t) * (size_t)F * L);
+        }
     }
-    free(fs); free(fnode); free(fseq); free(ns); free(nnode); free(nseq); free(cand);
+    free(fZ); free(fG); free(fnode); free(fseq); free(nZ); free(nG); free(nnode); free(nseq); free(cand);
+    if (rc) return rc;
     return next == N ? 0 : 3;
 }
 
 int oracle_tree_from_lists(int B, int d, int k, int W,
-                           const int32_t* ids, const double* logp,
+                           const int32_t* ids, const double* base, double invT, const double* off,
                            double lam, double beta, const oracle_ngram* tab, int n,
                            const int32_t* ctx,
                            int32_t* tokens, int32_t* parents, int32_t* pos,
                            uint32_t* mask, double* scores, double* min_pos_gap,
                            int threads) {
     int N = oracle_num_nodes(d, k, W);
-    if (B < 0 || N < 0 || !ids || !logp || !tokens || !parents || !pos) return 1;
+    if (B < 0 || N < 0 || !ids || !base || !tokens || !parents || !pos) return 1;
     if (tab && (n != tab->n || n < 2 || (!ctx && B > 0))) return 1;
     int fail = 0;
 #ifdef _OPENMP
@@ -330,7 +349,7 @@ int oracle_tree_from_lists(int B, int d, int k, int W,
 #pragma omp parallel for num_threads(threads) schedule(dynamic, 1) reduction(| : fail)
 #endif
     for (int b = 0; b < B; ++b)
-        fail |= one_tree(b, d, k, W, N, ids, logp, lam, beta, tab, tab ? n : 0, ctx,
+        fail |= one_tree(b, d, k, W, N, ids, base, invT, off, lam, beta, tab, tab ? n : 0, ctx,
                          tokens, parents, pos, scores, min_pos_gap);
     if (fail) return fail;
     if (mask) return oracle_mask_from_parents(B, N, parents, mask);
@@ -347,12 +366,21 @@ int oracle_tree_build(const void* logits, int dtype, int B, int d, int V, double
     size_t R = (size_t)B * d;
     int32_t* ids = row_ids ? row_ids : (int32_t*)malloc(sizeof(int32_t) * (R * k + 1));
     double* lp = row_logp ? row_logp : (double*)malloc(sizeof(double) * (R * k + 1));
-    int rc = (!ids || !lp) ? 1 : 0;
-    if (!rc) rc = oracle_rows(logits, dtype, (int64_t)R, V, T, k, ids, lp, row_lse, threads);
-    if (!rc) rc = oracle_tree_from_lists(B, d, k, W, ids, lp, lam, beta, tab, n, ctx,
-                                         tokens, parents, pos, mask, scores, min_pos_gap,
-                                         threads);
+    double* lse = row_lse ? row_lse : (double*)malloc(sizeof(double) * (R + 1));
+    double* zc = (double*)malloc(sizeof(double) * (R * k + 1));
+    int rc = (!ids || !lp || !lse || !zc) ? 1 : 0;
+    if (!rc) rc = oracle_rows(logits, dtype, (int64_t)R, V, T, k, ids, lp, lse, threads);
+    if (!rc) {
+        /* the candidates' own logits are the base values of the ranking key */
+        for (size_t r = 0; r < R; ++r)
+            for (int c = 0; c < k; ++c)
+                zc[r * k + c] = oracle_decode(logits, dtype, (int64_t)r * V + ids[r * k + c]);
+        rc = oracle_tree_from_lists(B, d, k, W, ids, zc, 1.0 / T, lse, lam, beta, tab, n, ctx,
+                                    tokens, parents, pos, mask, scores, min_pos_gap, threads);
+    }
     if (!row_ids) free(ids);
     if (!row_logp) free(lp);
+    if (!row_lse) free(lse);
+    free(zc);
     return rc;
 }

@@ -48,20 +48,26 @@ void oracle_ngram_free(oracle_ngram* t);
 void oracle_ngram_lookup(const oracle_ngram* t, const int32_t* keys, int64_t Q,
                          float* vals, int32_t* found);
 
-/* Tree construction from per-depth candidate lists ids/logp [B][d][k].
+/* Tree construction from per-depth candidate lists, ids/base [B][d][k].
+ * A candidate's log-probability is base * invT - off[b][j] (off may be NULL
+ * for 0); with invT = 1 and off = NULL, base holds log-probabilities.
+ * Children are ranked by key = Z * invT + lam * G (Z: sum of base values along
+ * the path, G: sum of n-gram values or beta), then lower parent index, then
+ * lower token id; scores[] = key - sum of off over the node's depths.
  * tab == NULL means no continuity term.  Outputs [B][N] (mask [B][N][MW]);
- * min_pos_gap[B][d] (may be NULL) is, per depth, the smallest positive score
+ * min_pos_gap[B][d] (may be NULL) is, per depth, the smallest positive key
  * gap between neighbours in the sorted candidate list among the pairs that
  * decide a kept node's rank or the cut (1e300 when there is none). */
 int oracle_tree_from_lists(int B, int d, int k, int W,
-                           const int32_t* ids, const double* logp,
+                           const int32_t* ids, const double* base, double invT, const double* off,
                            double lam, double beta, const oracle_ngram* tab, int n,
                            const int32_t* ctx,
                            int32_t* tokens, int32_t* parents, int32_t* pos,
                            uint32_t* mask, double* scores, double* min_pos_gap,
                            int threads);
 
-/* Rows, then the tree, as one call.  row_ids/row_logp/row_lse may be NULL. */
+/* Rows, then the tree, as one call (base = the candidates' logits, invT =
+ * 1 / T, off = each row's log-sum-exp).  row_ids/row_logp/row_lse may be NULL. */
 int oracle_tree_build(const void* logits, int dtype, int B, int d, int V, double T,
                       int k, int W, double lam, double beta,
                       const oracle_ngram* tab, int n, const int32_t* ctx,

@@ -228,8 +228,10 @@ def make_case(*, B, d, V, dtype, T, k, W, n, M, lam, beta, recipe, seed=0,
     zs = _as_f32(logits, dtype)  # the values actually stored
     ctx = rng.integers(0, V, size=(B, max(n - 1, 0))).astype(np.int32)
     keys, vals = make_ngram_table(rng, zs, ctx, k, n, M, vlo, vhi, V)
-    return Case(name=name, B=B, d=d, V=V, dtype=dtype, T=float(T), k=k, W=W, n=n,
-                lam=float(lam), beta=float(beta), logits=logits, ctx=ctx,
+    # T, lambda and beta cross the C ABI as fp32: keep the fp32 value on both sides
+    f32 = lambda x: float(np.float32(x))
+    return Case(name=name, B=B, d=d, V=V, dtype=dtype, T=f32(T), k=k, W=W, n=n,
+                lam=f32(lam), beta=f32(beta), logits=logits, ctx=ctx,
                 ng_keys=keys, ng_vals=vals, seed=seed, meta=dict(recipe=recipe, M=M))
 
 

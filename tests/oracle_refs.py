@@ -127,3 +127,35 @@ def mask_row_to_set(words) -> set:
             if (int(word) >> b) & 1:
                 s.add(w * 32 + b)
     return s
+
+
+def whole_path_brute_force_ok(lib=None, seed=3) -> bool:
+    """Rows + tree through oracle.tree_build at T != 1 with nothing pruned, against
+    scipy's log_softmax and an exhaustive enumeration of the paths."""
+    import scipy.special
+    import oracle
+    import synth
+    case = synth.make_case(B=2, d=3, V=40, dtype="bf16", T=0.7, k=3, W=27, n=2, M=600, lam=0.5,
+                           beta=-9.0, recipe=("normal", 3.0), seed=seed)
+    try:
+        out = oracle.tree_build(case, lib=lib)
+    except ValueError:
+        return False
+    z = decode_np(case.logits, "bf16")
+    table = dict_ngram(case.ng_keys, case.ng_vals)
+    for b in range(case.B):
+        lsm = [scipy.special.log_softmax(z[b, j] / case.T) for j in range(case.d)]
+        ids = [topk_lexsort(z[b, j], case.k).tolist() for j in range(case.d)]
+        logp = [[lsm[j][t] for t in ids[j]] for j in range(case.d)]
+        ref = brute_force_paths(ids, logp, lam=case.lam, beta=case.beta, table=table, n=case.n,
+                                ctx=case.ctx[b].tolist())
+        try:
+            paths = node_paths(out["tokens"][b].tolist(), out["parents"][b].tolist(), ids)
+        except (ValueError, IndexError):
+            return False
+        if sorted(paths) != sorted(ref.keys()):
+            return False
+        for x, p in enumerate(paths):
+            if abs(out["scores"][b, x] - ref[p]) > 1e-10:
+                return False
+    return True

@@ -31,7 +31,10 @@ MUTANTS = {
                                "    return (a->id < b->id) - (a->id > b->id);\n}\n\nstatic void one_row"),
     "rows_ascending": ("    if (a->z > b->z) return -1;\n    if (a->z < b->z) return 1;",
                        "    if (a->z < b->z) return -1;\n    if (a->z > b->z) return 1;"),
-    "lambda_dropped": ("s = s + lam * gg;", "s = s + gg;"),
+    "lambda_dropped": ("cand[m].key = Z * invT + lam * G;", "cand[m].key = Z * invT + G;"),
+    "temperature_dropped_in_key": ("cand[m].key = Z * invT + lam * G;", "cand[m].key = Z + lam * G;"),
+    "ngram_not_accumulated": ("double G = fG[i];", "double G = 0.0;"),
+    "row_offsets_dropped": ("if (off) Lsum = Lsum + off[(size_t)b * d + j];", "if (off) Lsum = off[(size_t)b * d + j];"),
     "beta_unscaled": ("(double)g : beta;", "(double)g : beta / lam;"),
     "context_off_by_one": ("key[q] = seq[len - (n - 1) + q];", "key[q] = seq[len - n + q];"),
     "parent_ties_reversed": ("return a->i < b->i ? -1 : 1;", "return a->i < b->i ? 1 : -1;"),
@@ -47,7 +50,7 @@ MUTANTS = {
     "bf16_decode_shift": ("uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
     "f16_exponent_bias": ("v = ldexp((double)(m + 1024), e - 25);", "v = ldexp((double)(m + 1024), e - 24);"),
     "path_not_extended": ("nseq[(size_t)r * L + len] = e->tok;", "nseq[(size_t)r * L + len] = 0;"),
-    "parent_score_dropped": ("double s = fs[i] + P[c];", "double s = P[c];"),
+    "parent_score_dropped": ("double Z = fZ[i] + P[c];", "double Z = P[c];"),
     "cut_at_w_minus_one": ("int keep = m < W ? m : W;", "int keep = m < W - 1 ? m : W - 1;"),
 }
 
@@ -163,7 +166,11 @@ def _pin_k_best(lib):
     return True
 
 
-PINS = [_pin_worked_examples, _pin_rows, _pin_brute_force, _pin_k_best]
+def _pin_whole_path_temperature(lib):
+    return R.whole_path_brute_force_ok(lib)
+
+
+PINS = [_pin_worked_examples, _pin_rows, _pin_brute_force, _pin_k_best, _pin_whole_path_temperature]
 
 
 def _all_pins_pass(lib) -> bool:

@@ -177,6 +177,12 @@ def test_lambda_zero_is_exact_k_best_sums(d, k, W):
             np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
 
 
+def test_whole_path_at_temperature_against_brute_force():
+    """oracle.tree_build at T = 0.7, W = k^d: scores from scipy log_softmax + enumeration."""
+    for seed in (3, 4, 5):
+        assert R.whole_path_brute_force_ok(seed=seed)
+
+
 # --------------------------------------------------------- output invariants
 
 @pytest.mark.parametrize("cfg", [0])

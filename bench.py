@@ -1,0 +1,389 @@
+#!/usr/bin/env python
+"""Throughput of continuity-aware draft-tree construction on GB300.
+
+One step = one dart_tree_build call over a batch: every logit row streamed
+once (log-softmax + top-k), then every tree grown depth by depth (expand,
+n-gram score, top-W), with token/parent/depth ids and ancestor masks written.
+
+Prints one JSON line: trees/s over the whole job (value), the streaming
+kernel's achieved HBM bandwidth against the measured copy peak (roofline),
+the same metric end to end with host buffers (e2e), and the CPU oracle on a
+bounded sample of the same workload (cpu_baseline).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl ours|reference]
+
+Under torchrun every rank builds its own batch (weak scaling, no collective
+on the data path); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+DEFAULT_CONFIG = 2
+METRIC = "draft trees/sec and achieved HBM GB/s (% of GB300 peak) at 1 GPU vs CPU oracle"
+
+
+def workload_name(i: int) -> str:
+    c = synth.CONFIGS[i]
+    return (f"config {i}: B={c['B']} d={c['d']} V={c['V']} {c['dtype']} logits {c['recipe'][0]}, "
+            f"T={c['T']} k={c['k']} W={c['W']}, {c['n']}-gram table {c['M']} keys, "
+            f"lambda={c['lam']} beta={c['beta']}")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ ranks
+
+def dist_setup():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world, local):
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- clocks
+
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def clocks_start(gpu_index: int):
+    try:
+        f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        p = subprocess.Popen(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={CLOCK_QUERY}",
+                              "--format=csv,noheader,nounits", "-lms", "100"],
+                             stdout=f, stderr=subprocess.DEVNULL)
+        return p, f.name
+    except (OSError, FileNotFoundError):
+        return None, None
+
+
+def clocks_stop(handle):
+    p, path = handle
+    if p is None:
+        return None
+    p.terminate()
+    try:
+        p.wait(timeout=5)
+    except subprocess.TimeoutExpired:
+        p.kill()
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in open(path):
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            mx.append(float(parts[2]))
+        except ValueError:
+            continue
+        for name, v in zip(names, parts[5:9]):
+            if v.lower() == "active":
+                reasons.add(name)
+    os.unlink(path)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+# ------------------------------------------------------------ measured peaks
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("dart_rows.cu", "dart_common.cuh"):
+        with open(os.path.join(ROOT, "draft_tree_construction_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def k1_traffic(config: int):
+    """DRAM bytes per launch of the streaming kernel from the committed ncu summary,
+    or None when the kernel source changed since that capture."""
+    path = os.path.join(ROOT, "profiles", "row_stream_dram.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha256") != kernel_source_hash():
+        return None
+    per = rec.get("dram_bytes_per_logit_byte")
+    if per is None:
+        return None
+    c = synth.CONFIGS[config]
+    return per * c["B"] * c["d"] * c["V"] * synth.ELEM_BYTES[c["dtype"]]
+
+
+# -------------------------------------------------------------- CPU oracle
+
+def _sub_case(case, S):
+    return synth.Case(name=case.name, B=S, d=case.d, V=case.V, dtype=case.dtype, T=case.T,
+                      k=case.k, W=case.W, n=case.n, lam=case.lam, beta=case.beta,
+                      logits=case.logits[:S], ctx=case.ctx[:S], ng_keys=case.ng_keys,
+                      ng_vals=case.ng_vals)
+
+
+def oracle_sample(case, budget_s: float, ngram=None):
+    """Times the oracle on the first S trees of `case` (S sized to the budget)."""
+    import oracle
+    if ngram is None and case.n >= 2:
+        ngram = oracle.NGram(case.n, case.ng_keys, case.ng_vals)
+    threads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle.tree_build(_sub_case(case, 1), ngram=ngram, threads=threads)
+    t1 = time.perf_counter() - t0
+    S = int(max(1, min(case.B, math.floor(budget_s / max(t1, 1e-6)))))
+    t0 = time.perf_counter()
+    oracle.tree_build(_sub_case(case, S), ngram=ngram, threads=threads)
+    dt = time.perf_counter() - t0
+    return S, dt, threads, ngram
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(args):
+    rank, world, local = dist_setup()
+    if rank != 0:
+        return 0
+    import oracle
+    case = synth.make_config(args.config, seed=args.seed)
+    ngram = oracle.NGram(case.n, case.ng_keys, case.ng_vals) if case.n >= 2 else None
+    per_step = min(10.0, 150.0 / max(1, args.steps + args.warmup))
+    S, _, threads, _ = oracle_sample(case, per_step, ngram)
+    sub = _sub_case(case, S)
+    for _ in range(args.warmup):
+        oracle.tree_build(sub, ngram=ngram, threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.tree_build(sub, ngram=ngram, threads=threads)
+    dt = time.perf_counter() - t0
+    value = S * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "trees/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": workload_name(args.config), "sample_trees_per_step": S},
+        "cpu_baseline": {"value": value, "unit": "trees/s", "cores": threads, "kind": "oracle",
+                         "sample": f"first {S} of {case.B} trees per step, full vocabulary and table"},
+        "e2e": {"value": value, "unit": "trees/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import ctypes as C
+
+    import torch
+    import draft_tree_construction_gb300 as D
+
+    rank, world, local = dist_setup()
+    dist_init(world, local)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    D.build()
+    L = D.lib()
+
+    case = synth.make_config(args.config, seed=args.seed + rank)
+    B, d, V, k = case.B, case.d, case.V, case.k
+    logit_bytes = case.logit_bytes
+    if case.dtype == "bf16":
+        host = torch.from_numpy(case.logits.view(np.int16).copy()).view(torch.bfloat16)
+    else:
+        host = torch.from_numpy(case.logits.copy())
+    z = host.to(dev)
+    tab = D.NGramTable(case.n, case.ng_keys, case.ng_vals, device=dev) if case.n >= 2 else None
+    ctx = torch.from_numpy(np.ascontiguousarray(case.ctx)).to(dev) if tab is not None else None
+    builder = D.TreeBuilder(B, d, V, z.dtype, case.T, k, case.W, case.lam, case.beta,
+                            table=tab, ctx=ctx, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    # L2 flush between timed steps: a read-only sweep of 256 MB (twice the L2)
+    # evicts the logits, the n-gram table and the workspace without leaving
+    # dirty lines to be written back inside the next timed window
+    flush_buf = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_buf.sum()
+
+    def timed(fn, steps):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for i in range(steps):
+            flush()
+            evs[i][0].record(stream)
+            fn(i)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b) for a, b in evs]
+
+    for _ in range(max(3, args.warmup)):
+        flush()
+        builder(z)
+    torch.cuda.synchronize(dev)
+    assert D.device_error(builder.ws) == 0, "device error during warm-up"
+
+    clk = clocks_start(dev.index or 0)
+    # ---- timed region: whole steps (memset + streaming kernel + tree kernel)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    step_times = timed(lambda i: builder(z), args.steps)
+    barrier(world)
+    step_ms = max_over_ranks(statistics.mean(step_times), world)
+
+    # ---- the streaming kernel alone (same launch configuration), for the roofline
+    code = D.DTYPE_CODES()[z.dtype]
+    ws = builder.ws
+
+    def rows_only(i):
+        rc = L.dart_row_topk(C.c_void_p(z.data_ptr()), B * d, V, code, float(case.T), k,
+                             None, None, None, C.c_void_p(ws.data_ptr()), ws.numel(),
+                             C.c_void_p(stream.cuda_stream))
+        assert rc == 0
+
+    k1_times = timed(rows_only, args.steps)
+    k1_ms = max_over_ranks(statistics.mean(k1_times), world)
+    clocks = clocks_stop(clk)
+
+    # ---- end to end: pinned host logits in, pinned host outputs back, every step
+    e2e = None
+    if not args.no_e2e:
+        pinned = host.pin_memory()
+        outs = {key: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                for key, v in builder.out.items() if v is not None}
+        d2h = sum(v.numel() * v.element_size() for v in outs.values())
+        h2d = pinned.numel() * pinned.element_size()
+
+        def e2e_step(i):
+            z.copy_(pinned, non_blocking=True)
+            builder(z)
+            for key, v in outs.items():
+                v.copy_(builder.out[key], non_blocking=True)
+
+        for i in range(2):
+            e2e_step(i)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e2e_times = timed(e2e_step, args.steps)
+        e2e_ms = max_over_ranks(statistics.mean(e2e_times), world)
+        e2e = {"value": B * world / (e2e_ms / 1e3), "unit": "trees/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+    assert D.device_error(builder.ws) == 0, "device error during the timed steps"
+
+    peaks, peaks_src = measured_peaks()
+    achieved = logit_bytes / (k1_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": k1_traffic(args.config),
+                "kernel": "row_stream_kernel (log-softmax + top-k stream)",
+                "peak_source": f"{peaks_src} hbm_gbs",
+                "k1_ms": k1_ms, "frac_of_8tbs_nominal": achieved / 8000.0}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        S, dt, threads, _ = oracle_sample(case, args.cpu_seconds)
+        cpu = {"value": S / dt, "unit": "trees/s", "cores": threads, "kind": "oracle",
+               "sample": f"first {S} of {B} trees of the same batch, full vocabulary and table"}
+
+    if rank == 0:
+        value = B * world / (step_ms / 1e3)
+        line = {
+            "metric": METRIC, "value": value, "unit": "trees/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": workload_name(args.config), "logit_dtype": case.dtype,
+                       "trees_per_gpu": B, "logit_bytes_per_step": logit_bytes,
+                       "l2": "flushed before every timed step (read-only sweep of 256 MB)",
+                       "step_ms_p10_p50_p90": [float(np.percentile(step_times, q)) for q in (10, 50, 90)],
+                       "k1_ms_p10_p50_p90": [float(np.percentile(k1_times, q)) for q in (10, 50, 90)],
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "hbm_gbs_whole_step": logit_bytes / (step_ms / 1e3) / 1e9,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,323 @@
+"""Continuity-aware draft-tree construction on one GB300 (sm_103a).
+
+A thin binding over the C ABI in include/darttree.h (libdarttree.so, built
+in-tree by ``build()``).  This module only marshals arguments: every step of
+the path runs in the library's CUDA kernels, PyTorch supplies device memory
+and streams.  Calls raise ``DartError`` when the library is missing or a call
+fails; there is no fallback.
+
+The computation (DART, Figure 3 caption; DARTree, Method / Tree
+Construction), made precise:
+  p_j = log_softmax(z_j / T); C_j = the k largest z_j (lower id first on ties);
+  child score = parent + p_j[c] + lam * ngram(last n-1 tokens, c), or
+  + lam * beta when the n-gram is missing; keep the W best children of the
+  whole frontier (score, then lower parent index, then lower token id);
+  emit tokens, parents (-1 at depth 1), depths and ancestor-or-self masks.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import numpy as np
+
+from ._build import LIB as _LIB_PATH, build as _build_lib
+
+__all__ = [
+    "DartError", "build", "lib", "NGramTable", "num_nodes", "mask_words", "workspace_bytes",
+    "tree_build", "tree_from_topk", "row_topk", "mask_pack", "device_error", "TreeBuilder",
+    "DTYPE_CODES",
+]
+
+DART_OK = 0
+DEVERR = {1: "bulk-copy wait timeout", 2: "row max mismatch", 4: "tree selection", 8: "bad parent"}
+
+
+class DartError(RuntimeError):
+    pass
+
+
+class _Table(C.Structure):
+    _fields_ = [("n", C.c_int32), ("reserved", C.c_int32), ("capacity", C.c_uint64),
+                ("slots", C.c_void_p)]
+
+
+_lock = threading.Lock()
+_handle = None
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libdarttree.so for sm_103a (nvcc) if it is missing or stale."""
+    return _build_lib(force=force, verbose=verbose)
+
+
+def _declare(L):
+    P, i32, i64, u64, f32, sz = C.c_void_p, C.c_int, C.c_int64, C.c_uint64, C.c_float, C.c_size_t
+    T = C.POINTER(_Table)
+    L.dart_tree_num_nodes.argtypes = [i32, i32, i32]
+    L.dart_tree_num_nodes.restype = i32
+    L.dart_tree_mask_words.argtypes = [i32]
+    L.dart_tree_mask_words.restype = i32
+    L.dart_tree_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    L.dart_tree_workspace_bytes.restype = sz
+    L.dart_tree_build.argtypes = [P, i32, i32, i32, i32, f32, i32, i32, f32, f32, T, P,
+                                  P, P, P, P, P, P, sz, P]
+    L.dart_tree_build.restype = i32
+    L.dart_tree_from_topk.argtypes = [P, P, i32, i32, i32, i32, f32, f32, T, P, P, P, P, P, P, P]
+    L.dart_tree_from_topk.restype = i32
+    L.dart_row_topk.argtypes = [P, i32, i32, i32, f32, i32, P, P, P, P, sz, P]
+    L.dart_row_topk.restype = i32
+    L.dart_mask_pack.argtypes = [P, i32, i32, P, P, P]
+    L.dart_mask_pack.restype = i32
+    L.dart_ngram_capacity_for.argtypes = [u64]
+    L.dart_ngram_capacity_for.restype = u64
+    L.dart_ngram_table_pack_host.argtypes = [i32, P, P, u64, u64, P, C.POINTER(C.c_uint64)]
+    L.dart_ngram_table_pack_host.restype = i32
+    L.dart_ngram_lookup.argtypes = [T, P, i64, P, P, P]
+    L.dart_ngram_lookup.restype = i32
+    L.dart_device_error.argtypes = [P, C.POINTER(C.c_uint32), P]
+    L.dart_device_error.restype = i32
+    L.dart_status_string.argtypes = [i32]
+    L.dart_status_string.restype = C.c_char_p
+    return L
+
+
+def lib():
+    """The loaded C library; raises DartError when it has not been built."""
+    global _handle
+    with _lock:
+        if _handle is None:
+            if not os.path.exists(_LIB_PATH):
+                raise DartError(f"{_LIB_PATH} is missing: run draft_tree_construction_gb300.build()")
+            _handle = _declare(C.CDLL(_LIB_PATH))
+    return _handle
+
+
+def _check(rc: int, what: str):
+    if rc != DART_OK:
+        msg = lib().dart_status_string(rc).decode()
+        raise DartError(f"{what} failed: {msg} ({rc})")
+
+
+# --------------------------------------------------------------- helpers
+
+def _torch():
+    import torch
+    return torch
+
+
+def DTYPE_CODES():
+    torch = _torch()
+    return {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _need_cuda(t, name, dtype=None, contiguous=True):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise DartError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise DartError(f"{name} must be {dtype}, got {t.dtype}")
+    if contiguous and not t.is_contiguous():
+        raise DartError(f"{name} must be contiguous")
+
+
+def num_nodes(d: int, k: int, W: int) -> int:
+    return lib().dart_tree_num_nodes(d, k, W)
+
+
+def mask_words(N: int) -> int:
+    return lib().dart_tree_mask_words(N)
+
+
+def workspace_bytes(B: int, d: int, V: int, dtype_code: int, k: int) -> int:
+    return lib().dart_tree_workspace_bytes(B, d, V, dtype_code, k)
+
+
+# ------------------------------------------------------------ n-gram model
+
+class NGramTable:
+    """Open-addressing n-gram table in device memory (format: include/darttree.h)."""
+
+    def __init__(self, n: int, keys: np.ndarray, vals: np.ndarray, device="cuda",
+                 capacity: int | None = None):
+        torch = _torch()
+        L = lib()
+        keys = np.ascontiguousarray(keys, dtype=np.int32).reshape(-1, n)
+        vals = np.ascontiguousarray(vals, dtype=np.float32).reshape(-1)
+        M = keys.shape[0]
+        cap = int(capacity) if capacity else int(L.dart_ngram_capacity_for(M))
+        host = np.empty(cap * 16, dtype=np.uint8)
+        distinct = C.c_uint64(0)
+        _check(L.dart_ngram_table_pack_host(n, keys.ctypes.data_as(C.c_void_p),
+                                            vals.ctypes.data_as(C.c_void_p), M, cap,
+                                            host.ctypes.data_as(C.c_void_p), C.byref(distinct)),
+               "dart_ngram_table_pack_host")
+        self.n = n
+        self.capacity = cap
+        self.distinct = int(distinct.value)
+        self.slots = torch.from_numpy(host).to(device)
+        self.desc = _Table(n, 0, cap, self.slots.data_ptr())
+
+    @property
+    def nbytes(self) -> int:
+        return self.capacity * 16
+
+    def lookup(self, keys, stream=None):
+        """keys: CUDA int32 [Q, n] -> (vals float32 [Q], found bool [Q])."""
+        torch = _torch()
+        _need_cuda(keys, "keys", torch.int32)
+        Q = keys.shape[0]
+        vals = torch.empty(Q, dtype=torch.float32, device=keys.device)
+        found = torch.empty(Q, dtype=torch.int32, device=keys.device)
+        _check(lib().dart_ngram_lookup(C.byref(self.desc), _ptr(keys), Q, _ptr(vals), _ptr(found),
+                                       _stream_ptr(stream)), "dart_ngram_lookup")
+        return vals, found.bool()
+
+
+# ------------------------------------------------------------ the tree path
+
+def _outputs(B, N, MW, device, scores: bool):
+    torch = _torch()
+    return dict(tokens=torch.empty((B, N), dtype=torch.int32, device=device),
+                parents=torch.empty((B, N), dtype=torch.int32, device=device),
+                pos=torch.empty((B, N), dtype=torch.int32, device=device),
+                mask=torch.empty((B, N, MW), dtype=torch.int32, device=device),
+                scores=torch.empty((B, N), dtype=torch.float32, device=device) if scores else None)
+
+
+def tree_build(logits, T: float, k: int, W: int, lam: float, beta: float,
+               table: NGramTable | None = None, ctx=None, *, out: dict | None = None,
+               workspace=None, stream=None, scores: bool = True) -> dict:
+    """logits: CUDA [B, d, V] float32/float16/bfloat16 -> dict of CUDA outputs.
+
+    mask is returned as int32 storage holding the uint32 bit pattern."""
+    torch = _torch()
+    codes = DTYPE_CODES()
+    _need_cuda(logits, "logits")
+    if logits.dtype not in codes or logits.dim() != 3:
+        raise DartError("logits must be [B, d, V] float32, float16 or bfloat16")
+    B, d, V = logits.shape
+    N = num_nodes(d, k, W)
+    if N < 0:
+        raise DartError("invalid d/k/W")
+    MW = mask_words(N)
+    o = out if out is not None else _outputs(B, N, MW, logits.device, scores)
+    need = workspace_bytes(B, d, V, codes[logits.dtype], k)
+    ws = workspace if workspace is not None else torch.empty(max(need, 1), dtype=torch.uint8,
+                                                             device=logits.device)
+    if table is not None:
+        _need_cuda(ctx, "ctx", torch.int32)
+    rc = lib().dart_tree_build(_ptr(logits), B, d, V, codes[logits.dtype], float(T), k, W,
+                               float(lam), float(beta),
+                               C.byref(table.desc) if table is not None else None,
+                               _ptr(ctx) if table is not None else None,
+                               _ptr(o["tokens"]), _ptr(o["parents"]), _ptr(o["pos"]), _ptr(o["mask"]),
+                               _ptr(o.get("scores")), _ptr(ws), ws.numel(), _stream_ptr(stream))
+    _check(rc, "dart_tree_build")
+    o["workspace"] = ws
+    return o
+
+
+def tree_from_topk(ids, logp, W: int, lam: float, beta: float, table: NGramTable | None = None,
+                   ctx=None, *, out: dict | None = None, stream=None, scores: bool = True) -> dict:
+    """ids: CUDA int32 [B, d, k]; logp: CUDA float64 [B, d, k] -> dict of CUDA outputs."""
+    torch = _torch()
+    _need_cuda(ids, "ids", torch.int32)
+    _need_cuda(logp, "logp", torch.float64)
+    B, d, k = ids.shape
+    N = num_nodes(d, k, W)
+    if N < 0:
+        raise DartError("invalid d/k/W")
+    MW = mask_words(N)
+    o = out if out is not None else _outputs(B, N, MW, ids.device, scores)
+    if table is not None:
+        _need_cuda(ctx, "ctx", torch.int32)
+    rc = lib().dart_tree_from_topk(_ptr(ids), _ptr(logp), B, d, k, W, float(lam), float(beta),
+                                   C.byref(table.desc) if table is not None else None,
+                                   _ptr(ctx) if table is not None else None,
+                                   _ptr(o["tokens"]), _ptr(o["parents"]), _ptr(o["pos"]),
+                                   _ptr(o["mask"]), _ptr(o.get("scores")), _stream_ptr(stream))
+    _check(rc, "dart_tree_from_topk")
+    return o
+
+
+def row_topk(logits, T: float, k: int, *, workspace=None, stream=None):
+    """logits: CUDA [R, V] -> (ids int32 [R,k], logp float32 [R,k], lse float32 [R], workspace)."""
+    torch = _torch()
+    codes = DTYPE_CODES()
+    _need_cuda(logits, "logits")
+    if logits.dtype not in codes or logits.dim() != 2:
+        raise DartError("logits must be [R, V] float32, float16 or bfloat16")
+    R, V = logits.shape
+    ids = torch.empty((R, k), dtype=torch.int32, device=logits.device)
+    logp = torch.empty((R, k), dtype=torch.float32, device=logits.device)
+    lse = torch.empty((R,), dtype=torch.float32, device=logits.device)
+    need = workspace_bytes(R, 1, V, codes[logits.dtype], k)
+    ws = workspace if workspace is not None else torch.empty(max(need, 1), dtype=torch.uint8,
+                                                             device=logits.device)
+    _check(lib().dart_row_topk(_ptr(logits), R, V, codes[logits.dtype], float(T), k, _ptr(ids),
+                               _ptr(logp), _ptr(lse), _ptr(ws), ws.numel(), _stream_ptr(stream)),
+           "dart_row_topk")
+    return ids, logp, lse, ws
+
+
+def mask_pack(parents, *, device_err=None, stream=None):
+    """parents: CUDA int32 [B, N] -> mask int32 [B, N, ceil(N/32)] (uint32 bits)."""
+    torch = _torch()
+    _need_cuda(parents, "parents", torch.int32)
+    B, N = parents.shape
+    out = torch.empty((B, N, (N + 31) // 32), dtype=torch.int32, device=parents.device)
+    _check(lib().dart_mask_pack(_ptr(parents), B, N, _ptr(out), _ptr(device_err), _stream_ptr(stream)),
+           "dart_mask_pack")
+    return out
+
+
+def device_error(workspace, stream=None) -> int:
+    """Synchronises the stream and returns the workspace's device error bits."""
+    flags = C.c_uint32(0)
+    _check(lib().dart_device_error(_ptr(workspace), C.byref(flags), _stream_ptr(stream)),
+           "dart_device_error")
+    return int(flags.value)
+
+
+class TreeBuilder:
+    """Fixed-shape driver: preallocated outputs and workspace, one C call per step."""
+
+    def __init__(self, B, d, V, dtype, T, k, W, lam, beta, table=None, ctx=None, device="cuda",
+                 scores=True):
+        torch = _torch()
+        self.shape = (B, d, V)
+        self.dtype = dtype
+        self.code = DTYPE_CODES()[dtype]
+        self.T, self.k, self.W, self.lam, self.beta = float(T), k, W, float(lam), float(beta)
+        self.table, self.ctx = table, ctx
+        self.N = num_nodes(d, k, W)
+        self.MW = mask_words(self.N)
+        self.out = _outputs(B, self.N, self.MW, device, scores)
+        self.ws = torch.empty(max(workspace_bytes(B, d, V, self.code, k), 1), dtype=torch.uint8,
+                              device=device)
+
+    def __call__(self, logits, stream=None):
+        B, d, V = self.shape
+        rc = lib().dart_tree_build(_ptr(logits), B, d, V, self.code, self.T, self.k, self.W,
+                                   self.lam, self.beta,
+                                   C.byref(self.table.desc) if self.table is not None else None,
+                                   _ptr(self.ctx) if self.table is not None else None,
+                                   _ptr(self.out["tokens"]), _ptr(self.out["parents"]),
+                                   _ptr(self.out["pos"]), _ptr(self.out["mask"]),
+                                   _ptr(self.out.get("scores")), _ptr(self.ws), self.ws.numel(),
+                                   _stream_ptr(stream))
+        _check(rc, "dart_tree_build")
+        return self.out

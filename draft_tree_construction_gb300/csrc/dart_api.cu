@@ -1,0 +1,266 @@
+// dart_api.cu -- the C ABI declared in include/darttree.h: argument checks,
+// workspace layout, kernel launches, and the host-side n-gram table packer.
+#include <cmath>
+#include <cstring>
+
+#include "dart_launch.h"
+
+using namespace dart;
+
+namespace {
+
+bool finite(float x) { return std::isfinite(x); }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+int elem_bytes(int dtype) { return dtype == DART_F32 ? 4 : 2; }
+bool valid_dtype(int dtype) { return dtype == DART_F32 || dtype == DART_F16 || dtype == DART_BF16; }
+bool pow2(uint64_t x) { return x >= 2 && (x & (x - 1)) == 0; }
+
+int num_nodes(int d, int k, int W) {
+  if (d < 1 || k < 1 || W < 1) return -1;
+  long long total = 0, width = 1;
+  for (int j = 1; j <= d; ++j) {
+    width *= k;
+    if (width > W) width = W;
+    total += width;
+    if (total > (1LL << 30)) return -1;
+  }
+  return int(total);
+}
+
+int check_table(const dart_ngram_table_t* t, const int32_t* ctx, int B) {
+  if (!t) return DART_OK;
+  if (t->n < 2 || t->n > 4 || t->reserved != 0) return DART_ERR_INVALID_ARG;
+  if (!pow2(t->capacity) || !t->slots || !aligned(t->slots, 16)) return DART_ERR_INVALID_ARG;
+  if (B > 0 && !ctx) return DART_ERR_INVALID_ARG;
+  return DART_OK;
+}
+
+// Shared checks of the tree-shape arguments.
+int check_tree_shape(int B, int d, int k, int W, float lambda, float beta) {
+  if (B < 0 || d < 1 || d > kMaxD || k < 1 || k > kMaxK || W < 1 || W > kMaxW) return DART_ERR_INVALID_ARG;
+  const int N = num_nodes(d, k, W);
+  if (N < 1 || N > kMaxN) return DART_ERR_INVALID_ARG;
+  if (!finite(lambda) || !finite(beta)) return DART_ERR_INVALID_ARG;
+  return DART_OK;
+}
+
+int device_sms(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DART_ERR_CUDA;
+  if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DART_ERR_CUDA;
+  return DART_OK;
+}
+
+TreeArgs tree_args(int B, int d, int k, int W, float lambda, float beta,
+                   const dart_ngram_table_t* t, const int32_t* ctx,
+                   int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
+                   uint32_t* out_mask, float* out_scores) {
+  TreeArgs a;
+  a.B = B; a.d = d; a.k = k; a.W = W;
+  a.N = num_nodes(d, k, W);
+  a.MW = (a.N + 31) / 32;
+  a.n = t ? t->n : 0;
+  a.lam = double(lambda);
+  a.beta = double(beta);
+  a.ids = nullptr;
+  a.base = nullptr;
+  a.off = nullptr;
+  a.invT = 1.0;
+  a.ctx = ctx;
+  a.slots = t ? t->slots : nullptr;
+  a.capacity = t ? t->capacity : 0;
+  a.out_tokens = out_tokens;
+  a.out_parents = out_parents;
+  a.out_pos = out_pos;
+  a.out_mask = out_mask;
+  a.out_scores = out_scores;
+  a.ctrl = nullptr;
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dart_tree_num_nodes(int d, int k, int W) { return num_nodes(d, k, W); }
+
+int dart_tree_mask_words(int num_nodes_) { return num_nodes_ < 0 ? -1 : (num_nodes_ + 31) / 32; }
+
+size_t dart_tree_workspace_bytes(int B, int d, int V, int dtype, int k) {
+  if (B < 0 || d < 1 || V < 1 || !valid_dtype(dtype) || k < 1 || k > kMaxK) return 0;
+  WsLayout L;
+  if (!ws_layout((long long)B * d, V, elem_bytes(dtype), k, &L)) return 0;
+  return L.total;
+}
+
+int dart_tree_build(const void* logits, int B, int d, int V, int dtype,
+                    float T, int k, int W, float lambda, float beta,
+                    const dart_ngram_table_t* ngram_table, const int32_t* ctx_tokens,
+                    int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
+                    uint32_t* out_mask, float* out_scores,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_tree_shape(B, d, k, W, lambda, beta);
+  if (rc) return rc;
+  if (V < 2 || V > kMaxV || k > V || !valid_dtype(dtype)) return DART_ERR_INVALID_ARG;
+  if (!finite(T) || !(T > 0.f)) return DART_ERR_INVALID_ARG;
+  if ((rc = check_table(ngram_table, ctx_tokens, B))) return rc;
+  if (B == 0) return DART_OK;
+  if (!logits || !aligned(logits, 16)) return DART_ERR_INVALID_ARG;
+  if (!out_tokens || !out_parents || !out_pos || !out_mask) return DART_ERR_INVALID_ARG;
+  WsLayout L;
+  const long long R = (long long)B * d;
+  if (!ws_layout(R, V, elem_bytes(dtype), k, &L)) return DART_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return DART_ERR_WORKSPACE;
+  int sms = 0;
+  if ((rc = device_sms(&sms))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (cudaMemsetAsync(ws, 0, L.clear_bytes, s) != cudaSuccess) return DART_ERR_CUDA;
+  if (launch_rows(logits, R, V, dtype, T, k, ws, L, sms, nullptr, nullptr, nullptr, s) != cudaSuccess)
+    return DART_ERR_CUDA;
+  TreeArgs a = tree_args(B, d, k, W, lambda, beta, ngram_table, ctx_tokens, out_tokens, out_parents,
+                         out_pos, out_mask, out_scores);
+  a.ids = reinterpret_cast<const int32_t*>(ws + L.row_ids);
+  a.base = reinterpret_cast<const double*>(ws + L.row_base);
+  a.off = reinterpret_cast<const double*>(ws + L.row_off);
+  a.invT = 1.0 / double(T);
+  a.ctrl = reinterpret_cast<uint32_t*>(ws + L.ctrl);
+  if (launch_tree(a, s) != cudaSuccess) return DART_ERR_CUDA;
+  return DART_OK;
+}
+
+int dart_tree_from_topk(const int32_t* cand_ids, const double* cand_logp,
+                        int B, int d, int k, int W, float lambda, float beta,
+                        const dart_ngram_table_t* ngram_table, const int32_t* ctx_tokens,
+                        int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
+                        uint32_t* out_mask, float* out_scores, void* stream) {
+  int rc = check_tree_shape(B, d, k, W, lambda, beta);
+  if (rc) return rc;
+  if ((rc = check_table(ngram_table, ctx_tokens, B))) return rc;
+  if (B == 0) return DART_OK;
+  if (!cand_ids || !cand_logp || !out_tokens || !out_parents || !out_pos || !out_mask)
+    return DART_ERR_INVALID_ARG;
+  TreeArgs a = tree_args(B, d, k, W, lambda, beta, ngram_table, ctx_tokens, out_tokens, out_parents,
+                         out_pos, out_mask, out_scores);
+  a.ids = cand_ids;
+  a.base = cand_logp;
+  if (launch_tree(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return DART_ERR_CUDA;
+  return DART_OK;
+}
+
+int dart_row_topk(const void* logits, int rows, int V, int dtype, float T, int k,
+                  int32_t* out_ids, float* out_logp, float* out_lse,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+  if (rows < 0 || V < 2 || V > kMaxV || !valid_dtype(dtype) || k < 1 || k > kMaxK || k > V)
+    return DART_ERR_INVALID_ARG;
+  if (!finite(T) || !(T > 0.f)) return DART_ERR_INVALID_ARG;
+  if (rows == 0) return DART_OK;
+  if (!logits || !aligned(logits, 16)) return DART_ERR_INVALID_ARG;
+  WsLayout L;
+  if (!ws_layout(rows, V, elem_bytes(dtype), k, &L)) return DART_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return DART_ERR_WORKSPACE;
+  int sms = 0;
+  int rc = device_sms(&sms);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, L.clear_bytes, s) != cudaSuccess) return DART_ERR_CUDA;
+  if (launch_rows(logits, rows, V, dtype, T, k, workspace, L, sms, out_ids, out_logp, out_lse, s) !=
+      cudaSuccess)
+    return DART_ERR_CUDA;
+  return DART_OK;
+}
+
+int dart_mask_pack(const int32_t* parents, int B, int N, uint32_t* out_mask, uint32_t* device_err,
+                   void* stream) {
+  if (B < 0 || N < 0 || N > (1 << 20)) return DART_ERR_INVALID_ARG;
+  if (B == 0 || N == 0) return DART_OK;
+  if (!parents || !out_mask) return DART_ERR_INVALID_ARG;
+  if (launch_mask_pack(parents, B, N, out_mask, device_err, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return DART_ERR_CUDA;
+  return DART_OK;
+}
+
+uint64_t dart_ngram_capacity_for(uint64_t M) {
+  if (M > (1ull << 62)) return 0;
+  uint64_t c = 2;
+  while (c < 2 * M) c <<= 1;
+  return c;
+}
+
+int dart_ngram_table_pack_host(int n, const int32_t* keys, const float* vals, uint64_t M,
+                               uint64_t capacity, void* host_slots, uint64_t* out_distinct) {
+  if (n < 1 || n > 4 || !pow2(capacity) || !host_slots) return DART_ERR_INVALID_ARG;
+  if (M > 0 && (!keys || !vals)) return DART_ERR_INVALID_ARG;
+  uint32_t* s = static_cast<uint32_t*>(host_slots);
+  for (uint64_t i = 0; i < capacity; ++i) {
+    s[4 * i + 0] = kEmpty;
+    s[4 * i + 1] = kEmpty;
+    s[4 * i + 2] = kEmpty;
+    s[4 * i + 3] = 0u;
+  }
+  const uint64_t mask = capacity - 1;
+  uint64_t distinct = 0;
+  int rc = DART_OK;
+  for (uint64_t i = 0; i < M && rc == DART_OK; ++i) {
+    const int32_t* t = keys + i * n;
+    for (int f = 0; f < n; ++f)
+      if (t[f] < 0 || t[f] >= kMaxV) rc = DART_ERR_INVALID_ARG;
+    if (rc) break;
+    const Key96 key = pack_ngram(t, n);
+    uint64_t idx = hash_key(key) & mask;
+    for (uint64_t step = 0; step <= mask; ++step) {
+      uint32_t* slot = s + 4 * idx;
+      if (slot[0] == key.w0 && slot[1] == key.w1 && slot[2] == key.w2) break;  // first value kept
+      if (slot[0] == kEmpty && slot[1] == kEmpty && slot[2] == kEmpty) {
+        if (distinct >= capacity / 2) { rc = DART_ERR_TABLE_FULL; break; }
+        slot[0] = key.w0;
+        slot[1] = key.w1;
+        slot[2] = key.w2;
+        memcpy(&slot[3], &vals[i], 4);
+        ++distinct;
+        break;
+      }
+      idx = (idx + 1) & mask;
+    }
+  }
+  if (out_distinct) *out_distinct = distinct;
+  return rc;
+}
+
+int dart_ngram_lookup(const dart_ngram_table_t* table, const int32_t* keys, int64_t Q,
+                      float* vals, int32_t* found, void* stream) {
+  if (!table || table->n < 1 || table->n > 4 || !pow2(table->capacity) || !table->slots ||
+      !aligned(table->slots, 16) || Q < 0)
+    return DART_ERR_INVALID_ARG;
+  if (Q == 0) return DART_OK;
+  if (!keys || !vals || !found) return DART_ERR_INVALID_ARG;
+  if (launch_ngram_lookup(table->slots, table->capacity, table->n, keys, Q, vals, found,
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return DART_ERR_CUDA;
+  return DART_OK;
+}
+
+int dart_device_error(const void* workspace, uint32_t* out_flags, void* stream) {
+  if (!workspace || !out_flags) return DART_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DART_ERR_CUDA;
+  if (cudaMemcpy(out_flags, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DART_ERR_CUDA;
+  return DART_OK;
+}
+
+const char* dart_status_string(int status) {
+  switch (status) {
+    case DART_OK: return "ok";
+    case DART_ERR_INVALID_ARG: return "invalid argument";
+    case DART_ERR_UNSUPPORTED: return "unsupported";
+    case DART_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case DART_ERR_CUDA: return "CUDA runtime error";
+    case DART_ERR_INTERNAL: return "internal inconsistency reported by a kernel";
+    case DART_ERR_TIMEOUT: return "bounded device wait ran out";
+    case DART_ERR_TABLE_FULL: return "n-gram table full (more than capacity/2 keys)";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,234 @@
+// dart_common.cuh -- shared pieces of the CUDA path (sm_103a).
+//
+// Ordered keys, the n-gram key packing and hash, PTX wrappers for mbarrier /
+// bulk copies / ex2, warp bitonic networks, and the workspace layout that the
+// host code and the kernels agree on.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cstring>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+
+#include "darttree.h"
+
+namespace dart {
+
+constexpr int kMaxK = 32;          // candidates per position
+constexpr int kMaxW = 64;          // frontier width
+constexpr int kMaxD = 32;          // depths
+constexpr int kMaxN = 1024;        // nodes per tree
+constexpr int kMaxMW = kMaxN / 32; // mask words per row
+constexpr int kMaxV = (1 << 24) - 1;
+
+// ------------------------------------------------------------ ordered keys
+// A float maps to a uint32 whose unsigned order is the float order; -0.0 is
+// first turned into +0.0 so that equal values give equal keys.
+__host__ __device__ __forceinline__ uint32_t ord_f32(float z) {
+  uint32_t u;
+#ifdef __CUDA_ARCH__
+  u = __float_as_uint(z);
+#else
+  memcpy(&u, &z, 4);
+#endif
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__host__ __device__ __forceinline__ float unord_f32(uint32_t o) {
+  uint32_t u = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+#ifdef __CUDA_ARCH__
+  return __uint_as_float(u);
+#else
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+#endif
+}
+// Candidate key of a row element: larger key = larger logit, then lower id.
+// Key 0 never occurs for a real element (it would be a negative NaN).
+__device__ __forceinline__ uint64_t elem_key(float z, uint32_t id) {
+  return (uint64_t(ord_f32(z)) << 32) | uint64_t(~id);
+}
+__device__ __forceinline__ float key_value(uint64_t key) { return unord_f32(uint32_t(key >> 32)); }
+__device__ __forceinline__ uint32_t key_id(uint64_t key) { return ~uint32_t(key); }
+
+__device__ __forceinline__ uint64_t ord_f64(double s) {
+  uint64_t u = uint64_t(__double_as_longlong(s));
+  if (u == 0x8000000000000000ull) u = 0ull;
+  return (u & 0x8000000000000000ull) ? ~u : (u | 0x8000000000000000ull);
+}
+__device__ __forceinline__ double unord_f64(uint64_t o) {
+  uint64_t u = (o & 0x8000000000000000ull) ? (o & 0x7FFFFFFFFFFFFFFFull) : ~o;
+  return __longlong_as_double((long long)u);
+}
+
+// --------------------------------------------------------- n-gram hashing
+constexpr uint32_t kEmpty = 0xFFFFFFFFu;
+
+struct Key96 { uint32_t w0, w1, w2; };
+
+// tokens t[0..n) as 24-bit fields, t[0] in the lowest bits
+__host__ __device__ __forceinline__ Key96 pack_ngram(const int32_t* t, int n) {
+  uint64_t f[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) f[i] = i < n ? (uint64_t(uint32_t(t[i])) & 0xFFFFFFull) : 0ull;
+  uint64_t lo = f[0] | (f[1] << 24) | (f[2] << 48);
+  uint32_t hi = uint32_t(f[2] >> 16) | uint32_t(f[3] << 8);
+  return Key96{uint32_t(lo), uint32_t(lo >> 32), hi};
+}
+
+// splitmix64 output function (Steele, Lea & Flood, "Fast splittable
+// pseudorandom number generators", OOPSLA 2014) applied to the folded key.
+__host__ __device__ __forceinline__ uint64_t hash_key(Key96 k) {
+  uint64_t x = uint64_t(k.w0) | (uint64_t(k.w1) << 32);
+  x ^= uint64_t(k.w2) * 0x9E3779B97F4A7C15ull;
+  x ^= x >> 30;
+  x *= 0xBF58476D1CE4E5B9ull;
+  x ^= x >> 27;
+  x *= 0x94D049BB133111EBull;
+  x ^= x >> 31;
+  return x;
+}
+
+// ------------------------------------------------------- workspace layout
+// [ctrl 256 B][row_cnt R x u32][row_tau R x u32]   <- cleared by every call
+// [row_off R x f64][row_ids R*k x i32][row_base R*k x f64][partials]
+// row_off = the row's log-sum-exp of z / T; row_base = the candidates' logits.
+constexpr int kCtrlBytes = 256;
+constexpr size_t kMinSpanBytes = 16384;   // smallest contiguous span of logits per warp
+
+struct WsLayout {
+  size_t ctrl, row_cnt, row_tau, clear_bytes;
+  size_t row_off, row_ids, row_base, partials, total;
+  int pmax;          // partial slots per row
+  int pstride;       // bytes per partial
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline bool ws_layout(long long R, int V, int es, int k, WsLayout* L) {
+  if (R < 0 || V < 1 || es < 1 || k < 1 || k > kMaxK) return false;
+  const size_t row_bytes = size_t(V) * size_t(es);
+  L->pmax = int((row_bytes + kMinSpanBytes - 1) / kMinSpanBytes) + 1;
+  L->pstride = int(align_up(16 + 8 * size_t(k), 16));
+  size_t o = 0;
+  L->ctrl = o;      o += kCtrlBytes;
+  L->row_cnt = o;   o = align_up(o + 4 * size_t(R), 16);
+  L->row_tau = o;   o = align_up(o + 4 * size_t(R), 16);
+  L->clear_bytes = o;
+  L->row_off = o;   o = align_up(o + 8 * size_t(R), 256);
+  L->row_ids = o;   o = align_up(o + 4 * size_t(R) * k, 256);
+  L->row_base = o;  o = align_up(o + 8 * size_t(R) * k, 256);
+  L->partials = o;  o = align_up(o + size_t(R) * L->pmax * L->pstride, 256);
+  L->total = o;
+  return true;
+}
+
+// --------------------------------------------------------------- PTX glue
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+               :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Bounded wait: gives up after `limit` clock cycles and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, long long limit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > limit) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// One bulk copy global -> shared (both 16-byte aligned, size a multiple of 16),
+// completing `bytes` of transaction count on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;"
+      :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol) : "memory");
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void set_dev_error(uint32_t* ctrl, uint32_t bits) {
+  if (ctrl) atomicOr(ctrl, bits);
+}
+
+// ------------------------------------------------- warp bitonic networks
+// One 64-bit key per lane, 32 keys per warp, sorted descending (lane 0 best).
+__device__ __forceinline__ uint64_t warp_sort_desc_u64(uint64_t key) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, key, stride);
+      bool desc = (lane & size) == 0;
+      bool lower = (lane & stride) == 0;
+      bool keep_max = (lower == desc);
+      uint64_t mx = key > other ? key : other;
+      uint64_t mn = key > other ? other : key;
+      key = keep_max ? mx : mn;
+    }
+  }
+  return key;
+}
+// Finishes a bitonic sequence (one key per lane) into descending order.
+__device__ __forceinline__ uint64_t warp_bitonic_merge_desc_u64(uint64_t key) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int stride = 16; stride > 0; stride >>= 1) {
+    uint64_t other = __shfl_xor_sync(0xFFFFFFFFu, key, stride);
+    bool lower = (lane & stride) == 0;
+    uint64_t mx = key > other ? key : other;
+    uint64_t mn = key > other ? other : key;
+    key = lower ? mx : mn;
+  }
+  return key;
+}
+// list (sorted desc, one per lane) <- top 32 of list U chunk (any order).
+__device__ __forceinline__ uint64_t warp_merge_top32(uint64_t list, uint64_t chunk) {
+  const int lane = threadIdx.x & 31;
+  uint64_t s = warp_sort_desc_u64(chunk);
+  uint64_t rev = __shfl_sync(0xFFFFFFFFu, s, 31 - lane);
+  uint64_t c = list > rev ? list : rev;
+  return warp_bitonic_merge_desc_u64(c);
+}
+
+}  // namespace dart

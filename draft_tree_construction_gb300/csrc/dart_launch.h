@@ -1,0 +1,40 @@
+// dart_launch.h -- host-side launchers shared between the C-ABI layer and the
+// kernel translation units (internal; not part of the public header).
+#pragma once
+
+#include "dart_common.cuh"
+
+namespace dart {
+
+cudaError_t launch_rows(const void* logits, long long R, int V, int dtype, float T, int k,
+                        void* ws, const WsLayout& L, int sms,
+                        int32_t* out_ids, float* out_logp, float* out_lse, cudaStream_t stream);
+
+struct TreeArgs {
+  int B, d, k, W, N, MW, n;    // n = 0: no continuity term
+  double lam, beta;
+  const int32_t* ids;          // [B][d][k] candidate tokens
+  const double* base;          // [B][d][k] candidate base values (logits, or log-probabilities)
+  const double* off;           // [B][d] per-row offset subtracted from reported scores, or nullptr
+  double invT;                 // ranking key = (sum of base) * invT + lam * (sum of n-gram terms)
+  const int32_t* ctx;          // [B][n-1]
+  const void* slots;
+  unsigned long long capacity;
+  int32_t* out_tokens;
+  int32_t* out_parents;
+  int32_t* out_pos;
+  uint32_t* out_mask;
+  float* out_scores;
+  uint32_t* ctrl;              // device error word or nullptr
+};
+
+cudaError_t launch_tree(const TreeArgs& a, cudaStream_t stream);
+
+cudaError_t launch_mask_pack(const int32_t* parents, int B, int N, uint32_t* out_mask,
+                             uint32_t* err, cudaStream_t stream);
+
+cudaError_t launch_ngram_lookup(const void* slots, unsigned long long capacity, int n,
+                                const int32_t* keys, long long Q, float* vals, int32_t* found,
+                                cudaStream_t stream);
+
+}  // namespace dart

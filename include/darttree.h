@@ -1,0 +1,199 @@
+/* darttree.h -- continuity-aware draft-tree construction on one GPU (C ABI).
+ *
+ * What the library computes (page titles and sections):
+ *  - "DART: Diffusion-Inspired Speculative Decoding for Fast LLM Inference",
+ *    Figure 3 caption: a draft model emits d logit vectors per sequence in one
+ *    forward pass (vector 0 from the last prefix position, so vector j
+ *    predicts depth j+1); candidates at each position come from that
+ *    position's own logits; an N-gram model keeps expanded tokens continuous;
+ *    the pruned tree goes to tree-attention verification.
+ *  - "DARTree: Speculative Diffusion Decoding with Autoregressive Draft
+ *    Trees", Method / Tree Construction: every node of the previous depth is
+ *    expanded and scored together, then only the W best-scoring children of
+ *    the whole frontier survive (best-first pruning per depth, no heap).
+ *
+ * Made precise (the readings where the pages are silent):
+ *   p_j   = log_softmax(z_j / T)                           for j = 0..d-1
+ *   C_j   = the k tokens with the largest z_j, lower id first on equal values
+ *   child = parent score + p_j[c] + lambda * g,  g = ngram(last n-1 tokens of
+ *           (committed context ++ path), c), or beta when the model lacks it
+ *   keep  = the min(W, |frontier| * k) best children, ordered by score
+ *           (descending), then lower parent index, then lower token id
+ *   The root (last committed token) is not a node.  Nodes are numbered depth
+ *   by depth in that order; a depth-1 node has parent -1.
+ * All children of one depth share the sum of their rows' log-sum-exp terms,
+ * so the ranking uses key = (sum of the path's logits) * (1/T) + lambda *
+ * (sum of its g terms), both sums accumulated in double along the path; a
+ * node's reported score is key minus that shared sum.  Ties that the inputs
+ * hold exactly therefore stay exact ties and fall to the tie rule.
+ *
+ * Conventions for every entry point:
+ *  - All buffers belong to the caller.  The library allocates no memory and
+ *    keeps no state between calls; calls on different streams with different
+ *    workspaces may run concurrently.
+ *  - Pointers documented as "device" must point to memory of the current CUDA
+ *    device; "host" pointers to ordinary host memory.  `stream` is a
+ *    cudaStream_t (NULL = the legacy default stream).
+ *  - Argument errors are detected on the host and returned before anything is
+ *    launched.  Launch errors return DART_ERR_CUDA.  Kernels never trap: a
+ *    problem they detect (a wait that ran out, an inconsistency) sets a bit in
+ *    the workspace's device error word, read with dart_device_error().
+ *  - Every call that launches work is asynchronous with respect to the host.
+ */
+#ifndef DARTTREE_H
+#define DARTTREE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Logit element types. */
+enum { DART_F32 = 0, DART_F16 = 1, DART_BF16 = 2 };
+
+/* Status codes returned by every entry point (0 = success). */
+enum {
+  DART_OK = 0,
+  DART_ERR_INVALID_ARG = 1,   /* an argument is out of range, NULL or misaligned */
+  DART_ERR_UNSUPPORTED = 2,   /* valid request this build does not handle */
+  DART_ERR_WORKSPACE = 3,     /* workspace NULL, misaligned or too small */
+  DART_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+  DART_ERR_INTERNAL = 5,      /* a kernel reported an inconsistency */
+  DART_ERR_TIMEOUT = 6,       /* a bounded device wait ran out */
+  DART_ERR_TABLE_FULL = 7     /* n-gram packing: no free slot (load over 1/2) */
+};
+
+/* Bits of the device error word (see dart_device_error). */
+enum {
+  DART_DEVERR_WAIT_TIMEOUT = 1u << 0,  /* a bulk-copy wait ran out; the call's output is invalid */
+  DART_DEVERR_ROW_MAX = 1u << 1,       /* a row's maximum and its best candidate disagreed */
+  DART_DEVERR_SELECT = 1u << 2,        /* the tree selection produced an invalid candidate */
+  DART_DEVERR_PARENT = 1u << 3         /* dart_mask_pack: a parent index was not below its child */
+};
+
+/* An n-gram model in device memory: open addressing, linear probing.
+ * Each slot is 16 bytes {uint32 key[3]; float logprob}.  A key packs the n
+ * tokens (t_0 = oldest context token ... t_{n-1} = the predicted token) as
+ * 24-bit fields, t_f at bits [24f, 24f+24) of the 96-bit value key[0] |
+ * key[1] << 32 | key[2] << 64, unused fields zero.  An empty slot holds
+ * 0xFFFFFFFF in all three key words.  The home slot of a key is
+ * splitmix64-finalizer((key[0] | key[1] << 32) ^ (key[2] * 0x9E3779B97F4A7C15))
+ * & (capacity - 1).  Build the slots with dart_ngram_table_pack_host. */
+typedef struct {
+  int32_t n;            /* order, 2..4 */
+  int32_t reserved;     /* must be 0 */
+  uint64_t capacity;    /* number of slots, a power of two >= 2 */
+  const void* slots;    /* device, capacity * 16 bytes, 16-byte aligned */
+} dart_ngram_table_t;
+
+/* N = sum over j = 1..d of min(W, k^j): nodes per tree (the root excluded).
+ * Returns -1 when d, k or W is below 1 or N would exceed 2^30. */
+int dart_tree_num_nodes(int d, int k, int W);
+
+/* MW = ceil(N / 32): 32-bit words per ancestor-mask row; -1 if N < 0. */
+int dart_tree_mask_words(int num_nodes);
+
+/* Device workspace bytes that dart_tree_build / dart_row_topk need for these
+ * sizes (rows = B * d).  The result does not depend on the device.  0 when
+ * the arguments are invalid. */
+size_t dart_tree_workspace_bytes(int B, int d, int V, int dtype, int k);
+
+/* The whole hot path in one call: per-row temperature log-softmax and top-k
+ * (one streaming pass over the logits), then per-depth expansion, n-gram
+ * scoring and top-W pruning for every sequence, then token ids, parents,
+ * depths and ancestor masks.
+ *
+ *  logits      device [B][d][V], element type `dtype`, row-major, base
+ *              16-byte aligned.  Row j of sequence b predicts depth j+1.
+ *              Every row needs at least one finite value; NaN and +inf are
+ *              not supported (results unspecified).
+ *  B           sequences, >= 0 (0 = nothing to do, returns DART_OK)
+ *  d           depths, 1..32          V  vocabulary, 2..2^24-1
+ *  T           temperature, finite and > 0 (T = 0, greedy, is not a
+ *              log-softmax and is rejected)
+ *  k           candidates per position, 1..min(32, V)
+ *  W           frontier width, 1..64; N = dart_tree_num_nodes(d,k,W) <= 1024
+ *  lambda,beta finite; lambda scales the n-gram log-probability, beta is the
+ *              value used when the model lacks the n-gram (so a miss adds
+ *              lambda * beta)
+ *  ngram_table host pointer to a table descriptor, or NULL for no
+ *              continuity term (then child = parent + p_j[c])
+ *  ctx_tokens  device int32 [B][n-1]: the committed context, oldest first,
+ *              the root last; may be NULL only when ngram_table is NULL
+ *  out_tokens, out_parents, out_pos   device int32 [B][N]
+ *  out_mask    device uint32 [B][N][MW]; bit (i & 31) of word (i >> 5) in
+ *              row x is set iff node i is x or an ancestor of x
+ *  out_scores  device float [B][N] or NULL: each node's path score
+ *  workspace   device, >= dart_tree_workspace_bytes(B,d,V,dtype,k) bytes,
+ *              256-byte aligned; its contents need no preparation, the call
+ *              clears what it uses on `stream`
+ * Returns DART_OK or an error code; see the conventions above. */
+int dart_tree_build(const void* logits, int B, int d, int V, int dtype,
+                    float T, int k, int W, float lambda, float beta,
+                    const dart_ngram_table_t* ngram_table, const int32_t* ctx_tokens,
+                    int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
+                    uint32_t* out_mask, float* out_scores,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* The tree stage alone, from candidate lists a caller already has (for
+ * example a drafter that emits its own top-k):
+ *  cand_ids   device int32 [B][d][k], token ids in [0, 2^24-1), distinct
+ *             within a row (any order)
+ *  cand_logp  device double [B][d][k], the candidates' log-probabilities
+ * Children are ranked by (sum of logp along the path) + lambda * (sum of g),
+ * both sums in double, and that value is the reported score.  Other
+ * arguments and outputs as in dart_tree_build; no workspace. */
+int dart_tree_from_topk(const int32_t* cand_ids, const double* cand_logp,
+                        int B, int d, int k, int W, float lambda, float beta,
+                        const dart_ngram_table_t* ngram_table, const int32_t* ctx_tokens,
+                        int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
+                        uint32_t* out_mask, float* out_scores, void* stream);
+
+/* The row stage alone: for each of `rows` rows of logits[rows][V] (device,
+ * 16-byte aligned): the k best ids (value descending, lower id first),
+ * their log-probabilities log_softmax(z / T)[id] and the row's
+ * log-sum-exp of z / T.  out_ids device int32 [rows][k], out_logp device
+ * float [rows][k], out_lse device float [rows] (each may be NULL).
+ * workspace as for dart_tree_build with B = rows, d = 1. */
+int dart_row_topk(const void* logits, int rows, int V, int dtype, float T, int k,
+                  int32_t* out_ids, float* out_logp, float* out_lse,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Ancestor-or-self masks from a parent array (DART, Figure 3 caption: the
+ * tree-attention input).  parents device int32 [B][N], each entry -1 or a
+ * smaller node index; out_mask device uint32 [B][N][ceil(N/32)].  An entry
+ * that is not below its node stops that walk and sets DART_DEVERR_PARENT in
+ * *device_err (device uint32, may be NULL). */
+int dart_mask_pack(const int32_t* parents, int B, int N, uint32_t* out_mask,
+                   uint32_t* device_err, void* stream);
+
+/* Smallest power of two >= 2 * M (load factor at most 1/2); 0 on overflow. */
+uint64_t dart_ngram_capacity_for(uint64_t M);
+
+/* Build the slots of an n-gram table on the host.
+ *  keys host int32 [M][n] (t_0 oldest ... t_{n-1} predicted), each in
+ *  [0, 2^24-1); vals host float [M]; host_slots host, capacity * 16 bytes.
+ * A repeated key keeps its first value; *out_distinct (may be NULL)
+ * receives the number of distinct keys stored.  Returns DART_ERR_TABLE_FULL
+ * if more than capacity / 2 distinct keys arrive. */
+int dart_ngram_table_pack_host(int n, const int32_t* keys, const float* vals, uint64_t M,
+                               uint64_t capacity, void* host_slots, uint64_t* out_distinct);
+
+/* Batch lookup in a device table: keys device int32 [Q][n]; vals device
+ * float [Q] (0 when absent); found device int32 [Q] (1 / 0). */
+int dart_ngram_lookup(const dart_ngram_table_t* table, const int32_t* keys, int64_t Q,
+                      float* vals, int32_t* found, void* stream);
+
+/* Waits for `stream`, then copies the workspace's device error word to
+ * *out_flags (host).  Returns DART_OK, or DART_ERR_CUDA. */
+int dart_device_error(const void* workspace, uint32_t* out_flags, void* stream);
+
+/* Static text for a status code. */
+const char* dart_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DARTTREE_H */

@@ -1,0 +1,198 @@
+"""The C ABI without a GPU: symbols, argument checks, sizes, the host packer.
+
+Every check here returns before any CUDA call, so it runs on a machine with
+no GPU.  Fake device pointers are never dereferenced (the library rejects the
+call first).  The n-gram packer is checked against an independent reading of
+the slot format documented in include/darttree.h.
+"""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import draft_tree_construction_gb300 as D
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "darttree.h")
+
+OK, INVALID, WORKSPACE, FULL = 0, 1, 3, 7
+
+
+@pytest.fixture(scope="module")
+def L():
+    D.build()
+    return D.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dart_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 12
+    out = subprocess.run(["nm", "-D", "--defined-only", D._LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r" T (dart_\w+)", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert hasattr(L, n)
+
+
+def test_sizes(L):
+    assert L.dart_tree_num_nodes(4, 4, 4) == 16
+    assert L.dart_tree_num_nodes(8, 8, 8) == 64
+    assert L.dart_tree_num_nodes(8, 8, 10) == 8 + 10 * 7
+    assert L.dart_tree_num_nodes(8, 10, 16) == 10 + 16 * 7
+    assert L.dart_tree_num_nodes(16, 16, 32) == 16 + 32 * 15
+    assert L.dart_tree_num_nodes(0, 4, 4) == -1
+    assert L.dart_tree_mask_words(496) == 16
+    assert L.dart_tree_mask_words(1) == 1
+    assert L.dart_tree_mask_words(-1) == -1
+    assert L.dart_tree_workspace_bytes(64, 8, 151936, 2, 8) > 0
+    assert L.dart_tree_workspace_bytes(64, 8, 151936, 5, 8) == 0
+    assert L.dart_tree_workspace_bytes(64, 8, 151936, 2, 33) == 0
+    assert L.dart_ngram_capacity_for(4096) == 8192
+    assert L.dart_ngram_capacity_for(5000) == 16384
+    assert L.dart_ngram_capacity_for(0) == 2
+
+
+FAKE = 0x10000000          # 16- and 256-byte aligned, never dereferenced
+
+
+def _build(L, **over):
+    a = dict(logits=FAKE, B=2, d=4, V=1000, dtype=2, T=1.0, k=4, W=4, lam=0.5, beta=-10.0, table=None,
+             ctx=None, tok=FAKE, par=FAKE, pos=FAKE, mask=FAKE, scores=None, ws=None, wsb=0, stream=None)
+    a.update(over)
+    v = lambda key: C.c_void_p(a[key]) if a[key] else None
+    return L.dart_tree_build(v("logits"), a["B"], a["d"], a["V"], a["dtype"], a["T"], a["k"], a["W"],
+                             a["lam"], a["beta"], a["table"], v("ctx"), v("tok"), v("par"), v("pos"),
+                             v("mask"), v("scores"), v("ws"), a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(d=0), INVALID), (dict(d=33), INVALID), (dict(V=1), INVALID), (dict(V=1 << 24), INVALID),
+    (dict(k=0), INVALID), (dict(k=33), INVALID), (dict(k=5, V=4), INVALID), (dict(W=0), INVALID),
+    (dict(W=65), INVALID), (dict(d=32, k=32, W=64), INVALID),       # N > 1024
+    (dict(T=0.0), INVALID), (dict(T=-1.0), INVALID), (dict(T=float("nan")), INVALID),
+    (dict(T=float("inf")), INVALID), (dict(lam=float("nan")), INVALID),
+    (dict(beta=float("-inf")), INVALID), (dict(dtype=3), INVALID), (dict(B=-1), INVALID),
+    (dict(logits=0), INVALID), (dict(logits=FAKE + 8), INVALID), (dict(tok=0), INVALID),
+    (dict(mask=0), INVALID),
+    (dict(ws=None, wsb=0), WORKSPACE), (dict(ws=FAKE + 16, wsb=1 << 30), WORKSPACE),
+    (dict(ws=FAKE, wsb=100), WORKSPACE),
+    (dict(B=0), OK), (dict(B=0, logits=0, tok=0), OK),
+])
+def test_tree_build_argument_checks(L, over, code):
+    assert _build(L, **over) == code
+
+
+def _table(n=3, cap=1024, slots=FAKE, reserved=0):
+    return D._Table(n, reserved, cap, slots)
+
+
+@pytest.mark.parametrize("tab,ctx,code", [
+    (dict(n=1), FAKE, INVALID), (dict(n=5), FAKE, INVALID), (dict(cap=1000), FAKE, INVALID),
+    (dict(cap=1), FAKE, INVALID), (dict(slots=0), FAKE, INVALID), (dict(slots=FAKE + 4), FAKE, INVALID),
+    (dict(reserved=1), FAKE, INVALID), (dict(), 0, INVALID),
+])
+def test_table_argument_checks(L, tab, ctx, code):
+    t = _table(**tab)
+    assert _build(L, table=C.byref(t), ctx=ctx) == code
+
+
+def test_other_entry_points_check_arguments(L):
+    P = C.c_void_p
+    assert L.dart_row_topk(P(FAKE), 4, 1, 2, 1.0, 1, None, None, None, None, 0, None) == INVALID
+    assert L.dart_row_topk(P(FAKE), 4, 100, 2, 0.0, 4, None, None, None, None, 0, None) == INVALID
+    assert L.dart_row_topk(P(FAKE), 4, 100, 2, 1.0, 4, None, None, None, None, 0, None) == WORKSPACE
+    assert L.dart_row_topk(None, 0, 100, 2, 1.0, 4, None, None, None, None, 0, None) == OK
+    assert L.dart_tree_from_topk(None, None, 2, 4, 4, 4, 0.5, -1.0, None, None, None, None, None, None,
+                                 None, None) == INVALID
+    assert L.dart_tree_from_topk(None, None, 0, 4, 4, 4, 0.5, -1.0, None, None, None, None, None, None,
+                                 None, None) == OK
+    assert L.dart_mask_pack(None, 2, 10, None, None, None) == INVALID
+    assert L.dart_mask_pack(None, 0, 10, None, None, None) == OK
+    assert L.dart_ngram_lookup(None, None, 10, None, None, None) == INVALID
+    assert L.dart_device_error(None, None, None) == INVALID
+    assert L.dart_status_string(1).decode() == "invalid argument"
+
+
+# ------------------------------------------------------------ host packer
+
+def _splitmix_fold(w0, w1, w2):
+    """The home-slot hash as the header describes it (splitmix64 output function)."""
+    M64 = (1 << 64) - 1
+    x = (w0 | (w1 << 32)) ^ ((w2 * 0x9E3779B97F4A7C15) & M64)
+    x ^= x >> 30
+    x = (x * 0xBF58476D1CE4E5B9) & M64
+    x ^= x >> 27
+    x = (x * 0x94D049BB133111EB) & M64
+    x ^= x >> 31
+    return x
+
+
+def _key_words(tokens):
+    v = 0
+    for f, t in enumerate(tokens):
+        v |= int(t) << (24 * f)
+    return v & 0xFFFFFFFF, (v >> 32) & 0xFFFFFFFF, (v >> 64) & 0xFFFFFFFF
+
+
+def _find(slots, cap, tokens):
+    w = _key_words(tokens)
+    idx = _splitmix_fold(*w) & (cap - 1)
+    for _ in range(cap):
+        s = slots[idx]
+        if tuple(int(x) for x in s[:3]) == w:
+            return True, s[3:4].view(np.float32)[0]
+        if (s[:3] == 0xFFFFFFFF).all():
+            return False, None
+        idx = (idx + 1) & (cap - 1)
+    return False, None
+
+
+@pytest.mark.parametrize("n", [2, 3, 4])
+def test_packer_against_documented_format(L, n):
+    rng = np.random.default_rng(n)
+    M = 3000
+    keys = rng.integers(0, (1 << 24) - 1, size=(M, n)).astype(np.int32)
+    keys[100:200] = keys[:100]                                   # repeats: first value wins
+    vals = rng.uniform(-9, -1, size=M).astype(np.float32)
+    cap = L.dart_ngram_capacity_for(M)
+    slots = np.zeros((cap, 4), dtype=np.uint32)
+    distinct = C.c_uint64(0)
+    rc = L.dart_ngram_table_pack_host(n, keys.ctypes.data_as(C.c_void_p), vals.ctypes.data_as(C.c_void_p),
+                                      M, cap, slots.ctypes.data_as(C.c_void_p), C.byref(distinct))
+    assert rc == OK
+    first = {}
+    for key, v in zip(map(tuple, keys.tolist()), vals):
+        first.setdefault(key, v)
+    assert distinct.value == len(first)
+    for key, v in first.items():
+        ok, got = _find(slots, cap, key)
+        assert ok and got == v
+    for key in rng.integers(0, 1 << 20, size=(500, n)).tolist():
+        if tuple(key) not in first:
+            assert not _find(slots, cap, key)[0]
+
+
+def test_packer_refuses_overfull_and_bad_tokens(L):
+    keys = np.arange(10, dtype=np.int32).reshape(5, 2)
+    vals = np.zeros(5, dtype=np.float32)
+    slots = np.zeros((8, 4), dtype=np.uint32)
+    P = lambda a: a.ctypes.data_as(C.c_void_p)
+    assert L.dart_ngram_table_pack_host(2, P(keys), P(vals), 5, 8, P(slots), None) == FULL
+    assert L.dart_ngram_table_pack_host(2, P(keys), P(vals), 4, 8, P(slots), None) == OK
+    bad = keys.copy()
+    bad[2, 1] = (1 << 24) - 1
+    assert L.dart_ngram_table_pack_host(2, P(bad), P(vals), 4, 8, P(slots), None) == INVALID
+    bad[2, 1] = -5
+    assert L.dart_ngram_table_pack_host(2, P(bad), P(vals), 4, 8, P(slots), None) == INVALID
+    assert L.dart_ngram_table_pack_host(2, P(keys), P(vals), 4, 6, P(slots), None) == INVALID

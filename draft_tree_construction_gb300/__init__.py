@@ -26,7 +26,7 @@ from ._build import LIB as _LIB_PATH, build as _build_lib
 
 __all__ = [
     "DartError", "build", "lib", "NGramTable", "num_nodes", "mask_words", "workspace_bytes",
-    "tree_build", "tree_from_topk", "row_topk", "mask_pack", "device_error", "TreeBuilder",
+    "tree_build", "tree_build_noalloc", "tree_from_topk", "row_topk", "mask_pack", "device_error", "TreeBuilder",
     "DTYPE_CODES",
 ]
 
@@ -64,6 +64,9 @@ def _declare(L):
     L.dart_tree_build.argtypes = [P, i32, i32, i32, i32, f32, i32, i32, f32, f32, T, P,
                                   P, P, P, P, P, P, sz, P]
     L.dart_tree_build.restype = i32
+    L.dart_tree_build_noalloc.argtypes = [P, i32, i32, i32, i32, f32, i32, i32, f32, f32, T, P,
+                                          P, P, P, P, P, P]
+    L.dart_tree_build_noalloc.restype = i32
     L.dart_tree_from_topk.argtypes = [P, P, i32, i32, i32, i32, f32, f32, T, P, P, P, P, P, P, P]
     L.dart_tree_from_topk.restype = i32
     L.dart_row_topk.argtypes = [P, i32, i32, i32, f32, i32, P, P, P, P, sz, P]
@@ -227,6 +230,34 @@ def tree_build(logits, T: float, k: int, W: int, lam: float, beta: float,
                                _ptr(o.get("scores")), _ptr(ws), ws.numel(), _stream_ptr(stream))
     _check(rc, "dart_tree_build")
     o["workspace"] = ws
+    return o
+
+
+def tree_build_noalloc(logits, T: float, k: int, W: int, lam: float, beta: float,
+                       table: NGramTable | None = None, ctx=None, *, out: dict | None = None,
+                       stream=None, scores: bool = True) -> dict:
+    """tree_build for callers that cannot allocate device scratch: the library's
+    fixed 16 MiB buffer stands in for the workspace (see dart_tree_build_noalloc
+    in include/darttree.h for its limits and sharing rules)."""
+    torch = _torch()
+    codes = DTYPE_CODES()
+    _need_cuda(logits, "logits")
+    if logits.dtype not in codes or logits.dim() != 3:
+        raise DartError("logits must be [B, d, V] float32, float16 or bfloat16")
+    B, d, V = logits.shape
+    N = num_nodes(d, k, W)
+    if N < 0:
+        raise DartError("invalid d/k/W")
+    o = out if out is not None else _outputs(B, N, mask_words(N), logits.device, scores)
+    if table is not None:
+        _need_cuda(ctx, "ctx", torch.int32)
+    rc = lib().dart_tree_build_noalloc(_ptr(logits), B, d, V, codes[logits.dtype], float(T), k, W,
+                                       float(lam), float(beta),
+                                       C.byref(table.desc) if table is not None else None,
+                                       _ptr(ctx) if table is not None else None,
+                                       _ptr(o["tokens"]), _ptr(o["parents"]), _ptr(o["pos"]),
+                                       _ptr(o["mask"]), _ptr(o.get("scores")), _stream_ptr(stream))
+    _check(rc, "dart_tree_build_noalloc")
     return o
 
 

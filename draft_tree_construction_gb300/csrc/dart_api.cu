@@ -2,6 +2,7 @@
 // workspace layout, kernel launches, and the host-side n-gram table packer.
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "dart_launch.h"
 
@@ -80,6 +81,38 @@ TreeArgs tree_args(int B, int d, int k, int W, float lambda, float beta,
 
 }  // namespace
 
+// ---------------------------------------------------- fixed device scratch
+// Scratch for dart_tree_build_noalloc: the workspace that dart_tree_build
+// takes from its caller lives here instead.  Every device that loads the
+// library holds these bytes until the process exits.
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+namespace {
+
+constexpr int kMaxScratchDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxScratchDevices] = {};
+
+// Device address of g_static_scratch on the current device.  In host code the
+// array's name only stands in for the symbol, so the address is looked up once
+// per device (with that device current) and cached.
+int static_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DART_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxScratchDevices) return DART_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return DART_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return DART_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int dart_tree_num_nodes(int d, int k, int W) { return num_nodes(d, k, W); }
@@ -115,6 +148,44 @@ int dart_tree_build(const void* logits, int B, int d, int V, int dtype,
   if ((rc = device_sms(&sms))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (cudaMemsetAsync(ws, 0, L.clear_bytes, s) != cudaSuccess) return DART_ERR_CUDA;
+  if (launch_rows(logits, R, V, dtype, T, k, ws, L, sms, nullptr, nullptr, nullptr, s) != cudaSuccess)
+    return DART_ERR_CUDA;
+  TreeArgs a = tree_args(B, d, k, W, lambda, beta, ngram_table, ctx_tokens, out_tokens, out_parents,
+                         out_pos, out_mask, out_scores);
+  a.ids = reinterpret_cast<const int32_t*>(ws + L.row_ids);
+  a.base = reinterpret_cast<const double*>(ws + L.row_base);
+  a.off = reinterpret_cast<const double*>(ws + L.row_off);
+  a.invT = 1.0 / double(T);
+  a.ctrl = reinterpret_cast<uint32_t*>(ws + L.ctrl);
+  if (launch_tree(a, s) != cudaSuccess) return DART_ERR_CUDA;
+  return DART_OK;
+}
+
+int dart_tree_build_noalloc(const void* logits, int B, int d, int V, int dtype,
+                            float T, int k, int W, float lambda, float beta,
+                            const dart_ngram_table_t* ngram_table, const int32_t* ctx_tokens,
+                            int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
+                            uint32_t* out_mask, float* out_scores, void* stream) {
+  int rc = check_tree_shape(B, d, k, W, lambda, beta);
+  if (rc) return rc;
+  if (V < 2 || V > kMaxV || k > V || !valid_dtype(dtype)) return DART_ERR_INVALID_ARG;
+  if (!finite(T) || !(T > 0.f)) return DART_ERR_INVALID_ARG;
+  if ((rc = check_table(ngram_table, ctx_tokens, B))) return rc;
+  if (B == 0) return DART_OK;
+  if (!logits || !aligned(logits, 16)) return DART_ERR_INVALID_ARG;
+  if (!out_tokens || !out_parents || !out_pos || !out_mask) return DART_ERR_INVALID_ARG;
+  WsLayout L;
+  const long long R = (long long)B * d;
+  if (!ws_layout(R, V, elem_bytes(dtype), k, &L)) return DART_ERR_INVALID_ARG;
+  if (L.total > kStaticScratchBytes) return DART_ERR_WORKSPACE;   // sizes beyond the fixed scratch
+  void* scratch = nullptr;
+  if ((rc = static_scratch(&scratch))) return rc;
+  int sms = 0;
+  if ((rc = device_sms(&sms))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(scratch);
+  // the previous call's counters are still there: clear them on this stream
   if (cudaMemsetAsync(ws, 0, L.clear_bytes, s) != cudaSuccess) return DART_ERR_CUDA;
   if (launch_rows(logits, R, V, dtype, T, k, ws, L, sms, nullptr, nullptr, nullptr, s) != cudaSuccess)
     return DART_ERR_CUDA;

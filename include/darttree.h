@@ -137,6 +137,31 @@ int dart_tree_build(const void* logits, int B, int d, int V, int dtype,
                     uint32_t* out_mask, float* out_scores,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* dart_tree_build without a workspace argument, for callers that cannot
+ * allocate device memory: an engine whose own pool allocator has reserved
+ * the device's memory (a side cudaMalloc would fail or fragment it), a
+ * plugin or language binding with no handle on the application's
+ * allocator, or a latency-critical decode loop where cudaMalloc / cudaFree
+ * would synchronise the device.  The pages have no counterpart; this is a
+ * deployment variant of the same computation.
+ * Arguments and outputs are those of dart_tree_build; the workspace is a
+ * fixed 16 MiB buffer inside the library that every device loading the
+ * library holds until the process exits.  Sizes whose
+ * dart_tree_workspace_bytes(B, d, V, dtype, k) exceeds 16 MiB are rejected
+ * with DART_ERR_WORKSPACE before anything is launched.  The call allocates
+ * nothing; it clears the buffer's counters on `stream` itself.
+ * The first call on each device looks up the buffer's device address (with
+ * that device current) and caches it; make that first call before any
+ * stream capture.  All calls on a device share the one buffer, which keeps
+ * the last call's contents: calls that overlap on the GPU (other streams,
+ * other host threads) race and must be serialised by the caller.  Device
+ * error bits are kept in that buffer and are not reported. */
+int dart_tree_build_noalloc(const void* logits, int B, int d, int V, int dtype,
+                            float T, int k, int W, float lambda, float beta,
+                            const dart_ngram_table_t* ngram_table, const int32_t* ctx_tokens,
+                            int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
+                            uint32_t* out_mask, float* out_scores, void* stream);
+
 /* The tree stage alone, from candidate lists a caller already has (for
  * example a drafter that emits its own top-k):
  *  cand_ids   device int32 [B][d][k], token ids in [0, 2^24-1), distinct

@@ -1,0 +1,80 @@
+"""dart_tree_build_noalloc against dart_tree_build, through the C ABI.
+
+The no-allocation entry point serves callers that cannot hand the library a
+workspace of their own: engines whose pool allocator owns the device memory,
+plugins without access to the application's allocator, or decode loops that
+must not pay for cudaMalloc's device synchronisation.  It runs the same
+kernels on a fixed buffer inside the library, so its outputs must equal those
+of dart_tree_build.  Several calls in a row check that each call clears what
+the previous one left in the shared buffer.
+"""
+import ctypes as C
+
+import numpy as np
+import pytest
+
+import synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+WORKSPACE_TOO_SMALL = 3
+
+
+@pytest.fixture(scope="module")
+def D():
+    import draft_tree_construction_gb300 as D
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    D.build()
+    return D
+
+
+def _noalloc(D, case, z, tab, ctx):
+    """Call dart_tree_build_noalloc directly; outputs are caller-owned tensors."""
+    N = D.num_nodes(case.d, case.k, case.W)
+    MW = D.mask_words(N)
+    out = {key: torch.empty((case.B, N), dtype=torch.int32, device="cuda")
+           for key in ("tokens", "parents", "pos")}
+    out["mask"] = torch.empty((case.B, N, MW), dtype=torch.int32, device="cuda")
+    out["scores"] = torch.empty((case.B, N), dtype=torch.float32, device="cuda")
+    p = lambda t: C.c_void_p(t.data_ptr()) if t is not None else None
+    rc = D.lib().dart_tree_build_noalloc(
+        p(z), case.B, case.d, case.V, D.DTYPE_CODES()[z.dtype], case.T, case.k, case.W,
+        case.lam, case.beta, C.byref(tab.desc) if tab is not None else None,
+        p(ctx) if tab is not None else None, p(out["tokens"]), p(out["parents"]), p(out["pos"]),
+        p(out["mask"]), p(out["scores"]), C.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0, D.lib().dart_status_string(rc).decode()
+    torch.cuda.synchronize()
+    return out
+
+
+def test_noalloc_matches_tree_build_on_consecutive_calls(D):
+    cases = [synth.make_config(2, seed=1, B=6, M=1 << 15),
+             synth.make_config(0, seed=0),
+             synth.make_config(4, seed=2, B=2, V=20011, M=1 << 15, dtype="f16")]
+    for case in cases + cases[:1]:          # the last call repeats the first on a dirty buffer
+        z = parity.to_device(case)
+        tab, ctx = parity.gpu_table(case)
+        ref = D.tree_build(z, case.T, case.k, case.W, case.lam, case.beta, table=tab, ctx=ctx)
+        assert D.device_error(ref["workspace"]) == 0
+        got = _noalloc(D, case, z, tab, ctx)
+        for key in ("tokens", "parents", "pos", "mask"):
+            assert torch.equal(got[key], ref[key]), key
+        err = (got["scores"].double() - ref["scores"].double()).abs().max().item()
+        assert err <= parity.SCORE_TOL
+
+
+def test_noalloc_rejects_sizes_beyond_its_buffer(D):
+    # 4096 rows of a 1M-token vocabulary need far more than the 16 MiB buffer;
+    # the call must refuse before touching the (never allocated) logits
+    B, d, V = 512, 8, 1 << 20
+    assert D.workspace_bytes(B, d, V, 2, 16) > (16 << 20)
+    N = D.num_nodes(d, 16, 32)
+    fake = C.c_void_p(0x10000000)
+    rc = D.lib().dart_tree_build_noalloc(fake, B, d, V, 2, 1.0, 16, 32, 0.25, -14.0, None, None,
+                                         fake, fake, fake, fake, None, None)
+    assert rc == WORKSPACE_TOO_SMALL
+    assert N > 0

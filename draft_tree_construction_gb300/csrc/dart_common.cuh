@@ -93,14 +93,15 @@ __host__ __device__ __forceinline__ uint64_t hash_key(Key96 k) {
 }
 
 // ------------------------------------------------------- workspace layout
-// [ctrl 256 B][row_cnt R x u32][row_tau R x u32]   <- cleared by every call
+// [ctrl 256 B][row_cnt R x u32]   <- cleared by every call
 // [row_off R x f64][row_ids R*k x i32][row_base R*k x f64][partials]
-// row_off = the row's log-sum-exp of z / T; row_base = the candidates' logits.
+// row_off = the row's log-sum-exp of z / T; row_base = the candidates' logits;
+// a partial is one CTA's (max, scaled sum, k best keys) of a row.
 constexpr int kCtrlBytes = 256;
-constexpr size_t kMinSpanBytes = 16384;   // smallest contiguous span of logits per warp
+constexpr size_t kMinSpanBytes = 65536;   // smallest contiguous span of logits per CTA
 
 struct WsLayout {
-  size_t ctrl, row_cnt, row_tau, clear_bytes;
+  size_t ctrl, row_cnt, clear_bytes;
   size_t row_off, row_ids, row_base, partials, total;
   int pmax;          // partial slots per row
   int pstride;       // bytes per partial
@@ -111,12 +112,12 @@ __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a -
 inline bool ws_layout(long long R, int V, int es, int k, WsLayout* L) {
   if (R < 0 || V < 1 || es < 1 || k < 1 || k > kMaxK) return false;
   const size_t row_bytes = size_t(V) * size_t(es);
+  // every CTA whose span meets the row leaves one partial
   L->pmax = int((row_bytes + kMinSpanBytes - 1) / kMinSpanBytes) + 1;
   L->pstride = int(align_up(16 + 8 * size_t(k), 16));
   size_t o = 0;
   L->ctrl = o;      o += kCtrlBytes;
   L->row_cnt = o;   o = align_up(o + 4 * size_t(R), 16);
-  L->row_tau = o;   o = align_up(o + 4 * size_t(R), 16);
   L->clear_bytes = o;
   L->row_off = o;   o = align_up(o + 8 * size_t(R), 256);
   L->row_ids = o;   o = align_up(o + 4 * size_t(R) * k, 256);
@@ -147,10 +148,22 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile("{\n\t.reg .pred p;\n\t"
                "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Non-blocking probe of a phase (try_wait may suspend the thread for a while).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
                "selp.u32 %0, 1, 0, p;\n\t}"
                : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
   return ok != 0;

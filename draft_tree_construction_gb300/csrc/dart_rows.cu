@@ -5,39 +5,57 @@
 // the candidates of one depth.  Here every row z[b][j][:] is read exactly once
 // from HBM and reduced to (max, sum of exp((z - max) / T), k best (z, id)).
 //
-// Work split.  The logits are one flat byte stream.  Each warp owns one
-// contiguous, 16-byte-aligned span of it (equal spans, so every warp moves the
-// same number of bytes) and streams that span through its own ring of shared
-// memory stages filled by cp.async.bulk (one elected lane issues, an mbarrier
-// per stage counts the bytes).  A span cuts rows into segments; every segment
-// yields a partial (running max, scaled sum, top-k keys).  The last warp to
-// finish a row (an arrival counter, no waiting) merges that row's partials and
-// writes the row's results.  No warp ever waits on another warp.
+// Work split.  The logits are one flat byte stream cut into equal,
+// contiguous, 16-byte-aligned spans, one per CTA (one CTA per SM).  Inside a
+// CTA one producer thread streams its span through a ring of 24 KiB
+// shared-memory stages with cp.async.bulk (an mbarrier per stage counts the
+// bytes in, another counts the 12 consumer warps out); each consumer warp
+// reduces its own 2 KiB slice of every stage.  Stages never straddle a row, so
+// all consumer warps of a CTA work on the same row at the same time.
 //
-// Per stage a lane holds four 16-byte vectors.  One running-max update covers
+// Per slice a lane holds four 16-byte vectors.  One running-max update covers
 // all of them (maxima taken on packed bf16x2 / f16x2 words), the exponentials
-// use packed f32x2 subtract / multiply and accumulate, and one warp vote
-// decides whether any element can enter the top-k.
+// use packed f32x2 subtract / multiply / add, and one warp vote decides
+// whether any element can enter the top-k.
 //
 // Top-k.  Candidates are 64-bit keys (ordered value, then inverted id), so a
 // larger key is a better candidate and equal values fall back to the lower id.
-// A warp keeps its best 32 keys spread over its lanes.  An element can only
-// matter if it is >= tau, a lower bound of the row's k-th value: the k-th best
-// key value the warp has merged, the k-th largest of the 32 lane maxima of the
-// segment's first stage, or any value another warp of the same row published.
-// Qualifying elements are appended to a per-warp buffer (slots from a shared
-// counter); every 32 buffered keys are bitonic-sorted and merged into the list.
+// An element can only matter if it is >= tau, a lower bound of the row's k-th
+// value.  Consumer warps keep no lists: they append the rare qualifying
+// elements to a per-row key ring in shared memory.  A merger warp drains the
+// ring into the CTA's best-32 list of the row and publishes the list's k-th
+// value as the row's tau, so every consumer filters against the k-th best
+// element the whole CTA has seen so far.  The first slice of a row is filtered
+// against the k-th largest of the warp's 32 lane maxima (k distinct elements
+// are at least that large).
+//
+// Row end.  Each consumer warp leaves its (max, scaled sum) in a shared slot
+// and moves on; the merger combines them with the list.  A row inside one
+// span is finished there; a row cut by span borders leaves one partial per
+// CTA, and the last CTA to arrive (an arrival counter, no waiting) merges them
+// and writes the row's results.  All global round trips of a row's end sit on
+// the merger warp, off the stream.
+//
+// Every wait is bounded: on a timeout the kernel raises a flag in shared
+// memory that ends all other waits of the CTA, records the error bit and
+// returns.
 #include "dart_common.cuh"
 
 #include <cfloat>
 
 namespace dart {
 
-constexpr int kRowWarps = 16;                   // 16 independent streams per CTA, one CTA per SM
-constexpr int kStageBytes = 2048;               // one stage = 4 vectors of 16 B per lane
-constexpr int kStages = 4;                      // 8 KB in flight per warp, 128 KB per SM
-constexpr int kVecPerLane = kStageBytes / 16 / 32;
-constexpr int kBufCap = 32 + 256 + 32;
+constexpr int kConsumers = 12;                  // reducing warps per CTA (plus a producer and a merger warp)
+constexpr int kSlice = 2048;                    // bytes of a stage per consumer warp: 4 vectors per lane
+constexpr int kStageBytes = kSlice * kConsumers;
+constexpr int kStages = 5;                      // 120 KiB in flight per SM
+constexpr int kVecPerLane = kSlice / 16 / 32;
+constexpr int kRowSlots = 4;                    // rows in flight between the consumers and the merger
+constexpr int kRingKeys = 1024;                 // key ring per row slot (power of two)
+constexpr int kMergerWarp = kConsumers + 1;
+constexpr int kRowThreads = (kConsumers + 2) * 32;
+static_assert(kVecPerLane == 4, "consume_slice reduces exactly four vectors per lane");
+static_assert((kRingKeys & (kRingKeys - 1)) == 0, "ring index masking");
 
 struct RowsParams {
   const uint8_t* logits;
@@ -45,13 +63,13 @@ struct RowsParams {
   int V, k, es;
   float c;                    // log2(e) / T
   double T;
+  double invT;                // 1 / T
   unsigned long long total;   // R * V * es bytes
-  unsigned long long span;    // bytes per warp, multiple of 16
-  int nwarps, grid;
+  unsigned long long span;    // bytes per CTA, multiple of 16
+  int grid;
   int pmax, pstride;
   uint32_t* ctrl;
   uint32_t* row_cnt;
-  uint32_t* row_tau;
   uint8_t* partials;
   double* row_off;
   int32_t* row_ids;
@@ -62,13 +80,23 @@ struct RowsParams {
   long long wait_limit;
 };
 
-struct __align__(128) WarpSmem {
+struct __align__(128) RowSmem {
   uint8_t ring[kStages][kStageBytes];
-  uint64_t buf[kBufCap];
-  uint64_t bar[kStages];
-  int nbuf;
+  uint64_t keys[kRowSlots][kRingKeys];   // candidate keys of a row; 0 = slot not written yet
+  float2 part[kRowSlots][kConsumers];    // per consumer warp: (max, sum of 2^((z - max) c))
+  uint64_t full[kStages];                // bytes of a stage have landed
+  uint64_t empty[kStages];               // every consumer warp is done with a stage
+  uint64_t row_full[kRowSlots];          // every consumer lane is done with a row
+  uint64_t row_free[kRowSlots];          // the merger is done with a row slot
+  uint32_t tail[kRowSlots];              // keys reserved in a row's ring
+  uint32_t head[kRowSlots];              // keys the merger has taken
+  uint32_t tau[kRowSlots];               // ordered form of the row's best published threshold
+  uint32_t seed[2][kConsumers][32];      // lane maxima of a row's first stage (alternating rows)
+  uint64_t seed_bar[2];                  // every consumer lane has written its lane maximum
+  uint32_t abort;                        // a wait timed out: every wait gives up
 };
 
+// ------------------------------------------------------------- element types
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -86,6 +114,7 @@ __device__ __forceinline__ uint32_t word(const uint4& r, int i) {
 template <int DT> struct Elem;
 template <> struct Elem<DART_F32> {
   static constexpr int kPerVec = 4;
+  static constexpr int kShift = 2;      // log2 of the element size
   __device__ static uint4 neg_inf() { return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u); }
   __device__ static float2 pair(const uint4& r, int p) {
     return make_float2(__uint_as_float(word(r, 2 * p)), __uint_as_float(word(r, 2 * p + 1)));
@@ -94,18 +123,26 @@ template <> struct Elem<DART_F32> {
     return fmaxf(fmaxf(__uint_as_float(r.x), __uint_as_float(r.y)),
                  fmaxf(__uint_as_float(r.z), __uint_as_float(r.w)));
   }
+  __device__ static float vmax4(const uint4* r) {
+    return fmaxf(fmaxf(vmax(r[0]), vmax(r[1])), fmaxf(vmax(r[2]), vmax(r[3])));
+  }
   __device__ static float scalar(const uint8_t* p) { return __ldg(reinterpret_cast<const float*>(p)); }
 };
 template <> struct Elem<DART_BF16> {
   static constexpr int kPerVec = 8;
+  static constexpr int kShift = 1;
   __device__ static uint4 neg_inf() { return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u); }
   __device__ static float2 pair(const uint4& r, int p) {
     const uint32_t w = word(r, p);
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
   }
-  __device__ static float vmax(const uint4& r) {
-    const uint32_t m = bmax2(bmax2(r.x, r.y), bmax2(r.z, r.w));
+  __device__ static float unpack_max(uint32_t m) {
     return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+  }
+  __device__ static uint32_t pmax(const uint4& r) { return bmax2(bmax2(r.x, r.y), bmax2(r.z, r.w)); }
+  __device__ static float vmax(const uint4& r) { return unpack_max(pmax(r)); }
+  __device__ static float vmax4(const uint4* r) {
+    return unpack_max(bmax2(bmax2(pmax(r[0]), pmax(r[1])), bmax2(pmax(r[2]), pmax(r[3]))));
   }
   __device__ static float scalar(const uint8_t* p) {
     const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(p));
@@ -114,15 +151,20 @@ template <> struct Elem<DART_BF16> {
 };
 template <> struct Elem<DART_F16> {
   static constexpr int kPerVec = 8;
+  static constexpr int kShift = 1;
   __device__ static uint4 neg_inf() { return make_uint4(0xFC00FC00u, 0xFC00FC00u, 0xFC00FC00u, 0xFC00FC00u); }
   __device__ static float2 pair(const uint4& r, int p) {
     const uint32_t w = word(r, p);
     return __half22float2(*reinterpret_cast<const __half2*>(&w));
   }
-  __device__ static float vmax(const uint4& r) {
-    const uint32_t m = hmax2(hmax2(r.x, r.y), hmax2(r.z, r.w));
+  __device__ static float unpack_max(uint32_t m) {
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&m));
     return fmaxf(f.x, f.y);
+  }
+  __device__ static uint32_t pmax(const uint4& r) { return hmax2(hmax2(r.x, r.y), hmax2(r.z, r.w)); }
+  __device__ static float vmax(const uint4& r) { return unpack_max(pmax(r)); }
+  __device__ static float vmax4(const uint4* r) {
+    return unpack_max(hmax2(hmax2(pmax(r[0]), pmax(r[1])), hmax2(pmax(r[2]), pmax(r[3]))));
   }
   __device__ static float scalar(const uint8_t* p) {
     const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(p));
@@ -130,145 +172,245 @@ template <> struct Elem<DART_F16> {
   }
 };
 
-// Per-warp running state for one row segment.
-struct SegState {
-  float m, s;        // per lane: running max of z and sum of 2^((z - m) c)
-  uint64_t list;     // per lane: entry `lane` of the warp's best 32 keys (desc)
-  uint32_t tau_ord;  // ordered form of the filter threshold (0 = none yet)
-  float tau;         // filter threshold value (-inf = none yet)
-  int nbuf;          // keys waiting in the buffer (warp-uniform copy of WarpSmem::nbuf)
+// ------------------------------------------------------------ bounded waits
+// Rarely taken paths are kept out of line (__noinline__) so that the
+// per-slice loop stays small in the instruction cache.
+__device__ __forceinline__ bool aborted(const RowSmem& S) {
+  return *reinterpret_cast<const volatile uint32_t*>(&S.abort) != 0u;
+}
+__device__ __forceinline__ void raise_abort(RowSmem& S, uint32_t* ctrl) {
+  *reinterpret_cast<volatile uint32_t*>(&S.abort) = 1u;
+  set_dev_error(ctrl, DART_DEVERR_WAIT_TIMEOUT);
+}
+__device__ __noinline__ bool wait_phase_spin(RowSmem& S, uint64_t* bar, uint32_t parity, long long limit,
+                                             uint32_t* ctrl) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (aborted(S)) return false;
+    if (clock64() - t0 > limit) {
+      raise_abort(S, ctrl);
+      return false;
+    }
+  }
+  return true;
+}
+// Waits for the phase of `bar` with the given parity; false on a timeout or
+// when another wait of the CTA has timed out.
+__device__ __forceinline__ bool wait_phase(RowSmem& S, uint64_t* bar, uint32_t parity, long long limit,
+                                           uint32_t* ctrl) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_phase_spin(S, bar, parity, limit, ctrl);
+}
+
+// ----------------------------------------------------------------- consumers
+// Where a consumer warp appends candidate keys of the current row.
+struct KeyRing {
+  uint32_t* tail;                  // reservation counter
+  const volatile uint32_t* head;   // keys the merger has taken
+  volatile uint64_t* keys;         // kRingKeys slots, 0 = not written yet
+  RowSmem* S;
+  uint32_t* ctrl;
+  long long limit;
 };
 
-__device__ __forceinline__ void update_tau(SegState& st, int k, uint32_t* tau_slot) {
-  const uint64_t kth = __shfl_sync(0xFFFFFFFFu, st.list, k - 1);
-  const uint32_t o = uint32_t(kth >> 32);
-  if (kth != 0 && o > st.tau_ord) {
-    uint32_t old = 0;
-    if ((threadIdx.x & 31) == 0) old = atomicMax(tau_slot, o);
-    old = __shfl_sync(0xFFFFFFFFu, old, 0);
-    st.tau_ord = o > old ? o : old;
-    st.tau = unord_f32(st.tau_ord);
-  }
-}
-
-// After lanes appended keys through the shared counter: pick up the count and
-// merge whole chunks of 32 into the list.
-__device__ __forceinline__ void after_push(SegState& st, WarpSmem& S, int k, uint32_t* tau_slot) {
-  const int lane = threadIdx.x & 31;
-  __syncwarp();
-  st.nbuf = *reinterpret_cast<volatile int*>(&S.nbuf);
-  if (st.nbuf >= 32) {
-    while (st.nbuf >= 32) {
-      const uint64_t chunk = S.buf[st.nbuf - 32 + lane];
-      st.list = warp_merge_top32(st.list, chunk);
-      st.nbuf -= 32;
+__device__ __noinline__ void ring_wait(const KeyRing kr, uint32_t pos) {
+  const long long t0 = clock64();
+  while (pos - *kr.head >= uint32_t(kRingKeys)) {
+    if (aborted(*kr.S)) return;
+    if (clock64() - t0 > kr.limit) {
+      raise_abort(*kr.S, kr.ctrl);
+      return;
     }
-    __syncwarp();
-    if (lane == 0) S.nbuf = st.nbuf;
-    __syncwarp();
-    update_tau(st, k, tau_slot);
   }
 }
-
-// k-th largest of the lanes' maxima: k distinct elements of this row are at
-// least that large, so it is a lower bound of the row's k-th value.
-__device__ __forceinline__ void seed_tau(SegState& st, float vm, bool valid, int k, uint32_t* tau_slot) {
-  uint64_t key = valid ? (uint64_t(ord_f32(vm)) << 32) : 0ull;
-  key = warp_sort_desc_u64(key);
-  const uint64_t kth = __shfl_sync(0xFFFFFFFFu, key, k - 1);
-  const uint32_t o = uint32_t(kth >> 32);
-  if (kth != 0 && o > st.tau_ord) {
-    st.tau_ord = o;
-    st.tau = unord_f32(o);
-    if ((threadIdx.x & 31) == 0) atomicMax(tau_slot, o);
-  }
+// Appends one key at reserved position `pos`, waiting while the ring is full.
+__device__ __forceinline__ void ring_put(const KeyRing& kr, uint32_t pos, uint64_t key) {
+  if (pos - *kr.head >= uint32_t(kRingKeys)) ring_wait(kr, pos);
+  kr.keys[pos & uint32_t(kRingKeys - 1)] = key;
 }
 
-// One unaligned element per lane (head or tail of a segment).
-__device__ __forceinline__ void consume_scalar(SegState& st, WarpSmem& S, float z, bool valid,
-                                               uint32_t id, float c, int k, uint32_t* tau_slot) {
-  if (valid) {
-    if (z > st.m) {
-      st.s *= ex2_approx((st.m - z) * c);
-      st.m = z;
-    }
-    st.s += ex2_approx((z - st.m) * c);
-  }
-  const bool h = valid && z >= st.tau;
-  if (__any_sync(0xFFFFFFFFu, h)) {
-    if (h) {
-      const int pos = atomicAdd(&S.nbuf, 1);
-      S.buf[pos] = elem_key(z, id);
-    }
-    after_push(st, S, k, tau_slot);
-  }
-}
-
-// One stage from shared memory: vector v = u*32 + lane (u < kVecPerLane) holds
-// elements id_base + v*EPV ...; vectors at or past nvec are absent.
+// Appends the elements >= tau of this lane's vectors of a slice (vectors
+// lane, lane + 32, ... below nvec).
 template <int DT>
-__device__ __forceinline__ void consume_stage(SegState& st, WarpSmem& S, const uint4* ring, int nvec,
-                                              uint32_t id_base, float c, int k, uint32_t* tau_slot,
-                                              bool seed) {
+__device__ __noinline__ void push_hits(const uint4* src, int nvec, uint32_t id_base, float tau, const KeyRing kr) {
+  using E = Elem<DT>;
+  constexpr int EPV = E::kPerVec;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int u = 0; u < kVecPerLane; ++u) {
+    const int v = u * 32 + lane;
+    if (v < nvec) {
+      const uint4 r = src[v];
+      if (E::vmax(r) >= tau) {
+        uint32_t em = 0;
+#pragma unroll
+        for (int p = 0; p < EPV / 2; ++p) {
+          const float2 z = E::pair(r, p);
+          em |= (z.x >= tau ? 1u : 0u) << (2 * p);
+          em |= (z.y >= tau ? 1u : 0u) << (2 * p + 1);
+        }
+        uint32_t pos = atomicAdd(kr.tail, uint32_t(__popc(em)));
+        const uint32_t id0 = id_base + uint32_t(v * EPV);
+#pragma unroll
+        for (int p = 0; p < EPV / 2; ++p) {
+          const float2 z = E::pair(r, p);
+          if ((em >> (2 * p)) & 1u) ring_put(kr, pos++, elem_key(z.x, id0 + 2 * p));
+          if ((em >> (2 * p + 1)) & 1u) ring_put(kr, pos++, elem_key(z.y, id0 + 2 * p + 1));
+        }
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// Bitonic sort of one 32-bit value per lane, descending (lane 0 largest).
+__device__ __forceinline__ uint32_t warp_sort_desc_u32(uint32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, v, stride);
+      const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+      v = keep_max ? max(v, o) : min(v, o);
+    }
+  }
+  return v;
+}
+
+// CTA-wide seed of a row's threshold from its first stage.  Every consumer
+// lane posts the maximum of its elements of the stage; lane j then takes the
+// maximum of column j (the twelve warps' lane j), and the k-th largest of
+// those 32 column maxima is a lower bound of the row's k-th value: the
+// columns cover disjoint elements, so k distinct elements are at least that
+// large.  Returns the bound in ordered form (0 = none or a wait gave up).
+template <int DT>
+__device__ __noinline__ uint32_t seed_stage(const uint4* src, int nvec, RowSmem* Sp, int nseed, int w, int k,
+                                            long long limit, uint32_t* ctrl) {
+  using E = Elem<DT>;
+  RowSmem& S = *Sp;
+  const int lane = threadIdx.x & 31;
+  float vm = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < kVecPerLane; ++u) {
+    const int v = u * 32 + lane;
+    if (v < nvec) vm = fmaxf(vm, E::vmax(src[v]));
+  }
+  const int sb = nseed & 1;
+  S.seed[sb][w][lane] = lane < nvec ? ord_f32(vm) : 0u;
+  mbar_arrive(&S.seed_bar[sb]);
+  if (!__all_sync(0xFFFFFFFFu, wait_phase(S, &S.seed_bar[sb], uint32_t(nseed >> 1) & 1u, limit, ctrl))) return 0u;
+  uint32_t col = 0;
+#pragma unroll
+  for (int i = 0; i < kConsumers; ++i) col = max(col, S.seed[sb][i][lane]);
+  const uint32_t v = warp_sort_desc_u32(col);
+  return __shfl_sync(0xFFFFFFFFu, v, k - 1);
+}
+
+// Per-warp state for one row segment.
+struct RowCtx {
+  float m, s;            // per lane: running max of z and sum of 2^((z - m) c)
+  uint32_t tau_ord;      // ordered form of the filter threshold (0 = none yet)
+  float tau;             // filter threshold value (-inf = none yet)
+  uint32_t* tau_slot;    // the row's shared threshold
+};
+
+__device__ __forceinline__ void raise_tau(RowCtx& rc, uint32_t o) {
+  if (o > rc.tau_ord) {
+    rc.tau_ord = o;
+    rc.tau = unord_f32(o);
+  }
+}
+// Adopt a larger threshold published for the row.
+__device__ __forceinline__ void refresh_tau(RowCtx& rc) {
+  raise_tau(rc, *reinterpret_cast<volatile uint32_t*>(rc.tau_slot));
+}
+
+// The hot path: one full 2 KiB slice (four vectors per lane).  Updates the
+// lane's (max, sum) and returns whether any element can pass tau.
+template <int DT>
+__device__ __forceinline__ bool reduce_full(RowCtx& rc, const uint4* src, float c) {
   using E = Elem<DT>;
   constexpr int EPV = E::kPerVec;
   constexpr int U = kVecPerLane;
   const int lane = threadIdx.x & 31;
   uint4 raw[U];
 #pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int v = u * 32 + lane;
-    raw[u] = v < nvec ? ring[v] : E::neg_inf();
+  for (int u = 0; u < U; ++u) raw[u] = src[u * 32 + lane];
+  refresh_tau(rc);
+  const float vm = E::vmax4(raw);
+  if (vm > rc.m) {
+    rc.s *= ex2_approx((rc.m - vm) * c);
+    rc.m = vm;
   }
-  float vmu[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) vmu[u] = E::vmax(raw[u]);
-  float vm = vmu[0];
-#pragma unroll
-  for (int u = 1; u < U; ++u) vm = fmaxf(vm, vmu[u]);
-  const bool lane_valid = lane < nvec;
-  if (seed) seed_tau(st, vm, lane_valid, k, tau_slot);
-  if (vm > st.m) {
-    st.s *= ex2_approx((st.m - vm) * c);
-    st.m = vm;
-  }
-  const float2 nm2 = make_float2(-st.m, -st.m);
+  const float2 nm2 = make_float2(-rc.m, -rc.m);
   const float2 c2 = make_float2(c, c);
-  float2 acc = make_float2(0.f, 0.f);
+  float2 acc[U];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
+    acc[u] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int p = 0; p < EPV / 2; ++p) {
       const float2 t = __fmul2_rn(__fadd2_rn(E::pair(raw[u], p), nm2), c2);
-      acc = __fadd2_rn(acc, make_float2(ex2_approx(t.x), ex2_approx(t.y)));
+      acc[u] = __fadd2_rn(acc[u], make_float2(ex2_approx(t.x), ex2_approx(t.y)));
     }
   }
-  st.s += acc.x + acc.y;
-  // absent vectors hold -inf, which must not pass while tau is still -inf
-  if (__any_sync(0xFFFFFFFFu, lane_valid && vm >= st.tau)) {
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const bool h = (u * 32 + lane < nvec) && vmu[u] >= st.tau;
-      if (__any_sync(0xFFFFFFFFu, h)) {
-        if (h) {
-          const uint32_t id0 = id_base + uint32_t((u * 32 + lane) * EPV);
-#pragma unroll
-          for (int p = 0; p < EPV / 2; ++p) {
-            const float2 z = E::pair(raw[u], p);
-            if (z.x >= st.tau) {
-              const int pos = atomicAdd(&S.nbuf, 1);
-              S.buf[pos] = elem_key(z.x, id0 + 2 * p);
-            }
-            if (z.y >= st.tau) {
-              const int pos = atomicAdd(&S.nbuf, 1);
-              S.buf[pos] = elem_key(z.y, id0 + 2 * p + 1);
-            }
-          }
-        }
-        after_push(st, S, k, tau_slot);
+  const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+  rc.s += a.x + a.y;
+  return __ballot_sync(0xFFFFFFFFu, vm >= rc.tau) != 0u;
+}
+
+// A slice shorter than 2 KiB (the end of a row): (max, sum) in, (max, sum) out.
+template <int DT>
+__device__ __noinline__ float2 reduce_partial(const uint4* src, int nvec, uint32_t id_base, float c, float m, float s,
+                                              float tau, const KeyRing kr) {
+  using E = Elem<DT>;
+  constexpr int EPV = E::kPerVec;
+  const int lane = threadIdx.x & 31;
+  bool hit = false;
+#pragma unroll 1
+  for (int u = 0; u < kVecPerLane; ++u) {
+    const int v = u * 32 + lane;
+    if (v < nvec) {
+      const uint4 r = src[v];
+      const float vm = E::vmax(r);
+      if (vm > m) {
+        s *= ex2_approx((m - vm) * c);
+        m = vm;
       }
+#pragma unroll
+      for (int p = 0; p < EPV / 2; ++p) {
+        const float2 z = E::pair(r, p);
+        s += ex2_approx((z.x - m) * c) + ex2_approx((z.y - m) * c);
+      }
+      hit = hit || vm >= tau;
     }
   }
+  if (__ballot_sync(0xFFFFFFFFu, hit) != 0u) push_hits<DT>(src, nvec, id_base, tau, kr);
+  return make_float2(m, s);
+}
+
+// Unaligned elements [b0, b1) of a segment (its head or tail), one per lane.
+template <int DT>
+__device__ __noinline__ float2 reduce_scalars(const uint8_t* logits, unsigned long long b0, unsigned long long b1,
+                                              int es, uint32_t id0, float c, float m, float s, float tau,
+                                              const KeyRing kr) {
+  const int lane = threadIdx.x & 31;
+  const int cnt = int((b1 - b0) / es);
+  for (int base = 0; base < cnt; base += 32) {
+    const int i = base + lane;
+    if (i < cnt) {
+      const float z = Elem<DT>::scalar(logits + b0 + (unsigned long long)i * es);
+      if (z > m) {
+        s *= ex2_approx((m - z) * c);
+        m = z;
+      }
+      s += ex2_approx((z - m) * c);
+      if (z >= tau) ring_put(kr, atomicAdd(kr.tail, 1u), elem_key(z, id0 + uint32_t(i)));
+    }
+  }
+  __syncwarp();
+  return make_float2(m, s);
 }
 
 struct Seg {
@@ -289,33 +431,63 @@ __device__ __forceinline__ Seg segment(const RowsParams& P, unsigned long long e
   return g;
 }
 
+// ------------------------------------------------------------------ row end
+// Writes a row's results from its maximum M, its sum S of 2^((z - M) c) and
+// its best keys (lanes 0..k-1 hold them, descending).
+__device__ __forceinline__ void finish_row(const RowsParams& P, long long r, float M, double S, uint64_t list) {
+  const int lane = threadIdx.x & 31;
+  const int k = P.k;
+  const float zmax = key_value(__shfl_sync(0xFFFFFFFFu, list, 0));
+  if (lane == 0 && zmax != M) set_dev_error(P.ctrl, DART_DEVERR_ROW_MAX);
+  // log S = e ln 2 + log f with S = f 2^e, f in [0.5, 1): one float log of
+  // the mantissa keeps the slow double unit to a multiply and an add
+  int e2;
+  const double f = frexp(S, &e2);
+  const double logS = double(e2) * 0.6931471805599453 + double(logf(float(f)));
+  if (lane < k) {
+    const float z = key_value(list);
+    const int32_t id = int32_t(key_id(list));
+    P.row_ids[(size_t)r * k + lane] = id;
+    P.row_base[(size_t)r * k + lane] = double(z);
+    if (P.out_ids) P.out_ids[(size_t)r * k + lane] = id;
+    if (P.out_logp) P.out_logp[(size_t)r * k + lane] = float((double(z) - double(zmax)) * P.invT - logS);
+  }
+  if (lane == 0) {
+    const double lse = double(zmax) * P.invT + logS;
+    P.row_off[r] = lse;
+    if (P.out_lse) P.out_lse[r] = float(lse);
+  }
+}
+
+// Global partial of one CTA for one row: [f32 max][4 pad][f64 sum][k keys].
+// The last CTA to finish a row merges all of that row's partials.
 __device__ __forceinline__ void merge_row(const RowsParams& P, long long r, int nseg) {
   const int lane = threadIdx.x & 31;
   const int k = P.k;
   const uint8_t* base = P.partials + (size_t)r * P.pmax * P.pstride;
-  // maximum over the partials
   float M = -FLT_MAX;
-  for (int p = lane; p < nseg; p += 32)
-    M = fmaxf(M, __ldcg(reinterpret_cast<const float*>(base + (size_t)p * P.pstride)));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-  // sum of the partial sums rescaled to M, accumulated in double
-  double S = 0.0;
   uint64_t tstar = 0;
   for (int p = lane; p < nseg; p += 32) {
     const uint8_t* q = base + (size_t)p * P.pstride;
-    const float mp = __ldcg(reinterpret_cast<const float*>(q));
-    const float sp = __ldcg(reinterpret_cast<const float*>(q + 4));
-    S += double(sp) * double(ex2_approx((mp - M) * P.c));
+    M = fmaxf(M, __ldcg(reinterpret_cast<const float*>(q)));
     const uint64_t kth = __ldcg(reinterpret_cast<const unsigned long long*>(q + 16) + (k - 1));
     tstar = kth > tstar ? kth : tstar;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    S += __shfl_xor_sync(0xFFFFFFFFu, S, o);
+    M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
     const uint64_t t = __shfl_xor_sync(0xFFFFFFFFu, tstar, o);
     tstar = t > tstar ? t : tstar;
   }
+  double S = 0.0;
+  for (int p = lane; p < nseg; p += 32) {
+    const uint8_t* q = base + (size_t)p * P.pstride;
+    const float mp = __ldcg(reinterpret_cast<const float*>(q));
+    const double sp = __ldcg(reinterpret_cast<const double*>(q + 8));
+    S += sp * double(ex2_approx((mp - M) * P.c));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xFFFFFFFFu, S, o);
   // keys >= tstar (the largest k-th key of any partial) contain the row's best k
   uint64_t list = 0;
   const int total = nseg * k;
@@ -329,158 +501,127 @@ __device__ __forceinline__ void merge_row(const RowsParams& P, long long r, int 
     }
     if (__any_sync(0xFFFFFFFFu, key != 0)) list = warp_merge_top32(list, key);
   }
-  const float zmax = key_value(__shfl_sync(0xFFFFFFFFu, list, 0));
-  if (lane == 0 && zmax != M) set_dev_error(P.ctrl, DART_DEVERR_ROW_MAX);
-  const double logS = log(S);
-  if (lane < k) {
-    const float z = key_value(list);
-    const int32_t id = int32_t(key_id(list));
-    P.row_ids[(size_t)r * k + lane] = id;
-    P.row_base[(size_t)r * k + lane] = double(z);
-    if (P.out_ids) P.out_ids[(size_t)r * k + lane] = id;
-    if (P.out_logp) P.out_logp[(size_t)r * k + lane] = float((double(z) - double(zmax)) / P.T - logS);
-  }
-  if (lane == 0) {
-    const double lse = double(zmax) / P.T + logS;
-    P.row_off[r] = lse;
-    if (P.out_lse) P.out_lse[r] = float(lse);
-  }
+  finish_row(P, r, M, S, list);
 }
 
-template <int DT>
-__global__ void __launch_bounds__(kRowWarps * 32, 1)
-row_stream_kernel(const RowsParams P) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
+// Adds up to 32 keys (one per lane, 0 = none) to the best-32 list.  Keys not
+// above the list's k-th key cannot reach the row's best k and are dropped; a
+// few survivors are inserted one at a time (a vote finds the position), more
+// go through a bitonic merge.  Returns whether the list changed.
+__device__ __forceinline__ bool merge_keys(uint64_t& list, uint64_t key, int k) {
   const int lane = threadIdx.x & 31;
-  const int wib = threadIdx.x >> 5;
-  const int gw = wib * P.grid + blockIdx.x;
-  if (gw >= P.nwarps) return;
-  WarpSmem& S = reinterpret_cast<WarpSmem*>(smem_raw)[wib];
-
-  const unsigned long long B0 = (unsigned long long)gw * P.span;
-  const unsigned long long B1 = (B0 + P.span < P.total) ? B0 + P.span : P.total;
-  const unsigned long long e0 = B0 / P.es, e1 = B1 / P.es;
-  const long long r_first = (long long)(e0 / P.V);
-  const long long r_last = (long long)((e1 - 1) / P.V);
-
-  if (lane == 0) {
-    for (int i = 0; i < kStages; ++i) mbar_init(&S.bar[i], 1);
-    fence_mbar_init();
+  const uint64_t kth = __shfl_sync(0xFFFFFFFFu, list, k - 1);
+  const bool keep = key > kth;   // keys are distinct; 0 never passes
+  uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
+  if (bal == 0u) return false;
+  if (__popc(bal) > 4) {
+    list = warp_merge_top32(list, keep ? key : 0ull);
+    return true;
   }
-  __syncwarp();
-  const uint64_t pol = policy_evict_first();
+  while (bal) {
+    const int src = __ffs(bal) - 1;
+    bal &= bal - 1u;
+    const uint64_t x = __shfl_sync(0xFFFFFFFFu, key, src);
+    const int pos = __popc(__ballot_sync(0xFFFFFFFFu, list > x));   // < k: x beats the k-th
+    const uint64_t up = __shfl_up_sync(0xFFFFFFFFu, list, 1);
+    list = lane < pos ? list : (lane == pos ? x : up);
+  }
+  return true;
+}
 
-  // producer cursor over (row segment, stage) in stream order
-  long long pr = r_first;
-  unsigned long long poff = 0, pend = 0;
-  bool pvalid = false;
-  auto prod_seek = [&](long long r) {
-    pvalid = false;
-    for (; r <= r_last; ++r) {
-      const Seg g = segment(P, e0, e1, r);
-      if (g.a < g.b) { pr = r; poff = g.a; pend = g.b; pvalid = true; return; }
-    }
-  };
-  long long issued = 0;
-  auto prod_issue = [&]() {
-    const int slot = int(issued % kStages);
-    const uint32_t bytes = uint32_t((pend - poff) < (unsigned long long)kStageBytes ? (pend - poff) : kStageBytes);
-    if (lane == 0) {
-      mbar_expect_tx(&S.bar[slot], bytes);
-      bulk_g2s(S.ring[slot], P.logits + poff, bytes, &S.bar[slot], pol);
-    }
-    ++issued;
-    poff += bytes;
-    if (poff >= pend) prod_seek(pr + 1);
-  };
-  prod_seek(r_first);
-  for (int i = 0; i < kStages && pvalid; ++i) prod_issue();
-
-  long long consumed = 0;
-  bool aborted = false;
-  for (long long r = r_first; r <= r_last && !aborted; ++r) {
-    const Seg g = segment(P, e0, e1, r);
-    const unsigned long long rs = (unsigned long long)r * P.V;
-    uint32_t* tau_slot = P.row_tau + r;
-    SegState st;
-    st.m = -FLT_MAX;
-    st.s = 0.f;
-    st.list = 0;
-    st.nbuf = 0;
-    st.tau_ord = __ldcg(tau_slot);
-    st.tau = st.tau_ord ? unord_f32(st.tau_ord) : -INFINITY;
-    if (lane == 0) S.nbuf = 0;
-    __syncwarp();
-
-    // head: [s0, a) (or the whole segment when nothing is aligned)
-    {
-      const unsigned long long hb0 = g.s0 * P.es;
-      const unsigned long long hb1 = (g.a < g.b) ? g.a : g.s1 * P.es;
-      const int cnt = int((hb1 - hb0) / P.es);
-      for (int base = 0; base < cnt; base += 32) {
-        const int i = base + lane;
-        const bool valid = i < cnt;
-        const float z = valid ? Elem<DT>::scalar(P.logits + hb0 + (unsigned long long)i * P.es) : -INFINITY;
-        consume_scalar(st, S, z, valid, uint32_t(g.s0 - rs) + uint32_t(i), P.c, P.k, tau_slot);
+// The merger warp: per row of the span, drains the row's key ring into the
+// CTA's best-32 list (publishing its k-th value as the row's threshold) until
+// every consumer lane is done with the row, then combines the consumer warps'
+// (max, sum) and finishes the row or leaves the CTA's partial.
+__device__ __forceinline__ void merge_span_rows(const RowsParams& P, RowSmem& S, long long r_first,
+                                                long long r_last) {
+  const int lane = threadIdx.x & 31;
+  const int k = P.k;
+  for (long long r = r_first; r <= r_last; ++r) {
+    const int rowseq = int(r - r_first);
+    const int rslot = rowseq % kRowSlots;
+    const uint32_t parity = uint32_t(rowseq / kRowSlots) & 1u;
+    volatile uint64_t* keys = S.keys[rslot];
+    uint32_t head = 0;
+    uint64_t list = 0;
+    long long t0 = clock64();
+    for (;;) {
+      // read "done" before the tail: once done, the tail read after it is final
+      const bool done = __shfl_sync(0xFFFFFFFFu, mbar_test_wait(&S.row_full[rslot], parity) ? 1 : 0, 0) != 0;
+      const uint32_t tail = __shfl_sync(0xFFFFFFFFu, *reinterpret_cast<volatile uint32_t*>(&S.tail[rslot]), 0);
+      if (tail != head) {
+        const uint32_t n = (tail - head) < 32u ? (tail - head) : 32u;
+        uint64_t key = 0;
+        if (uint32_t(lane) < n) {
+          volatile uint64_t* slot = keys + ((head + uint32_t(lane)) & uint32_t(kRingKeys - 1));
+          key = *slot;
+          if (key == 0) {
+            const long long t1 = clock64();
+            while ((key = *slot) == 0) {
+              if (aborted(S)) break;
+              if (clock64() - t1 > P.wait_limit) {
+                raise_abort(S, P.ctrl);
+                break;
+              }
+            }
+          }
+          *slot = 0ull;
+        }
+        if (__any_sync(0xFFFFFFFFu, aborted(S))) return;
+        head += n;
+        __threadfence_block();
+        if (lane == 0) *reinterpret_cast<volatile uint32_t*>(&S.head[rslot]) = head;
+        if (merge_keys(list, key, k)) {
+          const uint64_t kth = __shfl_sync(0xFFFFFFFFu, list, k - 1);
+          if (kth != 0 && lane == 0) atomicMax(&S.tau[rslot], uint32_t(kth >> 32));
+        }
+        t0 = clock64();
+        continue;
+      }
+      if (done) break;
+      __nanosleep(64);
+      if (__any_sync(0xFFFFFFFFu, aborted(S))) return;
+      if (__any_sync(0xFFFFFFFFu, clock64() - t0 > P.wait_limit)) {
+        raise_abort(S, P.ctrl);
+        return;
       }
     }
-    // aligned interior through the ring
-    bool first_stage = true;
-    for (unsigned long long off = g.a; off < g.b; off += kStageBytes) {
-      const uint32_t bytes = uint32_t((g.b - off) < (unsigned long long)kStageBytes ? (g.b - off) : kStageBytes);
-      const int slot = int(consumed % kStages);
-      const uint32_t parity = uint32_t((consumed / kStages) & 1);
-      if (!mbar_wait_bounded(&S.bar[slot], parity, P.wait_limit)) {
-        aborted = true;
-        break;
-      }
-      consume_stage<DT>(st, S, reinterpret_cast<const uint4*>(S.ring[slot]), int(bytes / 16),
-                        uint32_t(off / P.es - rs), P.c, P.k, tau_slot, first_stage);
-      first_stage = false;
-      __syncwarp();
-      ++consumed;
-      if (pvalid) prod_issue();
-    }
-    if (aborted) break;
-    // tail: [b, s1)
-    if (g.a < g.b) {
-      const unsigned long long tb0 = g.b, tb1 = g.s1 * P.es;
-      const int cnt = int((tb1 - tb0) / P.es);
-      for (int base = 0; base < cnt; base += 32) {
-        const int i = base + lane;
-        const bool valid = i < cnt;
-        const float z = valid ? Elem<DT>::scalar(P.logits + tb0 + (unsigned long long)i * P.es) : -INFINITY;
-        consume_scalar(st, S, z, valid, uint32_t(tb0 / P.es - rs) + uint32_t(i), P.c, P.k, tau_slot);
-      }
-    }
-    // finish the segment: remaining buffer, cross-lane (max, sum)
-    __syncwarp();
-    st.nbuf = *reinterpret_cast<volatile int*>(&S.nbuf);
-    if (st.nbuf > 0) {
-      const uint64_t chunk = lane < st.nbuf ? S.buf[lane] : 0ull;
-      st.list = warp_merge_top32(st.list, chunk);
-      st.nbuf = 0;
-    }
-    float m = st.m, s = st.s;
+    // every lane acquires the completed phase (it cannot move on before the
+    // slot is handed back)
+    (void)mbar_test_wait(&S.row_full[rslot], parity);
+    // the consumer warps' (max, sum) of the row
+    const float2 pw = lane < kConsumers ? S.part[rslot][lane] : make_float2(-FLT_MAX, 0.f);
+    float M = pw.x;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-      const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
-      const float M = fmaxf(m, m2);
-      s = s * ex2_approx((m - M) * P.c) + s2 * ex2_approx((m2 - M) * P.c);
-      m = M;
-    }
-    const unsigned long long rb0 = rs * P.es;
-    const long long wfirst = (long long)(rb0 / P.span);
-    const long long wlast = (long long)((rb0 + (unsigned long long)P.V * P.es - 1) / P.span);
-    const int p = int(gw - wfirst);
-    const int nseg = int(wlast - wfirst + 1);
-    uint8_t* part = P.partials + ((size_t)r * P.pmax + p) * P.pstride;
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+    float Sf = pw.y * ex2_approx((pw.x - M) * P.c);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Sf += __shfl_xor_sync(0xFFFFFFFFu, Sf, o);
+    const double Ssum = double(Sf);
+    // hand the slot back (its ring is all zeros again)
     if (lane == 0) {
-      reinterpret_cast<float*>(part)[0] = m;
-      reinterpret_cast<float*>(part)[1] = s;
+      S.tail[rslot] = 0u;
+      S.head[rslot] = 0u;
+      S.tau[rslot] = 0u;
     }
-    if (lane < P.k) reinterpret_cast<unsigned long long*>(part + 16)[lane] = st.list;
+    __syncwarp();
+    __threadfence_block();
+    mbar_arrive(&S.row_free[rslot]);
+
+    const unsigned long long rb0 = (unsigned long long)r * P.V * P.es;
+    const long long cfirst = (long long)(rb0 / P.span);
+    const long long clast = (long long)((rb0 + (unsigned long long)P.V * P.es - 1) / P.span);
+    if (cfirst == clast) {
+      finish_row(P, r, M, Ssum, list);
+      continue;
+    }
+    const int nseg = int(clast - cfirst + 1);
+    uint8_t* part = P.partials + ((size_t)r * P.pmax + (blockIdx.x - cfirst)) * P.pstride;
+    if (lane == 0) {
+      reinterpret_cast<float*>(part)[0] = M;
+      reinterpret_cast<double*>(part)[1] = Ssum;
+    }
+    if (lane < k) reinterpret_cast<unsigned long long*>(part + 16)[lane] = list;
     __threadfence();
     __syncwarp();
     uint32_t old = 0;
@@ -491,18 +632,182 @@ row_stream_kernel(const RowsParams P) {
       merge_row(P, r, nseg);
     }
   }
-  if (aborted) {
-    if (lane == 0) set_dev_error(P.ctrl, DART_DEVERR_WAIT_TIMEOUT);
-    // let copies still in flight land before the warp's shared memory is released
-    for (long long q = consumed; q < issued; ++q) {
-      const int slot = int(q % kStages);
-      (void)mbar_wait_bounded(&S.bar[slot], uint32_t((q / kStages) & 1), P.wait_limit);
+}
+
+// -------------------------------------------------------------------- kernel
+template <int DT>
+__global__ void __launch_bounds__(kRowThreads, 1)
+row_stream_kernel(const RowsParams P) {
+  constexpr int SH = Elem<DT>::kShift;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  RowSmem& S = *reinterpret_cast<RowSmem*>(smem_raw);
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;          // 0 producer, 1..kConsumers consumers, then the merger
+
+  const unsigned long long B0 = (unsigned long long)blockIdx.x * P.span;
+  const unsigned long long B1 = (B0 + P.span < P.total) ? B0 + P.span : P.total;
+  const unsigned long long e0 = B0 / P.es, e1 = B1 / P.es;
+  const long long r_first = (long long)(e0 / P.V);
+  const long long r_last = (long long)((e1 - 1) / P.V);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&S.full[i], 1);
+      mbar_init(&S.empty[i], kConsumers);
     }
+    for (int i = 0; i < kRowSlots; ++i) {
+      mbar_init(&S.row_full[i], kConsumers * 32);
+      mbar_init(&S.row_free[i], 32);
+    }
+    mbar_init(&S.seed_bar[0], kConsumers * 32);
+    mbar_init(&S.seed_bar[1], kConsumers * 32);
+    fence_mbar_init();
+  }
+  {
+    uint64_t* kz = &S.keys[0][0];
+    for (int i = threadIdx.x; i < kRowSlots * kRingKeys; i += blockDim.x) kz[i] = 0ull;
+    if (threadIdx.x < kRowSlots) {
+      S.tail[threadIdx.x] = 0u;
+      S.head[threadIdx.x] = 0u;
+      S.tau[threadIdx.x] = 0u;
+    }
+    if (threadIdx.x == 0) S.abort = 0u;
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------------------- producer
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int q = 0;
+      bool ok = true;
+      for (long long r = r_first; r <= r_last && ok; ++r) {
+        const Seg g = segment(P, e0, e1, r);
+        for (unsigned long long off = g.a; off < g.b; off += kStageBytes) {
+          const int slot = q % kStages;
+          if (q >= kStages && !wait_phase(S, &S.empty[slot], uint32_t(q / kStages - 1) & 1u, P.wait_limit, P.ctrl)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bytes = uint32_t((g.b - off) < (unsigned long long)kStageBytes ? (g.b - off) : kStageBytes);
+          mbar_expect_tx(&S.full[slot], bytes);
+          bulk_g2s(S.ring[slot], P.logits + off, bytes, &S.full[slot], pol);
+          ++q;
+        }
+      }
+      // the CTA may not retire while a copy still writes its shared memory;
+      // these waits are bounded by the clock alone
+      for (int j = q - kStages < 0 ? 0 : q - kStages; j < q; ++j) {
+        if (!mbar_wait_bounded(&S.full[j % kStages], uint32_t(j / kStages) & 1u, P.wait_limit)) {
+          set_dev_error(P.ctrl, DART_DEVERR_WAIT_TIMEOUT);
+          break;
+        }
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ merger
+  if (warp == kMergerWarp) {
+    merge_span_rows(P, S, r_first, r_last);
+    return;
+  }
+
+  // --------------------------------------------------------------- consumers
+  const int w = warp - 1;
+  const long long lim = P.wait_limit;
+  int q = 0;
+  int nseed = 0;   // seeds taken so far (rows with an aligned interior), the same in every consumer warp
+  for (long long r = r_first; r <= r_last; ++r) {
+    const int rowseq = int(r - r_first);
+    const int rslot = rowseq % kRowSlots;
+    if (rowseq >= kRowSlots &&
+        !__all_sync(0xFFFFFFFFu, wait_phase(S, &S.row_free[rslot], uint32_t(rowseq / kRowSlots - 1) & 1u, lim, P.ctrl)))
+      return;
+    const Seg g = segment(P, e0, e1, r);
+    const unsigned long long rs = (unsigned long long)r * P.V;
+    RowCtx rc;
+    rc.m = -FLT_MAX;
+    rc.s = 0.f;
+    rc.tau_ord = 0u;
+    rc.tau = -INFINITY;
+    rc.tau_slot = &S.tau[rslot];
+    KeyRing kr;
+    kr.tail = &S.tail[rslot];
+    kr.head = &S.head[rslot];
+    kr.keys = S.keys[rslot];
+    kr.S = &S;
+    kr.ctrl = P.ctrl;
+    kr.limit = lim;
+
+    // head: [s0, a) (or the whole segment when nothing is aligned), warp 0 only
+    if (w == 0) {
+      const unsigned long long hb0 = g.s0 * P.es;
+      const unsigned long long hb1 = (g.a < g.b) ? g.a : g.s1 * P.es;
+      if (hb1 > hb0) {
+        refresh_tau(rc);
+        const float2 ms = reduce_scalars<DT>(P.logits, hb0, hb1, P.es, uint32_t(g.s0 - rs), P.c, rc.m, rc.s, rc.tau, kr);
+        rc.m = ms.x;
+        rc.s = ms.y;
+      }
+    }
+    // aligned interior: this warp's slice of every stage
+    const uint32_t ilen = uint32_t(g.b - g.a);
+    const uint32_t id_a = uint32_t((g.a >> SH) - rs);
+    const uint32_t s0 = uint32_t(w) * kSlice;
+    for (uint32_t o = 0; o < ilen; o += kStageBytes) {
+      const uint32_t rem = ilen - o;
+      const uint32_t bytes = rem < uint32_t(kStageBytes) ? rem : uint32_t(kStageBytes);
+      const int slot = q % kStages;
+      if (!__all_sync(0xFFFFFFFFu, wait_phase(S, &S.full[slot], uint32_t(q / kStages) & 1u, lim, P.ctrl))) return;
+      const int nvec = s0 < bytes ? int(((bytes - s0) < uint32_t(kSlice) ? (bytes - s0) : uint32_t(kSlice)) / 16) : 0;
+      const uint4* src = reinterpret_cast<const uint4*>(S.ring[slot] + s0);
+      const uint32_t id_base = id_a + ((o + s0) >> SH);
+      if (o == 0) {
+        const uint32_t kth = seed_stage<DT>(src, nvec, &S, nseed, w, P.k, lim, P.ctrl);
+        if (__any_sync(0xFFFFFFFFu, aborted(S))) return;
+        raise_tau(rc, kth);
+        if (lane == 0 && kth != 0u) atomicMax(rc.tau_slot, kth);
+        ++nseed;
+      }
+      if (nvec == kSlice / 16) {
+        if (reduce_full<DT>(rc, src, P.c)) push_hits<DT>(src, nvec, id_base, rc.tau, kr);
+      } else if (nvec > 0) {
+        refresh_tau(rc);
+        const float2 ms = reduce_partial<DT>(src, nvec, id_base, P.c, rc.m, rc.s, rc.tau, kr);
+        rc.m = ms.x;
+        rc.s = ms.y;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[slot]);
+      ++q;
+    }
+    // tail: [b, s1), warp 0 only
+    if (w == 0 && g.a < g.b && g.s1 * P.es > g.b) {
+      refresh_tau(rc);
+      const float2 ms = reduce_scalars<DT>(P.logits, g.b, g.s1 * P.es, P.es, uint32_t((g.b >> SH) - rs), P.c, rc.m,
+                                           rc.s, rc.tau, kr);
+      rc.m = ms.x;
+      rc.s = ms.y;
+    }
+    // the warp's (max, sum) of the row
+    float m = rc.m, s = rc.s;
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) {
+      const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o2);
+      const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o2);
+      const float M = fmaxf(m, m2);
+      s = s * ex2_approx((m - M) * P.c) + s2 * ex2_approx((m2 - M) * P.c);
+      m = M;
+    }
+    if (lane == 0) S.part[rslot][w] = make_float2(m, s);
+    __syncwarp();
+    mbar_arrive(&S.row_full[rslot]);
   }
 }
 
 // ------------------------------------------------------------------ launch
-size_t rows_smem_bytes() { return sizeof(WarpSmem) * kRowWarps; }
+size_t rows_smem_bytes() { return sizeof(RowSmem); }
 
 cudaError_t launch_rows(const void* logits, long long R, int V, int dtype, float T, int k,
                         void* ws, const WsLayout& L, int sms,
@@ -515,21 +820,21 @@ cudaError_t launch_rows(const void* logits, long long R, int V, int dtype, float
   P.k = k;
   P.es = es;
   P.T = double(T);
+  P.invT = 1.0 / double(T);
   P.c = float(1.4426950408889634 / double(T));
   P.total = (unsigned long long)R * (unsigned long long)V * (unsigned long long)es;
-  const unsigned long long want = (P.total + (unsigned long long)sms * kRowWarps - 1) /
-                                  ((unsigned long long)sms * kRowWarps);
+  // one span per SM, whole 16-byte units, at least kMinSpanBytes
+  const unsigned long long want = (P.total + (unsigned long long)sms - 1) / (unsigned long long)sms;
   unsigned long long span = (want + 15) & ~15ull;
   if (span < kMinSpanBytes) span = kMinSpanBytes;
+  if (span >= (1ull << 31)) return cudaErrorInvalidValue;   // 32-bit offsets inside a span
   P.span = span;
-  P.nwarps = int((P.total + span - 1) / span);
-  P.grid = P.nwarps < sms ? P.nwarps : sms;
+  P.grid = int((P.total + span - 1) / span);
   P.pmax = L.pmax;
   P.pstride = L.pstride;
   uint8_t* w = static_cast<uint8_t*>(ws);
   P.ctrl = reinterpret_cast<uint32_t*>(w + L.ctrl);
   P.row_cnt = reinterpret_cast<uint32_t*>(w + L.row_cnt);
-  P.row_tau = reinterpret_cast<uint32_t*>(w + L.row_tau);
   P.partials = w + L.partials;
   P.row_off = reinterpret_cast<double*>(w + L.row_off);
   P.row_ids = reinterpret_cast<int32_t*>(w + L.row_ids);
@@ -544,15 +849,15 @@ cudaError_t launch_rows(const void* logits, long long R, int V, int dtype, float
   switch (dtype) {
     case DART_F32:
       e = cudaFuncSetAttribute(row_stream_kernel<DART_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-      if (e == cudaSuccess) row_stream_kernel<DART_F32><<<P.grid, kRowWarps * 32, smem, stream>>>(P);
+      if (e == cudaSuccess) row_stream_kernel<DART_F32><<<P.grid, kRowThreads, smem, stream>>>(P);
       break;
     case DART_F16:
       e = cudaFuncSetAttribute(row_stream_kernel<DART_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-      if (e == cudaSuccess) row_stream_kernel<DART_F16><<<P.grid, kRowWarps * 32, smem, stream>>>(P);
+      if (e == cudaSuccess) row_stream_kernel<DART_F16><<<P.grid, kRowThreads, smem, stream>>>(P);
       break;
     default:
       e = cudaFuncSetAttribute(row_stream_kernel<DART_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-      if (e == cudaSuccess) row_stream_kernel<DART_BF16><<<P.grid, kRowWarps * 32, smem, stream>>>(P);
+      if (e == cudaSuccess) row_stream_kernel<DART_BF16><<<P.grid, kRowThreads, smem, stream>>>(P);
       break;
   }
   if (e != cudaSuccess) return e;

@@ -10,7 +10,7 @@
 //
 // Per depth the CTA scores all n_j * k children at once (one thread per
 // child: one hash probe, a few double adds), turns each into a 96-bit key
-// (ordered ranking key, then inverted (parent rank, token)), sorts 32- or
+// (ordered ranking key, then inverted (parent rank, token rank)), sorts 32- or
 // 64-key runs with warp bitonic networks and merges runs pairwise, keeping
 // only the best run length, until one run holds the survivors in order.
 #include "dart_launch.h"
@@ -18,11 +18,11 @@
 namespace dart {
 
 constexpr int kTreeThreads = 512;
-constexpr uint32_t kTieMax = 0x3FFFFFFFu;   // (rank << 24 | token) < 2^30
+constexpr uint32_t kTieMax = 0xFFFFFu;      // (parent rank << 5 | token rank) < 2^11
 
 struct CKey {
   uint64_t s;   // ordered ranking key
-  uint32_t t;   // kTieMax - (parent rank << 24 | token): larger = lower rank, lower token
+  uint32_t t;   // kTieMax - (parent rank << 5 | token rank): larger = lower parent, lower token
 };
 
 __device__ __forceinline__ bool ck_gt(const CKey& a, const CKey& b) {
@@ -131,15 +131,43 @@ inline size_t tree_smem_bytes(int W, int k, int MW) {
   const size_t np = size_t(tree_pad(W, k));
   size_t b = 0;
   b += 4 * kMaxW * sizeof(double);                // frontier Z and G (ping-pong)
-  b += kMaxK * sizeof(double);                    // candidate base values
-  b += 3 * np * sizeof(uint64_t);                 // sort keys (ping-pong), candidate G
+  b += 2 * kMaxK * sizeof(double);                // candidate base values of two rows
+  b += 4 * np * sizeof(uint64_t);                 // sort keys (ping-pong), candidate G (ping-pong)
   b += 2 * np * sizeof(uint32_t);                 // tie keys (ping-pong)
   b += 2 * kMaxW * sizeof(int);                   // frontier node ids
   b += 2 * kMaxW * 3 * sizeof(int);               // frontier n-gram contexts
   b += 2 * size_t(kMaxW) * MW * sizeof(uint32_t); // frontier mask rows
-  b += kMaxK * sizeof(int);                       // candidate ids
-  b += kMaxW * sizeof(int);                       // chosen parent ranks
+  b += 6 * kMaxK * sizeof(int);                   // ids, token ranks, inverse ranks of two rows
   return b + 64;
+}
+
+// Row j's candidate lists, with each candidate's rank by token id (ties on the
+// ranking key fall to the lower token id, which is the lower token rank).
+struct RowBuf {
+  int* rid;      // [kMaxK] token ids in list order
+  double* rb;    // [kMaxK] base values
+  int* rrank;    // [kMaxK] rank of rid[c] among the row's ids
+  int* rinv;     // [kMaxK] list position of the id with a given rank
+};
+
+__device__ __forceinline__ void load_row(const TreeArgs& A, int b, int j, const RowBuf& R) {
+  const int k = A.k;
+  const int tid = threadIdx.x;
+  if (tid < k) {
+    R.rid[tid] = A.ids[((size_t)b * A.d + j) * k + tid];
+    R.rb[tid] = A.base[((size_t)b * A.d + j) * k + tid];
+  }
+}
+// ranks by token id; needs the ids visible (call after a barrier)
+__device__ __forceinline__ void rank_row(int k, const RowBuf& R) {
+  const int tid = threadIdx.x;
+  if (tid < k) {
+    const int t = R.rid[tid];
+    int r = 0;
+    for (int c = 0; c < k; ++c) r += R.rid[c] < t;
+    R.rrank[tid] = r;
+    R.rinv[r] = tid;
+  }
 }
 
 // One CTA per tree.  A frontier node carries Z (sum of its candidates' base
@@ -147,7 +175,10 @@ inline size_t tree_smem_bytes(int W, int k, int MW) {
 // Z * invT + lam * G, accumulated in double exactly as the oracle does it, so
 // equal keys (ties the inputs hold exactly) stay equal.  The reported score
 // subtracts the rows' offsets (their log-sum-exp), which every node of one
-// depth shares.
+// depth shares.  After the survivors of a depth are sorted, each thread
+// decodes its child's parent straight from the sorted list, writes that
+// node's outputs and frontier state, and scores the child (one probe), so a
+// depth costs one scoring phase, one sort and the merge levels.
 template <int R>
 __global__ void __launch_bounds__(kTreeThreads)
 tree_kernel(const TreeArgs A) {
@@ -168,10 +199,13 @@ tree_kernel(const TreeArgs A) {
   double* fZ_b = reinterpret_cast<double*>(take(kMaxW * sizeof(double)));
   double* fG_a = reinterpret_cast<double*>(take(kMaxW * sizeof(double)));
   double* fG_b = reinterpret_cast<double*>(take(kMaxW * sizeof(double)));
-  double* rbase = reinterpret_cast<double*>(take(kMaxK * sizeof(double)));
+  RowBuf row0, row1;
+  row0.rb = reinterpret_cast<double*>(take(kMaxK * sizeof(double)));
+  row1.rb = reinterpret_cast<double*>(take(kMaxK * sizeof(double)));
   uint64_t* ks_a = reinterpret_cast<uint64_t*>(take(size_t(npad_max) * 8));
   uint64_t* ks_b = reinterpret_cast<uint64_t*>(take(size_t(npad_max) * 8));
-  double* cG = reinterpret_cast<double*>(take(size_t(npad_max) * 8));
+  double* cG_a = reinterpret_cast<double*>(take(size_t(npad_max) * 8));
+  double* cG_b = reinterpret_cast<double*>(take(size_t(npad_max) * 8));
   uint32_t* kt_a = reinterpret_cast<uint32_t*>(take(size_t(npad_max) * 4));
   uint32_t* kt_b = reinterpret_cast<uint32_t*>(take(size_t(npad_max) * 4));
   int* fnode_a = reinterpret_cast<int*>(take(kMaxW * sizeof(int)));
@@ -180,15 +214,67 @@ tree_kernel(const TreeArgs A) {
   int* fctx_b = reinterpret_cast<int*>(take(kMaxW * 3 * sizeof(int)));
   uint32_t* fmask_a = reinterpret_cast<uint32_t*>(take(size_t(kMaxW) * MW * 4));
   uint32_t* fmask_b = reinterpret_cast<uint32_t*>(take(size_t(kMaxW) * MW * 4));
-  int* rid = reinterpret_cast<int*>(take(kMaxK * sizeof(int)));
-  int* sel = reinterpret_cast<int*>(take(kMaxW * sizeof(int)));
+  row0.rid = reinterpret_cast<int*>(take(kMaxK * sizeof(int)));
+  row0.rrank = reinterpret_cast<int*>(take(kMaxK * sizeof(int)));
+  row0.rinv = reinterpret_cast<int*>(take(kMaxK * sizeof(int)));
+  row1.rid = reinterpret_cast<int*>(take(kMaxK * sizeof(int)));
+  row1.rrank = reinterpret_cast<int*>(take(kMaxK * sizeof(int)));
+  row1.rinv = reinterpret_cast<int*>(take(kMaxK * sizeof(int)));
 
   const uint4* slots = static_cast<const uint4*>(A.slots);
   const unsigned long long cmask = A.capacity - 1;
   const int nctx = n > 1 ? n - 1 : 0;
   const double invT = A.invT, lam = A.lam;
 
-  // frontier of the current depth (cur) and of the next (nxt)
+  // child key of frontier entry (Zp, Gp, context ctx) with candidate c of row R
+  auto child = [&](double Zp, double Gp, int x0, int x1, int x2, const RowBuf& Rw, int c, double* Gout) {
+    const int tok = Rw.rid[c];
+    const double Z = __dadd_rn(Zp, Rw.rb[c]);
+    double G = Gp;
+    if (n > 0) {
+      int32_t t[4] = {x0, x1, x2, 0};
+      if (nctx == 1) t[1] = tok;
+      else if (nctx == 2) t[2] = tok;
+      else t[3] = tok;
+      float g = 0.f;
+      const double gg = probe(slots, cmask, pack_ngram(t, n), &g) ? double(g) : A.beta;
+      G = __dadd_rn(G, gg);
+    }
+    *Gout = G;
+    return __dadd_rn(__dmul_rn(Z, invT), __dmul_rn(lam, G));
+  };
+
+  // ---- depth 1: the root's children
+  load_row(A, b, 0, row0);
+  if (A.d > 1) load_row(A, b, 1, row1);
+  __syncthreads();
+  rank_row(k, row0);
+  if (A.d > 1) rank_row(k, row1);
+  int rootctx[3] = {0, 0, 0};
+#pragma unroll
+  for (int f = 0; f < 3; ++f)
+    if (f < nctx) rootctx[f] = A.ctx[(size_t)b * nctx + f];
+  __syncthreads();
+  uint64_t* keys = ks_a;     // unsorted keys of the current depth
+  uint32_t* ties = kt_a;
+  double* cG = cG_a;         // G of each current candidate
+  {
+    const int npad = (k + RUN - 1) / RUN * RUN;
+    for (int q = tid; q < npad; q += blockDim.x) {
+      uint64_t ks = 0;
+      uint32_t kt = 0;
+      if (q < k) {
+        double G;
+        const double key = child(0.0, 0.0, rootctx[0], rootctx[1], rootctx[2], row0, q, &G);
+        cG[q] = G;
+        ks = ord_f64(key);
+        kt = kTieMax - uint32_t(row0.rrank[q]);             // parent rank 0
+      }
+      keys[q] = ks;
+      ties[q] = kt;
+    }
+  }
+  // frontier of the current depth: the root (only its context and mask are read)
   double* fZ_cur = fZ_a;
   double* fZ_nxt = fZ_b;
   double* fG_cur = fG_a;
@@ -199,56 +285,22 @@ tree_kernel(const TreeArgs A) {
   int* fctx_nxt = fctx_b;
   uint32_t* fmask_cur = fmask_a;
   uint32_t* fmask_nxt = fmask_b;
-
   if (tid == 0) {
     fZ_cur[0] = 0.0;
     fG_cur[0] = 0.0;
     fnode_cur[0] = -1;
-  }
-  if (tid < nctx) fctx_cur[tid] = A.ctx[(size_t)b * nctx + tid];
-  if (tid < k) {
-    rid[tid] = A.ids[(size_t)b * A.d * k + tid];
-    rbase[tid] = A.base[(size_t)b * A.d * k + tid];
+    for (int f = 0; f < nctx; ++f) fctx_cur[f] = rootctx[f];
   }
   int nf = 1, node_base = 0;
   double Lsum = 0.0;   // sum of the row offsets down to this depth (same in every thread)
   __syncthreads();
 
   for (int j = 0; j < A.d; ++j) {
+    const RowBuf Rc = (j & 1) ? row1 : row0;   // row j: candidates of the children sorted now
+    const RowBuf Rn = (j & 1) ? row0 : row1;   // row j+1: candidates of the next depth
     if (A.off) Lsum = __dadd_rn(Lsum, A.off[(size_t)b * A.d + j]);
     const int m = nf * k;
     const int npad = (m + RUN - 1) / RUN * RUN;
-    // expand and score every child of the frontier: one probe per child
-    for (int q = tid; q < npad; q += blockDim.x) {
-      uint64_t ks = 0;
-      uint32_t kt = 0;
-      if (q < m) {
-        const int i = q / k;
-        const int c = q - i * k;
-        const int tok = rid[c];
-        const double Z = __dadd_rn(fZ_cur[i], rbase[c]);
-        double G = fG_cur[i];
-        if (n > 0) {
-          int32_t t[4] = {0, 0, 0, 0};
-#pragma unroll
-          for (int f = 0; f < 3; ++f)
-            if (f < nctx) t[f] = fctx_cur[i * 3 + f];
-          if (nctx == 1) t[1] = tok;
-          else if (nctx == 2) t[2] = tok;
-          else t[3] = tok;
-          float g = 0.f;
-          const double gg = probe(slots, cmask, pack_ngram(t, n), &g) ? double(g) : A.beta;
-          G = __dadd_rn(G, gg);
-        }
-        cG[q] = G;
-        const double key = __dadd_rn(__dmul_rn(Z, invT), __dmul_rn(lam, G));
-        ks = ord_f64(key);
-        kt = kTieMax - ((uint32_t(i) << 24) | (uint32_t(tok) & 0xFFFFFFu));
-      }
-      ks_a[q] = ks;
-      kt_a[q] = kt;
-    }
-    __syncthreads();
     // sort runs of RUN keys, one warp per run
     int nr = npad / RUN;
     for (int run = warp; run < nr; run += nwarps) {
@@ -256,23 +308,23 @@ tree_kernel(const TreeArgs A) {
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const int e = run * RUN + r * 32 + lane;
-        v[r].s = ks_a[e];
-        v[r].t = kt_a[e];
+        v[r].s = keys[e];
+        v[r].t = ties[e];
       }
       run_sort<R>(v);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const int e = run * RUN + r * 32 + lane;
-        ks_a[e] = v[r].s;
-        kt_a[e] = v[r].t;
+        keys[e] = v[r].s;
+        ties[e] = v[r].t;
       }
     }
     __syncthreads();
     // merge runs pairwise, keeping the best RUN keys of each pair
-    uint64_t* ks_src = ks_a;
-    uint32_t* kt_src = kt_a;
-    uint64_t* ks_dst = ks_b;
-    uint32_t* kt_dst = kt_b;
+    uint64_t* ks_src = keys;
+    uint32_t* kt_src = ties;
+    uint64_t* ks_dst = (keys == ks_a) ? ks_b : ks_a;
+    uint32_t* kt_dst = (ties == kt_a) ? kt_b : kt_a;
     while (nr > 1) {
       const int nout = (nr + 1) >> 1;
       for (int t = warp; t < nout; t += nwarps) {
@@ -309,53 +361,86 @@ tree_kernel(const TreeArgs A) {
       uint32_t* tt = kt_src; kt_src = kt_dst; kt_dst = tt;
       nr = nout;
     }
-    // the survivors, best first
+    // survivors of depth j+1 are ks_src[0..nsel); decode each one, emit it and
+    // (unless this is the last depth) score its k children of row j+1
     const int nsel = m < W ? m : W;
-    for (int x = tid; x < nsel; x += blockDim.x) {
-      const uint64_t ks = ks_src[x];
-      const uint32_t tie = kTieMax - kt_src[x];
-      int i = int(tie >> 24);
-      const int tok = int(tie & 0xFFFFFFu);
-      int c = 0;
-      while (c < k && rid[c] != tok) ++c;
-      if (ks == 0 || i >= nf || c == k) {
-        set_dev_error(A.ctrl, DART_DEVERR_SELECT);
-        i = 0;
-        c = 0;
+    const bool last = (j + 1 == A.d);
+    const int kk = last ? 1 : k;
+    const int m2 = nsel * kk;
+    const int npad2 = last ? m2 : (m2 + RUN - 1) / RUN * RUN;
+    double* cG_next = (cG == cG_a) ? cG_b : cG_a;
+    for (int q = tid; q < npad2; q += blockDim.x) {
+      uint64_t ks2 = 0;
+      uint32_t kt2 = 0;
+      if (q < m2) {
+        const int x = q / kk;             // survivor rank = node index within the depth
+        const int c2 = q - x * kk;        // its child column in row j+1
+        const uint64_t ks = ks_src[x];
+        const uint32_t tie = kTieMax - kt_src[x];
+        int i = int(tie >> 5);
+        int c = (i < nf) ? Rc.rinv[tie & 31u] : 0;
+        if (ks == 0 || i >= nf) {
+          set_dev_error(A.ctrl, DART_DEVERR_SELECT);
+          i = 0;
+          c = 0;
+        }
+        const int tok = Rc.rid[c];
+        const int node = node_base + x;
+        const double Zp = __dadd_rn(fZ_cur[i], Rc.rb[c]);
+        const double Gp = cG[i * k + c];
+        int ctx[3] = {0, 0, 0};
+#pragma unroll
+        for (int f = 0; f + 1 < 3; ++f)
+          if (f + 1 < nctx) ctx[f] = fctx_cur[i * 3 + f + 1];
+        if (nctx > 0) {
+          if (nctx == 1) ctx[0] = tok;
+          else if (nctx == 2) ctx[1] = tok;
+          else ctx[2] = tok;
+        }
+        // ancestor-mask words of the node, spread over its k child threads
+        for (int w = c2; w < MW; w += kk) {
+          uint32_t val = (j == 0) ? 0u : fmask_cur[i * MW + w];
+          if (w == (node >> 5)) val |= 1u << (node & 31);
+          fmask_nxt[x * MW + w] = val;
+          A.out_mask[((size_t)b * N + node) * MW + w] = val;
+        }
+        if (c2 == 0) {
+          const size_t o = (size_t)b * N + node;
+          A.out_tokens[o] = tok;
+          A.out_parents[o] = j == 0 ? -1 : fnode_cur[i];
+          A.out_pos[o] = j + 1;
+          if (A.out_scores) A.out_scores[o] = float(__dsub_rn(unord_f64(ks), Lsum));
+          fZ_nxt[x] = Zp;
+          fG_nxt[x] = Gp;
+          fnode_nxt[x] = node;
+#pragma unroll
+          for (int f = 0; f < 3; ++f)
+            if (f < nctx) fctx_nxt[x * 3 + f] = ctx[f];
+        }
+        if (!last) {
+          double G;
+          const double key = child(Zp, Gp, ctx[0], ctx[1], ctx[2], Rn, c2, &G);
+          cG_next[q] = G;
+          ks2 = ord_f64(key);
+          kt2 = kTieMax - ((uint32_t(x) << 5) | uint32_t(Rn.rrank[c2]));
+        }
       }
-      const double key = unord_f64(ks);
-      const int node = node_base + x;
-      const size_t o = (size_t)b * N + node;
-      A.out_tokens[o] = tok;
-      A.out_parents[o] = j == 0 ? -1 : fnode_cur[i];
-      A.out_pos[o] = j + 1;
-      if (A.out_scores) A.out_scores[o] = float(__dsub_rn(key, Lsum));
-      fZ_nxt[x] = __dadd_rn(fZ_cur[i], rbase[c]);
-      fG_nxt[x] = cG[i * k + c];
-      fnode_nxt[x] = node;
-      if (nctx > 0) {
-        for (int f = 0; f + 1 < nctx; ++f) fctx_nxt[x * 3 + f] = fctx_cur[i * 3 + f + 1];
-        fctx_nxt[x * 3 + nctx - 1] = tok;
+      if (!last) {
+        ks_dst[q] = ks2;
+        kt_dst[q] = kt2;
       }
-      sel[x] = i;
     }
+    if (last) break;
     __syncthreads();
-    // ancestor masks: the parent's row plus the node's own bit; the next
-    // depth's candidate lists are fetched in the same phase
-    for (int w = tid; w < nsel * MW; w += blockDim.x) {
-      const int x = w / MW;
-      const int word = w - x * MW;
-      const int node = node_base + x;
-      uint32_t val = (j == 0) ? 0u : fmask_cur[sel[x] * MW + word];
-      if (word == (node >> 5)) val |= 1u << (node & 31);
-      fmask_nxt[x * MW + word] = val;
-      A.out_mask[((size_t)b * N + node) * MW + word] = val;
+    // row j+2 goes into row j's buffer, now free
+    if (j + 2 < A.d) {
+      load_row(A, b, j + 2, Rc);
+      __syncthreads();
+      rank_row(k, Rc);
     }
-    if (j + 1 < A.d && tid < k) {
-      rid[tid] = A.ids[((size_t)b * A.d + j + 1) * k + tid];
-      rbase[tid] = A.base[((size_t)b * A.d + j + 1) * k + tid];
-    }
-    __syncthreads();
+    keys = ks_dst;
+    ties = kt_dst;
+    cG = cG_next;
     { double* t = fZ_cur; fZ_cur = fZ_nxt; fZ_nxt = t; }
     { double* t = fG_cur; fG_cur = fG_nxt; fG_nxt = t; }
     { int* t = fnode_cur; fnode_cur = fnode_nxt; fnode_nxt = t; }
@@ -363,6 +448,7 @@ tree_kernel(const TreeArgs A) {
     { uint32_t* t = fmask_cur; fmask_cur = fmask_nxt; fmask_nxt = t; }
     nf = nsel;
     node_base += nsel;
+    __syncthreads();
   }
 }
 

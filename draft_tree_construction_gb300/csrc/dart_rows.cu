@@ -7,11 +7,12 @@
 //
 // Work split.  The logits are one flat byte stream cut into equal,
 // contiguous, 16-byte-aligned spans, one per CTA (one CTA per SM).  Inside a
-// CTA one producer thread streams its span through a ring of 24 KiB
-// shared-memory stages with cp.async.bulk (an mbarrier per stage counts the
-// bytes in, another counts the 12 consumer warps out); each consumer warp
-// reduces its own 2 KiB slice of every stage.  Stages never straddle a row, so
-// all consumer warps of a CTA work on the same row at the same time.
+// CTA one producer thread streams its span through a 192 KiB shared-memory
+// ring of stages with cp.async.bulk (an mbarrier per stage counts the bytes
+// in, another counts the 12 consumer warps out); each consumer warp reduces
+// its own slice of every stage: 2 KiB of 24 KiB stages for rows under 256 KiB,
+// 4 KiB of 48 KiB stages for longer rows.  Stages never straddle a row, so all
+// consumer warps of a CTA work on the same row at the same time.
 //
 // Per slice a lane holds four 16-byte vectors.  One running-max update covers
 // all of them (maxima taken on packed bf16x2 / f16x2 words), the exponentials
@@ -46,15 +47,16 @@
 namespace dart {
 
 constexpr int kConsumers = 12;                  // reducing warps per CTA (plus a producer and a merger warp)
-constexpr int kSlice = 2048;                    // bytes of a stage per consumer warp: 4 vectors per lane
-constexpr int kStageBytes = kSlice * kConsumers;
-constexpr int kStages = 5;                      // 120 KiB in flight per SM
+constexpr int kSlice = 2048;                    // bytes one reduce step covers: 4 vectors per lane
+constexpr int kRingBytes = 196608;              // 192 KiB of stages in flight per SM
+constexpr int kMaxStages = 8;                   // 8 x 24 KiB (short rows) or 4 x 48 KiB stages
 constexpr int kVecPerLane = kSlice / 16 / 32;
 constexpr int kRowSlots = 4;                    // rows in flight between the consumers and the merger
-constexpr int kRingKeys = 1024;                 // key ring per row slot (power of two)
+constexpr int kRingKeys = 512;                  // key ring per row slot (power of two)
+constexpr uint32_t kSleepNs = 100000;           // longest sleep of one barrier probe
 constexpr int kMergerWarp = kConsumers + 1;
 constexpr int kRowThreads = (kConsumers + 2) * 32;
-static_assert(kVecPerLane == 4, "consume_slice reduces exactly four vectors per lane");
+static_assert(kVecPerLane == 4, "reduce_full reduces exactly four vectors per lane");
 static_assert((kRingKeys & (kRingKeys - 1)) == 0, "ring index masking");
 
 struct RowsParams {
@@ -67,6 +69,9 @@ struct RowsParams {
   unsigned long long total;   // R * V * es bytes
   unsigned long long span;    // bytes per CTA, multiple of 16
   int grid;
+  int nsub;                   // 2 KiB steps per consumer warp and stage (1 or 2)
+  int nst;                    // stages in the ring (kMaxStages / nsub)
+  uint32_t stage_bytes;       // kConsumers * nsub * kSlice
   int pmax, pstride;
   uint32_t* ctrl;
   uint32_t* row_cnt;
@@ -81,11 +86,11 @@ struct RowsParams {
 };
 
 struct __align__(128) RowSmem {
-  uint8_t ring[kStages][kStageBytes];
+  uint8_t ring[kRingBytes];
   uint64_t keys[kRowSlots][kRingKeys];   // candidate keys of a row; 0 = slot not written yet
   float2 part[kRowSlots][kConsumers];    // per consumer warp: (max, sum of 2^((z - max) c))
-  uint64_t full[kStages];                // bytes of a stage have landed
-  uint64_t empty[kStages];               // every consumer warp is done with a stage
+  uint64_t full[kMaxStages];             // bytes of a stage have landed
+  uint64_t empty[kMaxStages];            // every consumer warp is done with a stage
   uint64_t row_full[kRowSlots];          // every consumer lane is done with a row
   uint64_t row_free[kRowSlots];          // the merger is done with a row slot
   uint32_t tail[kRowSlots];              // keys reserved in a row's ring
@@ -185,7 +190,7 @@ __device__ __forceinline__ void raise_abort(RowSmem& S, uint32_t* ctrl) {
 __device__ __noinline__ bool wait_phase_spin(RowSmem& S, uint64_t* bar, uint32_t parity, long long limit,
                                              uint32_t* ctrl) {
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_hint(bar, parity, kSleepNs)) {
     if (aborted(S)) return false;
     if (clock64() - t0 > limit) {
       raise_abort(S, ctrl);
@@ -236,10 +241,9 @@ __device__ __noinline__ void push_hits(const uint4* src, int nvec, uint32_t id_b
   using E = Elem<DT>;
   constexpr int EPV = E::kPerVec;
   const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int u = 0; u < kVecPerLane; ++u) {
-    const int v = u * 32 + lane;
-    if (v < nvec) {
+#pragma unroll 1
+  for (int v = lane; v < nvec; v += 32) {
+    {
       const uint4 r = src[v];
       if (E::vmax(r) >= tau) {
         uint32_t em = 0;
@@ -291,11 +295,8 @@ __device__ __noinline__ uint32_t seed_stage(const uint4* src, int nvec, RowSmem*
   RowSmem& S = *Sp;
   const int lane = threadIdx.x & 31;
   float vm = -INFINITY;
-#pragma unroll
-  for (int u = 0; u < kVecPerLane; ++u) {
-    const int v = u * 32 + lane;
-    if (v < nvec) vm = fmaxf(vm, E::vmax(src[v]));
-  }
+#pragma unroll 2
+  for (int v = lane; v < nvec; v += 32) vm = fmaxf(vm, E::vmax(src[v]));
   const int sb = nseed & 1;
   S.seed[sb][w][lane] = lane < nvec ? ord_f32(vm) : 0u;
   mbar_arrive(&S.seed_bar[sb]);
@@ -369,9 +370,8 @@ __device__ __noinline__ float2 reduce_partial(const uint4* src, int nvec, uint32
   const int lane = threadIdx.x & 31;
   bool hit = false;
 #pragma unroll 1
-  for (int u = 0; u < kVecPerLane; ++u) {
-    const int v = u * 32 + lane;
-    if (v < nvec) {
+  for (int v = lane; v < nvec; v += 32) {
+    {
       const uint4 r = src[v];
       const float vm = E::vmax(r);
       if (vm > m) {
@@ -579,7 +579,7 @@ __device__ __forceinline__ void merge_span_rows(const RowsParams& P, RowSmem& S,
         continue;
       }
       if (done) break;
-      __nanosleep(64);
+      __nanosleep(256);
       if (__any_sync(0xFFFFFFFFu, aborted(S))) return;
       if (__any_sync(0xFFFFFFFFu, clock64() - t0 > P.wait_limit)) {
         raise_abort(S, P.ctrl);
@@ -651,7 +651,7 @@ row_stream_kernel(const RowsParams P) {
   const long long r_last = (long long)((e1 - 1) / P.V);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(&S.full[i], 1);
       mbar_init(&S.empty[i], kConsumers);
     }
@@ -679,26 +679,36 @@ row_stream_kernel(const RowsParams P) {
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int q = 0;
+      const int nst = P.nst;
+      int slot = 0;
+      uint32_t round = 0;   // fills of `slot` so far
+      int issued = 0;
       bool ok = true;
       for (long long r = r_first; r <= r_last && ok; ++r) {
         const Seg g = segment(P, e0, e1, r);
-        for (unsigned long long off = g.a; off < g.b; off += kStageBytes) {
-          const int slot = q % kStages;
-          if (q >= kStages && !wait_phase(S, &S.empty[slot], uint32_t(q / kStages - 1) & 1u, P.wait_limit, P.ctrl)) {
+        for (unsigned long long off = g.a; off < g.b; off += P.stage_bytes) {
+          if (round > 0 && !wait_phase(S, &S.empty[slot], (round - 1) & 1u, P.wait_limit, P.ctrl)) {
             ok = false;
             break;
           }
-          const uint32_t bytes = uint32_t((g.b - off) < (unsigned long long)kStageBytes ? (g.b - off) : kStageBytes);
+          const uint32_t bytes = uint32_t((g.b - off) < (unsigned long long)P.stage_bytes ? (g.b - off) : P.stage_bytes);
+          uint8_t* dst = S.ring + size_t(slot) * P.stage_bytes;
           mbar_expect_tx(&S.full[slot], bytes);
-          bulk_g2s(S.ring[slot], P.logits + off, bytes, &S.full[slot], pol);
-          ++q;
+          bulk_g2s(dst, P.logits + off, bytes, &S.full[slot], pol);
+          ++issued;
+          if (++slot == nst) {
+            slot = 0;
+            ++round;
+          }
         }
       }
       // the CTA may not retire while a copy still writes its shared memory;
       // these waits are bounded by the clock alone
-      for (int j = q - kStages < 0 ? 0 : q - kStages; j < q; ++j) {
-        if (!mbar_wait_bounded(&S.full[j % kStages], uint32_t(j / kStages) & 1u, P.wait_limit)) {
+      for (int j = 0; j < nst && j < issued; ++j) {
+        // the last fill of each slot used so far
+        const int sl = (slot + nst - 1 - j) % nst;
+        const uint32_t rd = (sl < slot) ? round : round - 1;
+        if (!mbar_wait_bounded(&S.full[sl], rd & 1u, P.wait_limit)) {
           set_dev_error(P.ctrl, DART_DEVERR_WAIT_TIMEOUT);
           break;
         }
@@ -716,7 +726,8 @@ row_stream_kernel(const RowsParams P) {
   // --------------------------------------------------------------- consumers
   const int w = warp - 1;
   const long long lim = P.wait_limit;
-  int q = 0;
+  int slot = 0;         // ring stage of the next stage
+  uint32_t round = 0;   // fills of `slot` before this one
   int nseed = 0;   // seeds taken so far (rows with an aligned interior), the same in every consumer warp
   for (long long r = r_first; r <= r_last; ++r) {
     const int rowseq = int(r - r_first);
@@ -754,14 +765,14 @@ row_stream_kernel(const RowsParams P) {
     // aligned interior: this warp's slice of every stage
     const uint32_t ilen = uint32_t(g.b - g.a);
     const uint32_t id_a = uint32_t((g.a >> SH) - rs);
-    const uint32_t s0 = uint32_t(w) * kSlice;
-    for (uint32_t o = 0; o < ilen; o += kStageBytes) {
+    const uint32_t s0 = uint32_t(w) * uint32_t(P.nsub * kSlice);
+    for (uint32_t o = 0; o < ilen; o += P.stage_bytes) {
       const uint32_t rem = ilen - o;
-      const uint32_t bytes = rem < uint32_t(kStageBytes) ? rem : uint32_t(kStageBytes);
-      const int slot = q % kStages;
-      if (!__all_sync(0xFFFFFFFFu, wait_phase(S, &S.full[slot], uint32_t(q / kStages) & 1u, lim, P.ctrl))) return;
-      const int nvec = s0 < bytes ? int(((bytes - s0) < uint32_t(kSlice) ? (bytes - s0) : uint32_t(kSlice)) / 16) : 0;
-      const uint4* src = reinterpret_cast<const uint4*>(S.ring[slot] + s0);
+      const uint32_t bytes = rem < P.stage_bytes ? rem : P.stage_bytes;
+      if (!__all_sync(0xFFFFFFFFu, wait_phase(S, &S.full[slot], round & 1u, lim, P.ctrl))) return;
+      const uint8_t* stage = S.ring + size_t(slot) * P.stage_bytes;
+      const int nvec = s0 < bytes ? int(min(bytes - s0, uint32_t(P.nsub * kSlice)) / 16) : 0;
+      const uint4* src = reinterpret_cast<const uint4*>(stage + s0);
       const uint32_t id_base = id_a + ((o + s0) >> SH);
       if (o == 0) {
         const uint32_t kth = seed_stage<DT>(src, nvec, &S, nseed, w, P.k, lim, P.ctrl);
@@ -770,8 +781,11 @@ row_stream_kernel(const RowsParams P) {
         if (lane == 0 && kth != 0u) atomicMax(rc.tau_slot, kth);
         ++nseed;
       }
-      if (nvec == kSlice / 16) {
-        if (reduce_full<DT>(rc, src, P.c)) push_hits<DT>(src, nvec, id_base, rc.tau, kr);
+      if (nvec == P.nsub * (kSlice / 16)) {
+        for (int j = 0; j < P.nsub; ++j) {
+          const uint4* sj = src + j * (kSlice / 16);
+          if (reduce_full<DT>(rc, sj, P.c)) push_hits<DT>(sj, kSlice / 16, id_base + uint32_t(j * (kSlice >> SH)), rc.tau, kr);
+        }
       } else if (nvec > 0) {
         refresh_tau(rc);
         const float2 ms = reduce_partial<DT>(src, nvec, id_base, P.c, rc.m, rc.s, rc.tau, kr);
@@ -780,7 +794,10 @@ row_stream_kernel(const RowsParams P) {
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[slot]);
-      ++q;
+      if (++slot == P.nst) {
+        slot = 0;
+        ++round;
+      }
     }
     // tail: [b, s1), warp 0 only
     if (w == 0 && g.a < g.b && g.s1 * P.es > g.b) {
@@ -830,6 +847,12 @@ cudaError_t launch_rows(const void* logits, long long R, int V, int dtype, float
   if (span >= (1ull << 31)) return cudaErrorInvalidValue;   // 32-bit offsets inside a span
   P.span = span;
   P.grid = int((P.total + span - 1) / span);
+  // long rows take 48 KiB stages (less loop overhead per byte); rows shorter
+  // than about five of those take 24 KiB stages (less idle tail per row)
+  const unsigned long long row_bytes = (unsigned long long)V * (unsigned long long)es;
+  P.nsub = row_bytes >= 262144ull ? 2 : 1;
+  P.nst = kMaxStages / P.nsub;
+  P.stage_bytes = uint32_t(kConsumers * P.nsub * kSlice);
   P.pmax = L.pmax;
   P.pstride = L.pstride;
   uint8_t* w = static_cast<uint8_t*>(ws);

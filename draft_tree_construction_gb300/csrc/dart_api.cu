@@ -31,7 +31,8 @@ int num_nodes(int d, int k, int W) {
 int check_table(const dart_ngram_table_t* t, const int32_t* ctx, int B) {
   if (!t) return DART_OK;
   if (t->n < 2 || t->n > 4 || t->reserved != 0) return DART_ERR_INVALID_ARG;
-  if (!pow2(t->capacity) || !t->slots || !aligned(t->slots, 16)) return DART_ERR_INVALID_ARG;
+  if (!pow2(t->capacity) || t->capacity < kMinTableSlots || !t->slots || !aligned(t->slots, 64))
+    return DART_ERR_INVALID_ARG;
   if (B > 0 && !ctx) return DART_ERR_INVALID_ARG;
   return DART_OK;
 }
@@ -253,23 +254,34 @@ int dart_mask_pack(const int32_t* parents, int B, int N, uint32_t* out_mask, uin
 
 uint64_t dart_ngram_capacity_for(uint64_t M) {
   if (M > (1ull << 62)) return 0;
-  uint64_t c = 2;
+  uint64_t c = kMinTableSlots;
   while (c < 2 * M) c <<= 1;
   return c;
 }
 
+namespace {
+bool slot_is(const uint32_t* slot, const Key96& k) { return slot[0] == k.w0 && slot[1] == k.w1 && slot[2] == k.w2; }
+bool slot_empty(const uint32_t* slot) { return slot[0] == kEmpty && slot[1] == kEmpty && slot[2] == kEmpty; }
+uint32_t* free_slot(uint32_t* s, uint64_t bucket) {
+  for (int t = 0; t < 4; ++t)
+    if (slot_empty(s + 4 * (4 * bucket + t))) return s + 4 * (4 * bucket + t);
+  return nullptr;
+}
+void put(uint32_t* slot, const Key96& k, uint32_t v) {
+  slot[0] = k.w0;
+  slot[1] = k.w1;
+  slot[2] = k.w2;
+  slot[3] = v;
+}
+}  // namespace
+
 int dart_ngram_table_pack_host(int n, const int32_t* keys, const float* vals, uint64_t M,
                                uint64_t capacity, void* host_slots, uint64_t* out_distinct) {
-  if (n < 1 || n > 4 || !pow2(capacity) || !host_slots) return DART_ERR_INVALID_ARG;
+  if (n < 1 || n > 4 || !pow2(capacity) || capacity < kMinTableSlots || !host_slots) return DART_ERR_INVALID_ARG;
   if (M > 0 && (!keys || !vals)) return DART_ERR_INVALID_ARG;
   uint32_t* s = static_cast<uint32_t*>(host_slots);
-  for (uint64_t i = 0; i < capacity; ++i) {
-    s[4 * i + 0] = kEmpty;
-    s[4 * i + 1] = kEmpty;
-    s[4 * i + 2] = kEmpty;
-    s[4 * i + 3] = 0u;
-  }
-  const uint64_t mask = capacity - 1;
+  for (uint64_t i = 0; i < capacity; ++i) put(s + 4 * i, Key96{kEmpty, kEmpty, kEmpty}, 0u);
+  const uint64_t nb = capacity / 4;
   uint64_t distinct = 0;
   int rc = DART_OK;
   for (uint64_t i = 0; i < M && rc == DART_OK; ++i) {
@@ -277,22 +289,39 @@ int dart_ngram_table_pack_host(int n, const int32_t* keys, const float* vals, ui
     for (int f = 0; f < n; ++f)
       if (t[f] < 0 || t[f] >= kMaxV) rc = DART_ERR_INVALID_ARG;
     if (rc) break;
-    const Key96 key = pack_ngram(t, n);
-    uint64_t idx = hash_key(key) & mask;
-    for (uint64_t step = 0; step <= mask; ++step) {
-      uint32_t* slot = s + 4 * idx;
-      if (slot[0] == key.w0 && slot[1] == key.w1 && slot[2] == key.w2) break;  // first value kept
-      if (slot[0] == kEmpty && slot[1] == kEmpty && slot[2] == kEmpty) {
-        if (distinct >= capacity / 2) { rc = DART_ERR_TABLE_FULL; break; }
-        slot[0] = key.w0;
-        slot[1] = key.w1;
-        slot[2] = key.w2;
-        memcpy(&slot[3], &vals[i], 4);
-        ++distinct;
-        break;
-      }
-      idx = (idx + 1) & mask;
+    Key96 key = pack_ngram(t, n);
+    uint32_t val;
+    memcpy(&val, &vals[i], 4);
+    const Buckets bk = key_buckets(key, nb);
+    bool present = false;
+    for (int tt = 0; tt < 8 && !present; ++tt)
+      present = slot_is(s + 4 * (4 * (tt < 4 ? bk.b1 : bk.b2) + (tt & 3)), key);
+    if (present) continue;   // the first value of a key is kept
+    if (distinct >= capacity / 2) {
+      rc = DART_ERR_TABLE_FULL;
+      break;
     }
+    uint32_t* slot = free_slot(s, bk.b1);
+    if (!slot) slot = free_slot(s, bk.b2);
+    // both buckets full: displace along the chain b -> the victim's other bucket
+    uint64_t b = bk.b1;
+    for (int kick = 0; !slot && kick < 500; ++kick) {
+      uint32_t* victim = s + 4 * (4 * b + uint64_t(kick & 3));
+      const Key96 vk{victim[0], victim[1], victim[2]};
+      const uint32_t vv = victim[3];
+      put(victim, key, val);
+      key = vk;
+      val = vv;
+      const Buckets vb = key_buckets(key, nb);
+      b = (vb.b1 == b) ? vb.b2 : vb.b1;
+      slot = free_slot(s, b);
+    }
+    if (!slot) {
+      rc = DART_ERR_TABLE_FULL;
+      break;
+    }
+    put(slot, key, val);
+    ++distinct;
   }
   if (out_distinct) *out_distinct = distinct;
   return rc;
@@ -300,8 +329,8 @@ int dart_ngram_table_pack_host(int n, const int32_t* keys, const float* vals, ui
 
 int dart_ngram_lookup(const dart_ngram_table_t* table, const int32_t* keys, int64_t Q,
                       float* vals, int32_t* found, void* stream) {
-  if (!table || table->n < 1 || table->n > 4 || !pow2(table->capacity) || !table->slots ||
-      !aligned(table->slots, 16) || Q < 0)
+  if (!table || table->n < 1 || table->n > 4 || !pow2(table->capacity) || table->capacity < kMinTableSlots ||
+      !table->slots || !aligned(table->slots, 64) || Q < 0)
     return DART_ERR_INVALID_ARG;
   if (Q == 0) return DART_OK;
   if (!keys || !vals || !found) return DART_ERR_INVALID_ARG;

@@ -92,6 +92,18 @@ __host__ __device__ __forceinline__ uint64_t hash_key(Key96 k) {
   return x;
 }
 
+// The two buckets (4 slots each) a key may live in; nb = capacity / 4 >= 2.
+struct Buckets { uint64_t b1, b2; };
+__host__ __device__ __forceinline__ Buckets key_buckets(Key96 k, uint64_t nb) {
+  const uint64_t h = hash_key(k);
+  Buckets b;
+  b.b1 = h & (nb - 1);
+  b.b2 = (h >> 32) & (nb - 1);
+  if (b.b2 == b.b1) b.b2 = b.b1 ^ 1ull;
+  return b;
+}
+constexpr uint64_t kMinTableSlots = 8;
+
 // ------------------------------------------------------- workspace layout
 // [ctrl 256 B][row_cnt R x u32]   <- cleared by every call
 // [row_off R x f64][row_ids R*k x i32][row_base R*k x f64][partials]

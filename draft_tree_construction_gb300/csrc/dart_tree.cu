@@ -91,30 +91,25 @@ __device__ __forceinline__ void run_merge_desc(CKey (&v)[R]) {
   }
 }
 
-// Linear probing from the key's home slot.  Each round trip reads the aligned
-// pair of 32-byte sectors around the current slot (4 slots) at once, so most
-// lookups (load factor <= 1/2) finish after one memory latency.
-__device__ __forceinline__ bool probe(const uint4* slots, unsigned long long mask, Key96 key, float* val) {
-  unsigned long long idx = hash_key(key) & mask;
-  for (unsigned long long done = 0; done <= mask;) {
-    const unsigned long long base = idx & ~1ull;
-    uint4 s[4];
+// A lookup reads the key's two buckets (eight slots, 128 bytes) at once: one
+// memory round trip whether the key is present or not.
+__device__ __forceinline__ bool probe(const uint4* slots, unsigned long long nb, Key96 key, float* val) {
+  const Buckets bk = key_buckets(key, nb);
+  uint4 s[8];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) s[t] = ldg_nc_v4(slots + ((base + t) & mask));
-    const int start = int(idx - base);
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      if (t < start) continue;
-      if (s[t].x == key.w0 && s[t].y == key.w1 && s[t].z == key.w2) {
-        *val = __uint_as_float(s[t].w);
-        return true;
-      }
-      if (s[t].x == kEmpty && s[t].y == kEmpty && s[t].z == kEmpty) return false;
-      ++done;
-    }
-    idx = (base + 4) & mask;
+  for (int t = 0; t < 4; ++t) {
+    s[t] = ldg_nc_v4(slots + 4 * bk.b1 + t);
+    s[4 + t] = ldg_nc_v4(slots + 4 * bk.b2 + t);
   }
-  return false;
+  bool hit = false;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    if (s[t].x == key.w0 && s[t].y == key.w1 && s[t].z == key.w2) {
+      *val = __uint_as_float(s[t].w);
+      hit = true;
+    }
+  }
+  return hit;
 }
 
 __host__ __device__ inline int tree_run_len(int W) { return W <= 32 ? 32 : 64; }
@@ -127,58 +122,46 @@ inline int tree_threads(int W, int k) {
   int t = (W * k + 31) / 32 * 32;
   return t < 32 ? 32 : (t > kTreeThreads ? kTreeThreads : t);
 }
-inline size_t tree_smem_bytes(int W, int k, int MW) {
+constexpr int kRankMax = 256;   // up to this many children a depth selects by ranking
+
+inline size_t tree_smem_bytes(int d, int W, int k, int MW) {
   const size_t np = size_t(tree_pad(W, k));
+  const size_t dk = size_t(d) * k;
   size_t b = 0;
   b += 4 * kMaxW * sizeof(double);                // frontier Z and G (ping-pong)
-  b += 2 * kMaxK * sizeof(double);                // candidate base values of two rows
-  b += 4 * np * sizeof(uint64_t);                 // sort keys (ping-pong), candidate G (ping-pong)
+  b += align_up(dk * sizeof(double), 16);         // candidate base values of every row
+  b += align_up(size_t(d) * sizeof(double), 16);  // row offsets
+  b += 4 * np * sizeof(uint64_t);                 // keys (ping-pong), candidate G (ping-pong)
+  b += kMaxW * sizeof(uint64_t);                  // selected keys
   b += 2 * np * sizeof(uint32_t);                 // tie keys (ping-pong)
+  b += kMaxW * sizeof(uint32_t);                  // selected tie keys
   b += 2 * kMaxW * sizeof(int);                   // frontier node ids
   b += 2 * kMaxW * 3 * sizeof(int);               // frontier n-gram contexts
   b += 2 * size_t(kMaxW) * MW * sizeof(uint32_t); // frontier mask rows
-  b += 6 * kMaxK * sizeof(int);                   // ids, token ranks, inverse ranks of two rows
+  b += 3 * align_up(dk * sizeof(int), 16);        // ids, token ranks, inverse ranks of every row
   return b + 64;
 }
 
-// Row j's candidate lists, with each candidate's rank by token id (ties on the
-// ranking key fall to the lower token id, which is the lower token rank).
+// One row's candidate lists, with each candidate's rank by token id (ties on
+// the ranking key fall to the lower token id, which is the lower token rank).
 struct RowBuf {
-  int* rid;      // [kMaxK] token ids in list order
-  double* rb;    // [kMaxK] base values
-  int* rrank;    // [kMaxK] rank of rid[c] among the row's ids
-  int* rinv;     // [kMaxK] list position of the id with a given rank
+  const int* rid;      // [k] token ids in list order
+  const double* rb;    // [k] base values
+  const int* rrank;    // [k] rank of rid[c] among the row's ids
+  const int* rinv;     // [k] list position of the id with a given rank
 };
-
-__device__ __forceinline__ void load_row(const TreeArgs& A, int b, int j, const RowBuf& R) {
-  const int k = A.k;
-  const int tid = threadIdx.x;
-  if (tid < k) {
-    R.rid[tid] = A.ids[((size_t)b * A.d + j) * k + tid];
-    R.rb[tid] = A.base[((size_t)b * A.d + j) * k + tid];
-  }
-}
-// ranks by token id; needs the ids visible (call after a barrier)
-__device__ __forceinline__ void rank_row(int k, const RowBuf& R) {
-  const int tid = threadIdx.x;
-  if (tid < k) {
-    const int t = R.rid[tid];
-    int r = 0;
-    for (int c = 0; c < k; ++c) r += R.rid[c] < t;
-    R.rrank[tid] = r;
-    R.rinv[r] = tid;
-  }
-}
 
 // One CTA per tree.  A frontier node carries Z (sum of its candidates' base
 // values) and G (sum of its n-gram terms); a child's ranking key is
 // Z * invT + lam * G, accumulated in double exactly as the oracle does it, so
 // equal keys (ties the inputs hold exactly) stay equal.  The reported score
 // subtracts the rows' offsets (their log-sum-exp), which every node of one
-// depth shares.  After the survivors of a depth are sorted, each thread
-// decodes its child's parent straight from the sorted list, writes that
-// node's outputs and frontier state, and scores the child (one probe), so a
-// depth costs one scoring phase, one sort and the merge levels.
+// depth shares.  All d candidate rows are read once at the start.  A depth
+// then selects its W best children -- by ranking (each child counts the keys
+// that beat it) when there are at most kRankMax, else by sorting runs and
+// merging them -- and each thread decodes one survivor's child straight from
+// the selected list, writes that node's outputs and frontier state, and scores
+// the child (one probe).
 template <int R>
 __global__ void __launch_bounds__(kTreeThreads)
 tree_kernel(const TreeArgs A) {
@@ -189,8 +172,9 @@ tree_kernel(const TreeArgs A) {
   const int warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
   const int b = blockIdx.x;
-  const int k = A.k, W = A.W, N = A.N, MW = A.MW, n = A.n;
+  const int k = A.k, W = A.W, N = A.N, MW = A.MW, n = A.n, d = A.d;
   const int npad_max = tree_pad(W, k);
+  const int dk = d * k;
 
   // carve shared memory (8-byte members first); every size is a multiple of 16
   uint8_t* p = smem_raw;
@@ -199,30 +183,36 @@ tree_kernel(const TreeArgs A) {
   double* fZ_b = reinterpret_cast<double*>(take(kMaxW * sizeof(double)));
   double* fG_a = reinterpret_cast<double*>(take(kMaxW * sizeof(double)));
   double* fG_b = reinterpret_cast<double*>(take(kMaxW * sizeof(double)));
-  RowBuf row0, row1;
-  row0.rb = reinterpret_cast<double*>(take(kMaxK * sizeof(double)));
-  row1.rb = reinterpret_cast<double*>(take(kMaxK * sizeof(double)));
+  double* rows_b = reinterpret_cast<double*>(take(size_t(dk) * sizeof(double)));
+  double* offs = reinterpret_cast<double*>(take(size_t(d) * sizeof(double)));
   uint64_t* ks_a = reinterpret_cast<uint64_t*>(take(size_t(npad_max) * 8));
   uint64_t* ks_b = reinterpret_cast<uint64_t*>(take(size_t(npad_max) * 8));
   double* cG_a = reinterpret_cast<double*>(take(size_t(npad_max) * 8));
   double* cG_b = reinterpret_cast<double*>(take(size_t(npad_max) * 8));
+  uint64_t* sel_s = reinterpret_cast<uint64_t*>(take(kMaxW * sizeof(uint64_t)));
   uint32_t* kt_a = reinterpret_cast<uint32_t*>(take(size_t(npad_max) * 4));
   uint32_t* kt_b = reinterpret_cast<uint32_t*>(take(size_t(npad_max) * 4));
+  uint32_t* sel_t = reinterpret_cast<uint32_t*>(take(kMaxW * sizeof(uint32_t)));
   int* fnode_a = reinterpret_cast<int*>(take(kMaxW * sizeof(int)));
   int* fnode_b = reinterpret_cast<int*>(take(kMaxW * sizeof(int)));
   int* fctx_a = reinterpret_cast<int*>(take(kMaxW * 3 * sizeof(int)));
   int* fctx_b = reinterpret_cast<int*>(take(kMaxW * 3 * sizeof(int)));
   uint32_t* fmask_a = reinterpret_cast<uint32_t*>(take(size_t(kMaxW) * MW * 4));
   uint32_t* fmask_b = reinterpret_cast<uint32_t*>(take(size_t(kMaxW) * MW * 4));
-  row0.rid = reinterpret_cast<int*>(take(kMaxK * sizeof(int)));
-  row0.rrank = reinterpret_cast<int*>(take(kMaxK * sizeof(int)));
-  row0.rinv = reinterpret_cast<int*>(take(kMaxK * sizeof(int)));
-  row1.rid = reinterpret_cast<int*>(take(kMaxK * sizeof(int)));
-  row1.rrank = reinterpret_cast<int*>(take(kMaxK * sizeof(int)));
-  row1.rinv = reinterpret_cast<int*>(take(kMaxK * sizeof(int)));
+  int* rows_id = reinterpret_cast<int*>(take(size_t(dk) * sizeof(int)));
+  int* rows_rank = reinterpret_cast<int*>(take(size_t(dk) * sizeof(int)));
+  int* rows_inv = reinterpret_cast<int*>(take(size_t(dk) * sizeof(int)));
+  auto row = [&](int j) {
+    RowBuf r;
+    r.rid = rows_id + j * k;
+    r.rb = rows_b + j * k;
+    r.rrank = rows_rank + j * k;
+    r.rinv = rows_inv + j * k;
+    return r;
+  };
 
   const uint4* slots = static_cast<const uint4*>(A.slots);
-  const unsigned long long cmask = A.capacity - 1;
+  const unsigned long long nbuckets = A.capacity / 4;
   const int nctx = n > 1 ? n - 1 : 0;
   const double invT = A.invT, lam = A.lam;
 
@@ -237,38 +227,52 @@ tree_kernel(const TreeArgs A) {
       else if (nctx == 2) t[2] = tok;
       else t[3] = tok;
       float g = 0.f;
-      const double gg = probe(slots, cmask, pack_ngram(t, n), &g) ? double(g) : A.beta;
+      const double gg = probe(slots, nbuckets, pack_ngram(t, n), &g) ? double(g) : A.beta;
       G = __dadd_rn(G, gg);
     }
     *Gout = G;
     return __dadd_rn(__dmul_rn(Z, invT), __dmul_rn(lam, G));
   };
 
-  // ---- depth 1: the root's children
-  load_row(A, b, 0, row0);
-  if (A.d > 1) load_row(A, b, 1, row1);
-  __syncthreads();
-  rank_row(k, row0);
-  if (A.d > 1) rank_row(k, row1);
+  // ---- every row's candidates and offset, then their token ranks
+  const size_t row0 = (size_t)b * dk;
+  for (int e = tid; e < dk; e += blockDim.x) {
+    rows_id[e] = A.ids[row0 + e];
+    rows_b[e] = A.base[row0 + e];
+  }
+  for (int j = tid; j < d; j += blockDim.x) offs[j] = A.off ? A.off[(size_t)b * d + j] : 0.0;
   int rootctx[3] = {0, 0, 0};
 #pragma unroll
   for (int f = 0; f < 3; ++f)
     if (f < nctx) rootctx[f] = A.ctx[(size_t)b * nctx + f];
   __syncthreads();
+  for (int e = tid; e < dk; e += blockDim.x) {
+    const int j = e / k, c = e - j * k;
+    const int* ids = rows_id + j * k;
+    const int t = ids[c];
+    int r = 0;
+    for (int c2 = 0; c2 < k; ++c2) r += ids[c2] < t;
+    rows_rank[e] = r;
+    rows_inv[j * k + r] = c;
+  }
+  __syncthreads();
+
+  // ---- depth 1: the root's children
   uint64_t* keys = ks_a;     // unsorted keys of the current depth
   uint32_t* ties = kt_a;
   double* cG = cG_a;         // G of each current candidate
   {
+    const RowBuf R0 = row(0);
     const int npad = (k + RUN - 1) / RUN * RUN;
     for (int q = tid; q < npad; q += blockDim.x) {
       uint64_t ks = 0;
       uint32_t kt = 0;
       if (q < k) {
         double G;
-        const double key = child(0.0, 0.0, rootctx[0], rootctx[1], rootctx[2], row0, q, &G);
+        const double key = child(0.0, 0.0, rootctx[0], rootctx[1], rootctx[2], R0, q, &G);
         cG[q] = G;
         ks = ord_f64(key);
-        kt = kTieMax - uint32_t(row0.rrank[q]);             // parent rank 0
+        kt = kTieMax - uint32_t(R0.rrank[q]);             // parent rank 0
       }
       keys[q] = ks;
       ties[q] = kt;
@@ -295,76 +299,117 @@ tree_kernel(const TreeArgs A) {
   double Lsum = 0.0;   // sum of the row offsets down to this depth (same in every thread)
   __syncthreads();
 
-  for (int j = 0; j < A.d; ++j) {
-    const RowBuf Rc = (j & 1) ? row1 : row0;   // row j: candidates of the children sorted now
-    const RowBuf Rn = (j & 1) ? row0 : row1;   // row j+1: candidates of the next depth
-    if (A.off) Lsum = __dadd_rn(Lsum, A.off[(size_t)b * A.d + j]);
+  for (int j = 0; j < d; ++j) {
+    const RowBuf Rc = row(j);                      // row j: candidates of the children selected now
+    const RowBuf Rn = row(j + 1 < d ? j + 1 : j);  // row j+1: candidates of the next depth
+    Lsum = __dadd_rn(Lsum, offs[j]);
     const int m = nf * k;
-    const int npad = (m + RUN - 1) / RUN * RUN;
-    // sort runs of RUN keys, one warp per run
-    int nr = npad / RUN;
-    for (int run = warp; run < nr; run += nwarps) {
-      CKey v[R];
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int e = run * RUN + r * 32 + lane;
-        v[r].s = keys[e];
-        v[r].t = ties[e];
-      }
-      run_sort<R>(v);
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int e = run * RUN + r * 32 + lane;
-        keys[e] = v[r].s;
-        ties[e] = v[r].t;
-      }
-    }
-    __syncthreads();
-    // merge runs pairwise, keeping the best RUN keys of each pair
-    uint64_t* ks_src = keys;
-    uint32_t* kt_src = ties;
-    uint64_t* ks_dst = (keys == ks_a) ? ks_b : ks_a;
-    uint32_t* kt_dst = (ties == kt_a) ? kt_b : kt_a;
-    while (nr > 1) {
-      const int nout = (nr + 1) >> 1;
-      for (int t = warp; t < nout; t += nwarps) {
-        CKey v[R];
-        if (2 * t + 1 < nr) {
-#pragma unroll
-          for (int r = 0; r < R; ++r) {
-            const int e = r * 32 + lane;
-            CKey x, y;
-            x.s = ks_src[(2 * t) * RUN + e];
-            x.t = kt_src[(2 * t) * RUN + e];
-            y.s = ks_src[(2 * t + 1) * RUN + (RUN - 1 - e)];
-            y.t = kt_src[(2 * t + 1) * RUN + (RUN - 1 - e)];
-            v[r] = ck_gt(y, x) ? y : x;
-          }
-          run_merge_desc<R>(v);
-        } else {
-#pragma unroll
-          for (int r = 0; r < R; ++r) {
-            const int e = r * 32 + lane;
-            v[r].s = ks_src[(2 * t) * RUN + e];
-            v[r].t = kt_src[(2 * t) * RUN + e];
-          }
+    const int nsel = m < W ? m : W;
+    const uint64_t* src_s;     // the nsel survivors, best first
+    const uint32_t* src_t;
+    uint64_t* ks_dst;          // keys of the next depth go here
+    uint32_t* kt_dst;
+    if (m <= kRankMax) {
+      // rank: the number of keys better than mine (keys are distinct)
+      if (tid < m) {
+        const uint64_t sq = keys[tid];
+        const uint32_t tq = ties[tid];
+        int rank = 0;
+        // eight keys per step from 16-byte loads; the zero padding up to a
+        // multiple of 32 never beats a real key
+        const ulonglong2* k2 = reinterpret_cast<const ulonglong2*>(keys);
+        const uint4* t4 = reinterpret_cast<const uint4*>(ties);
+        for (int q = 0; q < m; q += 8) {
+          const ulonglong2 a0 = k2[(q >> 1) + 0], a1 = k2[(q >> 1) + 1];
+          const ulonglong2 a2 = k2[(q >> 1) + 2], a3 = k2[(q >> 1) + 3];
+          const uint4 b0 = t4[(q >> 2) + 0], b1 = t4[(q >> 2) + 1];
+          rank += (a0.x > sq || (a0.x == sq && b0.x > tq)) ? 1 : 0;
+          rank += (a0.y > sq || (a0.y == sq && b0.y > tq)) ? 1 : 0;
+          rank += (a1.x > sq || (a1.x == sq && b0.z > tq)) ? 1 : 0;
+          rank += (a1.y > sq || (a1.y == sq && b0.w > tq)) ? 1 : 0;
+          rank += (a2.x > sq || (a2.x == sq && b1.x > tq)) ? 1 : 0;
+          rank += (a2.y > sq || (a2.y == sq && b1.y > tq)) ? 1 : 0;
+          rank += (a3.x > sq || (a3.x == sq && b1.z > tq)) ? 1 : 0;
+          rank += (a3.y > sq || (a3.y == sq && b1.w > tq)) ? 1 : 0;
         }
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const int e = r * 32 + lane;
-          ks_dst[t * RUN + e] = v[r].s;
-          kt_dst[t * RUN + e] = v[r].t;
+        if (rank < nsel) {
+          sel_s[rank] = sq;
+          sel_t[rank] = tq;
         }
       }
       __syncthreads();
-      uint64_t* ts = ks_src; ks_src = ks_dst; ks_dst = ts;
-      uint32_t* tt = kt_src; kt_src = kt_dst; kt_dst = tt;
-      nr = nout;
+      src_s = sel_s;
+      src_t = sel_t;
+      ks_dst = (keys == ks_a) ? ks_b : ks_a;
+      kt_dst = (ties == kt_a) ? kt_b : kt_a;
+    } else {
+      const int npad = (m + RUN - 1) / RUN * RUN;
+      // sort runs of RUN keys, one warp per run
+      int nr = npad / RUN;
+      for (int run = warp; run < nr; run += nwarps) {
+        CKey v[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const int e = run * RUN + r * 32 + lane;
+          v[r].s = keys[e];
+          v[r].t = ties[e];
+        }
+        run_sort<R>(v);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const int e = run * RUN + r * 32 + lane;
+          keys[e] = v[r].s;
+          ties[e] = v[r].t;
+        }
+      }
+      __syncthreads();
+      // merge runs pairwise, keeping the best RUN keys of each pair
+      uint64_t* ks_src = keys;
+      uint32_t* kt_src = ties;
+      ks_dst = (keys == ks_a) ? ks_b : ks_a;
+      kt_dst = (ties == kt_a) ? kt_b : kt_a;
+      while (nr > 1) {
+        const int nout = (nr + 1) >> 1;
+        for (int t = warp; t < nout; t += nwarps) {
+          CKey v[R];
+          if (2 * t + 1 < nr) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              const int e = r * 32 + lane;
+              CKey x, y;
+              x.s = ks_src[(2 * t) * RUN + e];
+              x.t = kt_src[(2 * t) * RUN + e];
+              y.s = ks_src[(2 * t + 1) * RUN + (RUN - 1 - e)];
+              y.t = kt_src[(2 * t + 1) * RUN + (RUN - 1 - e)];
+              v[r] = ck_gt(y, x) ? y : x;
+            }
+            run_merge_desc<R>(v);
+          } else {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              const int e = r * 32 + lane;
+              v[r].s = ks_src[(2 * t) * RUN + e];
+              v[r].t = kt_src[(2 * t) * RUN + e];
+            }
+          }
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const int e = r * 32 + lane;
+            ks_dst[t * RUN + e] = v[r].s;
+            kt_dst[t * RUN + e] = v[r].t;
+          }
+        }
+        __syncthreads();
+        uint64_t* ts = ks_src; ks_src = ks_dst; ks_dst = ts;
+        uint32_t* tt = kt_src; kt_src = kt_dst; kt_dst = tt;
+        nr = nout;
+      }
+      src_s = ks_src;
+      src_t = kt_src;
     }
-    // survivors of depth j+1 are ks_src[0..nsel); decode each one, emit it and
+    // survivors of depth j+1 are src[0..nsel); decode each one, emit it and
     // (unless this is the last depth) score its k children of row j+1
-    const int nsel = m < W ? m : W;
-    const bool last = (j + 1 == A.d);
+    const bool last = (j + 1 == d);
     const int kk = last ? 1 : k;
     const int m2 = nsel * kk;
     const int npad2 = last ? m2 : (m2 + RUN - 1) / RUN * RUN;
@@ -375,8 +420,8 @@ tree_kernel(const TreeArgs A) {
       if (q < m2) {
         const int x = q / kk;             // survivor rank = node index within the depth
         const int c2 = q - x * kk;        // its child column in row j+1
-        const uint64_t ks = ks_src[x];
-        const uint32_t tie = kTieMax - kt_src[x];
+        const uint64_t ks = src_s[x];
+        const uint32_t tie = kTieMax - src_t[x];
         int i = int(tie >> 5);
         int c = (i < nf) ? Rc.rinv[tie & 31u] : 0;
         if (ks == 0 || i >= nf) {
@@ -431,13 +476,6 @@ tree_kernel(const TreeArgs A) {
       }
     }
     if (last) break;
-    __syncthreads();
-    // row j+2 goes into row j's buffer, now free
-    if (j + 2 < A.d) {
-      load_row(A, b, j + 2, Rc);
-      __syncthreads();
-      rank_row(k, Rc);
-    }
     keys = ks_dst;
     ties = kt_dst;
     cG = cG_next;
@@ -454,7 +492,7 @@ tree_kernel(const TreeArgs A) {
 
 cudaError_t launch_tree(const TreeArgs& a, cudaStream_t stream) {
   if (a.B == 0) return cudaSuccess;
-  const size_t smem = tree_smem_bytes(a.W, a.k, a.MW);
+  const size_t smem = tree_smem_bytes(a.d, a.W, a.k, a.MW);
   const int threads = tree_threads(a.W, a.k);
   cudaError_t e;
   if (a.W <= 32) {
@@ -503,7 +541,7 @@ cudaError_t launch_mask_pack(const int32_t* parents, int B, int N, uint32_t* out
 }
 
 // ----------------------------------------------------- n-gram batch lookup
-__global__ void ngram_lookup_kernel(const uint4* __restrict__ slots, unsigned long long mask, int n,
+__global__ void ngram_lookup_kernel(const uint4* __restrict__ slots, unsigned long long nb, int n,
                                     const int32_t* __restrict__ keys, long long Q,
                                     float* __restrict__ vals, int32_t* __restrict__ found) {
   const long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -513,7 +551,7 @@ __global__ void ngram_lookup_kernel(const uint4* __restrict__ slots, unsigned lo
   for (int f = 0; f < 4; ++f)
     if (f < n) t[f] = keys[q * n + f];
   float v = 0.f;
-  const bool hit = probe(slots, mask, pack_ngram(t, n), &v);
+  const bool hit = probe(slots, nb, pack_ngram(t, n), &v);
   vals[q] = hit ? v : 0.f;
   found[q] = hit ? 1 : 0;
 }
@@ -525,7 +563,7 @@ cudaError_t launch_ngram_lookup(const void* slots, unsigned long long capacity, 
   const int threads = 256;
   const long long blocks = (Q + threads - 1) / threads;
   ngram_lookup_kernel<<<unsigned(blocks), threads, 0, stream>>>(
-      static_cast<const uint4*>(slots), capacity - 1, n, keys, Q, vals, found);
+      static_cast<const uint4*>(slots), capacity / 4, n, keys, Q, vals, found);
   return cudaGetLastError();
 }
 

@@ -62,7 +62,7 @@ enum {
   DART_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
   DART_ERR_INTERNAL = 5,      /* a kernel reported an inconsistency */
   DART_ERR_TIMEOUT = 6,       /* a bounded device wait ran out */
-  DART_ERR_TABLE_FULL = 7     /* n-gram packing: no free slot (load over 1/2) */
+  DART_ERR_TABLE_FULL = 7     /* n-gram packing: load over 1/2, or no slot after displacements */
 };
 
 /* Bits of the device error word (see dart_device_error). */
@@ -73,19 +73,23 @@ enum {
   DART_DEVERR_PARENT = 1u << 3         /* dart_mask_pack: a parent index was not below its child */
 };
 
-/* An n-gram model in device memory: open addressing, linear probing.
- * Each slot is 16 bytes {uint32 key[3]; float logprob}.  A key packs the n
- * tokens (t_0 = oldest context token ... t_{n-1} = the predicted token) as
- * 24-bit fields, t_f at bits [24f, 24f+24) of the 96-bit value key[0] |
+/* An n-gram model in device memory: a two-choice bucketed hash table.
+ * Each slot is 16 bytes {uint32 key[3]; float logprob}; four consecutive slots
+ * form a 64-byte bucket, and the table holds capacity / 4 buckets.  A key packs
+ * the n tokens (t_0 = oldest context token ... t_{n-1} = the predicted token)
+ * as 24-bit fields, t_f at bits [24f, 24f+24) of the 96-bit value key[0] |
  * key[1] << 32 | key[2] << 64, unused fields zero.  An empty slot holds
- * 0xFFFFFFFF in all three key words.  The home slot of a key is
+ * 0xFFFFFFFF in all three key words.  With h =
  * splitmix64-finalizer((key[0] | key[1] << 32) ^ (key[2] * 0x9E3779B97F4A7C15))
- * & (capacity - 1).  Build the slots with dart_ngram_table_pack_host. */
+ * and nb = capacity / 4, a key lives in bucket b1 = h & (nb - 1) or bucket
+ * b2 = (h >> 32) & (nb - 1), where b2 = b1 ^ 1 when the two coincide; a lookup
+ * reads both buckets (128 bytes) at once, so it always takes one memory round
+ * trip.  Build the slots with dart_ngram_table_pack_host. */
 typedef struct {
   int32_t n;            /* order, 2..4 */
   int32_t reserved;     /* must be 0 */
-  uint64_t capacity;    /* number of slots, a power of two >= 2 */
-  const void* slots;    /* device, capacity * 16 bytes, 16-byte aligned */
+  uint64_t capacity;    /* number of slots, a power of two >= 8 */
+  const void* slots;    /* device, capacity * 16 bytes, 64-byte aligned */
 } dart_ngram_table_t;
 
 /* N = sum over j = 1..d of min(W, k^j): nodes per tree (the root excluded).
@@ -194,15 +198,20 @@ int dart_row_topk(const void* logits, int rows, int V, int dtype, float T, int k
 int dart_mask_pack(const int32_t* parents, int B, int N, uint32_t* out_mask,
                    uint32_t* device_err, void* stream);
 
-/* Smallest power of two >= 2 * M (load factor at most 1/2); 0 on overflow. */
+/* Smallest power of two >= max(2 * M, 8) (load factor at most 1/2); 0 on
+ * overflow. */
 uint64_t dart_ngram_capacity_for(uint64_t M);
 
 /* Build the slots of an n-gram table on the host.
  *  keys host int32 [M][n] (t_0 oldest ... t_{n-1} predicted), each in
- *  [0, 2^24-1); vals host float [M]; host_slots host, capacity * 16 bytes.
+ *  [0, 2^24-1); vals host float [M]; host_slots host, capacity * 16 bytes;
+ *  capacity a power of two >= 8.
  * A repeated key keeps its first value; *out_distinct (may be NULL)
- * receives the number of distinct keys stored.  Returns DART_ERR_TABLE_FULL
- * if more than capacity / 2 distinct keys arrive. */
+ * receives the number of distinct keys stored.  Keys whose two buckets are
+ * full move earlier keys to their other bucket (cuckoo displacement, a fixed
+ * deterministic order).  Returns DART_ERR_TABLE_FULL if more than
+ * capacity / 2 distinct keys arrive, or if 500 displacements do not free a
+ * slot (the slots are then unusable). */
 int dart_ngram_table_pack_host(int n, const int32_t* keys, const float* vals, uint64_t M,
                                uint64_t capacity, void* host_slots, uint64_t* out_distinct);
 

@@ -60,7 +60,8 @@ def test_sizes(L):
     assert L.dart_tree_workspace_bytes(64, 8, 151936, 2, 33) == 0
     assert L.dart_ngram_capacity_for(4096) == 8192
     assert L.dart_ngram_capacity_for(5000) == 16384
-    assert L.dart_ngram_capacity_for(0) == 2
+    assert L.dart_ngram_capacity_for(0) == 8
+    assert L.dart_ngram_capacity_for(3) == 8
 
 
 FAKE = 0x10000000          # 16- and 256-byte aligned, never dereferenced
@@ -99,7 +100,8 @@ def _table(n=3, cap=1024, slots=FAKE, reserved=0):
 
 @pytest.mark.parametrize("tab,ctx,code", [
     (dict(n=1), FAKE, INVALID), (dict(n=5), FAKE, INVALID), (dict(cap=1000), FAKE, INVALID),
-    (dict(cap=1), FAKE, INVALID), (dict(slots=0), FAKE, INVALID), (dict(slots=FAKE + 4), FAKE, INVALID),
+    (dict(cap=1), FAKE, INVALID), (dict(cap=4), FAKE, INVALID), (dict(slots=0), FAKE, INVALID),
+    (dict(slots=FAKE + 4), FAKE, INVALID), (dict(slots=FAKE + 16), FAKE, INVALID),
     (dict(reserved=1), FAKE, INVALID), (dict(), 0, INVALID),
 ])
 def test_table_argument_checks(L, tab, ctx, code):
@@ -127,7 +129,7 @@ def test_other_entry_points_check_arguments(L):
 # ------------------------------------------------------------ host packer
 
 def _splitmix_fold(w0, w1, w2):
-    """The home-slot hash as the header describes it (splitmix64 output function)."""
+    """The key hash as the header describes it (splitmix64 output function)."""
     M64 = (1 << 64) - 1
     x = (w0 | (w1 << 32)) ^ ((w2 * 0x9E3779B97F4A7C15) & M64)
     x ^= x >> 30
@@ -145,16 +147,21 @@ def _key_words(tokens):
     return v & 0xFFFFFFFF, (v >> 32) & 0xFFFFFFFF, (v >> 64) & 0xFFFFFFFF
 
 
+def _buckets(w, cap):
+    """The key's two 4-slot buckets, as the header describes them."""
+    h = _splitmix_fold(*w)
+    nb = cap // 4
+    b1, b2 = h & (nb - 1), (h >> 32) & (nb - 1)
+    return b1, (b1 ^ 1 if b2 == b1 else b2)
+
+
 def _find(slots, cap, tokens):
     w = _key_words(tokens)
-    idx = _splitmix_fold(*w) & (cap - 1)
-    for _ in range(cap):
-        s = slots[idx]
-        if tuple(int(x) for x in s[:3]) == w:
-            return True, s[3:4].view(np.float32)[0]
-        if (s[:3] == 0xFFFFFFFF).all():
-            return False, None
-        idx = (idx + 1) & (cap - 1)
+    for b in _buckets(w, cap):
+        for t in range(4):
+            s = slots[4 * b + t]
+            if tuple(int(x) for x in s[:3]) == w:
+                return True, s[3:4].view(np.float32)[0]
     return False, None
 
 
@@ -181,6 +188,31 @@ def test_packer_against_documented_format(L, n):
     for key in rng.integers(0, 1 << 20, size=(500, n)).tolist():
         if tuple(key) not in first:
             assert not _find(slots, cap, key)[0]
+    # every other slot is empty
+    assert int((slots[:, :3] != 0xFFFFFFFF).any(axis=1).sum()) == len(first)
+
+
+def test_packer_at_half_load_displaces_and_keeps_every_key(L):
+    """capacity / 2 distinct keys: some keys find both buckets full and move
+    earlier keys to their other bucket; every key must stay findable."""
+    rng = np.random.default_rng(11)
+    cap = 4096
+    M = cap // 2
+    keys = rng.choice((1 << 24) - 1, size=(M, 3), replace=True).astype(np.int32)
+    keys[:, 0] = np.arange(M)                                    # distinct keys
+    vals = rng.uniform(-9, -1, size=M).astype(np.float32)
+    slots = np.zeros((cap, 4), dtype=np.uint32)
+    distinct = C.c_uint64(0)
+    rc = L.dart_ngram_table_pack_host(3, keys.ctypes.data_as(C.c_void_p), vals.ctypes.data_as(C.c_void_p),
+                                      M, cap, slots.ctypes.data_as(C.c_void_p), C.byref(distinct))
+    assert rc == OK and distinct.value == M
+    home = sum(1 for key in keys.tolist()
+               if any(tuple(int(x) for x in slots[4 * _buckets(_key_words(key), cap)[0] + t][:3])
+                      == _key_words(key) for t in range(4)))
+    assert home < M                                              # some keys sit in their second bucket
+    for key, v in zip(keys.tolist(), vals):
+        ok, got = _find(slots, cap, key)
+        assert ok and got == v
 
 
 def test_packer_refuses_overfull_and_bad_tokens(L):
@@ -196,3 +228,4 @@ def test_packer_refuses_overfull_and_bad_tokens(L):
     bad[2, 1] = -5
     assert L.dart_ngram_table_pack_host(2, P(bad), P(vals), 4, 8, P(slots), None) == INVALID
     assert L.dart_ngram_table_pack_host(2, P(keys), P(vals), 4, 6, P(slots), None) == INVALID
+    assert L.dart_ngram_table_pack_host(2, P(keys), P(vals), 2, 4, P(slots), None) == INVALID   # below 8 slots

@@ -92,24 +92,33 @@ __device__ __forceinline__ void run_merge_desc(CKey (&v)[R]) {
 }
 
 // A lookup reads the key's two buckets (eight slots, 128 bytes) at once: one
-// memory round trip whether the key is present or not.
-__device__ __forceinline__ bool probe(const uint4* slots, unsigned long long nb, Key96 key, float* val) {
+// memory round trip whether the key is present or not.  probe_issue starts
+// the loads; probe_match, called once the caller has done other work,
+// compares.
+struct Probe { uint4 s[8]; };
+__device__ __forceinline__ void probe_issue(const uint4* slots, unsigned long long nb, Key96 key, Probe& pr) {
   const Buckets bk = key_buckets(key, nb);
-  uint4 s[8];
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
-    s[t] = ldg_nc_v4(slots + 4 * bk.b1 + t);
-    s[4 + t] = ldg_nc_v4(slots + 4 * bk.b2 + t);
+    pr.s[t] = ldg_nc_v4(slots + 4 * bk.b1 + t);
+    pr.s[4 + t] = ldg_nc_v4(slots + 4 * bk.b2 + t);
   }
+}
+__device__ __forceinline__ bool probe_match(const Probe& pr, Key96 key, float* val) {
   bool hit = false;
 #pragma unroll
   for (int t = 0; t < 8; ++t) {
-    if (s[t].x == key.w0 && s[t].y == key.w1 && s[t].z == key.w2) {
-      *val = __uint_as_float(s[t].w);
+    if (pr.s[t].x == key.w0 && pr.s[t].y == key.w1 && pr.s[t].z == key.w2) {
+      *val = __uint_as_float(pr.s[t].w);
       hit = true;
     }
   }
   return hit;
+}
+__device__ __forceinline__ bool probe(const uint4* slots, unsigned long long nb, Key96 key, float* val) {
+  Probe pr;
+  probe_issue(slots, nb, key, pr);
+  return probe_match(pr, key, val);
 }
 
 __host__ __device__ inline int tree_run_len(int W) { return W <= 32 ? 32 : 64; }
@@ -119,7 +128,7 @@ __host__ __device__ inline int tree_pad(int W, int k) {
 }
 // Threads per tree: one per child of a full frontier, 32..512.
 inline int tree_threads(int W, int k) {
-  int t = (W * k + 31) / 32 * 32;
+  const int t = (W * k + 31) / 32 * 32;
   return t < 32 ? 32 : (t > kTreeThreads ? kTreeThreads : t);
 }
 constexpr int kRankMax = 256;   // up to this many children a depth selects by ranking
@@ -431,8 +440,6 @@ tree_kernel(const TreeArgs A) {
         }
         const int tok = Rc.rid[c];
         const int node = node_base + x;
-        const double Zp = __dadd_rn(fZ_cur[i], Rc.rb[c]);
-        const double Gp = cG[i * k + c];
         int ctx[3] = {0, 0, 0};
 #pragma unroll
         for (int f = 0; f + 1 < 3; ++f)
@@ -442,6 +449,20 @@ tree_kernel(const TreeArgs A) {
           else if (nctx == 2) ctx[1] = tok;
           else ctx[2] = tok;
         }
+        // start the lookup of child (x, c2) before the rest of the work
+        Probe pr;
+        Key96 ckey{0u, 0u, 0u};
+        if (!last && n > 0) {
+          const int ctok = Rn.rid[c2];
+          int32_t t[4] = {ctx[0], ctx[1], ctx[2], 0};
+          if (nctx == 1) t[1] = ctok;
+          else if (nctx == 2) t[2] = ctok;
+          else t[3] = ctok;
+          ckey = pack_ngram(t, n);
+          probe_issue(slots, nbuckets, ckey, pr);
+        }
+        const double Zp = __dadd_rn(fZ_cur[i], Rc.rb[c]);
+        const double Gp = cG[i * k + c];
         // ancestor-mask words of the node, spread over its k child threads
         for (int w = c2; w < MW; w += kk) {
           uint32_t val = (j == 0) ? 0u : fmask_cur[i * MW + w];
@@ -463,10 +484,15 @@ tree_kernel(const TreeArgs A) {
             if (f < nctx) fctx_nxt[x * 3 + f] = ctx[f];
         }
         if (!last) {
-          double G;
-          const double key = child(Zp, Gp, ctx[0], ctx[1], ctx[2], Rn, c2, &G);
+          // key of child (x, c2): (Zp + base) * invT + lam * (Gp + g), as in child()
+          const double ZinvT = __dmul_rn(__dadd_rn(Zp, Rn.rb[c2]), invT);
+          double G = Gp;
+          if (n > 0) {
+            float g = 0.f;
+            G = __dadd_rn(G, probe_match(pr, ckey, &g) ? double(g) : A.beta);
+          }
           cG_next[q] = G;
-          ks2 = ord_f64(key);
+          ks2 = ord_f64(__dadd_rn(ZinvT, __dmul_rn(lam, G)));
           kt2 = kTieMax - ((uint32_t(x) << 5) | uint32_t(Rn.rrank[c2]));
         }
       }

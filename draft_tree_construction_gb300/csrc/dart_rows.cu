@@ -39,7 +39,8 @@
 //
 // Every wait is bounded: on a timeout the kernel raises a flag in shared
 // memory that ends all other waits of the CTA, records the error bit and
-// returns.
+// returns.  Keys enter the ring in per-warp blocks reserved (and waited for)
+// before any lane writes, so a reserved slot is always written promptly.
 #include "dart_common.cuh"
 
 #include <cfloat>
@@ -58,6 +59,9 @@ constexpr int kMergerWarp = kConsumers + 1;
 constexpr int kRowThreads = (kConsumers + 2) * 32;
 static_assert(kVecPerLane == 4, "reduce_full reduces exactly four vectors per lane");
 static_assert((kRingKeys & (kRingKeys - 1)) == 0, "ring index masking");
+// one warp reserves at most 32 lanes x 8 keys, and the merger takes at most
+// 32 slots past its head: both fit, so the oldest reservation always proceeds
+static_assert(kRingKeys >= 32 * 8 + 32, "key ring too small for one warp's reservation");
 
 struct RowsParams {
   const uint8_t* logits;
@@ -70,8 +74,6 @@ struct RowsParams {
   unsigned long long span;    // bytes per CTA, multiple of 16
   int grid;
   int nsub;                   // 2 KiB steps per consumer warp and stage (1 or 2)
-  int nst;                    // stages in the ring (kMaxStages / nsub)
-  uint32_t stage_bytes;       // kConsumers * nsub * kSlice
   int pmax, pstride;
   uint32_t* ctrl;
   uint32_t* row_cnt;
@@ -190,7 +192,8 @@ __device__ __forceinline__ void raise_abort(RowSmem& S, uint32_t* ctrl) {
 __device__ __noinline__ bool wait_phase_spin(RowSmem& S, uint64_t* bar, uint32_t parity, long long limit,
                                              uint32_t* ctrl) {
   const long long t0 = clock64();
-  while (!mbar_try_wait_hint(bar, parity, kSleepNs)) {
+  for (uint32_t it = 1; !mbar_try_wait_hint(bar, parity, kSleepNs); ++it) {
+    if ((it & 63u) != 0u) continue;   // the clock and the abort flag every 64 probes
     if (aborted(S)) return false;
     if (clock64() - t0 > limit) {
       raise_abort(S, ctrl);
@@ -228,39 +231,68 @@ __device__ __noinline__ void ring_wait(const KeyRing kr, uint32_t pos) {
     }
   }
 }
-// Appends one key at reserved position `pos`, waiting while the ring is full.
-__device__ __forceinline__ void ring_put(const KeyRing& kr, uint32_t pos, uint64_t key) {
-  if (pos - *kr.head >= uint32_t(kRingKeys)) ring_wait(kr, pos);
+// Reserves ring positions for `cnt` keys of each lane (at most 8) as one
+// block for the whole warp and waits, warp-uniformly and before any lane
+// writes, until the ring has room for all of them.  Every reserved slot is
+// then written without waiting, so the merger, which takes slots in order,
+// never waits on a slot whose writer waits on the merger.  Returns false
+// (nothing reserved) when no lane has a key; *pos is the lane's first slot.
+__device__ __forceinline__ bool warp_reserve(const KeyRing& kr, uint32_t cnt, uint32_t* pos) {
+  const int lane = threadIdx.x & 31;
+  uint32_t incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  if (total == 0u) return false;
+  uint32_t base = 0;
+  if (lane == 0) {
+    base = atomicAdd(kr.tail, total);
+    if (base + total - 1u - *kr.head >= uint32_t(kRingKeys)) ring_wait(kr, base + total - 1u);
+  }
+  base = __shfl_sync(0xFFFFFFFFu, base, 0);
+  *pos = base + incl - cnt;
+  return true;
+}
+__device__ __forceinline__ void ring_store(const KeyRing& kr, uint32_t pos, uint64_t key) {
   kr.keys[pos & uint32_t(kRingKeys - 1)] = key;
 }
 
-// Appends the elements >= tau of this lane's vectors of a slice (vectors
-// lane, lane + 32, ... below nvec).
+// Appends the elements >= tau of the slice's vectors 0..nvec-1 (lane l
+// holds vectors l, l + 32, ...).
 template <int DT>
 __device__ __noinline__ void push_hits(const uint4* src, int nvec, uint32_t id_base, float tau, const KeyRing kr) {
   using E = Elem<DT>;
   constexpr int EPV = E::kPerVec;
   const int lane = threadIdx.x & 31;
 #pragma unroll 1
-  for (int v = lane; v < nvec; v += 32) {
-    {
-      const uint4 r = src[v];
+  for (int v0 = 0; v0 < nvec; v0 += 32) {
+    const int v = v0 + lane;
+    uint4 r = make_uint4(0u, 0u, 0u, 0u);
+    uint32_t em = 0;
+    if (v < nvec) {
+      r = src[v];
       if (E::vmax(r) >= tau) {
-        uint32_t em = 0;
 #pragma unroll
         for (int p = 0; p < EPV / 2; ++p) {
           const float2 z = E::pair(r, p);
           em |= (z.x >= tau ? 1u : 0u) << (2 * p);
           em |= (z.y >= tau ? 1u : 0u) << (2 * p + 1);
         }
-        uint32_t pos = atomicAdd(kr.tail, uint32_t(__popc(em)));
-        const uint32_t id0 = id_base + uint32_t(v * EPV);
+      }
+    }
+    if (__ballot_sync(0xFFFFFFFFu, em != 0u) == 0u) continue;
+    uint32_t pos;
+    if (!warp_reserve(kr, uint32_t(__popc(em)), &pos)) continue;
+    if (em) {
+      const uint32_t id0 = id_base + uint32_t(v * EPV);
 #pragma unroll
-        for (int p = 0; p < EPV / 2; ++p) {
-          const float2 z = E::pair(r, p);
-          if ((em >> (2 * p)) & 1u) ring_put(kr, pos++, elem_key(z.x, id0 + 2 * p));
-          if ((em >> (2 * p + 1)) & 1u) ring_put(kr, pos++, elem_key(z.y, id0 + 2 * p + 1));
-        }
+      for (int p = 0; p < EPV / 2; ++p) {
+        const float2 z = E::pair(r, p);
+        if ((em >> (2 * p)) & 1u) ring_store(kr, pos++, elem_key(z.x, id0 + 2 * p));
+        if ((em >> (2 * p + 1)) & 1u) ring_store(kr, pos++, elem_key(z.y, id0 + 2 * p + 1));
       }
     }
   }
@@ -309,8 +341,12 @@ __device__ __noinline__ uint32_t seed_stage(const uint4* src, int nvec, RowSmem*
 }
 
 // Per-warp state for one row segment.
+// A lane's sum s is kept against mc = fl(m c) rather than m c: each term is
+// 2^fma(z, c, -mc), one fused multiply-add per element.  Since m c - mc is
+// exact in float (fma(m, c, -mc)), the row end turns s back into the sum of
+// 2^((z - m) c).
 struct RowCtx {
-  float m, s;            // per lane: running max of z and sum of 2^((z - m) c)
+  float m, mc, s;        // per lane: running max of z, fl(m c), sum of 2^(z c - mc)
   uint32_t tau_ord;      // ordered form of the filter threshold (0 = none yet)
   float tau;             // filter threshold value (-inf = none yet)
   uint32_t* tau_slot;    // the row's shared threshold
@@ -327,6 +363,23 @@ __device__ __forceinline__ void refresh_tau(RowCtx& rc) {
   raise_tau(rc, *reinterpret_cast<volatile uint32_t*>(rc.tau_slot));
 }
 
+// fl(m c), kept finite (-FLT_MAX before the first element) so that
+// fma(-inf, c, -mc) stays -inf.
+__device__ __forceinline__ float scaled_max(float m, float c) { return fmaxf(m * c, -FLT_MAX); }
+// Raises the lane's running max to v (if larger), rescaling its sum.
+__device__ __forceinline__ void raise_max(float& m, float& mc, float& s, float v, float c) {
+  if (v > m) {
+    const float mcn = scaled_max(v, c);
+    s *= ex2_approx(mc - mcn);
+    m = v;
+    mc = mcn;
+  }
+}
+// s against exact m c: s * 2^-(m c - mc).  0 stays 0.
+__device__ __forceinline__ float exact_sum(float m, float mc, float s, float c) {
+  return s > 0.f ? s * ex2_approx(-fmaf(m, c, -mc)) : 0.f;
+}
+
 // The hot path: one full 2 KiB slice (four vectors per lane).  Updates the
 // lane's (max, sum) and returns whether any element can pass tau.
 template <int DT>
@@ -338,13 +391,9 @@ __device__ __forceinline__ bool reduce_full(RowCtx& rc, const uint4* src, float 
   uint4 raw[U];
 #pragma unroll
   for (int u = 0; u < U; ++u) raw[u] = src[u * 32 + lane];
-  refresh_tau(rc);
   const float vm = E::vmax4(raw);
-  if (vm > rc.m) {
-    rc.s *= ex2_approx((rc.m - vm) * c);
-    rc.m = vm;
-  }
-  const float2 nm2 = make_float2(-rc.m, -rc.m);
+  raise_max(rc.m, rc.mc, rc.s, vm, c);
+  const float2 nmc2 = make_float2(-rc.mc, -rc.mc);
   const float2 c2 = make_float2(c, c);
   float2 acc[U];
 #pragma unroll
@@ -352,7 +401,7 @@ __device__ __forceinline__ bool reduce_full(RowCtx& rc, const uint4* src, float 
     acc[u] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int p = 0; p < EPV / 2; ++p) {
-      const float2 t = __fmul2_rn(__fadd2_rn(E::pair(raw[u], p), nm2), c2);
+      const float2 t = __ffma2_rn(E::pair(raw[u], p), c2, nmc2);
       acc[u] = __fadd2_rn(acc[u], make_float2(ex2_approx(t.x), ex2_approx(t.y)));
     }
   }
@@ -368,23 +417,19 @@ __device__ __noinline__ float2 reduce_partial(const uint4* src, int nvec, uint32
   using E = Elem<DT>;
   constexpr int EPV = E::kPerVec;
   const int lane = threadIdx.x & 31;
+  float mc = scaled_max(m, c);
   bool hit = false;
 #pragma unroll 1
   for (int v = lane; v < nvec; v += 32) {
-    {
-      const uint4 r = src[v];
-      const float vm = E::vmax(r);
-      if (vm > m) {
-        s *= ex2_approx((m - vm) * c);
-        m = vm;
-      }
+    const uint4 r = src[v];
+    const float vm = E::vmax(r);
+    raise_max(m, mc, s, vm, c);
 #pragma unroll
-      for (int p = 0; p < EPV / 2; ++p) {
-        const float2 z = E::pair(r, p);
-        s += ex2_approx((z.x - m) * c) + ex2_approx((z.y - m) * c);
-      }
-      hit = hit || vm >= tau;
+    for (int p = 0; p < EPV / 2; ++p) {
+      const float2 z = E::pair(r, p);
+      s += ex2_approx(fmaf(z.x, c, -mc)) + ex2_approx(fmaf(z.y, c, -mc));
     }
+    hit = hit || vm >= tau;
   }
   if (__ballot_sync(0xFFFFFFFFu, hit) != 0u) push_hits<DT>(src, nvec, id_base, tau, kr);
   return make_float2(m, s);
@@ -399,15 +444,17 @@ __device__ __noinline__ float2 reduce_scalars(const uint8_t* logits, unsigned lo
   const int cnt = int((b1 - b0) / es);
   for (int base = 0; base < cnt; base += 32) {
     const int i = base + lane;
+    bool hit = false;
+    float z = 0.f;
     if (i < cnt) {
-      const float z = Elem<DT>::scalar(logits + b0 + (unsigned long long)i * es);
-      if (z > m) {
-        s *= ex2_approx((m - z) * c);
-        m = z;
-      }
-      s += ex2_approx((z - m) * c);
-      if (z >= tau) ring_put(kr, atomicAdd(kr.tail, 1u), elem_key(z, id0 + uint32_t(i)));
+      z = Elem<DT>::scalar(logits + b0 + (unsigned long long)i * es);
+      float mc = scaled_max(m, c);
+      raise_max(m, mc, s, z, c);
+      s += ex2_approx(fmaf(z, c, -mc));
+      hit = z >= tau;
     }
+    uint32_t pos;
+    if (warp_reserve(kr, hit ? 1u : 0u, &pos) && hit) ring_store(kr, pos, elem_key(z, id0 + uint32_t(i)));
   }
   __syncwarp();
   return make_float2(m, s);
@@ -579,7 +626,7 @@ __device__ __forceinline__ void merge_span_rows(const RowsParams& P, RowSmem& S,
         continue;
       }
       if (done) break;
-      __nanosleep(256);
+      __nanosleep(1000);   // an idle merger must not take issue slots from the consumers
       if (__any_sync(0xFFFFFFFFu, aborted(S))) return;
       if (__any_sync(0xFFFFFFFFu, clock64() - t0 > P.wait_limit)) {
         raise_abort(S, P.ctrl);
@@ -635,10 +682,12 @@ __device__ __forceinline__ void merge_span_rows(const RowsParams& P, RowSmem& S,
 }
 
 // -------------------------------------------------------------------- kernel
-template <int DT>
+template <int DT, int NSUB>
 __global__ void __launch_bounds__(kRowThreads, 1)
 row_stream_kernel(const RowsParams P) {
   constexpr int SH = Elem<DT>::kShift;
+  constexpr uint32_t SB = uint32_t(kConsumers * NSUB * kSlice);   // stage bytes
+  constexpr int NST = kMaxStages / NSUB;                          // stages in the ring
   extern __shared__ __align__(128) uint8_t smem_raw[];
   RowSmem& S = *reinterpret_cast<RowSmem*>(smem_raw);
   const int lane = threadIdx.x & 31;
@@ -679,24 +728,22 @@ row_stream_kernel(const RowsParams P) {
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      const int nst = P.nst;
       int slot = 0;
       uint32_t round = 0;   // fills of `slot` so far
       int issued = 0;
       bool ok = true;
       for (long long r = r_first; r <= r_last && ok; ++r) {
         const Seg g = segment(P, e0, e1, r);
-        for (unsigned long long off = g.a; off < g.b; off += P.stage_bytes) {
+        for (unsigned long long off = g.a; off < g.b; off += SB) {
           if (round > 0 && !wait_phase(S, &S.empty[slot], (round - 1) & 1u, P.wait_limit, P.ctrl)) {
             ok = false;
             break;
           }
-          const uint32_t bytes = uint32_t((g.b - off) < (unsigned long long)P.stage_bytes ? (g.b - off) : P.stage_bytes);
-          uint8_t* dst = S.ring + size_t(slot) * P.stage_bytes;
+          const uint32_t bytes = uint32_t((g.b - off) < (unsigned long long)SB ? (g.b - off) : SB);
           mbar_expect_tx(&S.full[slot], bytes);
-          bulk_g2s(dst, P.logits + off, bytes, &S.full[slot], pol);
+          bulk_g2s(S.ring + size_t(slot) * SB, P.logits + off, bytes, &S.full[slot], pol);
           ++issued;
-          if (++slot == nst) {
+          if (++slot == NST) {
             slot = 0;
             ++round;
           }
@@ -704,9 +751,9 @@ row_stream_kernel(const RowsParams P) {
       }
       // the CTA may not retire while a copy still writes its shared memory;
       // these waits are bounded by the clock alone
-      for (int j = 0; j < nst && j < issued; ++j) {
+      for (int j = 0; j < NST && j < issued; ++j) {
         // the last fill of each slot used so far
-        const int sl = (slot + nst - 1 - j) % nst;
+        const int sl = (slot + NST - 1 - j) % NST;
         const uint32_t rd = (sl < slot) ? round : round - 1;
         if (!mbar_wait_bounded(&S.full[sl], rd & 1u, P.wait_limit)) {
           set_dev_error(P.ctrl, DART_DEVERR_WAIT_TIMEOUT);
@@ -739,6 +786,7 @@ row_stream_kernel(const RowsParams P) {
     const unsigned long long rs = (unsigned long long)r * P.V;
     RowCtx rc;
     rc.m = -FLT_MAX;
+    rc.mc = scaled_max(rc.m, P.c);
     rc.s = 0.f;
     rc.tau_ord = 0u;
     rc.tau = -INFINITY;
@@ -759,21 +807,20 @@ row_stream_kernel(const RowsParams P) {
         refresh_tau(rc);
         const float2 ms = reduce_scalars<DT>(P.logits, hb0, hb1, P.es, uint32_t(g.s0 - rs), P.c, rc.m, rc.s, rc.tau, kr);
         rc.m = ms.x;
+        rc.mc = scaled_max(rc.m, P.c);
         rc.s = ms.y;
       }
     }
     // aligned interior: this warp's slice of every stage
     const uint32_t ilen = uint32_t(g.b - g.a);
     const uint32_t id_a = uint32_t((g.a >> SH) - rs);
-    const uint32_t s0 = uint32_t(w) * uint32_t(P.nsub * kSlice);
-    for (uint32_t o = 0; o < ilen; o += P.stage_bytes) {
-      const uint32_t rem = ilen - o;
-      const uint32_t bytes = rem < P.stage_bytes ? rem : P.stage_bytes;
+    constexpr uint32_t kMine = uint32_t(NSUB * kSlice);   // bytes of a full stage per warp
+    const uint32_t s0 = uint32_t(w) * kMine;
+    for (uint32_t o = 0; o < ilen; o += SB) {
       if (!__all_sync(0xFFFFFFFFu, wait_phase(S, &S.full[slot], round & 1u, lim, P.ctrl))) return;
-      const uint8_t* stage = S.ring + size_t(slot) * P.stage_bytes;
-      const int nvec = s0 < bytes ? int(min(bytes - s0, uint32_t(P.nsub * kSlice)) / 16) : 0;
-      const uint4* src = reinterpret_cast<const uint4*>(stage + s0);
-      const uint32_t id_base = id_a + ((o + s0) >> SH);
+      const uint4* src = reinterpret_cast<const uint4*>(S.ring + size_t(slot) * SB + s0);
+      const uint32_t rem = ilen - o;
+      const int nvec = s0 < rem ? int(min(rem - s0, kMine) / 16) : 0;
       if (o == 0) {
         const uint32_t kth = seed_stage<DT>(src, nvec, &S, nseed, w, P.k, lim, P.ctrl);
         if (__any_sync(0xFFFFFFFFu, aborted(S))) return;
@@ -781,20 +828,23 @@ row_stream_kernel(const RowsParams P) {
         if (lane == 0 && kth != 0u) atomicMax(rc.tau_slot, kth);
         ++nseed;
       }
-      if (nvec == P.nsub * (kSlice / 16)) {
-        for (int j = 0; j < P.nsub; ++j) {
+      refresh_tau(rc);
+      if (rem >= SB) {
+#pragma unroll
+        for (int j = 0; j < NSUB; ++j) {
           const uint4* sj = src + j * (kSlice / 16);
-          if (reduce_full<DT>(rc, sj, P.c)) push_hits<DT>(sj, kSlice / 16, id_base + uint32_t(j * (kSlice >> SH)), rc.tau, kr);
+          if (reduce_full<DT>(rc, sj, P.c))
+            push_hits<DT>(sj, kSlice / 16, id_a + ((o + s0 + uint32_t(j * kSlice)) >> SH), rc.tau, kr);
         }
       } else if (nvec > 0) {
-        refresh_tau(rc);
-        const float2 ms = reduce_partial<DT>(src, nvec, id_base, P.c, rc.m, rc.s, rc.tau, kr);
+        const float2 ms = reduce_partial<DT>(src, nvec, id_a + ((o + s0) >> SH), P.c, rc.m, rc.s, rc.tau, kr);
         rc.m = ms.x;
+        rc.mc = scaled_max(rc.m, P.c);
         rc.s = ms.y;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[slot]);
-      if (++slot == P.nst) {
+      if (++slot == NST) {
         slot = 0;
         ++round;
       }
@@ -805,10 +855,11 @@ row_stream_kernel(const RowsParams P) {
       const float2 ms = reduce_scalars<DT>(P.logits, g.b, g.s1 * P.es, P.es, uint32_t((g.b >> SH) - rs), P.c, rc.m,
                                            rc.s, rc.tau, kr);
       rc.m = ms.x;
+      rc.mc = scaled_max(rc.m, P.c);
       rc.s = ms.y;
     }
     // the warp's (max, sum) of the row
-    float m = rc.m, s = rc.s;
+    float m = rc.m, s = exact_sum(rc.m, rc.mc, rc.s, P.c);
 #pragma unroll
     for (int o2 = 16; o2 > 0; o2 >>= 1) {
       const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o2);
@@ -851,8 +902,6 @@ cudaError_t launch_rows(const void* logits, long long R, int V, int dtype, float
   // than about five of those take 24 KiB stages (less idle tail per row)
   const unsigned long long row_bytes = (unsigned long long)V * (unsigned long long)es;
   P.nsub = row_bytes >= 262144ull ? 2 : 1;
-  P.nst = kMaxStages / P.nsub;
-  P.stage_bytes = uint32_t(kConsumers * P.nsub * kSlice);
   P.pmax = L.pmax;
   P.pstride = L.pstride;
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -869,19 +918,18 @@ cudaError_t launch_rows(const void* logits, long long R, int V, int dtype, float
   if (P.total == 0) return cudaSuccess;
   const size_t smem = rows_smem_bytes();
   cudaError_t e = cudaSuccess;
-  switch (dtype) {
-    case DART_F32:
-      e = cudaFuncSetAttribute(row_stream_kernel<DART_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-      if (e == cudaSuccess) row_stream_kernel<DART_F32><<<P.grid, kRowThreads, smem, stream>>>(P);
-      break;
-    case DART_F16:
-      e = cudaFuncSetAttribute(row_stream_kernel<DART_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-      if (e == cudaSuccess) row_stream_kernel<DART_F16><<<P.grid, kRowThreads, smem, stream>>>(P);
-      break;
-    default:
-      e = cudaFuncSetAttribute(row_stream_kernel<DART_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-      if (e == cudaSuccess) row_stream_kernel<DART_BF16><<<P.grid, kRowThreads, smem, stream>>>(P);
-      break;
+  auto go = [&](auto kernel) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e == cudaSuccess) kernel<<<P.grid, kRowThreads, smem, stream>>>(P);
+  };
+  if (P.nsub == 2) {
+    if (dtype == DART_F32) go(row_stream_kernel<DART_F32, 2>);
+    else if (dtype == DART_F16) go(row_stream_kernel<DART_F16, 2>);
+    else go(row_stream_kernel<DART_BF16, 2>);
+  } else {
+    if (dtype == DART_F32) go(row_stream_kernel<DART_F32, 1>);
+    else if (dtype == DART_F16) go(row_stream_kernel<DART_F16, 1>);
+    else go(row_stream_kernel<DART_BF16, 1>);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

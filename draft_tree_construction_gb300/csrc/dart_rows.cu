@@ -57,7 +57,7 @@ constexpr int kRingKeys = 512;                  // key ring per row slot (power 
 constexpr uint32_t kSleepNs = 100000;           // longest sleep of one barrier probe
 constexpr int kMergerWarp = kConsumers + 1;
 constexpr int kRowThreads = (kConsumers + 2) * 32;
-static_assert(kVecPerLane == 4, "reduce_full reduces exactly four vectors per lane");
+static_assert(kVecPerLane == 4, "reduce_slice reduces exactly four vectors per lane");
 static_assert((kRingKeys & (kRingKeys - 1)) == 0, "ring index masking");
 // one warp reserves at most 32 lanes x 8 keys, and the merger takes at most
 // 32 slots past its head: both fit, so the oldest reservation always proceeds
@@ -180,8 +180,6 @@ template <> struct Elem<DART_F16> {
 };
 
 // ------------------------------------------------------------ bounded waits
-// Rarely taken paths are kept out of line (__noinline__) so that the
-// per-slice loop stays small in the instruction cache.
 __device__ __forceinline__ bool aborted(const RowSmem& S) {
   return *reinterpret_cast<const volatile uint32_t*>(&S.abort) != 0u;
 }
@@ -189,7 +187,7 @@ __device__ __forceinline__ void raise_abort(RowSmem& S, uint32_t* ctrl) {
   *reinterpret_cast<volatile uint32_t*>(&S.abort) = 1u;
   set_dev_error(ctrl, DART_DEVERR_WAIT_TIMEOUT);
 }
-__device__ __noinline__ bool wait_phase_spin(RowSmem& S, uint64_t* bar, uint32_t parity, long long limit,
+__device__ __forceinline__ bool wait_phase_spin(RowSmem& S, uint64_t* bar, uint32_t parity, long long limit,
                                              uint32_t* ctrl) {
   const long long t0 = clock64();
   for (uint32_t it = 1; !mbar_try_wait_hint(bar, parity, kSleepNs); ++it) {
@@ -221,7 +219,7 @@ struct KeyRing {
   long long limit;
 };
 
-__device__ __noinline__ void ring_wait(const KeyRing kr, uint32_t pos) {
+__device__ __forceinline__ void ring_wait(const KeyRing kr, uint32_t pos) {
   const long long t0 = clock64();
   while (pos - *kr.head >= uint32_t(kRingKeys)) {
     if (aborted(*kr.S)) return;
@@ -263,7 +261,7 @@ __device__ __forceinline__ void ring_store(const KeyRing& kr, uint32_t pos, uint
 // Appends the elements >= tau of the slice's vectors 0..nvec-1 (lane l
 // holds vectors l, l + 32, ...).
 template <int DT>
-__device__ __noinline__ void push_hits(const uint4* src, int nvec, uint32_t id_base, float tau, const KeyRing kr) {
+__device__ __forceinline__ void push_hits(const uint4* src, int nvec, uint32_t id_base, float tau, const KeyRing kr) {
   using E = Elem<DT>;
   constexpr int EPV = E::kPerVec;
   const int lane = threadIdx.x & 31;
@@ -321,7 +319,7 @@ __device__ __forceinline__ uint32_t warp_sort_desc_u32(uint32_t v) {
 // columns cover disjoint elements, so k distinct elements are at least that
 // large.  Returns the bound in ordered form (0 = none or a wait gave up).
 template <int DT>
-__device__ __noinline__ uint32_t seed_stage(const uint4* src, int nvec, RowSmem* Sp, int nseed, int w, int k,
+__device__ __forceinline__ uint32_t seed_stage(const uint4* src, int nvec, RowSmem* Sp, int nseed, int w, int k,
                                             long long limit, uint32_t* ctrl) {
   using E = Elem<DT>;
   RowSmem& S = *Sp;
@@ -380,17 +378,22 @@ __device__ __forceinline__ float exact_sum(float m, float mc, float s, float c) 
   return s > 0.f ? s * ex2_approx(-fmaf(m, c, -mc)) : 0.f;
 }
 
-// The hot path: one full 2 KiB slice (four vectors per lane).  Updates the
-// lane's (max, sum) and returns whether any element can pass tau.
-template <int DT>
-__device__ __forceinline__ bool reduce_full(RowCtx& rc, const uint4* src, float c) {
+// The hot path: one 2 KiB slice (four vectors per lane; a partial slice at
+// the end of a row holds nvec < 128 vectors, the rest read as -inf, whose
+// terms are exactly 0).  Updates the lane's (max, sum) and returns whether any
+// element can pass tau.
+template <int DT, bool FULL>
+__device__ __forceinline__ bool reduce_slice(RowCtx& rc, const uint4* src, int nvec, float c) {
   using E = Elem<DT>;
   constexpr int EPV = E::kPerVec;
   constexpr int U = kVecPerLane;
   const int lane = threadIdx.x & 31;
   uint4 raw[U];
 #pragma unroll
-  for (int u = 0; u < U; ++u) raw[u] = src[u * 32 + lane];
+  for (int u = 0; u < U; ++u) {
+    if (FULL) raw[u] = src[u * 32 + lane];
+    else raw[u] = (u * 32 + lane < nvec) ? src[u * 32 + lane] : E::neg_inf();
+  }
   const float vm = E::vmax4(raw);
   raise_max(rc.m, rc.mc, rc.s, vm, c);
   const float2 nmc2 = make_float2(-rc.mc, -rc.mc);
@@ -407,32 +410,24 @@ __device__ __forceinline__ bool reduce_full(RowCtx& rc, const uint4* src, float 
   }
   const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
   rc.s += a.x + a.y;
-  return __ballot_sync(0xFFFFFFFFu, vm >= rc.tau) != 0u;
+  // absent vectors hold -inf, which must not pass while tau is still -inf
+  const bool lane_hit = (FULL || lane < nvec) && vm >= rc.tau;
+  return __ballot_sync(0xFFFFFFFFu, lane_hit) != 0u;
 }
 
-// A slice shorter than 2 KiB (the end of a row): (max, sum) in, (max, sum) out.
-template <int DT>
-__device__ __noinline__ float2 reduce_partial(const uint4* src, int nvec, uint32_t id_base, float c, float m, float s,
-                                              float tau, const KeyRing kr) {
-  using E = Elem<DT>;
-  constexpr int EPV = E::kPerVec;
-  const int lane = threadIdx.x & 31;
-  float mc = scaled_max(m, c);
-  bool hit = false;
+// The end of a row: up to NSUB partial-or-full 2 KiB steps of nvec vectors.
+template <int DT, int NSUB>
+__device__ __forceinline__ void reduce_tail_stage(RowCtx* rcp, const uint4* src, int nvec, uint32_t id_base, int SH,
+                                               float c, const KeyRing kr) {
+  RowCtx rc = *rcp;
 #pragma unroll 1
-  for (int v = lane; v < nvec; v += 32) {
-    const uint4 r = src[v];
-    const float vm = E::vmax(r);
-    raise_max(m, mc, s, vm, c);
-#pragma unroll
-    for (int p = 0; p < EPV / 2; ++p) {
-      const float2 z = E::pair(r, p);
-      s += ex2_approx(fmaf(z.x, c, -mc)) + ex2_approx(fmaf(z.y, c, -mc));
-    }
-    hit = hit || vm >= tau;
+  for (int j = 0; j < NSUB; ++j) {
+    const int nv = min(nvec - j * (kSlice / 16), kSlice / 16);
+    if (nv <= 0) break;
+    const uint4* sj = src + j * (kSlice / 16);
+    if (reduce_slice<DT, false>(rc, sj, nv, c)) push_hits<DT>(sj, nv, id_base + uint32_t((j * kSlice) >> SH), rc.tau, kr);
   }
-  if (__ballot_sync(0xFFFFFFFFu, hit) != 0u) push_hits<DT>(src, nvec, id_base, tau, kr);
-  return make_float2(m, s);
+  *rcp = rc;
 }
 
 // Unaligned elements [b0, b1) of a segment (its head or tail), one per lane.
@@ -833,14 +828,11 @@ row_stream_kernel(const RowsParams P) {
 #pragma unroll
         for (int j = 0; j < NSUB; ++j) {
           const uint4* sj = src + j * (kSlice / 16);
-          if (reduce_full<DT>(rc, sj, P.c))
+          if (reduce_slice<DT, true>(rc, sj, kSlice / 16, P.c))
             push_hits<DT>(sj, kSlice / 16, id_a + ((o + s0 + uint32_t(j * kSlice)) >> SH), rc.tau, kr);
         }
       } else if (nvec > 0) {
-        const float2 ms = reduce_partial<DT>(src, nvec, id_a + ((o + s0) >> SH), P.c, rc.m, rc.s, rc.tau, kr);
-        rc.m = ms.x;
-        rc.mc = scaled_max(rc.m, P.c);
-        rc.s = ms.y;
+        reduce_tail_stage<DT, NSUB>(&rc, src, nvec, id_a + ((o + s0) >> SH), SH, P.c, kr);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[slot]);

@@ -18,6 +18,7 @@ on the data path); the step time is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -49,7 +50,7 @@ def workload_name(i: int) -> str:
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--config", type=int, default=DEFAULT_CONFIG)
     p.add_argument("--seed", type=int, default=0)
@@ -98,23 +99,39 @@ def max_over_ranks(x: float, world: int) -> float:
 
 # ----------------------------------------------------------------- clocks
 
-CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+CLOCK_QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
 def clocks_start(gpu_index: int):
+    """Starts nvidia-smi sampling every 20 ms; waits (up to 3 s) for its first line."""
     try:
         f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         p = subprocess.Popen(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={CLOCK_QUERY}",
-                              "--format=csv,noheader,nounits", "-lms", "100"],
+                              "--format=csv,noheader,nounits", "-lms", "20"],
                              stdout=f, stderr=subprocess.DEVNULL)
-        return p, f.name
     except (OSError, FileNotFoundError):
         return None, None
+    t0 = time.time()
+    while time.time() - t0 < 3.0 and os.path.getsize(f.name) == 0:
+        time.sleep(0.02)
+    return p, f.name
 
 
-def clocks_stop(handle):
+def _stamp(text: str):
+    for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+        try:
+            return datetime.datetime.strptime(text, fmt).timestamp()
+        except ValueError:
+            pass
+    return None
+
+
+def clocks_stop(handle, window):
+    """Median SM clock and throttle reasons of the samples inside `window`
+    (wall-clock start, end of the timed regions); if none fall inside it, of
+    every sample since warm-up, and the result says so."""
     p, path = handle
     if p is None:
         return None
@@ -123,25 +140,25 @@ def clocks_stop(handle):
         p.wait(timeout=5)
     except subprocess.TimeoutExpired:
         p.kill()
-    sm, mx, reasons = [], [], set()
+    rows = []
     names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
     for line in open(path):
         parts = [x.strip() for x in line.split(",")]
-        if len(parts) < 9:
+        if len(parts) < 10:
             continue
         try:
-            sm.append(float(parts[1]))
-            mx.append(float(parts[2]))
+            rows.append((_stamp(parts[0]), float(parts[2]), float(parts[3]),
+                         {n for n, v in zip(names, parts[6:10]) if v.lower() == "active"}))
         except ValueError:
             continue
-        for name, v in zip(names, parts[5:9]):
-            if v.lower() == "active":
-                reasons.add(name)
     os.unlink(path)
-    if not sm:
+    inside = [r for r in rows if r[0] is not None and window[0] - 0.02 <= r[0] <= window[1] + 0.02]
+    used, where = (inside, "timed region") if inside else (rows, "warm-up through timed region")
+    if not used:
         return None
-    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-            "samples": len(sm)}
+    reasons = set().union(*[r[3] for r in used])
+    return {"sm_mhz": statistics.median(r[1] for r in used), "sm_max_mhz": max(r[2] for r in used),
+            "reasons": sorted(reasons), "samples": len(used), "window": where}
 
 
 # ------------------------------------------------------------ measured peaks
@@ -284,16 +301,17 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         return [a.elapsed_time(b) for a, b in evs]
 
+    clk = clocks_start(dev.index or 0)
     for _ in range(max(3, args.warmup)):
         flush()
         builder(z)
     torch.cuda.synchronize(dev)
     assert D.device_error(builder.ws) == 0, "device error during warm-up"
 
-    clk = clocks_start(dev.index or 0)
     # ---- timed region: whole steps (memset + streaming kernel + tree kernel)
     barrier(world)
     torch.cuda.synchronize(dev)
+    t_timed = time.time()
     step_times = timed(lambda i: builder(z), args.steps)
     barrier(world)
     step_ms = max_over_ranks(statistics.mean(step_times), world)
@@ -310,7 +328,7 @@ def run_ours(args):
 
     k1_times = timed(rows_only, args.steps)
     k1_ms = max_over_ranks(statistics.mean(k1_times), world)
-    clocks = clocks_stop(clk)
+    clocks = clocks_stop(clk, (t_timed, time.time()))
 
     # ---- end to end: pinned host logits in, pinned host outputs back, every step
     e2e = None
@@ -356,7 +374,7 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": value, "unit": "trees/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32/f64",
             "data": "synthetic",
             "config": {"workload": workload_name(args.config), "logit_dtype": case.dtype,
                        "trees_per_gpu": B, "logit_bytes_per_step": logit_bytes,

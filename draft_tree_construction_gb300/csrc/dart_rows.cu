@@ -22,13 +22,14 @@
 // Top-k.  Candidates are 64-bit keys (ordered value, then inverted id), so a
 // larger key is a better candidate and equal values fall back to the lower id.
 // An element can only matter if it is >= tau, a lower bound of the row's k-th
-// value.  Consumer warps keep no lists: they append the rare qualifying
-// elements to a per-row key ring in shared memory.  A merger warp drains the
-// ring into the CTA's best-32 list of the row and publishes the list's k-th
-// value as the row's tau, so every consumer filters against the k-th best
-// element the whole CTA has seen so far.  The first slice of a row is filtered
-// against the k-th largest of the warp's 32 lane maxima (k distinct elements
-// are at least that large).
+// value.  At a row's first stage every consumer lane posts the maximum of its
+// elements and tau starts at the k-th largest of the 32 column maxima (twelve
+// warps' lane j): disjoint elements, so k of them are at least that large.
+// Consumer warps keep no lists: they append the rare 16-byte vectors whose
+// maximum reaches tau (straight from registers, with their first element id)
+// to a per-row ring in shared memory.  A merger warp expands them into keys,
+// keeps the CTA's best 32 of the row and publishes the list's k-th value as
+// the row's tau.
 //
 // Row end.  Each consumer warp leaves its (max, scaled sum) in a shared slot
 // and moves on; the merger combines them with the list.  A row inside one
@@ -39,8 +40,8 @@
 //
 // Every wait is bounded: on a timeout the kernel raises a flag in shared
 // memory that ends all other waits of the CTA, records the error bit and
-// returns.  Keys enter the ring in per-warp blocks reserved (and waited for)
-// before any lane writes, so a reserved slot is always written promptly.
+// returns.  Vectors enter the ring in per-warp blocks reserved (and waited
+// for) before any lane writes, so a reserved entry is always written promptly.
 #include "dart_common.cuh"
 
 #include <cfloat>
@@ -53,15 +54,15 @@ constexpr int kRingBytes = 196608;              // 192 KiB of stages in flight p
 constexpr int kMaxStages = 8;                   // 8 x 24 KiB (short rows) or 4 x 48 KiB stages
 constexpr int kVecPerLane = kSlice / 16 / 32;
 constexpr int kRowSlots = 4;                    // rows in flight between the consumers and the merger
-constexpr int kRingKeys = 512;                  // key ring per row slot (power of two)
+constexpr int kRingVecs = 256;                  // candidate-vector ring per row slot (power of two)
 constexpr uint32_t kSleepNs = 100000;           // longest sleep of one barrier probe
 constexpr int kMergerWarp = kConsumers + 1;
 constexpr int kRowThreads = (kConsumers + 2) * 32;
 static_assert(kVecPerLane == 4, "reduce_slice reduces exactly four vectors per lane");
-static_assert((kRingKeys & (kRingKeys - 1)) == 0, "ring index masking");
-// one warp reserves at most 32 lanes x 8 keys, and the merger takes at most
-// 32 slots past its head: both fit, so the oldest reservation always proceeds
-static_assert(kRingKeys >= 32 * 8 + 32, "key ring too small for one warp's reservation");
+static_assert((kRingVecs & (kRingVecs - 1)) == 0, "ring index masking");
+// one warp reserves at most 32 lanes x 4 vectors, and the merger takes at most
+// 32 entries past its head: both fit, so the oldest reservation always proceeds
+static_assert(kRingVecs >= 32 * 4 + 32, "vector ring too small for one warp's reservation");
 
 struct RowsParams {
   const uint8_t* logits;
@@ -89,7 +90,8 @@ struct RowsParams {
 
 struct __align__(128) RowSmem {
   uint8_t ring[kRingBytes];
-  uint64_t keys[kRowSlots][kRingKeys];   // candidate keys of a row; 0 = slot not written yet
+  uint4 vdata[kRowSlots][kRingVecs];     // candidate vectors of a row (16 bytes of logits each)
+  uint32_t vid[kRowSlots][kRingVecs];    // (element mask << 24) | (first id + 1); 0 = not written yet
   float2 part[kRowSlots][kConsumers];    // per consumer warp: (max, sum of 2^((z - max) c))
   uint64_t full[kMaxStages];             // bytes of a stage have landed
   uint64_t empty[kMaxStages];            // every consumer warp is done with a stage
@@ -134,6 +136,8 @@ template <> struct Elem<DART_F32> {
     return fmaxf(fmaxf(vmax(r[0]), vmax(r[1])), fmaxf(vmax(r[2]), vmax(r[3])));
   }
   __device__ static float scalar(const uint8_t* p) { return __ldg(reinterpret_cast<const float*>(p)); }
+  // a vector holding z as element 0 (the rest -inf)
+  __device__ static uint4 single(float z) { return make_uint4(__float_as_uint(z), 0xFF800000u, 0xFF800000u, 0xFF800000u); }
 };
 template <> struct Elem<DART_BF16> {
   static constexpr int kPerVec = 8;
@@ -154,6 +158,9 @@ template <> struct Elem<DART_BF16> {
   __device__ static float scalar(const uint8_t* p) {
     const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(p));
     return __uint_as_float(uint32_t(h) << 16);
+  }
+  __device__ static uint4 single(float z) {   // z came from a bf16: its top half is exact
+    return make_uint4((__float_as_uint(z) >> 16) | 0xFF800000u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
   }
 };
 template <> struct Elem<DART_F16> {
@@ -176,6 +183,9 @@ template <> struct Elem<DART_F16> {
   __device__ static float scalar(const uint8_t* p) {
     const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(p));
     return __half2float(__ushort_as_half(h));
+  }
+  __device__ static uint4 single(float z) {   // z came from an f16: exact
+    return make_uint4(uint32_t(__half_as_ushort(__float2half_rn(z))) | 0xFC000000u, 0xFC00FC00u, 0xFC00FC00u, 0xFC00FC00u);
   }
 };
 
@@ -209,91 +219,87 @@ __device__ __forceinline__ bool wait_phase(RowSmem& S, uint64_t* bar, uint32_t p
 }
 
 // ----------------------------------------------------------------- consumers
-// Where a consumer warp appends candidate keys of the current row.
-struct KeyRing {
+// Where a consumer warp appends candidate vectors of the current row.
+struct VecRing {
   uint32_t* tail;                  // reservation counter
-  const volatile uint32_t* head;   // keys the merger has taken
-  volatile uint64_t* keys;         // kRingKeys slots, 0 = not written yet
+  const volatile uint32_t* head;   // entries the merger has taken
+  uint4* vdata;                    // kRingVecs entries
+  volatile uint32_t* vid;          // their (mask << 24) | (id + 1), 0 = not written yet
   RowSmem* S;
   uint32_t* ctrl;
   long long limit;
 };
 
-__device__ __forceinline__ void ring_wait(const KeyRing kr, uint32_t pos) {
+__device__ __forceinline__ void sts_v4(void* p, const uint4& v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
+               :: "r"(smem_u32(p)), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ uint4 lds_v4_volatile(const void* p) {
+  uint4 v;
+  asm volatile("ld.volatile.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void ring_wait(const VecRing& vr, uint32_t pos) {
   const long long t0 = clock64();
-  while (pos - *kr.head >= uint32_t(kRingKeys)) {
-    if (aborted(*kr.S)) return;
-    if (clock64() - t0 > kr.limit) {
-      raise_abort(*kr.S, kr.ctrl);
+  while (pos - *vr.head >= uint32_t(kRingVecs)) {
+    if (aborted(*vr.S)) return;
+    if (clock64() - t0 > vr.limit) {
+      raise_abort(*vr.S, vr.ctrl);
       return;
     }
   }
 }
-// Reserves ring positions for `cnt` keys of each lane (at most 8) as one
-// block for the whole warp and waits, warp-uniformly and before any lane
-// writes, until the ring has room for all of them.  Every reserved slot is
-// then written without waiting, so the merger, which takes slots in order,
-// never waits on a slot whose writer waits on the merger.  Returns false
-// (nothing reserved) when no lane has a key; *pos is the lane's first slot.
-__device__ __forceinline__ bool warp_reserve(const KeyRing& kr, uint32_t cnt, uint32_t* pos) {
+// Reserves ring entries for `cnt` vectors of each lane (0..4) as one block for
+// the whole warp and waits, warp-uniformly and before any lane writes, until
+// the ring has room for all of them.  Every reserved entry is then written
+// without waiting, so the merger, which takes entries in order, never waits on
+// an entry whose writer waits on the merger.  Returns false (nothing
+// reserved) when no lane has a vector; *pos is the lane's first entry.
+__device__ __forceinline__ bool warp_reserve(const VecRing& vr, uint32_t cnt, uint32_t* pos) {
   const int lane = threadIdx.x & 31;
-  uint32_t incl = cnt;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, cnt & 1u);
+  const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, cnt & 2u);
+  const uint32_t b2 = __ballot_sync(0xFFFFFFFFu, cnt & 4u);
+  const uint32_t total = uint32_t(__popc(b0) + 2 * __popc(b1) + 4 * __popc(b2));
   if (total == 0u) return false;
+  const uint32_t below = (1u << lane) - 1u;
   uint32_t base = 0;
   if (lane == 0) {
-    base = atomicAdd(kr.tail, total);
-    if (base + total - 1u - *kr.head >= uint32_t(kRingKeys)) ring_wait(kr, base + total - 1u);
+    base = atomicAdd(vr.tail, total);
+    if (base + total - 1u - *vr.head >= uint32_t(kRingVecs)) ring_wait(vr, base + total - 1u);
   }
   base = __shfl_sync(0xFFFFFFFFu, base, 0);
-  *pos = base + incl - cnt;
+  *pos = base + uint32_t(__popc(b0 & below) + 2 * __popc(b1 & below) + 4 * __popc(b2 & below));
   return true;
 }
-__device__ __forceinline__ void ring_store(const KeyRing& kr, uint32_t pos, uint64_t key) {
-  kr.keys[pos & uint32_t(kRingKeys - 1)] = key;
+// One entry: the vector first, then (after a fence) its tag, which the merger polls.
+__device__ __forceinline__ void ring_put(const VecRing& vr, uint32_t pos, const uint4& v, uint32_t tag) {
+  const uint32_t i = pos & uint32_t(kRingVecs - 1);
+  sts_v4(vr.vdata + i, v);
+  __threadfence_block();
+  vr.vid[i] = tag;
 }
 
-// Appends the elements >= tau of the slice's vectors 0..nvec-1 (lane l
-// holds vectors l, l + 32, ...).
-template <int DT>
-__device__ __forceinline__ void push_hits(const uint4* src, int nvec, uint32_t id_base, float tau, const KeyRing kr) {
+// Appends the lane's vectors of a 2 KiB step whose maximum reaches tau
+// (vector u*32 + lane holds elements id_base + (u*32 + lane) * EPV ...).
+template <int DT, bool FULL>
+__device__ __forceinline__ void push_vectors(const uint4 (&raw)[kVecPerLane], int nvec, uint32_t id_base, float tau,
+                                             const VecRing& vr) {
   using E = Elem<DT>;
   constexpr int EPV = E::kPerVec;
+  constexpr uint32_t kMask = (1u << EPV) - 1u;
   const int lane = threadIdx.x & 31;
-#pragma unroll 1
-  for (int v0 = 0; v0 < nvec; v0 += 32) {
-    const int v = v0 + lane;
-    uint4 r = make_uint4(0u, 0u, 0u, 0u);
-    uint32_t em = 0;
-    if (v < nvec) {
-      r = src[v];
-      if (E::vmax(r) >= tau) {
+  uint32_t hm = 0;
 #pragma unroll
-        for (int p = 0; p < EPV / 2; ++p) {
-          const float2 z = E::pair(r, p);
-          em |= (z.x >= tau ? 1u : 0u) << (2 * p);
-          em |= (z.y >= tau ? 1u : 0u) << (2 * p + 1);
-        }
-      }
-    }
-    if (__ballot_sync(0xFFFFFFFFu, em != 0u) == 0u) continue;
-    uint32_t pos;
-    if (!warp_reserve(kr, uint32_t(__popc(em)), &pos)) continue;
-    if (em) {
-      const uint32_t id0 = id_base + uint32_t(v * EPV);
+  for (int u = 0; u < kVecPerLane; ++u)
+    if ((FULL || u * 32 + lane < nvec) && E::vmax(raw[u]) >= tau) hm |= 1u << u;
+  uint32_t pos;
+  if (!warp_reserve(vr, uint32_t(__popc(hm)), &pos)) return;
 #pragma unroll
-      for (int p = 0; p < EPV / 2; ++p) {
-        const float2 z = E::pair(r, p);
-        if ((em >> (2 * p)) & 1u) ring_store(kr, pos++, elem_key(z.x, id0 + 2 * p));
-        if ((em >> (2 * p + 1)) & 1u) ring_store(kr, pos++, elem_key(z.y, id0 + 2 * p + 1));
-      }
-    }
-  }
+  for (int u = 0; u < kVecPerLane; ++u)
+    if ((hm >> u) & 1u) ring_put(vr, pos++, raw[u], (kMask << 24) | (id_base + uint32_t((u * 32 + lane) * EPV) + 1u));
   __syncwarp();
 }
 
@@ -380,10 +386,11 @@ __device__ __forceinline__ float exact_sum(float m, float mc, float s, float c) 
 
 // The hot path: one 2 KiB slice (four vectors per lane; a partial slice at
 // the end of a row holds nvec < 128 vectors, the rest read as -inf, whose
-// terms are exactly 0).  Updates the lane's (max, sum) and returns whether any
-// element can pass tau.
+// terms are exactly 0).  Updates the lane's (max, sum) and, when some vector
+// reaches tau, appends those vectors to the row's ring.
 template <int DT, bool FULL>
-__device__ __forceinline__ bool reduce_slice(RowCtx& rc, const uint4* src, int nvec, float c) {
+__device__ __forceinline__ void reduce_slice(RowCtx& rc, const uint4* src, int nvec, float c, uint32_t id_base,
+                                             const VecRing& vr) {
   using E = Elem<DT>;
   constexpr int EPV = E::kPerVec;
   constexpr int U = kVecPerLane;
@@ -412,20 +419,19 @@ __device__ __forceinline__ bool reduce_slice(RowCtx& rc, const uint4* src, int n
   rc.s += a.x + a.y;
   // absent vectors hold -inf, which must not pass while tau is still -inf
   const bool lane_hit = (FULL || lane < nvec) && vm >= rc.tau;
-  return __ballot_sync(0xFFFFFFFFu, lane_hit) != 0u;
+  if (__ballot_sync(0xFFFFFFFFu, lane_hit) != 0u) push_vectors<DT, FULL>(raw, nvec, id_base, rc.tau, vr);
 }
 
 // The end of a row: up to NSUB partial-or-full 2 KiB steps of nvec vectors.
 template <int DT, int NSUB>
 __device__ __forceinline__ void reduce_tail_stage(RowCtx* rcp, const uint4* src, int nvec, uint32_t id_base, int SH,
-                                               float c, const KeyRing kr) {
+                                               float c, const VecRing& vr) {
   RowCtx rc = *rcp;
 #pragma unroll 1
   for (int j = 0; j < NSUB; ++j) {
     const int nv = min(nvec - j * (kSlice / 16), kSlice / 16);
     if (nv <= 0) break;
-    const uint4* sj = src + j * (kSlice / 16);
-    if (reduce_slice<DT, false>(rc, sj, nv, c)) push_hits<DT>(sj, nv, id_base + uint32_t((j * kSlice) >> SH), rc.tau, kr);
+    reduce_slice<DT, false>(rc, src + j * (kSlice / 16), nv, c, id_base + uint32_t((j * kSlice) >> SH), vr);
   }
   *rcp = rc;
 }
@@ -434,7 +440,7 @@ __device__ __forceinline__ void reduce_tail_stage(RowCtx* rcp, const uint4* src,
 template <int DT>
 __device__ __noinline__ float2 reduce_scalars(const uint8_t* logits, unsigned long long b0, unsigned long long b1,
                                               int es, uint32_t id0, float c, float m, float s, float tau,
-                                              const KeyRing kr) {
+                                              const VecRing vr) {
   const int lane = threadIdx.x & 31;
   const int cnt = int((b1 - b0) / es);
   for (int base = 0; base < cnt; base += 32) {
@@ -449,7 +455,7 @@ __device__ __noinline__ float2 reduce_scalars(const uint8_t* logits, unsigned lo
       hit = z >= tau;
     }
     uint32_t pos;
-    if (warp_reserve(kr, hit ? 1u : 0u, &pos) && hit) ring_store(kr, pos, elem_key(z, id0 + uint32_t(i)));
+    if (warp_reserve(vr, hit ? 1u : 0u, &pos) && hit) ring_put(vr, pos, Elem<DT>::single(z), (1u << 24) | (id0 + uint32_t(i) + 1u));
   }
   __syncwarp();
   return make_float2(m, s);
@@ -575,15 +581,18 @@ __device__ __forceinline__ bool merge_keys(uint64_t& list, uint64_t key, int k) 
 // CTA's best-32 list (publishing its k-th value as the row's threshold) until
 // every consumer lane is done with the row, then combines the consumer warps'
 // (max, sum) and finishes the row or leaves the CTA's partial.
+template <int DT>
 __device__ __forceinline__ void merge_span_rows(const RowsParams& P, RowSmem& S, long long r_first,
                                                 long long r_last) {
+  using E = Elem<DT>;
+  constexpr int EPV = E::kPerVec;
   const int lane = threadIdx.x & 31;
   const int k = P.k;
   for (long long r = r_first; r <= r_last; ++r) {
     const int rowseq = int(r - r_first);
     const int rslot = rowseq % kRowSlots;
     const uint32_t parity = uint32_t(rowseq / kRowSlots) & 1u;
-    volatile uint64_t* keys = S.keys[rslot];
+    volatile uint32_t* vid = S.vid[rslot];
     uint32_t head = 0;
     uint64_t list = 0;
     long long t0 = clock64();
@@ -593,13 +602,14 @@ __device__ __forceinline__ void merge_span_rows(const RowsParams& P, RowSmem& S,
       const uint32_t tail = __shfl_sync(0xFFFFFFFFu, *reinterpret_cast<volatile uint32_t*>(&S.tail[rslot]), 0);
       if (tail != head) {
         const uint32_t n = (tail - head) < 32u ? (tail - head) : 32u;
-        uint64_t key = 0;
+        uint32_t tag = 0;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (uint32_t(lane) < n) {
-          volatile uint64_t* slot = keys + ((head + uint32_t(lane)) & uint32_t(kRingKeys - 1));
-          key = *slot;
-          if (key == 0) {
+          const uint32_t i = (head + uint32_t(lane)) & uint32_t(kRingVecs - 1);
+          tag = vid[i];
+          if (tag == 0u) {
             const long long t1 = clock64();
-            while ((key = *slot) == 0) {
+            while ((tag = vid[i]) == 0u) {
               if (aborted(S)) break;
               if (clock64() - t1 > P.wait_limit) {
                 raise_abort(S, P.ctrl);
@@ -607,13 +617,26 @@ __device__ __forceinline__ void merge_span_rows(const RowsParams& P, RowSmem& S,
               }
             }
           }
-          *slot = 0ull;
+          __threadfence_block();   // the vector was stored before its tag
+          v = lds_v4_volatile(S.vdata[rslot] + i);
+          vid[i] = 0u;
         }
         if (__any_sync(0xFFFFFFFFu, aborted(S))) return;
         head += n;
         __threadfence_block();
         if (lane == 0) *reinterpret_cast<volatile uint32_t*>(&S.head[rslot]) = head;
-        if (merge_keys(list, key, k)) {
+        // expand the vectors: element e of lane's vector is id (tag & 0xFFFFFF) - 1 + e
+        const uint32_t id0 = (tag & 0xFFFFFFu) - 1u;
+        bool changed = false;
+#pragma unroll
+        for (int p = 0; p < EPV / 2; ++p) {
+          const float2 z = E::pair(v, p);
+          const uint64_t k0 = ((tag >> (24 + 2 * p)) & 1u) ? elem_key(z.x, id0 + 2 * p) : 0ull;
+          const uint64_t k1 = ((tag >> (25 + 2 * p)) & 1u) ? elem_key(z.y, id0 + 2 * p + 1) : 0ull;
+          changed |= merge_keys(list, k0, k);
+          changed |= merge_keys(list, k1, k);
+        }
+        if (changed) {
           const uint64_t kth = __shfl_sync(0xFFFFFFFFu, list, k - 1);
           if (kth != 0 && lane == 0) atomicMax(&S.tau[rslot], uint32_t(kth >> 32));
         }
@@ -708,8 +731,8 @@ row_stream_kernel(const RowsParams P) {
     fence_mbar_init();
   }
   {
-    uint64_t* kz = &S.keys[0][0];
-    for (int i = threadIdx.x; i < kRowSlots * kRingKeys; i += blockDim.x) kz[i] = 0ull;
+    uint32_t* vz = &S.vid[0][0];
+    for (int i = threadIdx.x; i < kRowSlots * kRingVecs; i += blockDim.x) vz[i] = 0u;
     if (threadIdx.x < kRowSlots) {
       S.tail[threadIdx.x] = 0u;
       S.head[threadIdx.x] = 0u;
@@ -761,7 +784,7 @@ row_stream_kernel(const RowsParams P) {
 
   // ------------------------------------------------------------------ merger
   if (warp == kMergerWarp) {
-    merge_span_rows(P, S, r_first, r_last);
+    merge_span_rows<DT>(P, S, r_first, r_last);
     return;
   }
 
@@ -786,13 +809,14 @@ row_stream_kernel(const RowsParams P) {
     rc.tau_ord = 0u;
     rc.tau = -INFINITY;
     rc.tau_slot = &S.tau[rslot];
-    KeyRing kr;
-    kr.tail = &S.tail[rslot];
-    kr.head = &S.head[rslot];
-    kr.keys = S.keys[rslot];
-    kr.S = &S;
-    kr.ctrl = P.ctrl;
-    kr.limit = lim;
+    VecRing vr;
+    vr.tail = &S.tail[rslot];
+    vr.head = &S.head[rslot];
+    vr.vdata = S.vdata[rslot];
+    vr.vid = S.vid[rslot];
+    vr.S = &S;
+    vr.ctrl = P.ctrl;
+    vr.limit = lim;
 
     // head: [s0, a) (or the whole segment when nothing is aligned), warp 0 only
     if (w == 0) {
@@ -800,7 +824,7 @@ row_stream_kernel(const RowsParams P) {
       const unsigned long long hb1 = (g.a < g.b) ? g.a : g.s1 * P.es;
       if (hb1 > hb0) {
         refresh_tau(rc);
-        const float2 ms = reduce_scalars<DT>(P.logits, hb0, hb1, P.es, uint32_t(g.s0 - rs), P.c, rc.m, rc.s, rc.tau, kr);
+        const float2 ms = reduce_scalars<DT>(P.logits, hb0, hb1, P.es, uint32_t(g.s0 - rs), P.c, rc.m, rc.s, rc.tau, vr);
         rc.m = ms.x;
         rc.mc = scaled_max(rc.m, P.c);
         rc.s = ms.y;
@@ -828,11 +852,10 @@ row_stream_kernel(const RowsParams P) {
 #pragma unroll
         for (int j = 0; j < NSUB; ++j) {
           const uint4* sj = src + j * (kSlice / 16);
-          if (reduce_slice<DT, true>(rc, sj, kSlice / 16, P.c))
-            push_hits<DT>(sj, kSlice / 16, id_a + ((o + s0 + uint32_t(j * kSlice)) >> SH), rc.tau, kr);
+          reduce_slice<DT, true>(rc, sj, kSlice / 16, P.c, id_a + ((o + s0 + uint32_t(j * kSlice)) >> SH), vr);
         }
       } else if (nvec > 0) {
-        reduce_tail_stage<DT, NSUB>(&rc, src, nvec, id_a + ((o + s0) >> SH), SH, P.c, kr);
+        reduce_tail_stage<DT, NSUB>(&rc, src, nvec, id_a + ((o + s0) >> SH), SH, P.c, vr);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[slot]);
@@ -845,7 +868,7 @@ row_stream_kernel(const RowsParams P) {
     if (w == 0 && g.a < g.b && g.s1 * P.es > g.b) {
       refresh_tau(rc);
       const float2 ms = reduce_scalars<DT>(P.logits, g.b, g.s1 * P.es, P.es, uint32_t((g.b >> SH) - rs), P.c, rc.m,
-                                           rc.s, rc.tau, kr);
+                                           rc.s, rc.tau, vr);
       rc.m = ms.x;
       rc.mc = scaled_max(rc.m, P.c);
       rc.s = ms.y;

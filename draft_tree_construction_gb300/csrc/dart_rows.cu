@@ -100,6 +100,7 @@ struct __align__(128) RowSmem {
   uint32_t tail[kRowSlots];              // keys reserved in a row's ring
   uint32_t head[kRowSlots];              // keys the merger has taken
   uint32_t tau[kRowSlots];               // ordered form of the row's best published threshold
+  uint64_t mkeys[32 * 8];                // the merger's surviving keys of one batch
   uint32_t seed[2][kConsumers][32];      // lane maxima of a row's first stage (alternating rows)
   uint64_t seed_bar[2];                  // every consumer lane has written its lane maximum
   uint32_t abort;                        // a wait timed out: every wait gives up
@@ -625,16 +626,51 @@ __device__ __forceinline__ void merge_span_rows(const RowsParams& P, RowSmem& S,
         head += n;
         __threadfence_block();
         if (lane == 0) *reinterpret_cast<volatile uint32_t*>(&S.head[rslot]) = head;
-        // expand the vectors: element e of lane's vector is id (tag & 0xFFFFFF) - 1 + e
+        // expand the vectors: element e of lane's vector is id (tag & 0xFFFFFF) - 1 + e;
+        // elements below the row's published threshold (seed or k-th so far)
+        // cannot reach the row's best k and are dropped before any merging
         const uint32_t id0 = (tag & 0xFFFFFFu) - 1u;
-        bool changed = false;
+        const uint32_t tau_o = __shfl_sync(0xFFFFFFFFu, *reinterpret_cast<volatile uint32_t*>(&S.tau[rslot]), 0);
+        // survivors: above the threshold and above the list's current k-th key
+        const uint64_t kth0 = __shfl_sync(0xFFFFFFFFu, list, k - 1);
+        uint64_t cand[EPV];
+        uint32_t cnt = 0;
 #pragma unroll
         for (int p = 0; p < EPV / 2; ++p) {
           const float2 z = E::pair(v, p);
-          const uint64_t k0 = ((tag >> (24 + 2 * p)) & 1u) ? elem_key(z.x, id0 + 2 * p) : 0ull;
-          const uint64_t k1 = ((tag >> (25 + 2 * p)) & 1u) ? elem_key(z.y, id0 + 2 * p + 1) : 0ull;
-          changed |= merge_keys(list, k0, k);
-          changed |= merge_keys(list, k1, k);
+          const bool q0 = ((tag >> (24 + 2 * p)) & 1u) && ord_f32(z.x) >= tau_o;
+          const bool q1 = ((tag >> (25 + 2 * p)) & 1u) && ord_f32(z.y) >= tau_o;
+          cand[2 * p] = q0 ? elem_key(z.x, id0 + 2 * p) : 0ull;
+          cand[2 * p + 1] = q1 ? elem_key(z.y, id0 + 2 * p + 1) : 0ull;
+          if (cand[2 * p] <= kth0) cand[2 * p] = 0ull;
+          if (cand[2 * p + 1] <= kth0) cand[2 * p + 1] = 0ull;
+          cnt += (cand[2 * p] != 0ull) + (cand[2 * p + 1] != 0ull);
+        }
+        // compact them into shared memory (prefix sum of counts <= 8 by ballots)
+        const uint32_t c0 = __ballot_sync(0xFFFFFFFFu, cnt & 1u), c1 = __ballot_sync(0xFFFFFFFFu, cnt & 2u);
+        const uint32_t c2 = __ballot_sync(0xFFFFFFFFu, cnt & 4u), c3 = __ballot_sync(0xFFFFFFFFu, cnt & 8u);
+        const int total = __popc(c0) + 2 * __popc(c1) + 4 * __popc(c2) + 8 * __popc(c3);
+        const bool changed = total > 0;
+        if (changed) {
+          const uint32_t below = (1u << lane) - 1u;
+          int at = __popc(c0 & below) + 2 * __popc(c1 & below) + 4 * __popc(c2 & below) + 8 * __popc(c3 & below);
+#pragma unroll
+          for (int e = 0; e < EPV; ++e)
+            if (cand[e] != 0ull) S.mkeys[at++] = cand[e];
+          __syncwarp();
+          if (total <= 4) {
+            // a few: insert one at a time (a vote finds the position)
+            for (int t = 0; t < total; ++t) {
+              const uint64_t x = S.mkeys[t];
+              const int pos = __popc(__ballot_sync(0xFFFFFFFFu, list > x));
+              const uint64_t up = __shfl_up_sync(0xFFFFFFFFu, list, 1);
+              list = lane < pos ? list : (lane == pos ? x : up);
+            }
+          } else {
+            for (int b0 = 0; b0 < total; b0 += 32)
+              list = warp_merge_top32(list, b0 + lane < total ? S.mkeys[b0 + lane] : 0ull);
+          }
+          __syncwarp();
         }
         if (changed) {
           const uint64_t kth = __shfl_sync(0xFFFFFFFFu, list, k - 1);

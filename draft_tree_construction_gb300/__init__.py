@@ -218,7 +218,7 @@ def tree_build(logits, T: float, k: int, W: int, lam: float, beta: float,
     MW = mask_words(N)
     o = out if out is not None else _outputs(B, N, MW, logits.device, scores)
     need = workspace_bytes(B, d, V, codes[logits.dtype], k)
-    ws = workspace if workspace is not None else torch.empty(max(need, 1), dtype=torch.uint8,
+    ws = workspace if workspace is not None else torch.zeros(max(need, 1), dtype=torch.uint8,
                                                              device=logits.device)
     if table is not None:
         _need_cuda(ctx, "ctx", torch.int32)
@@ -296,7 +296,7 @@ def row_topk(logits, T: float, k: int, *, workspace=None, stream=None):
     logp = torch.empty((R, k), dtype=torch.float32, device=logits.device)
     lse = torch.empty((R,), dtype=torch.float32, device=logits.device)
     need = workspace_bytes(R, 1, V, codes[logits.dtype], k)
-    ws = workspace if workspace is not None else torch.empty(max(need, 1), dtype=torch.uint8,
+    ws = workspace if workspace is not None else torch.zeros(max(need, 1), dtype=torch.uint8,
                                                              device=logits.device)
     _check(lib().dart_row_topk(_ptr(logits), R, V, codes[logits.dtype], float(T), k, _ptr(ids),
                                _ptr(logp), _ptr(lse), _ptr(ws), ws.numel(), _stream_ptr(stream)),
@@ -337,7 +337,7 @@ class TreeBuilder:
         self.N = num_nodes(d, k, W)
         self.MW = mask_words(self.N)
         self.out = _outputs(B, self.N, self.MW, device, scores)
-        self.ws = torch.empty(max(workspace_bytes(B, d, V, self.code, k), 1), dtype=torch.uint8,
+        self.ws = torch.zeros(max(workspace_bytes(B, d, V, self.code, k), 1), dtype=torch.uint8,
                               device=device)
 
     def __call__(self, logits, stream=None):

@@ -148,8 +148,7 @@ int dart_tree_build(const void* logits, int B, int d, int V, int dtype,
   int sms = 0;
   if ((rc = device_sms(&sms))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (cudaMemsetAsync(ws, 0, L.clear_bytes, s) != cudaSuccess) return DART_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);   // counters are zero between calls
   if (launch_rows(logits, R, V, dtype, T, k, ws, L, sms, nullptr, nullptr, nullptr, s) != cudaSuccess)
     return DART_ERR_CUDA;
   TreeArgs a = tree_args(B, d, k, W, lambda, beta, ngram_table, ctx_tokens, out_tokens, out_parents,
@@ -186,7 +185,8 @@ int dart_tree_build_noalloc(const void* logits, int B, int d, int V, int dtype,
   if ((rc = device_sms(&sms))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(scratch);
-  // the previous call's counters are still there: clear them on this stream
+  // errors are not reported on this path: clear the counters (and the error
+  // word) of a call that may have given up, on this stream
   if (cudaMemsetAsync(ws, 0, L.clear_bytes, s) != cudaSuccess) return DART_ERR_CUDA;
   if (launch_rows(logits, R, V, dtype, T, k, ws, L, sms, nullptr, nullptr, nullptr, s) != cudaSuccess)
     return DART_ERR_CUDA;
@@ -234,8 +234,7 @@ int dart_row_topk(const void* logits, int rows, int V, int dtype, float T, int k
   int sms = 0;
   int rc = device_sms(&sms);
   if (rc) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace, 0, L.clear_bytes, s) != cudaSuccess) return DART_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);   // counters are zero between calls
   if (launch_rows(logits, rows, V, dtype, T, k, workspace, L, sms, out_ids, out_logp, out_lse, s) !=
       cudaSuccess)
     return DART_ERR_CUDA;
@@ -344,8 +343,16 @@ int dart_device_error(const void* workspace, uint32_t* out_flags, void* stream) 
   if (!workspace || !out_flags) return DART_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return DART_ERR_CUDA;
-  if (cudaMemcpy(out_flags, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return DART_ERR_CUDA;
+  // word 0: error bits; words 2..3: rows of the last row-stream call (written by the kernel)
+  uint32_t head[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(head, workspace, sizeof(head), cudaMemcpyDeviceToHost) != cudaSuccess) return DART_ERR_CUDA;
+  *out_flags = head[0];
+  if (head[0] != 0u) {
+    const unsigned long long rows = (unsigned long long)head[2] | ((unsigned long long)head[3] << 32);
+    WsLayout L;
+    const size_t clear = ws_layout((long long)rows, 2, 1, 1, &L) ? L.clear_bytes : size_t(kCtrlBytes);
+    if (cudaMemset(const_cast<void*>(workspace), 0, clear) != cudaSuccess) return DART_ERR_CUDA;
+  }
   return DART_OK;
 }
 

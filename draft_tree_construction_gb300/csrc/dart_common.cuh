@@ -105,7 +105,9 @@ __host__ __device__ __forceinline__ Buckets key_buckets(Key96 k, uint64_t nb) {
 constexpr uint64_t kMinTableSlots = 8;
 
 // ------------------------------------------------------- workspace layout
-// [ctrl 256 B][row_cnt R x u32]   <- cleared by every call
+// [ctrl 256 B][row_cnt R x u32]   <- zero between calls (the last CTA of a row
+//                                     resets its counter; ctrl word 0 holds
+//                                     error bits until read, words 2..3 rows)
 // [row_off R x f64][row_ids R*k x i32][row_base R*k x f64][partials]
 // row_off = the row's log-sum-exp of z / T; row_base = the candidates' logits;
 // a partial is one CTA's (max, scaled sum, k best keys) of a row.

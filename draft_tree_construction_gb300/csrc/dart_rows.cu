@@ -731,6 +731,7 @@ __device__ __forceinline__ void merge_span_rows(const RowsParams& P, RowSmem& S,
     if (int(old) == nseg - 1) {
       __threadfence();
       merge_row(P, r, nseg);
+      if (lane == 0) P.row_cnt[r] = 0u;   // every CTA of the row has arrived: ready for the next call
     }
   }
 }
@@ -753,6 +754,11 @@ row_stream_kernel(const RowsParams P) {
   const long long r_first = (long long)(e0 / P.V);
   const long long r_last = (long long)((e1 - 1) / P.V);
 
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    // rows of this call, for clearing the counters after a failed call
+    P.ctrl[2] = uint32_t((unsigned long long)P.R);
+    P.ctrl[3] = uint32_t((unsigned long long)P.R >> 32);
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(&S.full[i], 1);

@@ -131,8 +131,10 @@ size_t dart_tree_workspace_bytes(int B, int d, int V, int dtype, int k);
  *              row x is set iff node i is x or an ancestor of x
  *  out_scores  device float [B][N] or NULL: each node's path score
  *  workspace   device, >= dart_tree_workspace_bytes(B,d,V,dtype,k) bytes,
- *              256-byte aligned; its contents need no preparation, the call
- *              clears what it uses on `stream`
+ *              256-byte aligned, zero-filled before its first use (the
+ *              library keeps its counters at zero from call to call, so no
+ *              per-call clearing is launched; after a nonzero device error,
+ *              dart_device_error clears it again)
  * Returns DART_OK or an error code; see the conventions above. */
 int dart_tree_build(const void* logits, int B, int d, int V, int dtype,
                     float T, int k, int W, float lambda, float beta,
@@ -153,7 +155,8 @@ int dart_tree_build(const void* logits, int B, int d, int V, int dtype,
  * library holds until the process exits.  Sizes whose
  * dart_tree_workspace_bytes(B, d, V, dtype, k) exceeds 16 MiB are rejected
  * with DART_ERR_WORKSPACE before anything is launched.  The call allocates
- * nothing; it clears the buffer's counters on `stream` itself.
+ * nothing; since its error bits are not reported, it clears the buffer's
+ * counters on `stream` before each use.
  * The first call on each device looks up the buffer's device address (with
  * that device current) and caches it; make that first call before any
  * stream capture.  All calls on a device share the one buffer, which keeps
@@ -221,7 +224,10 @@ int dart_ngram_lookup(const dart_ngram_table_t* table, const int32_t* keys, int6
                       float* vals, int32_t* found, void* stream);
 
 /* Waits for `stream`, then copies the workspace's device error word to
- * *out_flags (host).  Returns DART_OK, or DART_ERR_CUDA. */
+ * *out_flags (host).  The word collects the DART_DEVERR_* bits of every call
+ * since the last nonzero read; a nonzero read clears it together with the
+ * workspace's counters (a call that gave up may leave them set), so the
+ * workspace is ready for the next call.  Returns DART_OK, or DART_ERR_CUDA. */
 int dart_device_error(const void* workspace, uint32_t* out_flags, void* stream);
 
 /* Static text for a status code. */

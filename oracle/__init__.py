@@ -61,6 +61,8 @@ def _declare(lib):
     lib.oracle_num_nodes.restype = i32
     lib.oracle_mask_from_parents.argtypes = [i32, i32, P, P]
     lib.oracle_mask_from_parents.restype = i32
+    lib.oracle_select_tree.argtypes = [i32, i32, i32, P, P, P, P]
+    lib.oracle_select_tree.restype = i32
     return lib
 
 
@@ -199,3 +201,28 @@ def mask_from_parents(parents: np.ndarray, lib=None) -> np.ndarray:
     if rc:
         raise ValueError(f"oracle_mask_from_parents failed ({rc})")
     return mask
+
+
+def select_tree(tokens, parents, pos, scores, M: int, lib=None):
+    """Verification tree of budget M chosen best-first from candidate trees
+    [B, N] (see oracle_select_tree).  Returns index, tokens, parents, pos [B, M']
+    and the ancestor masks [B, M', ceil(M'/32)] of the chosen trees, M' = min(M, N)."""
+    lib = lib or load()
+    par = np.ascontiguousarray(parents, dtype=np.int32)
+    B, N = par.shape
+    s = np.ascontiguousarray(scores, dtype=np.float64).reshape(B, N)
+    Mp = min(int(M), N)
+    index = np.zeros((B, Mp), dtype=np.int32)
+    npar = np.zeros((B, Mp), dtype=np.int32)
+    rc = lib.oracle_select_tree(B, N, int(M), _p(par), _p(s), _p(index), _p(npar))
+    if rc:
+        raise ValueError(f"oracle_select_tree failed ({rc})")
+    tok = np.take_along_axis(np.asarray(tokens, dtype=np.int32).reshape(B, N), index, axis=1)
+    dep = np.take_along_axis(np.asarray(pos, dtype=np.int32).reshape(B, N), index, axis=1)
+    MW = (Mp + 31) // 32
+    mask = np.zeros((B, Mp, MW), dtype=np.uint32)
+    if Mp:
+        rc = lib.oracle_mask_from_parents(B, Mp, _p(npar), _p(mask))
+        if rc:
+            raise ValueError(f"oracle_mask_from_parents failed ({rc})")
+    return dict(index=index, tokens=tok, parents=npar, pos=dep, mask=mask)

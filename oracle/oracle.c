@@ -384,3 +384,64 @@ int oracle_tree_build(const void* logits, int dtype, int B, int d, int V, double
     free(zc);
     return rc;
 }
+
+/* ------------------------------------------------- verification tree selection */
+
+/* Node a beats node b: larger score, then lower index. */
+static int sel_better(const double* s, int a, int b) {
+    if (s[a] != s[b]) return s[a] > s[b];
+    return a < b;
+}
+
+int oracle_select_tree(int B, int N, int M, const int32_t* parents, const double* scores,
+                       int32_t* index, int32_t* new_parents) {
+    if (B < 0 || N < 0 || M < 0) return 1;
+    int Mp = M < N ? M : N;
+    if (B == 0 || Mp == 0) return 0;
+    if (!parents || !scores || !index || !new_parents) return 1;
+    int* avail = (int*)malloc(sizeof(int) * (size_t)N);   /* the available nodes, unordered */
+    char* taken = (char*)malloc((size_t)N);
+    int* newpos = (int*)malloc(sizeof(int) * (size_t)N);
+    if (!avail || !taken || !newpos) {
+        free(avail); free(taken); free(newpos);
+        return 1;
+    }
+    int rc = 0;
+    for (int b = 0; b < B && rc == 0; ++b) {
+        const int32_t* par = parents + (size_t)b * N;
+        const double* s = scores + (size_t)b * N;
+        for (int i = 0; i < N; ++i)
+            if (par[i] >= i) rc = 2;
+        if (rc) break;
+        int na = 0;
+        for (int i = 0; i < N; ++i) {
+            taken[i] = 0;
+            if (par[i] < 0) avail[na++] = i;
+        }
+        /* best-first: M' times pick the best available node (a plain scan of the
+         * available set stands in for the priority queue) */
+        for (int t = 0; t < Mp; ++t) {
+            if (na == 0) { rc = 2; break; }
+            int best = 0;
+            for (int a = 1; a < na; ++a)
+                if (sel_better(s, avail[a], avail[best])) best = a;
+            int x = avail[best];
+            avail[best] = avail[--na];
+            taken[x] = 1;
+            for (int c = x + 1; c < N; ++c)
+                if (par[c] == x) avail[na++] = c;
+        }
+        if (rc) break;
+        int m = 0;
+        for (int i = 0; i < N; ++i) {
+            newpos[i] = -1;
+            if (taken[i]) newpos[i] = m, index[(size_t)b * Mp + m++] = i;
+        }
+        for (int j = 0; j < Mp; ++j) {
+            int i = index[(size_t)b * Mp + j];
+            new_parents[(size_t)b * Mp + j] = par[i] < 0 ? -1 : newpos[par[i]];
+        }
+    }
+    free(avail); free(taken); free(newpos);
+    return rc;
+}

@@ -81,6 +81,20 @@ int oracle_num_nodes(int d, int k, int W);
 /* Ancestor-or-self mask rows from a parent array (parents[i] < i, -1 for depth 1). */
 int oracle_mask_from_parents(int B, int N, const int32_t* parents, uint32_t* mask);
 
+/* Verification tree by best-first selection from a candidate tree (DARTree,
+ * abstract and Verification: the candidate tree is built first, then only
+ * best-first pruning selects the tree sent to verification; PCTree, abstract:
+ * a fixed verification budget goes to the most probable paths).  Per tree b,
+ * with nodes 0..N-1 (parents[i] < i, -1 at depth 1) and path scores
+ * scores[i]: start with the depth-1 nodes available; M times take the
+ * available node of largest score (lower node index on equal scores) and make
+ * its children available.  index[b][0..M'-1] receives the taken nodes in
+ * increasing node index, M' = min(M, N); new_parents[b][m] is the position in
+ * that list of node index[m]'s parent (-1 at depth 1).  Returns 0, 1 on bad
+ * arguments, 2 on a parent array that does not point backwards. */
+int oracle_select_tree(int B, int N, int M, const int32_t* parents, const double* scores,
+                       int32_t* index, int32_t* new_parents);
+
 #ifdef __cplusplus
 }
 #endif

@@ -245,3 +245,48 @@ def make_config(i: int, seed: int = 0, **over) -> Case:
 def stored_as_f32(case: Case) -> np.ndarray:
     """The stored logits widened exactly to float32 (for generators and plots only)."""
     return _as_f32(case.logits, case.dtype)
+
+
+def make_candidate_trees(*, B: int, d: int, k: int, W: int, seed: int = 0, tie_frac: float = 0.1,
+                         zero_frac: float = 0.05):
+    """Random candidate trees shaped like the built ones, as input for choosing
+    verification trees: per depth j = 1..d there are min(W, k^j) nodes (depth
+    by depth, parents before children), each node below depth 1 hangs under a
+    random node of the depth above (at most k children each), and scores are
+    float32 values that never rise along a path: depth-1 scores are drawn
+    U(-8, -0.5), a child's score is its parent's minus a drop U(0, 6).  A share
+    `tie_frac` of nodes copies the score of an earlier node where that keeps
+    the path non-increasing, and a share `zero_frac` of drops is exactly 0, so
+    equal scores occur.  Tokens are U[0, 1000).  Returns dict(tokens, parents,
+    pos, scores) of shapes [B, N]."""
+    rng = np.random.default_rng(seed)
+    sizes = [min(W, k ** j) for j in range(1, d + 1)]
+    N = int(sum(sizes))
+    tokens = rng.integers(0, 1000, size=(B, N)).astype(np.int32)
+    parents = np.full((B, N), -1, dtype=np.int32)
+    pos = np.zeros((B, N), dtype=np.int32)
+    scores = np.zeros((B, N), dtype=np.float32)
+    for b in range(B):
+        start, prev = 0, None
+        for j, n_j in enumerate(sizes, start=1):
+            idx = np.arange(start, start + n_j)
+            pos[b, idx] = j
+            if prev is None:
+                scores[b, idx] = rng.uniform(-8.0, -0.5, size=n_j).astype(np.float32)
+            else:
+                slots = np.repeat(prev, k)                   # each parent has k child slots
+                par = np.sort(rng.choice(slots, size=n_j, replace=False))
+                parents[b, idx] = par
+                drop = rng.uniform(0.0, 6.0, size=n_j)
+                drop[rng.random(n_j) < zero_frac] = 0.0
+                scores[b, idx] = (scores[b, par].astype(np.float64) - drop).astype(np.float32)
+            # exact ties: copy an earlier node's score when the path stays non-increasing
+            for x in idx:
+                if rng.random() < tie_frac and x > 0:
+                    y = int(rng.integers(0, x))
+                    p = parents[b, x]
+                    if p < 0 or scores[b, y] <= scores[b, p]:
+                        scores[b, x] = scores[b, y]
+            start += n_j
+            prev = idx
+    return dict(tokens=tokens, parents=parents, pos=pos, scores=scores)

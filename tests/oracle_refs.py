@@ -159,3 +159,18 @@ def whole_path_brute_force_ok(lib=None, seed=3) -> bool:
             if abs(out["scores"][b, x] - ref[p]) > 1e-10:
                 return False
     return True
+
+
+def best_sum_subset(scores, M: int):
+    """Brute force: the size-M set of nodes with the largest score sum (sets
+    compared by their sorted score lists when sums are equal).  For scores that
+    never rise along a path this is the best-first verification tree: the M
+    largest scores form a set that holds every ancestor of its members."""
+    n = len(scores)
+    best, best_key = None, None
+    for comb in itertools.combinations(range(n), M):
+        vals = sorted((scores[i] for i in comb), reverse=True)
+        key = (math.fsum(vals), vals)
+        if best_key is None or key > best_key:
+            best, best_key = comb, key
+    return list(best)

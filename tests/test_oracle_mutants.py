@@ -52,6 +52,11 @@ MUTANTS = {
     "path_not_extended": ("nseq[(size_t)r * L + len] = e->tok;", "nseq[(size_t)r * L + len] = 0;"),
     "parent_score_dropped": ("double Z = fZ[i] + P[c];", "double Z = P[c];"),
     "cut_at_w_minus_one": ("int keep = m < W ? m : W;", "int keep = m < W - 1 ? m : W - 1;"),
+    "select_worst_first": ("if (s[a] != s[b]) return s[a] > s[b];", "if (s[a] != s[b]) return s[a] < s[b];"),
+    "select_ties_high_index": ("    return a < b;\n}", "    return a > b;\n}"),
+    "select_all_available": ("if (par[i] < 0) avail[na++] = i;", "avail[na++] = i;"),
+    "select_parent_not_renumbered": ("new_parents[(size_t)b * Mp + j] = par[i] < 0 ? -1 : newpos[par[i]];",
+                                     "new_parents[(size_t)b * Mp + j] = par[i];"),
 }
 
 
@@ -170,7 +175,44 @@ def _pin_whole_path_temperature(lib):
     return R.whole_path_brute_force_ok(lib)
 
 
-PINS = [_pin_worked_examples, _pin_rows, _pin_brute_force, _pin_k_best, _pin_whole_path_temperature]
+def _pin_select(lib):
+    import json
+    with open(os.path.join(R.GOLDEN, "we1_select.json")) as f:
+        ex = json.load(f)
+    t = ex["tree"]
+    sc = np.array([[R.eval_closed_form(x) for x in t["scores"]]])
+    for M, want in ex["expect"].items():
+        out = oracle.select_tree(np.array([t["tokens"]]), np.array([t["parents"]]), np.array([t["pos"]]), sc,
+                                 int(M), lib=lib)
+        if out["index"][0].tolist() != want["index"] or out["parents"][0].tolist() != want["parents"]:
+            return False
+    # availability: a child that outscores everything waits for its parent
+    out = oracle.select_tree(np.array([[7, 8, 9]]), np.array([[-1, -1, 1]]), np.array([[1, 1, 2]]),
+                             np.array([[-5.0, -6.0, -1.0]]), 2, lib=lib)
+    if out["index"][0].tolist() != [0, 1]:
+        return False
+    # renumbering: node 0 is not taken, so node 2's parent (node 1) becomes position 0
+    out = oracle.select_tree(np.array([[4, 5, 6]]), np.array([[-1, -1, 1]]), np.array([[1, 1, 2]]),
+                             np.array([[-9.0, -1.0, -2.0]]), 2, lib=lib)
+    if out["index"][0].tolist() != [1, 2] or out["parents"][0].tolist() != [-1, 0] or \
+            out["mask"][0, :, 0].tolist() != [1, 3]:
+        return False
+    # equal scores: lower index first
+    out = oracle.select_tree(np.arange(3)[None], np.array([[-1, -1, -1]]), np.ones((1, 3), dtype=np.int32),
+                             np.array([[-1.0, -1.0, -2.0]]), 1, lib=lib)
+    if out["index"][0].tolist() != [0]:
+        return False
+    for seed in (1, 2):
+        tree = synth.make_candidate_trees(B=1, d=3, k=2, W=4, seed=200 + seed, tie_frac=0.0, zero_frac=0.0)
+        N = tree["parents"].shape[1]
+        for M in range(1, N + 1):
+            out = oracle.select_tree(tree["tokens"], tree["parents"], tree["pos"], tree["scores"], M, lib=lib)
+            if out["index"][0].tolist() != sorted(R.best_sum_subset(tree["scores"][0].astype(np.float64).tolist(), M)):
+                return False
+    return True
+
+
+PINS = [_pin_worked_examples, _pin_rows, _pin_brute_force, _pin_k_best, _pin_whole_path_temperature, _pin_select]
 
 
 def _all_pins_pass(lib) -> bool:

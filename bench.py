@@ -328,6 +328,25 @@ def run_ours(args):
 
     k1_times = timed(rows_only, args.steps)
     k1_ms = max_over_ranks(statistics.mean(k1_times), world)
+
+    # ---- the verification tree chosen best-first from the step's candidate
+    # trees, budget 16 (one of the verification budgets PCTree quotes)
+    select = None
+    if builder.out.get("scores") is not None:
+        o = builder.out
+        budget = min(16, o["parents"].shape[1])
+        sel_err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def select_only(i):
+            D.tree_select(o["tokens"], o["parents"], o["pos"], o["scores"], budget, device_err=sel_err,
+                          stream=stream)
+
+        sel_times = timed(select_only, min(args.steps, 200))
+        sel_ms = max_over_ranks(statistics.mean(sel_times), world)
+        torch.cuda.synchronize(dev)
+        select = {"budget": budget, "us_per_call": sel_ms * 1e3, "trees_per_s": B * world / (sel_ms / 1e3),
+                  "kernel": "select_kernel (best-first verification tree)", "calls": len(sel_times),
+                  "device_error": int(sel_err.item())}
     clocks = clocks_stop(clk, (t_timed, time.time()))
 
     # ---- end to end: pinned host logits in, pinned host outputs back, every step
@@ -387,6 +406,7 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": 2 * args.steps,
+            "verification_tree_select": select,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

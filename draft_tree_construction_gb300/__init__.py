@@ -26,7 +26,7 @@ from ._build import LIB as _LIB_PATH, build as _build_lib
 
 __all__ = [
     "DartError", "build", "lib", "NGramTable", "num_nodes", "mask_words", "workspace_bytes",
-    "tree_build", "tree_build_noalloc", "tree_from_topk", "row_topk", "mask_pack", "device_error", "TreeBuilder",
+    "tree_build", "tree_build_noalloc", "tree_from_topk", "row_topk", "mask_pack", "tree_select", "device_error", "TreeBuilder",
     "DTYPE_CODES",
 ]
 
@@ -73,6 +73,8 @@ def _declare(L):
     L.dart_row_topk.restype = i32
     L.dart_mask_pack.argtypes = [P, i32, i32, P, P, P]
     L.dart_mask_pack.restype = i32
+    L.dart_tree_select.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, P, P, P, P]
+    L.dart_tree_select.restype = i32
     L.dart_ngram_capacity_for.argtypes = [u64]
     L.dart_ngram_capacity_for.restype = u64
     L.dart_ngram_table_pack_host.argtypes = [i32, P, P, u64, u64, P, C.POINTER(C.c_uint64)]
@@ -312,6 +314,34 @@ def mask_pack(parents, *, device_err=None, stream=None):
     out = torch.empty((B, N, (N + 31) // 32), dtype=torch.int32, device=parents.device)
     _check(lib().dart_mask_pack(_ptr(parents), B, N, _ptr(out), _ptr(device_err), _stream_ptr(stream)),
            "dart_mask_pack")
+    return out
+
+
+def tree_select(tokens, parents, pos, scores, M: int, *, device_err=None, stream=None) -> dict:
+    """Verification tree of budget M chosen best-first from candidate trees.
+
+    tokens, parents, pos: CUDA int32 [B, N]; scores: CUDA float32 [B, N] (as
+    returned by tree_build).  Returns index, tokens, parents, pos (int32 [B, M']),
+    mask (int32 [B, M', ceil(M'/32)], uint32 bits) and scores (float32 [B, M']),
+    M' = min(M, N)."""
+    torch = _torch()
+    for t, name in ((tokens, "tokens"), (parents, "parents"), (pos, "pos")):
+        _need_cuda(t, name, torch.int32)
+    _need_cuda(scores, "scores", torch.float32)
+    _need_cuda(device_err, "device_err", torch.int32)
+    B, N = parents.shape
+    Mp = min(int(M), N)
+    dev = parents.device
+    out = dict(index=torch.empty((B, Mp), dtype=torch.int32, device=dev),
+               tokens=torch.empty((B, Mp), dtype=torch.int32, device=dev),
+               parents=torch.empty((B, Mp), dtype=torch.int32, device=dev),
+               pos=torch.empty((B, Mp), dtype=torch.int32, device=dev),
+               mask=torch.empty((B, Mp, (Mp + 31) // 32), dtype=torch.int32, device=dev),
+               scores=torch.empty((B, Mp), dtype=torch.float32, device=dev))
+    _check(lib().dart_tree_select(_ptr(tokens), _ptr(parents), _ptr(pos), _ptr(scores), B, N, int(M),
+                                  _ptr(out["index"]), _ptr(out["tokens"]), _ptr(out["parents"]),
+                                  _ptr(out["pos"]), _ptr(out["mask"]), _ptr(out["scores"]),
+                                  _ptr(device_err), _stream_ptr(stream)), "dart_tree_select")
     return out
 
 

@@ -70,7 +70,9 @@ enum {
   DART_DEVERR_WAIT_TIMEOUT = 1u << 0,  /* a bulk-copy wait ran out; the call's output is invalid */
   DART_DEVERR_ROW_MAX = 1u << 1,       /* a row's maximum and its best candidate disagreed */
   DART_DEVERR_SELECT = 1u << 2,        /* the tree selection produced an invalid candidate */
-  DART_DEVERR_PARENT = 1u << 3         /* dart_mask_pack: a parent index was not below its child */
+  DART_DEVERR_PARENT = 1u << 3,        /* dart_mask_pack / dart_tree_select: a parent index was not below its child */
+  DART_DEVERR_SCORE_RISES = 1u << 4    /* dart_tree_select: a node outscored its parent (the result is the M best,
+                                          which best-first need not take) */
 };
 
 /* An n-gram model in device memory: a two-choice bucketed hash table.
@@ -200,6 +202,37 @@ int dart_row_topk(const void* logits, int rows, int V, int dtype, float T, int k
  * *device_err (device uint32, may be NULL). */
 int dart_mask_pack(const int32_t* parents, int B, int N, uint32_t* out_mask,
                    uint32_t* device_err, void* stream);
+
+/* Verification tree chosen best-first with a budget (DARTree, abstract and
+ * Verification: the candidate tree is built first, then best-first pruning
+ * alone picks the tree that is verified; PCTree, abstract: a fixed
+ * verification budget goes to the most probable paths).  Per tree b, M' =
+ * min(M, N) times, the node of largest score (lower index on equal scores)
+ * among those whose parent is already taken (depth-1 nodes need none) is
+ * taken.  When scores never rise from a parent to its children (true for
+ * dart_tree_build's scores whenever lambda >= 0, beta <= 0 and the table's
+ * values are <= 0) these are the M' best nodes by (score, lower index).
+ *  tokens, parents, pos  device int32 [B][N] (parents[i] < i, -1 at depth 1),
+ *                        and scores device float [B][N]: candidate trees as
+ *                        written by dart_tree_build (N <= 1024)
+ *  out_index             device int32 [B][M']: the taken nodes' indices,
+ *                        increasing (parents before children)
+ *  out_tokens, out_pos   device int32 [B][M']: their tokens and depths
+ *  out_parents           device int32 [B][M']: position of the parent within
+ *                        the chosen tree, -1 at depth 1
+ *  out_mask              device uint32 [B][M'][ceil(M'/32)]: ancestor-or-self
+ *                        rows of the chosen tree, LSB first
+ *  out_scores            device float [B][M'] or NULL
+ *  device_err            device uint32 or NULL: receives DART_DEVERR_PARENT
+ *                        for a parent index not below its node and
+ *                        DART_DEVERR_SCORE_RISES for a node scoring above its
+ *                        parent (its kept children may then lack a parent:
+ *                        out_parents -2)
+ * Nothing is launched when B or M is 0.  Returns DART_OK or an error code. */
+int dart_tree_select(const int32_t* tokens, const int32_t* parents, const int32_t* pos,
+                     const float* scores, int B, int N, int M, int32_t* out_index,
+                     int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
+                     uint32_t* out_mask, float* out_scores, uint32_t* device_err, void* stream);
 
 /* Smallest power of two >= max(2 * M, 8) (load factor at most 1/2); 0 on
  * overflow. */

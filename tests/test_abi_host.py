@@ -122,6 +122,14 @@ def test_other_entry_points_check_arguments(L):
     assert L.dart_mask_pack(None, 2, 10, None, None, None) == INVALID
     assert L.dart_mask_pack(None, 0, 10, None, None, None) == OK
     assert L.dart_ngram_lookup(None, None, 10, None, None, None) == INVALID
+    sel = lambda B, N, M, ptr: L.dart_tree_select(ptr, ptr, ptr, ptr, B, N, M, ptr, ptr, ptr, ptr, ptr,
+                                                  None, None, None)
+    assert sel(2, 0, 4, P(FAKE)) == INVALID          # no nodes
+    assert sel(2, 1025, 4, P(FAKE)) == INVALID       # above the node limit
+    assert sel(2, 16, -1, P(FAKE)) == INVALID        # negative budget
+    assert sel(2, 16, 4, None) == INVALID            # missing buffers
+    assert sel(0, 16, 4, None) == OK                 # nothing to do: no launch
+    assert sel(2, 16, 0, None) == OK
     assert L.dart_device_error(None, None, None) == INVALID
     assert L.dart_status_string(1).decode() == "invalid argument"
 

@@ -71,6 +71,11 @@ def _declare(L):
     L.dart_tree_from_topk.restype = i32
     L.dart_row_topk.argtypes = [P, i32, i32, i32, f32, i32, P, P, P, P, sz, P]
     L.dart_row_topk.restype = i32
+    L.dart_row_topk_strided.argtypes = [P, i32, i32, i64, i32, f32, i32, P, P, P, P, sz, P]
+    L.dart_row_topk_strided.restype = i32
+    L.dart_tree_build_strided.argtypes = [P, i32, i32, i32, i64, i32, f32, i32, i32, f32, f32, T, P,
+                                          P, P, P, P, P, P, sz, P]
+    L.dart_tree_build_strided.restype = i32
     L.dart_mask_pack.argtypes = [P, i32, i32, P, P, P]
     L.dart_mask_pack.restype = i32
     L.dart_tree_select.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, P, P, P, P]
@@ -202,18 +207,51 @@ def _outputs(B, N, MW, device, scores: bool):
                 scores=torch.empty((B, N), dtype=torch.float32, device=device) if scores else None)
 
 
+def _row_stride(logits) -> int:
+    """Elements between row starts of a [..., V] tensor whose rows are evenly
+    spaced with unit element stride (a contiguous tensor, or a view such as
+    z[..., :V] of a padded one); raises otherwise."""
+    shape, strides = logits.shape, logits.stride()
+    V = shape[-1]
+    if V > 1 and strides[-1] != 1:
+        raise DartError("logits rows must have unit element stride")
+    rows = 1
+    for s_ in shape[:-1]:
+        rows *= s_
+    if rows <= 1:
+        return V
+    # the innermost row dimension of size > 1 fixes the stride; every outer one must continue it
+    step = None
+    expect = None
+    for size, st in reversed(list(zip(shape[:-1], strides[:-1]))):
+        if size == 1:
+            continue
+        if step is None:
+            step, expect = st, st * size
+        elif st != expect:
+            raise DartError("logits rows must be evenly spaced")
+        else:
+            expect = st * size
+    if step < V:
+        raise DartError("logits rows overlap")
+    return int(step)
+
+
 def tree_build(logits, T: float, k: int, W: int, lam: float, beta: float,
                table: NGramTable | None = None, ctx=None, *, out: dict | None = None,
                workspace=None, stream=None, scores: bool = True) -> dict:
     """logits: CUDA [B, d, V] float32/float16/bfloat16 -> dict of CUDA outputs.
 
-    mask is returned as int32 storage holding the uint32 bit pattern."""
+    The rows may be a view of a padded vocabulary (z[..., :V] of [B, d, V_pad]):
+    only the V valid logits of each row are read.  mask is returned as int32
+    storage holding the uint32 bit pattern."""
     torch = _torch()
     codes = DTYPE_CODES()
-    _need_cuda(logits, "logits")
+    _need_cuda(logits, "logits", contiguous=False)
     if logits.dtype not in codes or logits.dim() != 3:
         raise DartError("logits must be [B, d, V] float32, float16 or bfloat16")
     B, d, V = logits.shape
+    stride = _row_stride(logits)
     N = num_nodes(d, k, W)
     if N < 0:
         raise DartError("invalid d/k/W")
@@ -224,13 +262,13 @@ def tree_build(logits, T: float, k: int, W: int, lam: float, beta: float,
                                                              device=logits.device)
     if table is not None:
         _need_cuda(ctx, "ctx", torch.int32)
-    rc = lib().dart_tree_build(_ptr(logits), B, d, V, codes[logits.dtype], float(T), k, W,
+    rc = lib().dart_tree_build_strided(_ptr(logits), B, d, V, stride, codes[logits.dtype], float(T), k, W,
                                float(lam), float(beta),
                                C.byref(table.desc) if table is not None else None,
                                _ptr(ctx) if table is not None else None,
                                _ptr(o["tokens"]), _ptr(o["parents"]), _ptr(o["pos"]), _ptr(o["mask"]),
                                _ptr(o.get("scores")), _ptr(ws), ws.numel(), _stream_ptr(stream))
-    _check(rc, "dart_tree_build")
+    _check(rc, "dart_tree_build_strided")
     o["workspace"] = ws
     return o
 
@@ -287,22 +325,25 @@ def tree_from_topk(ids, logp, W: int, lam: float, beta: float, table: NGramTable
 
 
 def row_topk(logits, T: float, k: int, *, workspace=None, stream=None):
-    """logits: CUDA [R, V] -> (ids int32 [R,k], logp float32 [R,k], lse float32 [R], workspace)."""
+    """logits: CUDA [R, V] -> (ids int32 [R,k], logp float32 [R,k], lse float32 [R], workspace).
+
+    The rows may be a view of a padded vocabulary (z[:, :V] of [R, V_pad])."""
     torch = _torch()
     codes = DTYPE_CODES()
-    _need_cuda(logits, "logits")
+    _need_cuda(logits, "logits", contiguous=False)
     if logits.dtype not in codes or logits.dim() != 2:
         raise DartError("logits must be [R, V] float32, float16 or bfloat16")
     R, V = logits.shape
+    stride = _row_stride(logits)
     ids = torch.empty((R, k), dtype=torch.int32, device=logits.device)
     logp = torch.empty((R, k), dtype=torch.float32, device=logits.device)
     lse = torch.empty((R,), dtype=torch.float32, device=logits.device)
     need = workspace_bytes(R, 1, V, codes[logits.dtype], k)
     ws = workspace if workspace is not None else torch.zeros(max(need, 1), dtype=torch.uint8,
                                                              device=logits.device)
-    _check(lib().dart_row_topk(_ptr(logits), R, V, codes[logits.dtype], float(T), k, _ptr(ids),
-                               _ptr(logp), _ptr(lse), _ptr(ws), ws.numel(), _stream_ptr(stream)),
-           "dart_row_topk")
+    _check(lib().dart_row_topk_strided(_ptr(logits), R, V, stride, codes[logits.dtype], float(T), k, _ptr(ids),
+                                       _ptr(logp), _ptr(lse), _ptr(ws), ws.numel(), _stream_ptr(stream)),
+           "dart_row_topk_strided")
     return ids, logp, lse, ws
 
 

@@ -133,9 +133,21 @@ int dart_tree_build(const void* logits, int B, int d, int V, int dtype,
                     int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
                     uint32_t* out_mask, float* out_scores,
                     void* workspace, size_t workspace_bytes, void* stream) {
+  return dart_tree_build_strided(logits, B, d, V, V, dtype, T, k, W, lambda, beta, ngram_table, ctx_tokens,
+                                 out_tokens, out_parents, out_pos, out_mask, out_scores, workspace,
+                                 workspace_bytes, stream);
+}
+
+int dart_tree_build_strided(const void* logits, int B, int d, int V, int64_t row_stride, int dtype,
+                            float T, int k, int W, float lambda, float beta,
+                            const dart_ngram_table_t* ngram_table, const int32_t* ctx_tokens,
+                            int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
+                            uint32_t* out_mask, float* out_scores,
+                            void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_tree_shape(B, d, k, W, lambda, beta);
   if (rc) return rc;
   if (V < 2 || V > kMaxV || k > V || !valid_dtype(dtype)) return DART_ERR_INVALID_ARG;
+  if (row_stride < V || row_stride > kMaxRowStride) return DART_ERR_INVALID_ARG;
   if (!finite(T) || !(T > 0.f)) return DART_ERR_INVALID_ARG;
   if ((rc = check_table(ngram_table, ctx_tokens, B))) return rc;
   if (B == 0) return DART_OK;
@@ -149,7 +161,7 @@ int dart_tree_build(const void* logits, int B, int d, int V, int dtype,
   if ((rc = device_sms(&sms))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);   // counters are zero between calls
-  if (launch_rows(logits, R, V, dtype, T, k, ws, L, sms, nullptr, nullptr, nullptr, s) != cudaSuccess)
+  if (launch_rows(logits, R, V, row_stride, dtype, T, k, ws, L, sms, nullptr, nullptr, nullptr, s) != cudaSuccess)
     return DART_ERR_CUDA;
   TreeArgs a = tree_args(B, d, k, W, lambda, beta, ngram_table, ctx_tokens, out_tokens, out_parents,
                          out_pos, out_mask, out_scores);
@@ -188,7 +200,7 @@ int dart_tree_build_noalloc(const void* logits, int B, int d, int V, int dtype,
   // errors are not reported on this path: clear the counters (and the error
   // word) of a call that may have given up, on this stream
   if (cudaMemsetAsync(ws, 0, L.clear_bytes, s) != cudaSuccess) return DART_ERR_CUDA;
-  if (launch_rows(logits, R, V, dtype, T, k, ws, L, sms, nullptr, nullptr, nullptr, s) != cudaSuccess)
+  if (launch_rows(logits, R, V, V, dtype, T, k, ws, L, sms, nullptr, nullptr, nullptr, s) != cudaSuccess)
     return DART_ERR_CUDA;
   TreeArgs a = tree_args(B, d, k, W, lambda, beta, ngram_table, ctx_tokens, out_tokens, out_parents,
                          out_pos, out_mask, out_scores);
@@ -223,8 +235,16 @@ int dart_tree_from_topk(const int32_t* cand_ids, const double* cand_logp,
 int dart_row_topk(const void* logits, int rows, int V, int dtype, float T, int k,
                   int32_t* out_ids, float* out_logp, float* out_lse,
                   void* workspace, size_t workspace_bytes, void* stream) {
+  return dart_row_topk_strided(logits, rows, V, V, dtype, T, k, out_ids, out_logp, out_lse, workspace,
+                               workspace_bytes, stream);
+}
+
+int dart_row_topk_strided(const void* logits, int rows, int V, int64_t row_stride, int dtype, float T, int k,
+                          int32_t* out_ids, float* out_logp, float* out_lse,
+                          void* workspace, size_t workspace_bytes, void* stream) {
   if (rows < 0 || V < 2 || V > kMaxV || !valid_dtype(dtype) || k < 1 || k > kMaxK || k > V)
     return DART_ERR_INVALID_ARG;
+  if (row_stride < V || row_stride > kMaxRowStride) return DART_ERR_INVALID_ARG;
   if (!finite(T) || !(T > 0.f)) return DART_ERR_INVALID_ARG;
   if (rows == 0) return DART_OK;
   if (!logits || !aligned(logits, 16)) return DART_ERR_INVALID_ARG;
@@ -235,7 +255,7 @@ int dart_row_topk(const void* logits, int rows, int V, int dtype, float T, int k
   int rc = device_sms(&sms);
   if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);   // counters are zero between calls
-  if (launch_rows(logits, rows, V, dtype, T, k, workspace, L, sms, out_ids, out_logp, out_lse, s) !=
+  if (launch_rows(logits, rows, V, row_stride, dtype, T, k, workspace, L, sms, out_ids, out_logp, out_lse, s) !=
       cudaSuccess)
     return DART_ERR_CUDA;
   return DART_OK;

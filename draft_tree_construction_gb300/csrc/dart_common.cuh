@@ -22,6 +22,7 @@ constexpr int kMaxD = 32;          // depths
 constexpr int kMaxN = 1024;        // nodes per tree
 constexpr int kMaxMW = kMaxN / 32; // mask words per row
 constexpr int kMaxV = (1 << 24) - 1;
+constexpr long long kMaxRowStride = 1ll << 30;   // elements from one row's start to the next
 
 // ------------------------------------------------------------ ordered keys
 // A float maps to a uint32 whose unsigned order is the float order; -0.0 is

@@ -6,7 +6,7 @@
 
 namespace dart {
 
-cudaError_t launch_rows(const void* logits, long long R, int V, int dtype, float T, int k,
+cudaError_t launch_rows(const void* logits, long long R, int V, long long stride, int dtype, float T, int k,
                         void* ws, const WsLayout& L, int sms,
                         int32_t* out_ids, float* out_logp, float* out_lse, cudaStream_t stream);
 

@@ -68,6 +68,7 @@ struct RowsParams {
   const uint8_t* logits;
   long long R;
   int V, k, es;
+  unsigned long long stride;  // elements from one row's start to the next (>= V; the rest is padding)
   float c;                    // log2(e) / T
   double T;
   double invT;                // 1 / T
@@ -467,13 +468,16 @@ struct Seg {
   unsigned long long a, b;    // aligned interior, bytes (a == b: none)
 };
 
+// The part of row r (its V valid elements; padding up to the row stride is
+// never read) that lies in the span [e0, e1).
 __device__ __forceinline__ Seg segment(const RowsParams& P, unsigned long long e0, unsigned long long e1,
                                        long long r) {
   Seg g;
-  const unsigned long long rs = (unsigned long long)r * P.V;
+  const unsigned long long rs = (unsigned long long)r * P.stride;
   g.s0 = e0 > rs ? e0 : rs;
   const unsigned long long re = rs + P.V;
   g.s1 = e1 < re ? e1 : re;
+  if (g.s1 < g.s0) g.s1 = g.s0;
   g.a = (g.s0 * P.es + 15) & ~15ull;
   g.b = (g.s1 * P.es) & ~15ull;
   if (g.a >= g.b) g.a = g.b = g.s1 * P.es;  // nothing aligned: all scalars
@@ -709,7 +713,7 @@ __device__ __forceinline__ void merge_span_rows(const RowsParams& P, RowSmem& S,
     __threadfence_block();
     mbar_arrive(&S.row_free[rslot]);
 
-    const unsigned long long rb0 = (unsigned long long)r * P.V * P.es;
+    const unsigned long long rb0 = (unsigned long long)r * P.stride * P.es;
     const long long cfirst = (long long)(rb0 / P.span);
     const long long clast = (long long)((rb0 + (unsigned long long)P.V * P.es - 1) / P.span);
     if (cfirst == clast) {
@@ -751,8 +755,10 @@ row_stream_kernel(const RowsParams P) {
   const unsigned long long B0 = (unsigned long long)blockIdx.x * P.span;
   const unsigned long long B1 = (B0 + P.span < P.total) ? B0 + P.span : P.total;
   const unsigned long long e0 = B0 / P.es, e1 = B1 / P.es;
-  const long long r_first = (long long)(e0 / P.V);
-  const long long r_last = (long long)((e1 - 1) / P.V);
+  // the rows whose valid elements meet the span (none when it holds padding only)
+  long long r_first = (long long)(e0 / P.stride);
+  if (e0 - (unsigned long long)r_first * P.stride >= (unsigned long long)P.V) ++r_first;
+  const long long r_last = (long long)((e1 - 1) / P.stride);
 
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     // rows of this call, for clearing the counters after a failed call
@@ -843,7 +849,7 @@ row_stream_kernel(const RowsParams P) {
         !__all_sync(0xFFFFFFFFu, wait_phase(S, &S.row_free[rslot], uint32_t(rowseq / kRowSlots - 1) & 1u, lim, P.ctrl)))
       return;
     const Seg g = segment(P, e0, e1, r);
-    const unsigned long long rs = (unsigned long long)r * P.V;
+    const unsigned long long rs = (unsigned long long)r * P.stride;
     RowCtx rc;
     rc.m = -FLT_MAX;
     rc.mc = scaled_max(rc.m, P.c);
@@ -934,7 +940,7 @@ row_stream_kernel(const RowsParams P) {
 // ------------------------------------------------------------------ launch
 size_t rows_smem_bytes() { return sizeof(RowSmem); }
 
-cudaError_t launch_rows(const void* logits, long long R, int V, int dtype, float T, int k,
+cudaError_t launch_rows(const void* logits, long long R, int V, long long stride, int dtype, float T, int k,
                         void* ws, const WsLayout& L, int sms,
                         int32_t* out_ids, float* out_logp, float* out_lse, cudaStream_t stream) {
   RowsParams P;
@@ -942,12 +948,14 @@ cudaError_t launch_rows(const void* logits, long long R, int V, int dtype, float
   P.logits = static_cast<const uint8_t*>(logits);
   P.R = R;
   P.V = V;
+  P.stride = (unsigned long long)stride;
   P.k = k;
   P.es = es;
   P.T = double(T);
   P.invT = 1.0 / double(T);
   P.c = float(1.4426950408889634 / double(T));
-  P.total = (unsigned long long)R * (unsigned long long)V * (unsigned long long)es;
+  // the stream ends at the last valid element (the last row's padding may be absent)
+  P.total = R > 0 ? ((unsigned long long)(R - 1) * P.stride + (unsigned long long)V) * (unsigned long long)es : 0ull;
   // one span per SM, whole 16-byte units, at least kMinSpanBytes
   const unsigned long long want = (P.total + (unsigned long long)sms - 1) / (unsigned long long)sms;
   unsigned long long span = (want + 15) & ~15ull;

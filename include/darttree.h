@@ -145,6 +145,21 @@ int dart_tree_build(const void* logits, int B, int d, int V, int dtype,
                     uint32_t* out_mask, float* out_scores,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* dart_tree_build for logits whose rows are row_stride >= V elements apart
+ * (a vocabulary padded for the projection that produced them): row r of
+ * [B][d] holds its V valid logits at logits + r * row_stride elements, and
+ * the elements from V up to the stride are never read (they may hold
+ * anything).  The buffer must reach (B*d - 1) * row_stride + V elements;
+ * its base is 16-byte aligned, rows need not be.  row_stride = V is
+ * dart_tree_build itself; row_stride < V or above 2^30 is
+ * DART_ERR_INVALID_ARG.  Every other argument as for dart_tree_build. */
+int dart_tree_build_strided(const void* logits, int B, int d, int V, int64_t row_stride, int dtype,
+                            float T, int k, int W, float lambda, float beta,
+                            const dart_ngram_table_t* ngram_table, const int32_t* ctx_tokens,
+                            int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
+                            uint32_t* out_mask, float* out_scores,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
 /* dart_tree_build without a workspace argument, for callers that cannot
  * allocate device memory: an engine whose own pool allocator has reserved
  * the device's memory (a side cudaMalloc would fail or fragment it), a
@@ -194,6 +209,12 @@ int dart_tree_from_topk(const int32_t* cand_ids, const double* cand_logp,
 int dart_row_topk(const void* logits, int rows, int V, int dtype, float T, int k,
                   int32_t* out_ids, float* out_logp, float* out_lse,
                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* dart_row_topk for rows row_stride >= V elements apart (see
+ * dart_tree_build_strided; the padding is never read). */
+int dart_row_topk_strided(const void* logits, int rows, int V, int64_t row_stride, int dtype, float T, int k,
+                          int32_t* out_ids, float* out_logp, float* out_lse,
+                          void* workspace, size_t workspace_bytes, void* stream);
 
 /* Ancestor-or-self masks from a parent array (DART, Figure 3 caption: the
  * tree-attention input).  parents device int32 [B][N], each entry -1 or a

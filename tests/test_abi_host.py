@@ -122,6 +122,14 @@ def test_other_entry_points_check_arguments(L):
     assert L.dart_mask_pack(None, 2, 10, None, None, None) == INVALID
     assert L.dart_mask_pack(None, 0, 10, None, None, None) == OK
     assert L.dart_ngram_lookup(None, None, 10, None, None, None) == INVALID
+    # padded rows: the stride must reach V, and stays below 2^30
+    assert L.dart_row_topk_strided(P(FAKE), 4, 100, 99, 2, 1.0, 4, None, None, None, None, 0, None) == INVALID
+    assert L.dart_row_topk_strided(P(FAKE), 4, 100, 1 << 31, 2, 1.0, 4, None, None, None, None, 0,
+                                   None) == INVALID
+    assert L.dart_row_topk_strided(P(FAKE), 4, 100, 128, 2, 1.0, 4, None, None, None, None, 0,
+                                   None) == WORKSPACE
+    assert L.dart_tree_build_strided(P(FAKE), 2, 3, 100, 50, 2, 1.0, 4, 4, 0.5, -1.0, None, None, P(FAKE),
+                                     P(FAKE), P(FAKE), P(FAKE), None, None, 0, None) == INVALID
     sel = lambda B, N, M, ptr: L.dart_tree_select(ptr, ptr, ptr, ptr, B, N, M, ptr, ptr, ptr, ptr, ptr,
                                                   None, None, None)
     assert sel(2, 0, 4, P(FAKE)) == INVALID          # no nodes
@@ -237,3 +245,18 @@ def test_packer_refuses_overfull_and_bad_tokens(L):
     assert L.dart_ngram_table_pack_host(2, P(bad), P(vals), 4, 8, P(slots), None) == INVALID
     assert L.dart_ngram_table_pack_host(2, P(keys), P(vals), 4, 6, P(slots), None) == INVALID
     assert L.dart_ngram_table_pack_host(2, P(keys), P(vals), 2, 4, P(slots), None) == INVALID   # below 8 slots
+
+
+def test_row_stride_of_views():
+    torch = pytest.importorskip("torch")
+    z = torch.zeros((3, 4, 130))
+    assert D._row_stride(z) == 130
+    assert D._row_stride(z[:, :, :100]) == 130          # a padded vocabulary
+    assert D._row_stride(z[:, 1:2, :100]) == 130 * 4    # one row per sequence
+    assert D._row_stride(z[:1, :1, :7]) == 7            # a single row
+    assert D._row_stride(z.reshape(12, 130)[:, :128]) == 130
+    assert D._row_stride(z[:, ::2, :100]) == 260        # every other row: still evenly spaced
+    with pytest.raises(D.DartError):
+        D._row_stride(z[:, :2, :100])                    # two rows of four: a gap after each pair
+    with pytest.raises(D.DartError):
+        D._row_stride(z[:, :, ::2])                      # elements not adjacent

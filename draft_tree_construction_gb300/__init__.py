@@ -26,7 +26,7 @@ from ._build import LIB as _LIB_PATH, build as _build_lib
 
 __all__ = [
     "DartError", "build", "lib", "NGramTable", "num_nodes", "mask_words", "workspace_bytes",
-    "tree_build", "tree_build_noalloc", "tree_from_topk", "row_topk", "mask_pack", "tree_select", "device_error", "TreeBuilder",
+    "tree_build", "tree_build_noalloc", "tree_from_topk", "row_topk", "mask_pack", "tree_select", "set_wait_limit", "device_error", "TreeBuilder",
     "DTYPE_CODES",
 ]
 
@@ -86,6 +86,8 @@ def _declare(L):
     L.dart_ngram_table_pack_host.restype = i32
     L.dart_ngram_lookup.argtypes = [T, P, i64, P, P, P]
     L.dart_ngram_lookup.restype = i32
+    L.dart_set_wait_limit.argtypes = [i64]
+    L.dart_set_wait_limit.restype = None
     L.dart_device_error.argtypes = [P, C.POINTER(C.c_uint32), P]
     L.dart_device_error.restype = i32
     L.dart_status_string.argtypes = [i32]
@@ -384,6 +386,13 @@ def tree_select(tokens, parents, pos, scores, M: int, *, device_err=None, stream
                                   _ptr(out["pos"]), _ptr(out["mask"]), _ptr(out["scores"]),
                                   _ptr(device_err), _stream_ptr(stream)), "dart_tree_select")
     return out
+
+
+def set_wait_limit(cycles: int) -> None:
+    """SM clock cycles any one wait of the row pass may take before it gives up
+    (<= 0 restores the default of about two seconds).  For tests of the timeout
+    path."""
+    lib().dart_set_wait_limit(int(cycles))
 
 
 def device_error(workspace, stream=None) -> int:

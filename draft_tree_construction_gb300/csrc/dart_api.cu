@@ -359,6 +359,8 @@ int dart_ngram_lookup(const dart_ngram_table_t* table, const int32_t* keys, int6
   return DART_OK;
 }
 
+void dart_set_wait_limit(int64_t cycles) { set_rows_wait_limit((long long)cycles); }
+
 int dart_device_error(const void* workspace, uint32_t* out_flags, void* stream) {
   if (!workspace || !out_flags) return DART_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

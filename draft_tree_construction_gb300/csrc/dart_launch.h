@@ -6,6 +6,9 @@
 
 namespace dart {
 
+long long rows_wait_limit();
+void set_rows_wait_limit(long long cycles);
+
 cudaError_t launch_rows(const void* logits, long long R, int V, long long stride, int dtype, float T, int k,
                         void* ws, const WsLayout& L, int sms,
                         int32_t* out_ids, float* out_logp, float* out_lse, cudaStream_t stream);

@@ -44,6 +44,7 @@
 // for) before any lane writes, so a reserved entry is always written promptly.
 #include "dart_common.cuh"
 
+#include <atomic>
 #include <cfloat>
 
 namespace dart {
@@ -56,6 +57,10 @@ constexpr int kVecPerLane = kSlice / 16 / 32;
 constexpr int kRowSlots = 4;                    // rows in flight between the consumers and the merger
 constexpr int kRingVecs = 256;                  // candidate-vector ring per row slot (power of two)
 constexpr uint32_t kSleepNs = 100000;           // longest sleep of one barrier probe
+// Copies in flight always land before their CTA retires: that drain is bounded
+// by about two seconds of SM clock whatever limit the other waits have.
+constexpr long long kDrainLimit = 4000000000LL;
+constexpr long long kDefaultWaitLimit = 4000000000LL;
 constexpr int kMergerWarp = kConsumers + 1;
 constexpr int kRowThreads = (kConsumers + 2) * 32;
 static_assert(kVecPerLane == 4, "reduce_slice reduces exactly four vectors per lane");
@@ -821,7 +826,7 @@ row_stream_kernel(const RowsParams P) {
         // the last fill of each slot used so far
         const int sl = (slot + NST - 1 - j) % NST;
         const uint32_t rd = (sl < slot) ? round : round - 1;
-        if (!mbar_wait_bounded(&S.full[sl], rd & 1u, P.wait_limit)) {
+        if (!mbar_wait_bounded(&S.full[sl], rd & 1u, kDrainLimit)) {
           set_dev_error(P.ctrl, DART_DEVERR_WAIT_TIMEOUT);
           break;
         }
@@ -940,6 +945,14 @@ row_stream_kernel(const RowsParams P) {
 // ------------------------------------------------------------------ launch
 size_t rows_smem_bytes() { return sizeof(RowSmem); }
 
+// Clock cycles any one wait of the row pass may take before the pass gives
+// up (default about two seconds; tests of the timeout path shorten it).
+static std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
+long long rows_wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
+void set_rows_wait_limit(long long cycles) {
+  g_wait_limit.store(cycles > 0 ? cycles : kDefaultWaitLimit, std::memory_order_relaxed);
+}
+
 cudaError_t launch_rows(const void* logits, long long R, int V, long long stride, int dtype, float T, int k,
                         void* ws, const WsLayout& L, int sms,
                         int32_t* out_ids, float* out_logp, float* out_lse, cudaStream_t stream) {
@@ -979,7 +992,7 @@ cudaError_t launch_rows(const void* logits, long long R, int V, long long stride
   P.out_ids = out_ids;
   P.out_logp = out_logp;
   P.out_lse = out_lse;
-  P.wait_limit = 4000000000LL;  // about two seconds of SM clock
+  P.wait_limit = rows_wait_limit();
   if (P.total == 0) return cudaSuccess;
   const size_t smem = rows_smem_bytes();
   cudaError_t e = cudaSuccess;

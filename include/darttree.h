@@ -284,6 +284,14 @@ int dart_ngram_lookup(const dart_ngram_table_t* table, const int32_t* keys, int6
  * workspace is ready for the next call.  Returns DART_OK, or DART_ERR_CUDA. */
 int dart_device_error(const void* workspace, uint32_t* out_flags, void* stream);
 
+/* Sets the number of SM clock cycles any one wait of the row pass (a bulk
+ * copy landing, a slot freeing, a barrier of the CTA) may take before the pass
+ * gives up: the CTA then ends every other wait, lets its copies in flight
+ * land, sets DART_DEVERR_WAIT_TIMEOUT and returns, and its outputs are
+ * invalid.  cycles <= 0 restores the default (4e9, about two seconds).  For
+ * tests of the timeout path; applies to later calls from every host thread. */
+void dart_set_wait_limit(int64_t cycles);
+
 /* Static text for a status code. */
 const char* dart_status_string(int status);
 

@@ -57,7 +57,7 @@ enum { DART_F32 = 0, DART_F16 = 1, DART_BF16 = 2 };
 enum {
   DART_OK = 0,
   DART_ERR_INVALID_ARG = 1,   /* an argument is out of range, NULL or misaligned */
-  DART_ERR_UNSUPPORTED = 2,   /* valid request this build does not handle */
+  DART_ERR_UNSUPPORTED = 2,   /* a valid request the library does not handle */
   DART_ERR_WORKSPACE = 3,     /* workspace NULL, misaligned or too small */
   DART_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
   DART_ERR_INTERNAL = 5,      /* a kernel reported an inconsistency */

@@ -4,7 +4,7 @@ This module only draws random numbers and lays them out; it holds none of the
 method's arithmetic (no softmax, no scoring, no pruning).  Both the CPU oracle
 and the CUDA path are fed from here, and nothing else is shared between them.
 
-Workloads follow the five configurations this build is measured on (DART,
+Workloads follow five configurations, numbered 0-4 (DART,
 "Figure 3" pipeline: d parallel logit vectors per sequence, an n-gram model for
 continuity; DARTree "Tree Construction": fixed width W per depth):
 

@@ -58,6 +58,8 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--probe-sfu", action="store_true",
+                   help="only measure the exponential unit's throughput (one JSON line)")
     return p.parse_args()
 
 
@@ -222,6 +224,65 @@ def oracle_sample(case, budget_s: float, ngram=None):
     return S, dt, threads, ngram
 
 
+def oracle_single_core(case, budget_s: float, ngram):
+    """Times the oracle on one host core (S trees sized to the budget)."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.tree_build(_sub_case(case, 1), ngram=ngram, threads=1)
+    t1 = time.perf_counter() - t0
+    S = int(max(1, min(case.B, math.floor(budget_s / max(t1, 1e-6)))))
+    t0 = time.perf_counter()
+    oracle.tree_build(_sub_case(case, S), ngram=ngram, threads=1)
+    return S, time.perf_counter() - t0
+
+
+def run_probe_sfu(args):
+    """Exponentials per second the GPU sustains (ex2.approx, the row pass's
+    exponential), against what the row pass needs at 70% of the measured copy
+    bandwidth on 2-byte logits (one exponential per logit)."""
+    import ctypes as C
+    import torch
+    import draft_tree_construction_gb300 as D
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    D.build()
+    L = D.lib()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks, threads, iters = sms * 4, 512, 4096
+    out = torch.empty(blocks * threads, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def go():
+        rc = L.dart_probe_ex2(blocks, threads, iters, C.c_void_p(out.data_ptr()), C.c_void_p(stream.cuda_stream))
+        assert rc == 0, rc
+
+    for _ in range(3):
+        go()
+    torch.cuda.synchronize(dev)
+    clk = clocks_start(0)
+    t0 = time.time()
+    times = []
+    for _ in range(10):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        go()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b))
+    clocks = clocks_stop(clk, (t0, time.time()))
+    ms = statistics.median(times)
+    rate = blocks * threads * iters * 8 / (ms / 1e3)
+    mhz = clocks.get("sm_mhz") or 2070.0
+    peaks, src = measured_peaks()
+    need = 0.7 * peaks["hbm_gbs"] * 1e9 / 2.0
+    print(json.dumps({"probe": "ex2.approx throughput", "exp2_per_s": rate,
+                      "per_sm_per_clock": rate / sms / (mhz * 1e6), "sms": sms, "ms_per_launch": ms,
+                      "exps_per_launch": blocks * threads * iters * 8,
+                      "row_pass_need_at_70pct_copy_peak_2byte_logits": need, "need_over_probe": need / rate,
+                      "peak_source": src, "clocks": clocks}), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------------ arms
 
 def run_reference(args):
@@ -384,9 +445,11 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        S, dt, threads, _ = oracle_sample(case, args.cpu_seconds)
+        S, dt, threads, ng = oracle_sample(case, args.cpu_seconds)
+        S1, dt1 = oracle_single_core(case, args.cpu_seconds / 3.0, ng)
         cpu = {"value": S / dt, "unit": "trees/s", "cores": threads, "kind": "oracle",
-               "sample": f"first {S} of {B} trees of the same batch, full vocabulary and table"}
+               "sample": f"first {S} of {B} trees of the same batch, full vocabulary and table",
+               "value_1_core": S1 / dt1, "sample_1_core": f"first {S1} of {B} trees, one thread"}
 
     if rank == 0:
         value = B * world / (step_ms / 1e3)
@@ -420,6 +483,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.probe_sfu:
+        return run_probe_sfu(args)
     return run_ours(args)
 
 

@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdarttree.so")
-SOURCES = ["dart_api.cu", "dart_rows.cu", "dart_tree.cu", "dart_select.cu"]
+SOURCES = ["dart_api.cu", "dart_rows.cu", "dart_tree.cu", "dart_select.cu", "dart_probe.cu"]
 
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

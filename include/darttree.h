@@ -292,6 +292,14 @@ int dart_device_error(const void* workspace, uint32_t* out_flags, void* stream);
  * tests of the timeout path; applies to later calls from every host thread. */
 void dart_set_wait_limit(int64_t cycles);
 
+/* Throughput probe of the exponential unit: blocks x threads threads (threads
+ * a multiple of 32, at most 1024) each run 8 independent chains of `iters`
+ * steps x <- 2^x - 1.5 (one ex2.approx and one add per step) and write one
+ * float to out (device, blocks * threads floats).  Time it on `stream` to get
+ * exponentials per second = blocks * threads * iters * 8 / time.  Returns
+ * DART_OK or an error code. */
+int dart_probe_ex2(int blocks, int threads, int iters, float* out, void* stream);
+
 /* Static text for a status code. */
 const char* dart_status_string(int status);
 

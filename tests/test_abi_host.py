@@ -130,6 +130,9 @@ def test_other_entry_points_check_arguments(L):
                                    None) == WORKSPACE
     assert L.dart_tree_build_strided(P(FAKE), 2, 3, 100, 50, 2, 1.0, 4, 4, 0.5, -1.0, None, None, P(FAKE),
                                      P(FAKE), P(FAKE), P(FAKE), None, None, 0, None) == INVALID
+    assert L.dart_probe_ex2(0, 64, 8, P(FAKE), None) == INVALID       # no blocks
+    assert L.dart_probe_ex2(4, 48, 8, P(FAKE), None) == INVALID       # threads not a multiple of 32
+    assert L.dart_probe_ex2(4, 64, 8, None, None) == INVALID          # no output
     sel = lambda B, N, M, ptr: L.dart_tree_select(ptr, ptr, ptr, ptr, B, N, M, ptr, ptr, ptr, ptr, ptr,
                                                   None, None, None)
     assert sel(2, 0, 4, P(FAKE)) == INVALID          # no nodes

@@ -374,6 +374,10 @@ def tree_select(tokens, parents, pos, scores, M: int, *, device_err=None, stream
         _need_cuda(t, name, torch.int32)
     _need_cuda(scores, "scores", torch.float32)
     _need_cuda(device_err, "device_err", torch.int32)
+    if parents.dim() != 2 or any(t.shape != parents.shape for t in (tokens, pos, scores)):
+        raise DartError("tokens, parents, pos and scores must all be [B, N]")
+    if int(M) < 0:
+        raise DartError("the budget M must be >= 0")
     B, N = parents.shape
     Mp = min(int(M), N)
     dev = parents.device

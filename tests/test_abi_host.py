@@ -263,3 +263,15 @@ def test_row_stride_of_views():
         D._row_stride(z[:, :2, :100])                    # two rows of four: a gap after each pair
     with pytest.raises(D.DartError):
         D._row_stride(z[:, :, ::2])                      # elements not adjacent
+
+
+def test_binding_rejects_host_tensors_and_bad_shapes():
+    torch = pytest.importorskip("torch")
+    z = torch.zeros((2, 3, 100))
+    with pytest.raises(D.DartError):
+        D.tree_build(z, 1.0, 4, 4, 0.5, -1.0)                 # host memory: no CPU fallback
+    with pytest.raises(D.DartError):
+        D.row_topk(z[0], 1.0, 4)
+    t = torch.zeros((2, 5), dtype=torch.int32)
+    with pytest.raises(D.DartError):
+        D.tree_select(t, t, t, torch.zeros((2, 5)), 3)         # host memory

@@ -119,3 +119,28 @@ def test_budget_edges():
 def test_bad_parent_array_is_rejected():
     with pytest.raises(ValueError):
         oracle.select_tree(np.zeros((1, 3)), np.array([[-1, 2, 0]]), np.ones((1, 3)), np.zeros((1, 3)), 2)
+
+
+@pytest.mark.parametrize("d,k,W", [(3, 3, 5), (8, 8, 10), (16, 16, 32), (32, 32, 32)])
+def test_seeded_candidate_trees_have_the_stated_shape(d, k, W):
+    """The generator feeding the GPU selection tests: depth-major nodes with
+    min(W, k^j) per depth, parents one depth up with at most k children each,
+    scores that never rise along a path, and some exact ties."""
+    tree = synth.make_candidate_trees(B=3, d=d, k=k, W=W, seed=d + k + W)
+    sizes = [min(W, k ** j) for j in range(1, d + 1)]
+    N = sum(sizes)
+    assert tree["parents"].shape == (3, N) and tree["scores"].dtype == np.float32
+    ties = 0
+    for b in range(3):
+        par, pos, sc = tree["parents"][b], tree["pos"][b], tree["scores"][b]
+        assert pos.tolist() == [j for j, n in enumerate(sizes, start=1) for _ in range(n)]
+        for i in range(N):
+            p = par[i]
+            if pos[i] == 1:
+                assert p == -1
+            else:
+                assert 0 <= p < i and pos[p] == pos[i] - 1 and sc[i] <= sc[p]
+        counts = np.bincount(par[par >= 0], minlength=N)
+        assert counts.max(initial=0) <= k
+        ties += N - len(np.unique(sc))
+    assert ties > 0

@@ -60,6 +60,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--probe-sfu", action="store_true",
                    help="only measure the exponential unit's throughput (one JSON line)")
+    p.add_argument("--probe-stream", action="store_true",
+                   help="only sweep the streaming-read probes (one JSON line per shape)")
     return p.parse_args()
 
 
@@ -283,6 +285,101 @@ def run_probe_sfu(args):
     return 0
 
 
+def hold_gpu(stream, steps, us_per_step=80.0):
+    """Queues a spin kernel on `stream` long enough for the host to queue the
+    `steps` timed steps behind it, so that no timed step waits for the host
+    (Python needs tens of microseconds to queue one step)."""
+    import torch
+    if hasattr(torch.cuda, "_sleep"):
+        ms = min(60.0, 1.0 + steps * us_per_step / 1e3)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(ms * 2.0e6))   # cycles, about 1 ms per 2e6 at 2 GHz
+
+
+def stream_probe(L, buf, mode, ctas, warps, stages, stream, steps=20, flush=None):
+    """Mean GB/s of dart_probe_stream over `steps` launches (L2 flushed before each)."""
+    import ctypes as C
+    import torch
+    dev = buf.device
+    out = torch.empty(ctas * warps * 32, dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    nbytes = buf.numel() * buf.element_size()
+
+    def go():
+        rc = L.dart_probe_stream(C.c_void_p(buf.data_ptr()), nbytes, mode, ctas, warps, stages,
+                                 C.c_void_p(out.data_ptr()), C.c_void_p(err.data_ptr()),
+                                 C.c_void_p(stream.cuda_stream))
+        assert rc == 0, rc
+
+    for _ in range(3):
+        go()
+    times = []
+    hold_gpu(stream, steps)
+    for _ in range(steps):
+        if flush is not None:
+            flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        go()
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize(dev)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in times)
+    assert int(err.item()) == 0, "stream probe: a bulk wait ran out"
+    return nbytes / (ms / 1e3) / 1e9, ms
+
+
+def run_probe_stream(args):
+    """Sweeps the streaming-read probe over loader kinds and launch shapes on a
+    buffer the size of the chosen config's logits (config 2: 155.6 MB)."""
+    import torch
+    import draft_tree_construction_gb300 as D
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    D.build()
+    L = D.lib()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    c = synth.CONFIGS[args.config]
+    nbytes = c["B"] * c["d"] * c["V"] * synth.ELEM_BYTES[c["dtype"]]
+    buf = (torch.randn(nbytes // 2, device=dev) * 3).to(torch.bfloat16)
+    flush_buf = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks, src = measured_peaks()
+    shapes = []
+    for math_ in (0, 2):
+        for warps in (8, 12, 16):
+            shapes.append((math_, 1, warps, 0))
+        shapes.append((math_, 2, 8, 0))
+        for warps, stages in ((8, 4), (8, 6), (12, 3), (12, 4), (16, 3), (6, 8)):
+            shapes.append((math_ | 1, 1, warps, stages))
+    clk = clocks_start(0)
+    t0 = time.time()
+    rows = []
+    for mode, per_sm, warps, stages in shapes:
+        gbs, ms = stream_probe(L, buf, mode, sms * per_sm, warps, stages, stream, steps=args.steps,
+                               flush=lambda: flush_buf.sum())
+        rows.append({"loader": "bulk ring" if mode & 1 else "direct", "math": bool(mode & 2),
+                     "ctas_per_sm": per_sm, "warps_per_cta": warps, "stages": stages,
+                     "gbs": gbs, "us": ms * 1e3, "frac_of_peak": gbs / peaks["hbm_gbs"]})
+    clocks = clocks_stop(clk, (t0, time.time()))
+    # torch's own read of the same buffer, for comparison
+    times = []
+    for _ in range(args.steps):
+        flush_buf.sum()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        buf.sum()
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize(dev)
+    tms = statistics.mean(a.elapsed_time(b) for a, b in times)
+    for r in rows:
+        print(json.dumps({"probe": "stream", "bytes": nbytes, **r}), flush=True)
+    print(json.dumps({"probe": "stream torch.sum", "bytes": nbytes, "gbs": nbytes / (tms / 1e3) / 1e9,
+                      "peak": peaks["hbm_gbs"], "peak_source": src, "clocks": clocks}), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------------ arms
 
 def run_reference(args):
@@ -354,6 +451,7 @@ def run_ours(args):
     def timed(fn, steps):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(steps)]
+        hold_gpu(stream, steps)
         for i in range(steps):
             flush()
             evs[i][0].record(stream)
@@ -485,6 +583,8 @@ def main():
         return run_reference(args)
     if args.probe_sfu:
         return run_probe_sfu(args)
+    if args.probe_stream:
+        return run_probe_stream(args)
     return run_ours(args)
 
 

@@ -88,6 +88,8 @@ def _declare(L):
     L.dart_ngram_lookup.restype = i32
     L.dart_probe_ex2.argtypes = [i32, i32, i32, P, P]
     L.dart_probe_ex2.restype = i32
+    L.dart_probe_stream.argtypes = [P, u64, i32, i32, i32, i32, P, P, P]
+    L.dart_probe_stream.restype = i32
     L.dart_set_wait_limit.argtypes = [i64]
     L.dart_set_wait_limit.restype = None
     L.dart_device_error.argtypes = [P, C.POINTER(C.c_uint32), P]

@@ -106,20 +106,38 @@ __host__ __device__ __forceinline__ Buckets key_buckets(Key96 k, uint64_t nb) {
 constexpr uint64_t kMinTableSlots = 8;
 
 // ------------------------------------------------------- workspace layout
-// [ctrl 256 B][row_cnt R x u32]   <- zero between calls (the last CTA of a row
-//                                     resets its counter; ctrl word 0 holds
-//                                     error bits until read, words 2..3 rows)
-// [row_off R x f64][row_ids R*k x i32][row_base R*k x f64][partials]
+// [ctrl 256 B]                    <- ctrl word 0 holds error bits until read,
+//                                    words 2..3 the rows of the last call
+// [row_off R x f64][row_ids R*k x i32][row_base R*k x f64][piece slots]
 // row_off = the row's log-sum-exp of z / T; row_base = the candidates' logits;
-// a partial is one CTA's (max, scaled sum, k best keys) of a row.
+// a piece slot holds one warp's share of a row: its (max, scaled sum), its
+// lower bound of the row's k-th value and its candidate vectors.
+//
+// The row pass cuts the logits into one contiguous span per warp of a fixed
+// nominal grid (152 SMs x 12 warps), so that the layout depends on the sizes
+// alone, never on the device.
 constexpr int kCtrlBytes = 256;
-constexpr size_t kMinSpanBytes = 65536;   // smallest contiguous span of logits per CTA
+constexpr size_t kMinSpanBytes = 8192;      // smallest contiguous span of logits per warp of the row pass
+constexpr unsigned long long kRowPassWarps = 152ull * 12ull;
+constexpr int kSlotHeader = 32;             // {f32 max; u32 count; f64 sum; u32 bound; pad}
+
+// Bytes per warp of the row pass for a stream of `total` bytes.
+__host__ __device__ inline unsigned long long row_pass_span(unsigned long long total) {
+  unsigned long long span = (total + kRowPassWarps - 1) / kRowPassWarps;
+  span = (span + 15) & ~15ull;
+  return span < kMinSpanBytes ? kMinSpanBytes : span;
+}
+// Candidate vectors one piece slot holds (about 2.5 times what a piece of
+// the streamed workloads typically keeps).
+__host__ __device__ inline int slot_capacity(int k) { return 8 + 12 * k; }
 
 struct WsLayout {
-  size_t ctrl, row_cnt, clear_bytes;
-  size_t row_off, row_ids, row_base, partials, total;
-  int pmax;          // partial slots per row
-  int pstride;       // bytes per partial
+  size_t ctrl, clear_bytes;
+  size_t row_off, row_ids, row_base, slots, total;
+  unsigned long long wspan;  // bytes per warp when rows are V apart (the smallest span)
+  int pmax;                  // piece slots per row
+  int cp;                    // candidate vectors per slot
+  size_t slot_bytes;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -127,17 +145,19 @@ __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a -
 inline bool ws_layout(long long R, int V, int es, int k, WsLayout* L) {
   if (R < 0 || V < 1 || es < 1 || k < 1 || k > kMaxK) return false;
   const size_t row_bytes = size_t(V) * size_t(es);
-  // every CTA whose span meets the row leaves one partial
-  L->pmax = int((row_bytes + kMinSpanBytes - 1) / kMinSpanBytes) + 1;
-  L->pstride = int(align_up(16 + 8 * size_t(k), 16));
+  // every warp whose span meets the row owns one slot of it; spans are
+  // smallest (so pieces most numerous) when rows are packed V apart
+  L->wspan = row_pass_span((unsigned long long)R * row_bytes);
+  L->pmax = int((row_bytes + L->wspan - 1) / L->wspan) + 1;
+  L->cp = slot_capacity(k);
+  L->slot_bytes = align_up(kSlotHeader + 20 * size_t(L->cp), 16);
   size_t o = 0;
   L->ctrl = o;      o += kCtrlBytes;
-  L->row_cnt = o;   o = align_up(o + 4 * size_t(R), 16);
   L->clear_bytes = o;
   L->row_off = o;   o = align_up(o + 8 * size_t(R), 256);
   L->row_ids = o;   o = align_up(o + 4 * size_t(R) * k, 256);
   L->row_base = o;  o = align_up(o + 8 * size_t(R) * k, 256);
-  L->partials = o;  o = align_up(o + size_t(R) * L->pmax * L->pstride, 256);
+  L->slots = o;     o = align_up(o + size_t(R) * L->pmax * L->slot_bytes, 256);
   L->total = o;
   return true;
 }

@@ -1,47 +1,46 @@
 // dart_rows.cu -- K1: one streaming pass over the logits computing, per row,
-// the temperature log-sum-exp and the k best candidates.
+// the temperature log-sum-exp and the k best candidates, and the row merge
+// that turns the pass's per-piece results into each row's answer.
 //
 // DART, Figure 3 caption: each of the d logit vectors of a sequence supplies
 // the candidates of one depth.  Here every row z[b][j][:] is read exactly once
 // from HBM and reduced to (max, sum of exp((z - max) / T), k best (z, id)).
 //
 // Work split.  The logits are one flat byte stream cut into equal,
-// contiguous, 16-byte-aligned spans, one per CTA (one CTA per SM).  Inside a
-// CTA one producer thread streams its span through a 192 KiB shared-memory
-// ring of stages with cp.async.bulk (an mbarrier per stage counts the bytes
-// in, another counts the 12 consumer warps out); each consumer warp reduces
-// its own slice of every stage: 2 KiB of 24 KiB stages for rows under 256 KiB,
-// 4 KiB of 48 KiB stages for longer rows.  Stages never straddle a row, so all
-// consumer warps of a CTA work on the same row at the same time.
+// contiguous, 16-byte-aligned spans, one per warp (twelve warps per CTA, one
+// CTA per SM).  Warps never wait for one another: each one streams its own
+// span through its own ring of three 4 KiB shared-memory stages, filled by
+// bulk copies (cp.async.bulk, L2 evict-first) that its lane 0 issues three
+// stages ahead of the stage being reduced.  A span may cover the end of one
+// row and the start of the next; each (warp, row) overlap is a piece, with a
+// slot of its own in the workspace.
 //
-// Per slice a lane holds four 16-byte vectors.  One running-max update covers
-// all of them (maxima taken on packed bf16x2 / f16x2 words), the exponentials
-// use packed f32x2 subtract / multiply / add, and one warp vote decides
-// whether any element can enter the top-k.
+// Per stage a lane holds eight 16-byte vectors.  One packed maximum per
+// vector (bf16x2 / f16x2 max on 16-bit types) feeds one running-max update
+// per stage; each element then costs one fused multiply-add, one ex2.approx
+// and one add.
 //
-// Top-k.  Candidates are 64-bit keys (ordered value, then inverted id), so a
-// larger key is a better candidate and equal values fall back to the lower id.
-// An element can only matter if it is >= tau, a lower bound of the row's k-th
-// value.  At a row's first stage every consumer lane posts the maximum of its
-// elements and tau starts at the k-th largest of the 32 column maxima (twelve
-// warps' lane j): disjoint elements, so k of them are at least that large.
-// Consumer warps keep no lists: they append the rare 16-byte vectors whose
-// maximum reaches tau (straight from registers, with their first element id)
-// to a per-row ring in shared memory.  A merger warp expands them into keys,
-// keeps the CTA's best 32 of the row and publishes the list's k-th value as
-// the row's tau.
+// Top-k.  The streaming warps keep no list.  Each lane's running maximum over
+// its elements of the piece is already at hand, and the lanes hold disjoint
+// elements, so the k-th largest of the 32 lane maxima is a lower bound tau of
+// the row's k-th value (k elements of the row reach it).  It only rises; it
+// is recomputed when k lanes have risen above it (one redux.sync min per lane
+// dropped), and warps of one CTA that work on the same row share it through
+// a word in shared memory (atomic max).  A stage's vectors whose maximum
+// reaches tau are copied, 16 bytes and an id with an element mask, into the
+// piece's slot: a vote and a few stores, no chain of shuffles.  Should a slot
+// fill up (inputs with very many near-equal values), the warp replaces its
+// candidates by their k best, which also lifts tau.
 //
-// Row end.  Each consumer warp leaves its (max, scaled sum) in a shared slot
-// and moves on; the merger combines them with the list.  A row inside one
-// span is finished there; a row cut by span borders leaves one partial per
-// CTA, and the last CTA to arrive (an arrival counter, no waiting) merges them
-// and writes the row's results.  All global round trips of a row's end sit on
-// the merger warp, off the stream.
+// Row merge.  A second, small kernel takes one warp per row: it merges the
+// pieces' (max, sum) in piece order, takes the largest of their bounds, keeps
+// the candidate elements that reach it and merges them into the row's k best
+// (warp bitonic merges), and writes the row's results.  Nothing in the
+// streaming kernel waits on another warp or on global memory.
 //
-// Every wait is bounded: on a timeout the kernel raises a flag in shared
-// memory that ends all other waits of the CTA, records the error bit and
-// returns.  Vectors enter the ring in per-warp blocks reserved (and waited
-// for) before any lane writes, so a reserved entry is always written promptly.
+// Every wait (a stage landing) is bounded: on a timeout the warp records the
+// error bit, lets its copies in flight land and returns; the call's results
+// are then invalid.
 #include "dart_common.cuh"
 
 #include <atomic>
@@ -49,25 +48,22 @@
 
 namespace dart {
 
-constexpr int kConsumers = 12;                  // reducing warps per CTA (plus a producer and a merger warp)
-constexpr int kSlice = 2048;                    // bytes one reduce step covers: 4 vectors per lane
-constexpr int kRingBytes = 196608;              // 192 KiB of stages in flight per SM
-constexpr int kMaxStages = 8;                   // 8 x 24 KiB (short rows) or 4 x 48 KiB stages
-constexpr int kVecPerLane = kSlice / 16 / 32;
-constexpr int kRowSlots = 4;                    // rows in flight between the consumers and the merger
-constexpr int kRingVecs = 256;                  // candidate-vector ring per row slot (power of two)
-constexpr uint32_t kSleepNs = 100000;           // longest sleep of one barrier probe
-// Copies in flight always land before their CTA retires: that drain is bounded
-// by about two seconds of SM clock whatever limit the other waits have.
+constexpr int kRowWarps = 12;                     // warps per CTA, one CTA per SM
+constexpr int kRowStages = 3;                     // bulk-copy stages in flight per warp
+constexpr int kStageBytes = 4096;                 // one stage: eight 16-byte vectors per lane
+constexpr int kStageVecs = kStageBytes / 16;
+constexpr int kVecPerLane = kStageVecs / 32;
+constexpr int kTauSlots = 64;                     // rows per CTA that can share a bound
+constexpr int kKeyStage = 32 * 8;                 // keys one expansion round can produce
+constexpr int kRowThreads = kRowWarps * 32;
+constexpr int kMergeWarps = 4;                    // rows per CTA of the row merge
+// Copies in flight always land before their warp retires: that drain is
+// bounded by about two seconds of SM clock whatever limit the other waits have.
 constexpr long long kDrainLimit = 4000000000LL;
 constexpr long long kDefaultWaitLimit = 4000000000LL;
-constexpr int kMergerWarp = kConsumers + 1;
-constexpr int kRowThreads = (kConsumers + 2) * 32;
-static_assert(kVecPerLane == 4, "reduce_slice reduces exactly four vectors per lane");
-static_assert((kRingVecs & (kRingVecs - 1)) == 0, "ring index masking");
-// one warp reserves at most 32 lanes x 4 vectors, and the merger takes at most
-// 32 entries past its head: both fit, so the oldest reservation always proceeds
-static_assert(kRingVecs >= 32 * 4 + 32, "vector ring too small for one warp's reservation");
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+static_assert(kVecPerLane == 8, "stage_reduce reduces exactly eight vectors per lane");
+static_assert(kRowPassWarps % kRowWarps == 0, "whole CTAs");
 
 struct RowsParams {
   const uint8_t* logits;
@@ -75,16 +71,13 @@ struct RowsParams {
   int V, k, es;
   unsigned long long stride;  // elements from one row's start to the next (>= V; the rest is padding)
   float c;                    // log2(e) / T
-  double T;
   double invT;                // 1 / T
-  unsigned long long total;   // R * V * es bytes
-  unsigned long long span;    // bytes per CTA, multiple of 16
-  int grid;
-  int nsub;                   // 2 KiB steps per consumer warp and stage (1 or 2)
-  int pmax, pstride;
+  unsigned long long total;   // bytes from the first element to the last valid one
+  unsigned long long wspan;   // bytes per warp, multiple of 16
+  int pmax, cp;               // slots per row, candidate vectors per slot
+  unsigned long long slot_bytes;
   uint32_t* ctrl;
-  uint32_t* row_cnt;
-  uint8_t* partials;
+  uint8_t* slots;
   double* row_off;
   int32_t* row_ids;
   double* row_base;
@@ -95,22 +88,32 @@ struct RowsParams {
 };
 
 struct __align__(128) RowSmem {
-  uint8_t ring[kRingBytes];
-  uint4 vdata[kRowSlots][kRingVecs];     // candidate vectors of a row (16 bytes of logits each)
-  uint32_t vid[kRowSlots][kRingVecs];    // (element mask << 24) | (first id + 1); 0 = not written yet
-  float2 part[kRowSlots][kConsumers];    // per consumer warp: (max, sum of 2^((z - max) c))
-  uint64_t full[kMaxStages];             // bytes of a stage have landed
-  uint64_t empty[kMaxStages];            // every consumer warp is done with a stage
-  uint64_t row_full[kRowSlots];          // every consumer lane is done with a row
-  uint64_t row_free[kRowSlots];          // the merger is done with a row slot
-  uint32_t tail[kRowSlots];              // keys reserved in a row's ring
-  uint32_t head[kRowSlots];              // keys the merger has taken
-  uint32_t tau[kRowSlots];               // ordered form of the row's best published threshold
-  uint64_t mkeys[32 * 8];                // the merger's surviving keys of one batch
-  uint32_t seed[2][kConsumers][32];      // lane maxima of a row's first stage (alternating rows)
-  uint64_t seed_bar[2];                  // every consumer lane has written its lane maximum
-  uint32_t abort;                        // a wait timed out: every wait gives up
+  uint8_t ring[kRowWarps][kRowStages][kStageBytes];
+  uint64_t keys[kRowWarps][kKeyStage];    // a warp's keys while it compacts a full slot
+  uint64_t full[kRowWarps][kRowStages];   // bytes of a stage have landed
+  uint32_t tau[kTauSlots];                // ordered form of each row's best published bound
 };
+
+// A piece slot: header, then cp vectors of 16 bytes, then cp tags.  A tag is
+// (element mask << 24) | (row index of the vector's first element); the mask
+// says which of the vector's elements are real (a scalar head or tail, or a
+// kept candidate, is a vector with one real element).
+struct SlotView {
+  uint8_t* base;
+  int cp;
+  __device__ float* max_p() const { return reinterpret_cast<float*>(base); }
+  __device__ uint32_t* count_p() const { return reinterpret_cast<uint32_t*>(base + 4); }
+  __device__ double* sum_p() const { return reinterpret_cast<double*>(base + 8); }
+  __device__ uint32_t* bound_p() const { return reinterpret_cast<uint32_t*>(base + 16); }
+  __device__ uint4* vecs() const { return reinterpret_cast<uint4*>(base + kSlotHeader); }
+  __device__ uint32_t* tags() const { return reinterpret_cast<uint32_t*>(base + kSlotHeader + 16 * (size_t)cp); }
+};
+__device__ __forceinline__ SlotView slot_of(const RowsParams& P, long long r, long long p) {
+  SlotView v;
+  v.base = P.slots + ((size_t)r * P.pmax + (size_t)p) * P.slot_bytes;
+  v.cp = P.cp;
+  return v;
+}
 
 // ------------------------------------------------------------- element types
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
@@ -127,6 +130,9 @@ __device__ __forceinline__ uint32_t word(const uint4& r, int i) {
   return i == 0 ? r.x : (i == 1 ? r.y : (i == 2 ? r.z : r.w));
 }
 
+// Per type: elements per vector, a packed maximum of a vector (vpack), the
+// maximum of two packed maxima (pcombine), its float value (punpack), element
+// e of a vector, element pair p as two floats, one scalar load.
 template <int DT> struct Elem;
 template <> struct Elem<DART_F32> {
   static constexpr int kPerVec = 4;
@@ -135,16 +141,16 @@ template <> struct Elem<DART_F32> {
   __device__ static float2 pair(const uint4& r, int p) {
     return make_float2(__uint_as_float(word(r, 2 * p)), __uint_as_float(word(r, 2 * p + 1)));
   }
-  __device__ static float vmax(const uint4& r) {
-    return fmaxf(fmaxf(__uint_as_float(r.x), __uint_as_float(r.y)),
-                 fmaxf(__uint_as_float(r.z), __uint_as_float(r.w)));
+  __device__ static float elem(const uint4& r, int e) { return __uint_as_float(word(r, e)); }
+  __device__ static uint32_t vpack(const uint4& r) {
+    return __float_as_uint(fmaxf(fmaxf(__uint_as_float(r.x), __uint_as_float(r.y)),
+                                 fmaxf(__uint_as_float(r.z), __uint_as_float(r.w))));
   }
-  __device__ static float vmax4(const uint4* r) {
-    return fmaxf(fmaxf(vmax(r[0]), vmax(r[1])), fmaxf(vmax(r[2]), vmax(r[3])));
+  __device__ static uint32_t pcombine(uint32_t a, uint32_t b) {
+    return __float_as_uint(fmaxf(__uint_as_float(a), __uint_as_float(b)));
   }
+  __device__ static float punpack(uint32_t p) { return __uint_as_float(p); }
   __device__ static float scalar(const uint8_t* p) { return __ldg(reinterpret_cast<const float*>(p)); }
-  // a vector holding z as element 0 (the rest -inf)
-  __device__ static uint4 single(float z) { return make_uint4(__float_as_uint(z), 0xFF800000u, 0xFF800000u, 0xFF800000u); }
 };
 template <> struct Elem<DART_BF16> {
   static constexpr int kPerVec = 8;
@@ -154,20 +160,18 @@ template <> struct Elem<DART_BF16> {
     const uint32_t w = word(r, p);
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
   }
-  __device__ static float unpack_max(uint32_t m) {
-    return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+  __device__ static float elem(const uint4& r, int e) {
+    const uint32_t w = word(r, e >> 1);
+    return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
   }
-  __device__ static uint32_t pmax(const uint4& r) { return bmax2(bmax2(r.x, r.y), bmax2(r.z, r.w)); }
-  __device__ static float vmax(const uint4& r) { return unpack_max(pmax(r)); }
-  __device__ static float vmax4(const uint4* r) {
-    return unpack_max(bmax2(bmax2(pmax(r[0]), pmax(r[1])), bmax2(pmax(r[2]), pmax(r[3]))));
+  __device__ static uint32_t vpack(const uint4& r) { return bmax2(bmax2(r.x, r.y), bmax2(r.z, r.w)); }
+  __device__ static uint32_t pcombine(uint32_t a, uint32_t b) { return bmax2(a, b); }
+  __device__ static float punpack(uint32_t m) {
+    return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
   }
   __device__ static float scalar(const uint8_t* p) {
     const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(p));
     return __uint_as_float(uint32_t(h) << 16);
-  }
-  __device__ static uint4 single(float z) {   // z came from a bf16: its top half is exact
-    return make_uint4((__float_as_uint(z) >> 16) | 0xFF800000u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
   }
 };
 template <> struct Elem<DART_F16> {
@@ -178,294 +182,319 @@ template <> struct Elem<DART_F16> {
     const uint32_t w = word(r, p);
     return __half22float2(*reinterpret_cast<const __half2*>(&w));
   }
-  __device__ static float unpack_max(uint32_t m) {
+  __device__ static float elem(const uint4& r, int e) {
+    const uint32_t w = word(r, e >> 1);
+    return __half2float(__ushort_as_half((unsigned short)((e & 1) ? (w >> 16) : (w & 0xFFFFu))));
+  }
+  __device__ static uint32_t vpack(const uint4& r) { return hmax2(hmax2(r.x, r.y), hmax2(r.z, r.w)); }
+  __device__ static uint32_t pcombine(uint32_t a, uint32_t b) { return hmax2(a, b); }
+  __device__ static float punpack(uint32_t m) {
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&m));
     return fmaxf(f.x, f.y);
-  }
-  __device__ static uint32_t pmax(const uint4& r) { return hmax2(hmax2(r.x, r.y), hmax2(r.z, r.w)); }
-  __device__ static float vmax(const uint4& r) { return unpack_max(pmax(r)); }
-  __device__ static float vmax4(const uint4* r) {
-    return unpack_max(hmax2(hmax2(pmax(r[0]), pmax(r[1])), hmax2(pmax(r[2]), pmax(r[3]))));
   }
   __device__ static float scalar(const uint8_t* p) {
     const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(p));
     return __half2float(__ushort_as_half(h));
   }
-  __device__ static uint4 single(float z) {   // z came from an f16: exact
-    return make_uint4(uint32_t(__half_as_ushort(__float2half_rn(z))) | 0xFC000000u, 0xFC00FC00u, 0xFC00FC00u, 0xFC00FC00u);
-  }
 };
 
-// ------------------------------------------------------------ bounded waits
-__device__ __forceinline__ bool aborted(const RowSmem& S) {
-  return *reinterpret_cast<const volatile uint32_t*>(&S.abort) != 0u;
-}
-__device__ __forceinline__ void raise_abort(RowSmem& S, uint32_t* ctrl) {
-  *reinterpret_cast<volatile uint32_t*>(&S.abort) = 1u;
-  set_dev_error(ctrl, DART_DEVERR_WAIT_TIMEOUT);
-}
-__device__ __forceinline__ bool wait_phase_spin(RowSmem& S, uint64_t* bar, uint32_t parity, long long limit,
-                                             uint32_t* ctrl) {
-  const long long t0 = clock64();
-  for (uint32_t it = 1; !mbar_try_wait_hint(bar, parity, kSleepNs); ++it) {
-    if ((it & 63u) != 0u) continue;   // the clock and the abort flag every 64 probes
-    if (aborted(S)) return false;
-    if (clock64() - t0 > limit) {
-      raise_abort(S, ctrl);
-      return false;
-    }
-  }
-  return true;
-}
-// Waits for the phase of `bar` with the given parity; false on a timeout or
-// when another wait of the CTA has timed out.
-__device__ __forceinline__ bool wait_phase(RowSmem& S, uint64_t* bar, uint32_t parity, long long limit,
-                                           uint32_t* ctrl) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return wait_phase_spin(S, bar, parity, limit, ctrl);
-}
 
-// ----------------------------------------------------------------- consumers
-// Where a consumer warp appends candidate vectors of the current row.
-struct VecRing {
-  uint32_t* tail;                  // reservation counter
-  const volatile uint32_t* head;   // entries the merger has taken
-  uint4* vdata;                    // kRingVecs entries
-  volatile uint32_t* vid;          // their (mask << 24) | (id + 1), 0 = not written yet
-  RowSmem* S;
-  uint32_t* ctrl;
-  long long limit;
-};
-
-__device__ __forceinline__ void sts_v4(void* p, const uint4& v) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
-               :: "r"(smem_u32(p)), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
-}
-__device__ __forceinline__ uint4 lds_v4_volatile(const void* p) {
-  uint4 v;
-  asm volatile("ld.volatile.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_u32(p)) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void ring_wait(const VecRing& vr, uint32_t pos) {
-  const long long t0 = clock64();
-  while (pos - *vr.head >= uint32_t(kRingVecs)) {
-    if (aborted(*vr.S)) return;
-    if (clock64() - t0 > vr.limit) {
-      raise_abort(*vr.S, vr.ctrl);
-      return;
-    }
-  }
-}
-// Reserves ring entries for `cnt` vectors of each lane (0..4) as one block for
-// the whole warp and waits, warp-uniformly and before any lane writes, until
-// the ring has room for all of them.  Every reserved entry is then written
-// without waiting, so the merger, which takes entries in order, never waits on
-// an entry whose writer waits on the merger.  Returns false (nothing
-// reserved) when no lane has a vector; *pos is the lane's first entry.
-__device__ __forceinline__ bool warp_reserve(const VecRing& vr, uint32_t cnt, uint32_t* pos) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, cnt & 1u);
-  const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, cnt & 2u);
-  const uint32_t b2 = __ballot_sync(0xFFFFFFFFu, cnt & 4u);
-  const uint32_t total = uint32_t(__popc(b0) + 2 * __popc(b1) + 4 * __popc(b2));
-  if (total == 0u) return false;
-  const uint32_t below = (1u << lane) - 1u;
-  uint32_t base = 0;
-  if (lane == 0) {
-    base = atomicAdd(vr.tail, total);
-    if (base + total - 1u - *vr.head >= uint32_t(kRingVecs)) ring_wait(vr, base + total - 1u);
-  }
-  base = __shfl_sync(0xFFFFFFFFu, base, 0);
-  *pos = base + uint32_t(__popc(b0 & below) + 2 * __popc(b1 & below) + 4 * __popc(b2 & below));
-  return true;
-}
-// One entry: the vector first, then (after a fence) its tag, which the merger polls.
-__device__ __forceinline__ void ring_put(const VecRing& vr, uint32_t pos, const uint4& v, uint32_t tag) {
-  const uint32_t i = pos & uint32_t(kRingVecs - 1);
-  sts_v4(vr.vdata + i, v);
-  __threadfence_block();
-  vr.vid[i] = tag;
-}
-
-// Appends the lane's vectors of a 2 KiB step whose maximum reaches tau
-// (vector u*32 + lane holds elements id_base + (u*32 + lane) * EPV ...).
-template <int DT, bool FULL>
-__device__ __forceinline__ void push_vectors(const uint4 (&raw)[kVecPerLane], int nvec, uint32_t id_base, float tau,
-                                             const VecRing& vr) {
-  using E = Elem<DT>;
-  constexpr int EPV = E::kPerVec;
-  constexpr uint32_t kMask = (1u << EPV) - 1u;
-  const int lane = threadIdx.x & 31;
-  uint32_t hm = 0;
-#pragma unroll
-  for (int u = 0; u < kVecPerLane; ++u)
-    if ((FULL || u * 32 + lane < nvec) && E::vmax(raw[u]) >= tau) hm |= 1u << u;
-  uint32_t pos;
-  if (!warp_reserve(vr, uint32_t(__popc(hm)), &pos)) return;
-#pragma unroll
-  for (int u = 0; u < kVecPerLane; ++u)
-    if ((hm >> u) & 1u) ring_put(vr, pos++, raw[u], (kMask << 24) | (id_base + uint32_t((u * 32 + lane) * EPV) + 1u));
-  __syncwarp();
-}
-
-// Bitonic sort of one 32-bit value per lane, descending (lane 0 largest).
-__device__ __forceinline__ uint32_t warp_sort_desc_u32(uint32_t v) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, v, stride);
-      const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
-      v = keep_max ? max(v, o) : min(v, o);
-    }
-  }
-  return v;
-}
-
-// CTA-wide seed of a row's threshold from its first stage.  Every consumer
-// lane posts the maximum of its elements of the stage; lane j then takes the
-// maximum of column j (the twelve warps' lane j), and the k-th largest of
-// those 32 column maxima is a lower bound of the row's k-th value: the
-// columns cover disjoint elements, so k distinct elements are at least that
-// large.  Returns the bound in ordered form (0 = none or a wait gave up).
+// A vector whose element 0 is z (from a logit of this type, so exact) and
+// whose other elements are -inf; its tag mask is 1.
 template <int DT>
-__device__ __forceinline__ uint32_t seed_stage(const uint4* src, int nvec, RowSmem* Sp, int nseed, int w, int k,
-                                            long long limit, uint32_t* ctrl) {
-  using E = Elem<DT>;
-  RowSmem& S = *Sp;
-  const int lane = threadIdx.x & 31;
-  float vm = -INFINITY;
-#pragma unroll 2
-  for (int v = lane; v < nvec; v += 32) vm = fmaxf(vm, E::vmax(src[v]));
-  const int sb = nseed & 1;
-  S.seed[sb][w][lane] = lane < nvec ? ord_f32(vm) : 0u;
-  mbar_arrive(&S.seed_bar[sb]);
-  if (!__all_sync(0xFFFFFFFFu, wait_phase(S, &S.seed_bar[sb], uint32_t(nseed >> 1) & 1u, limit, ctrl))) return 0u;
-  uint32_t col = 0;
-#pragma unroll
-  for (int i = 0; i < kConsumers; ++i) col = max(col, S.seed[sb][i][lane]);
-  const uint32_t v = warp_sort_desc_u32(col);
-  return __shfl_sync(0xFFFFFFFFu, v, k - 1);
+__device__ __forceinline__ uint4 single_vec(float z) {
+  uint4 v = Elem<DT>::neg_inf();
+  if (DT == DART_F32) v.x = __float_as_uint(z);
+  else if (DT == DART_BF16) v.x = (__float_as_uint(z) >> 16) | 0xFF800000u;
+  else v.x = uint32_t(__half_as_ushort(__float2half_rn(z))) | 0xFC000000u;
+  return v;
 }
 
-// Per-warp state for one row segment.
+// ----------------------------------------------------------- piece state
 // A lane's sum s is kept against mc = fl(m c) rather than m c: each term is
 // 2^fma(z, c, -mc), one fused multiply-add per element.  Since m c - mc is
-// exact in float (fma(m, c, -mc)), the row end turns s back into the sum of
+// exact in float (fma(m, c, -mc)), the piece end turns s back into the sum of
 // 2^((z - m) c).
-struct RowCtx {
-  float m, mc, s;        // per lane: running max of z, fl(m c), sum of 2^(z c - mc)
-  uint32_t tau_ord;      // ordered form of the filter threshold (0 = none yet)
-  float tau;             // filter threshold value (-inf = none yet)
-  uint32_t* tau_slot;    // the row's shared threshold
+struct Acc {
+  float m, mc, s;     // per lane: running max of z, fl(m c), sum of 2^(z c - mc)
 };
 
-__device__ __forceinline__ void raise_tau(RowCtx& rc, uint32_t o) {
-  if (o > rc.tau_ord) {
-    rc.tau_ord = o;
-    rc.tau = unord_f32(o);
-  }
-}
-// Adopt a larger threshold published for the row.
-__device__ __forceinline__ void refresh_tau(RowCtx& rc) {
-  raise_tau(rc, *reinterpret_cast<volatile uint32_t*>(rc.tau_slot));
-}
+__device__ __forceinline__ float tau_value(uint32_t o) { return o != 0u ? unord_f32(o) : -INFINITY; }
 
 // fl(m c), kept finite (-FLT_MAX before the first element) so that
 // fma(-inf, c, -mc) stays -inf.
 __device__ __forceinline__ float scaled_max(float m, float c) { return fmaxf(m * c, -FLT_MAX); }
 // Raises the lane's running max to v (if larger), rescaling its sum.
-__device__ __forceinline__ void raise_max(float& m, float& mc, float& s, float v, float c) {
-  if (v > m) {
+__device__ __forceinline__ void raise_max(Acc& a, float v, float c) {
+  if (v > a.m) {
     const float mcn = scaled_max(v, c);
-    s *= ex2_approx(mc - mcn);
-    m = v;
-    mc = mcn;
+    a.s *= ex2_approx(a.mc - mcn);
+    a.m = v;
+    a.mc = mcn;
   }
 }
 // s against exact m c: s * 2^-(m c - mc).  0 stays 0.
-__device__ __forceinline__ float exact_sum(float m, float mc, float s, float c) {
-  return s > 0.f ? s * ex2_approx(-fmaf(m, c, -mc)) : 0.f;
+__device__ __forceinline__ float exact_sum(const Acc& a, float c) {
+  return a.s > 0.f ? a.s * ex2_approx(-fmaf(a.m, c, -a.mc)) : 0.f;
 }
 
-// The hot path: one 2 KiB slice (four vectors per lane; a partial slice at
-// the end of a row holds nvec < 128 vectors, the rest read as -inf, whose
-// terms are exactly 0).  Updates the lane's (max, sum) and, when some vector
-// reaches tau, appends those vectors to the row's ring.
-template <int DT, bool FULL>
-__device__ __forceinline__ void reduce_slice(RowCtx& rc, const uint4* src, int nvec, float c, uint32_t id_base,
-                                             const VecRing& vr) {
+// Exclusive prefix and total over the warp of a per-lane count in 0..15.
+__device__ __forceinline__ int warp_prefix4(uint32_t cnt, int* total) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t below = (1u << lane) - 1u;
+  const uint32_t q0 = __ballot_sync(kFull, cnt & 1u), q1 = __ballot_sync(kFull, cnt & 2u);
+  const uint32_t q2 = __ballot_sync(kFull, cnt & 4u), q3 = __ballot_sync(kFull, cnt & 8u);
+  *total = __popc(q0) + 2 * __popc(q1) + 4 * __popc(q2) + 8 * __popc(q3);
+  return __popc(q0 & below) + 2 * __popc(q1 & below) + 4 * __popc(q2 & below) + 8 * __popc(q3 & below);
+}
+
+// The k-th largest of the lanes' values v (ordered floats, 0 = a lane
+// without elements) among those above `above`, or `above` when fewer than k
+// lanes are above it: the values below the k-th are dropped one lane at a
+// time (a redux.sync min each).
+__device__ __forceinline__ uint32_t kth_above(uint32_t v, uint32_t above, int k) {
+  const int lane = threadIdx.x & 31;
+  bool cand = v > above;
+  const int c = __popc(__ballot_sync(kFull, cand));
+  if (c < k) return above;
+  for (int i = c - k; i > 0; --i) {
+    const uint32_t mn = __reduce_min_sync(kFull, cand ? v : 0xFFFFFFFFu);
+    const uint32_t b = __ballot_sync(kFull, cand && v == mn);
+    if (lane == __ffs(b) - 1) cand = false;
+  }
+  return __reduce_min_sync(kFull, cand ? v : 0xFFFFFFFFu);
+}
+
+// Keys (ordered value, inverted id) of the real elements of a vector that
+// reach tau; element e of a vector tagged (mask << 24) | id0 has id id0 + e.
+template <int DT>
+__device__ __forceinline__ uint32_t vec_hits(const uint4& v, uint32_t tag, float tau) {
+  uint32_t cm = 0;
+#pragma unroll
+  for (int e = 0; e < Elem<DT>::kPerVec; ++e)
+    if (((tag >> (24 + e)) & 1u) && Elem<DT>::elem(v, e) >= tau) cm |= 1u << e;
+  return cm;
+}
+
+// Merges the keys of up to 32 vectors (one per lane, the elements in cm)
+// into the warp's best-32 list through the warp's key stage in shared memory.
+template <int DT>
+__device__ __forceinline__ uint64_t merge_vec_keys(uint64_t list, uint64_t* stage, const uint4& v, uint32_t tag,
+                                                   uint32_t cm) {
+  const int lane = threadIdx.x & 31;
+  int nkeys;
+  int at = warp_prefix4(uint32_t(__popc(cm)), &nkeys);
+  const uint32_t id0 = tag & 0xFFFFFFu;
+  while (cm) {
+    const int e = __ffs(cm) - 1;
+    cm &= cm - 1u;
+    stage[at++] = elem_key(Elem<DT>::elem(v, e), id0 + uint32_t(e));
+  }
+  __syncwarp();
+  for (int q0 = 0; q0 < nkeys; q0 += 32) {
+    const uint64_t x = q0 + lane < nkeys ? stage[q0 + lane] : 0ull;
+    if (__any_sync(kFull, x != 0ull)) list = warp_merge_top32(list, x);
+  }
+  __syncwarp();
+  return list;
+}
+
+// A full slot: its candidates are replaced by their k best (tau rises to the
+// k-th of them when there are k).  Rare: only inputs with very many
+// near-equal values get here.
+template <int DT>
+__device__ __forceinline__ void compact_slot(const SlotView& sv, int& cnt, uint32_t& tau_o, uint64_t* stage, int k) {
+  const int lane = threadIdx.x & 31;
+  __threadfence_block();   // the lanes' candidate stores before the reads below
+  __syncwarp();
+  const float tau = tau_value(tau_o);
+  uint64_t list = 0;
+  for (int b0 = 0; b0 < cnt; b0 += 32) {
+    const int i = b0 + lane;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    uint32_t tag = 0;
+    if (i < cnt) {
+      v = __ldcg(sv.vecs() + i);
+      tag = __ldcg(sv.tags() + i);
+    }
+    list = merge_vec_keys<DT>(list, stage, v, tag, i < cnt ? vec_hits<DT>(v, tag, tau) : 0u);
+  }
+  const bool keep = lane < k && list != 0ull;
+  cnt = __popc(__ballot_sync(kFull, keep));
+  if (keep) {
+    sv.vecs()[lane] = single_vec<DT>(key_value(list));
+    sv.tags()[lane] = (1u << 24) | key_id(list);
+  }
+  if (cnt == k) {
+    const uint32_t o = uint32_t(__shfl_sync(kFull, list, k - 1) >> 32);
+    if (o > tau_o) tau_o = o;
+  }
+  __syncwarp();
+}
+
+// Appends the lanes' candidate vectors (vector u of the lane when bit u of
+// hm is set; its tag in tags[u]) to the slot, compacting whenever it is full.
+template <int DT>
+__device__ __forceinline__ void slot_append(const SlotView& sv, int& cnt, uint32_t& tau_o, uint64_t* stage, int k,
+                                            const uint4 (&r)[kVecPerLane], uint32_t hm, uint32_t id0) {
+  constexpr int EPV = Elem<DT>::kPerVec;
+  constexpr uint32_t kMask = ((1u << EPV) - 1u) << 24;
+  const int lane = threadIdx.x & 31;
+  int total;
+  const int first = warp_prefix4(uint32_t(__popc(hm)), &total);
+  int done = 0;
+  while (done < total) {
+    if (cnt == sv.cp) compact_slot<DT>(sv, cnt, tau_o, stage, k);
+    const int take = min(sv.cp - cnt, total - done);
+    int q = first;
+#pragma unroll
+    for (int u = 0; u < kVecPerLane; ++u) {
+      if ((hm >> u) & 1u) {
+        if (q >= done && q < done + take) {
+          sv.vecs()[cnt + q - done] = r[u];
+          sv.tags()[cnt + q - done] = kMask | (id0 + uint32_t((u * 32 + lane) * EPV));
+        }
+        ++q;
+      }
+    }
+    cnt += take;
+    done += take;
+  }
+}
+
+// The hot path: one stage of nv vectors (nv <= 256; vectors past nv read as
+// -inf, whose terms are exactly 0).  id0 = row index of the stage's first
+// element.  SEED: the stage opens a piece (its lanes' maxima are all new).
+template <int DT, bool SEED>
+__device__ __forceinline__ void stage_reduce(Acc& a, uint32_t& tau_o, int& cnt, const SlotView& sv, uint64_t* kstage,
+                                             const uint4* src, int nv, uint32_t id0, float c, int k,
+                                             uint32_t* tau_slot) {
   using E = Elem<DT>;
   constexpr int EPV = E::kPerVec;
   constexpr int U = kVecPerLane;
   const int lane = threadIdx.x & 31;
-  uint4 raw[U];
+  const bool whole = nv == kStageVecs;
+  uint4 r[U];
+  uint32_t pm[U];
 #pragma unroll
-  for (int u = 0; u < U; ++u) {
-    if (FULL) raw[u] = src[u * 32 + lane];
-    else raw[u] = (u * 32 + lane < nvec) ? src[u * 32 + lane] : E::neg_inf();
+  for (int u = 0; u < U; ++u) r[u] = src[u * 32 + lane];   // a stage buffer is always 4 KiB
+  if (!whole) {
+    // a row's last stage: vectors past nv hold stale bytes; read them as -inf
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (u * 32 + lane >= nv) r[u] = E::neg_inf();
   }
-  const float vm = E::vmax4(raw);
-  raise_max(rc.m, rc.mc, rc.s, vm, c);
-  const float2 nmc2 = make_float2(-rc.mc, -rc.mc);
-  const float2 c2 = make_float2(c, c);
-  float2 acc[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) pm[u] = E::vpack(r[u]);
+  uint32_t pa = pm[0];
+#pragma unroll
+  for (int u = 1; u < U; ++u) pa = E::pcombine(pa, pm[u]);
+  const float vm = E::punpack(pa);
+  raise_max(a, vm, c);
+  // the bound: k-th largest lane maximum of the piece so far (lanes without
+  // an element post 0), raised only when k lanes are above it
+  {
+    const uint32_t post = a.m > -FLT_MAX ? ord_f32(a.m) : 0u;
+    uint32_t o = tau_o;
+    if (SEED || __popc(__ballot_sync(kFull, post > o)) >= k) o = kth_above(post, o, k);
+    if (tau_slot) {
+      if (o > tau_o && lane == 0) atomicMax(tau_slot, o);
+      const uint32_t so = *reinterpret_cast<volatile uint32_t*>(tau_slot);
+      if (so > o) o = so;
+    }
+    tau_o = o;
+  }
+  // one fused multiply-add, one exponential and one add per element, into
+  // eight independent sums (element e of every vector goes to sum e)
+  const float nmc = -a.mc;
+  float acc[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) acc[q] = 0.f;
 #pragma unroll
   for (int u = 0; u < U; ++u) {
-    acc[u] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int p = 0; p < EPV / 2; ++p) {
-      const float2 t = __ffma2_rn(E::pair(raw[u], p), c2, nmc2);
-      acc[u] = __fadd2_rn(acc[u], make_float2(ex2_approx(t.x), ex2_approx(t.y)));
+      const float2 z = E::pair(r[u], p);
+      acc[(2 * p) & 7] += ex2_approx(fmaf(z.x, c, nmc));
+      acc[(2 * p + 1) & 7] += ex2_approx(fmaf(z.y, c, nmc));
     }
   }
-  const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-  rc.s += a.x + a.y;
-  // absent vectors hold -inf, which must not pass while tau is still -inf
-  const bool lane_hit = (FULL || lane < nvec) && vm >= rc.tau;
-  if (__ballot_sync(0xFFFFFFFFu, lane_hit) != 0u) push_vectors<DT, FULL>(raw, nvec, id_base, rc.tau, vr);
-}
-
-// The end of a row: up to NSUB partial-or-full 2 KiB steps of nvec vectors.
-template <int DT, int NSUB>
-__device__ __forceinline__ void reduce_tail_stage(RowCtx* rcp, const uint4* src, int nvec, uint32_t id_base, int SH,
-                                               float c, const VecRing& vr) {
-  RowCtx rc = *rcp;
-#pragma unroll 1
-  for (int j = 0; j < NSUB; ++j) {
-    const int nv = min(nvec - j * (kSlice / 16), kSlice / 16);
-    if (nv <= 0) break;
-    reduce_slice<DT, false>(rc, src + j * (kSlice / 16), nv, c, id_base + uint32_t((j * kSlice) >> SH), vr);
+  a.s += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+  // candidates: absent vectors hold -inf, which must not pass while tau is -inf
+  const float tau = tau_value(tau_o);
+  if (__ballot_sync(kFull, lane < nv && vm >= tau) != 0u) {
+    // vectors past nv are -inf and tau is finite here unless no bound
+    // exists yet, so the index test only matters in partial stages
+    uint32_t hm = 0;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (E::punpack(pm[u]) >= tau) hm |= 1u << u;
+    if (!whole) {
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (u * 32 + lane >= nv) hm &= ~(1u << u);
+    }
+    int total;
+    int pos = warp_prefix4(uint32_t(__popc(hm)), &total);
+    if (cnt + total <= sv.cp) {
+      constexpr uint32_t kMask = ((1u << EPV) - 1u) << 24;
+      pos += cnt;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if ((hm >> u) & 1u) {
+          sv.vecs()[pos] = r[u];
+          sv.tags()[pos] = kMask | (id0 + uint32_t((u * 32 + lane) * EPV));
+          ++pos;
+        }
+      }
+      cnt += total;
+    } else {
+      slot_append<DT>(sv, cnt, tau_o, kstage, k, r, hm, id0);
+    }
   }
-  *rcp = rc;
 }
 
-// Unaligned elements [b0, b1) of a segment (its head or tail), one per lane.
+// Unaligned elements [b0, b1) of a piece (its head or tail), one per lane;
+// a candidate becomes a one-element vector.
 template <int DT>
-__device__ __noinline__ float2 reduce_scalars(const uint8_t* logits, unsigned long long b0, unsigned long long b1,
-                                              int es, uint32_t id0, float c, float m, float s, float tau,
-                                              const VecRing vr) {
+__device__ __forceinline__ void piece_scalars(Acc& a, uint32_t& tau_o, int& cnt, const SlotView& sv,
+                                              uint64_t* kstage, const uint8_t* logits, unsigned long long b0,
+                                              unsigned long long b1, int es, uint32_t id0, float c, int k) {
   const int lane = threadIdx.x & 31;
-  const int cnt = int((b1 - b0) / es);
-  for (int base = 0; base < cnt; base += 32) {
+  const int n = int((b1 - b0) / es);
+  for (int base = 0; base < n; base += 32) {
     const int i = base + lane;
-    bool hit = false;
-    float z = 0.f;
-    if (i < cnt) {
+    float z = -INFINITY;
+    if (i < n) {
       z = Elem<DT>::scalar(logits + b0 + (unsigned long long)i * es);
-      float mc = scaled_max(m, c);
-      raise_max(m, mc, s, z, c);
-      s += ex2_approx(fmaf(z, c, -mc));
-      hit = z >= tau;
+      raise_max(a, z, c);
+      a.s += ex2_approx(fmaf(z, c, -a.mc));
     }
-    uint32_t pos;
-    if (warp_reserve(vr, hit ? 1u : 0u, &pos) && hit) ring_put(vr, pos, Elem<DT>::single(z), (1u << 24) | (id0 + uint32_t(i) + 1u));
+    const bool hit = i < n && z >= tau_value(tau_o);
+    int total;
+    const int at = warp_prefix4(hit ? 1u : 0u, &total);
+    if (total == 0) continue;
+    if (cnt + total > sv.cp) compact_slot<DT>(sv, cnt, tau_o, kstage, k);
+    if (cnt + total > sv.cp) {
+      // still no room for 32 (k close to the slot size): one at a time
+      for (int j = 0; j < 32; ++j) {
+        const bool mine = hit && at == j;
+        if (!__any_sync(kFull, mine)) continue;
+        if (cnt == sv.cp) compact_slot<DT>(sv, cnt, tau_o, kstage, k);
+        if (mine) {
+          sv.vecs()[cnt] = single_vec<DT>(z);
+          sv.tags()[cnt] = (1u << 24) | (id0 + uint32_t(i));
+        }
+        ++cnt;
+      }
+      continue;
+    }
+    if (hit) {
+      sv.vecs()[cnt + at] = single_vec<DT>(z);
+      sv.tags()[cnt + at] = (1u << 24) | (id0 + uint32_t(i));
+    }
+    cnt += total;
   }
-  __syncwarp();
-  return make_float2(m, s);
 }
 
 struct Seg {
@@ -474,7 +503,7 @@ struct Seg {
 };
 
 // The part of row r (its V valid elements; padding up to the row stride is
-// never read) that lies in the span [e0, e1).
+// never read) that lies in the element range [e0, e1).
 __device__ __forceinline__ Seg segment(const RowsParams& P, unsigned long long e0, unsigned long long e1,
                                        long long r) {
   Seg g;
@@ -489,13 +518,211 @@ __device__ __forceinline__ Seg segment(const RowsParams& P, unsigned long long e
   return g;
 }
 
-// ------------------------------------------------------------------ row end
+// First and last warp whose span meets row r.
+__device__ __forceinline__ void row_warps(const RowsParams& P, long long r, long long* wa, long long* wb) {
+  const unsigned long long rb0 = (unsigned long long)r * P.stride * P.es;
+  *wa = (long long)(rb0 / P.wspan);
+  *wb = (long long)((rb0 + (unsigned long long)P.V * P.es - 1) / P.wspan);
+}
+
+// The end of a piece: the warp's (max, sum), count and bound into its slot.
+__device__ __forceinline__ void piece_end(const RowsParams& P, const SlotView& sv, const Acc& a, int cnt,
+                                          uint32_t tau_o) {
+  const int lane = threadIdx.x & 31;
+  float m = a.m, s = exact_sum(a, P.c);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(kFull, m, o);
+    const float s2 = __shfl_xor_sync(kFull, s, o);
+    const float M = fmaxf(m, m2);
+    s = s * ex2_approx((m - M) * P.c) + s2 * ex2_approx((m2 - M) * P.c);
+    m = M;
+  }
+  if (lane == 0) {
+    *sv.max_p() = m;
+    *sv.count_p() = uint32_t(cnt);
+    *sv.sum_p() = double(s);
+    *sv.bound_p() = tau_o;
+  }
+}
+
+// Next stage of a warp's span after byte `off` of row r (a stage starts at
+// off, covers min(4 KiB, end of the row's interior - off)); moves on to later
+// rows when the row's interior is used up.  valid = false past the span.
+struct Cursor {
+  long long r;
+  unsigned long long off, b;   // stage start, end of the row's interior (bytes)
+  bool valid;
+};
+__device__ __forceinline__ void cursor_seek(const RowsParams& P, Cursor& cu, unsigned long long e0,
+                                            unsigned long long e1, long long r_last) {
+  while (cu.r <= r_last) {
+    const Seg g = segment(P, e0, e1, cu.r);
+    if (g.a < g.b) {
+      cu.off = g.a;
+      cu.b = g.b;
+      cu.valid = true;
+      return;
+    }
+    ++cu.r;
+  }
+  cu.valid = false;
+}
+__device__ __forceinline__ void cursor_next(const RowsParams& P, Cursor& cu, unsigned long long e0,
+                                            unsigned long long e1, long long r_last) {
+  cu.off += kStageBytes;
+  if (cu.off < cu.b) return;
+  ++cu.r;
+  cursor_seek(P, cu, e0, e1, r_last);
+}
+
+// Waits for a stage to land until `limit` clock cycles have passed (false).
+// Probes may suspend the thread until the phase completes; short limits
+// (tests of the timeout path) probe without suspending, so that the clock
+// decides.
+constexpr long long kSuspendingWaitMin = 100000;
+__device__ __forceinline__ bool stage_wait(uint64_t* bar, uint32_t parity, long long limit) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (limit >= kSuspendingWaitMin ? mbar_try_wait(bar, parity) : mbar_test_wait(bar, parity)) return true;
+    if (clock64() - t0 > limit) return false;
+  }
+}
+
+// -------------------------------------------------------------------- kernel
+template <int DT>
+__global__ void __launch_bounds__(kRowThreads, 1)
+row_stream_kernel(const __grid_constant__ RowsParams P) {
+  constexpr int SH = Elem<DT>::kShift;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  RowSmem& S = *reinterpret_cast<RowSmem*>(smem_raw);
+  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  const long long gwarp = (long long)blockIdx.x * kRowWarps + w;
+
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    // rows of this call, for the error readout
+    P.ctrl[2] = uint32_t((unsigned long long)P.R);
+    P.ctrl[3] = uint32_t((unsigned long long)P.R >> 32);
+  }
+  for (int i = threadIdx.x; i < kTauSlots; i += blockDim.x) S.tau[i] = 0u;
+  if (lane == 0) {
+    for (int s = 0; s < kRowStages; ++s) mbar_init(&S.full[w][s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // the warp's span and the rows whose valid elements meet it
+  const unsigned long long B0 = (unsigned long long)gwarp * P.wspan;
+  if (B0 >= P.total) return;
+  const unsigned long long B1 = (B0 + P.wspan < P.total) ? B0 + P.wspan : P.total;
+  const unsigned long long e0 = B0 / P.es, e1 = B1 / P.es;
+  long long r_first = (long long)(e0 / P.stride);
+  if (e0 - (unsigned long long)r_first * P.stride >= (unsigned long long)P.V) ++r_first;
+  const long long r_last = (long long)((e1 - 1) / P.stride);
+  // rows of the CTA that share a bound word
+  const unsigned long long cta_e0 = ((unsigned long long)blockIdx.x * kRowWarps * P.wspan) / P.es;
+  const long long cta_r0 = (long long)(cta_e0 / P.stride);
+
+  const uint64_t pol = policy_evict_first();
+  uint8_t* ring = &S.ring[w][0][0];
+  uint64_t* full = &S.full[w][0];
+  uint64_t* kstage = S.keys[w];
+  // lane 0 issues the stages; every lane follows the same sequence to consume them
+  Cursor iss;
+  iss.r = r_first;
+  cursor_seek(P, iss, e0, e1, r_last);
+  // stages issued / consumed so far; a stage's ring slot and phase follow
+  // from its number (slot = n mod kRowStages, phase parity = (n / kRowStages) & 1)
+  uint32_t issued = 0, consumed = 0;
+  int islot = 0, cslot = 0;
+  uint32_t cpar = 0;
+  auto issue = [&]() {
+    const uint32_t bytes = uint32_t((iss.b - iss.off) < (unsigned long long)kStageBytes ? (iss.b - iss.off)
+                                                                                        : kStageBytes);
+    mbar_expect_tx(&full[islot], bytes);
+    bulk_g2s(ring + (size_t)islot * kStageBytes, P.logits + iss.off, bytes, &full[islot], pol);
+    ++issued;
+    if (++islot == kRowStages) islot = 0;
+    cursor_next(P, iss, e0, e1, r_last);
+  };
+  if (lane == 0)
+    for (int s = 0; s < kRowStages && iss.valid; ++s) issue();
+  issued = __shfl_sync(kFull, issued, 0);
+
+  bool ok = true;
+  for (long long r = r_first; r <= r_last && ok; ++r) {
+    const Seg g = segment(P, e0, e1, r);
+    if (g.s1 <= g.s0) continue;
+    const unsigned long long rs = (unsigned long long)r * P.stride;
+    const long long slot_i = r - cta_r0;
+    uint32_t* tau_slot = (slot_i >= 0 && slot_i < kTauSlots) ? &S.tau[slot_i] : nullptr;
+    long long wa, wb;
+    row_warps(P, r, &wa, &wb);
+    const SlotView sv = slot_of(P, r, gwarp - wa);
+    Acc a;
+    a.m = -FLT_MAX;
+    a.mc = scaled_max(a.m, P.c);
+    a.s = 0.f;
+    uint32_t tau_o = tau_slot ? *reinterpret_cast<volatile uint32_t*>(tau_slot) : 0u;
+    int cnt = 0;
+    // head: [s0, a) (or the whole piece when nothing is aligned)
+    {
+      const unsigned long long hb0 = g.s0 * P.es;
+      const unsigned long long hb1 = (g.a < g.b) ? g.a : g.s1 * P.es;
+      if (hb1 > hb0) piece_scalars<DT>(a, tau_o, cnt, sv, kstage, P.logits, hb0, hb1, P.es, uint32_t(g.s0 - rs), P.c, P.k);
+    }
+    // aligned interior, stage by stage (offsets within the interior fit 32 bits)
+    const uint32_t ilen = uint32_t(g.b - g.a);
+    const uint32_t id_a = uint32_t((g.a >> SH) - rs);
+    for (uint32_t o = 0; o < ilen; o += kStageBytes) {
+      if (!__all_sync(kFull, stage_wait(&full[cslot], cpar, P.wait_limit))) {
+        ok = false;
+        break;
+      }
+      const uint4* src = reinterpret_cast<const uint4*>(ring + cslot * kStageBytes);
+      const uint32_t rem = ilen - o;
+      const int nv = int((rem < uint32_t(kStageBytes) ? rem : uint32_t(kStageBytes)) >> 4);
+      const uint32_t id0 = id_a + (o >> SH);
+      if (o == 0) stage_reduce<DT, true>(a, tau_o, cnt, sv, kstage, src, nv, id0, P.c, P.k, tau_slot);
+      else stage_reduce<DT, false>(a, tau_o, cnt, sv, kstage, src, nv, id0, P.c, P.k, tau_slot);
+      __syncwarp();
+      ++consumed;
+      if (++cslot == kRowStages) {
+        cslot = 0;
+        cpar ^= 1u;
+      }
+      if (lane == 0 && iss.valid) issue();
+      issued = __shfl_sync(kFull, issued, 0);
+    }
+    if (!ok) break;
+    // tail: [b, s1)
+    if (g.a < g.b && g.s1 * P.es > g.b)
+      piece_scalars<DT>(a, tau_o, cnt, sv, kstage, P.logits, g.b, g.s1 * P.es, P.es, uint32_t((g.b >> SH) - rs), P.c,
+                        P.k);
+    piece_end(P, sv, a, cnt, tau_o);
+  }
+  if (!ok) {
+    set_dev_error(lane == 0 ? P.ctrl : nullptr, DART_DEVERR_WAIT_TIMEOUT);
+    // the warp may not retire while a copy still writes its ring; these
+    // waits are bounded by the clock alone
+    if (lane == 0) {
+      for (uint32_t q = consumed; q < issued; ++q) {
+        if (!mbar_wait_bounded(&full[q % kRowStages], (q / kRowStages) & 1u, kDrainLimit)) break;
+      }
+    }
+    __syncwarp();
+  }
+}
+
+// ---------------------------------------------------------------- row merge
 // Writes a row's results from its maximum M, its sum S of 2^((z - M) c) and
 // its best keys (lanes 0..k-1 hold them, descending).
 __device__ __forceinline__ void finish_row(const RowsParams& P, long long r, float M, double S, uint64_t list) {
   const int lane = threadIdx.x & 31;
   const int k = P.k;
-  const float zmax = key_value(__shfl_sync(0xFFFFFFFFu, list, 0));
+  const float zmax = key_value(__shfl_sync(kFull, list, 0));
   if (lane == 0 && zmax != M) set_dev_error(P.ctrl, DART_DEVERR_ROW_MAX);
   // log S = e ln 2 + log f with S = f 2^e, f in [0.5, 1): one float log of
   // the mantissa keeps the slow double unit to a multiply and an add
@@ -517,429 +744,137 @@ __device__ __forceinline__ void finish_row(const RowsParams& P, long long r, flo
   }
 }
 
-// Global partial of one CTA for one row: [f32 max][4 pad][f64 sum][k keys].
-// The last CTA to finish a row merges all of that row's partials.
-__device__ __forceinline__ void merge_row(const RowsParams& P, long long r, int nseg) {
+// Merges the first n keys of a warp's key stage into its best-32 list.
+__device__ __forceinline__ uint64_t merge_staged(uint64_t list, const uint64_t* stage, int n) {
   const int lane = threadIdx.x & 31;
-  const int k = P.k;
-  const uint8_t* base = P.partials + (size_t)r * P.pmax * P.pstride;
-  float M = -FLT_MAX;
-  uint64_t tstar = 0;
-  for (int p = lane; p < nseg; p += 32) {
-    const uint8_t* q = base + (size_t)p * P.pstride;
-    M = fmaxf(M, __ldcg(reinterpret_cast<const float*>(q)));
-    const uint64_t kth = __ldcg(reinterpret_cast<const unsigned long long*>(q + 16) + (k - 1));
-    tstar = kth > tstar ? kth : tstar;
+  for (int q0 = 0; q0 < n; q0 += 32) {
+    const uint64_t x = q0 + lane < n ? stage[q0 + lane] : 0ull;
+    if (__any_sync(kFull, x != 0ull)) list = warp_merge_top32(list, x);
   }
+  __syncwarp();
+  return list;
+}
+
+// One warp per row: the pieces' (max, sum) merged in piece order, the
+// largest of their bounds, and the row's k best among the candidates that
+// reach it.  All candidate loads of a round (eight per lane) are issued
+// together; the passing elements' keys are staged in shared memory and
+// merged once at the end (earlier only if the stage fills).
+template <int DT>
+__global__ void __launch_bounds__(kMergeWarps * 32, 1)
+row_merge_kernel(const __grid_constant__ RowsParams P) {
+  __shared__ uint64_t keys[kMergeWarps][kKeyStage];
+  __shared__ uint32_t pend[kMergeWarps][64];   // running end of each piece's candidates (pieces <= 64 per round)
+  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  const long long r = (long long)blockIdx.x * kMergeWarps + w;
+  if (r >= P.R) return;
+  long long wa, wb;
+  row_warps(P, r, &wa, &wb);
+  const int nseg = int(wb - wa + 1);
+  // headers: every piece's max, sum and bound in one round of loads
+  float M = -FLT_MAX;
+  uint32_t bound = 0;
+  float mp[2] = {-FLT_MAX, -FLT_MAX};
+  double sp[2] = {0.0, 0.0};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int p = lane + 32 * h;
+    if (p < nseg) {
+      const SlotView sv = slot_of(P, r, p);
+      mp[h] = __ldcg(sv.max_p());
+      sp[h] = __ldcg(sv.sum_p());
+      bound = max(bound, __ldcg(sv.bound_p()));
+    }
+  }
+  for (int p = lane + 64; p < nseg; p += 32) {   // rows cut into more than 64 pieces
+    const SlotView sv = slot_of(P, r, p);
+    const float m2 = __ldcg(sv.max_p());
+    const double s2 = __ldcg(sv.sum_p());
+    const float M2 = fmaxf(mp[1], m2);
+    sp[1] = sp[1] * double(ex2_approx((mp[1] - M2) * P.c)) + s2 * double(ex2_approx((m2 - M2) * P.c));
+    mp[1] = M2;
+    bound = max(bound, __ldcg(sv.bound_p()));
+  }
+  M = fmaxf(mp[0], mp[1]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-    const uint64_t t = __shfl_xor_sync(0xFFFFFFFFu, tstar, o);
-    tstar = t > tstar ? t : tstar;
+    M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+    bound = max(bound, __shfl_xor_sync(kFull, bound, o));
   }
-  double S = 0.0;
-  for (int p = lane; p < nseg; p += 32) {
-    const uint8_t* q = base + (size_t)p * P.pstride;
-    const float mp = __ldcg(reinterpret_cast<const float*>(q));
-    const double sp = __ldcg(reinterpret_cast<const double*>(q + 8));
-    S += sp * double(ex2_approx((mp - M) * P.c));
-  }
+  double S = sp[0] * double(ex2_approx((mp[0] - M) * P.c)) + sp[1] * double(ex2_approx((mp[1] - M) * P.c));
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xFFFFFFFFu, S, o);
-  // keys >= tstar (the largest k-th key of any partial) contain the row's best k
+  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(kFull, S, o);
+  const float tau = tau_value(bound);
+  // candidates, up to 64 pieces at a time: piece p's are entries
+  // [pend[p-1], pend[p]) of the round's flattened list
   uint64_t list = 0;
-  const int total = nseg * k;
-  for (int b0 = 0; b0 < total; b0 += 32) {
-    const int idx = b0 + lane;
-    uint64_t key = 0;
-    if (idx < total) {
-      const int p = idx / k, e = idx - p * k;
-      key = __ldcg(reinterpret_cast<const unsigned long long*>(base + (size_t)p * P.pstride + 16) + e);
-      if (key < tstar) key = 0;
-    }
-    if (__any_sync(0xFFFFFFFFu, key != 0)) list = warp_merge_top32(list, key);
-  }
-  finish_row(P, r, M, S, list);
-}
-
-// Adds up to 32 keys (one per lane, 0 = none) to the best-32 list.  Keys not
-// above the list's k-th key cannot reach the row's best k and are dropped; a
-// few survivors are inserted one at a time (a vote finds the position), more
-// go through a bitonic merge.  Returns whether the list changed.
-__device__ __forceinline__ bool merge_keys(uint64_t& list, uint64_t key, int k) {
-  const int lane = threadIdx.x & 31;
-  const uint64_t kth = __shfl_sync(0xFFFFFFFFu, list, k - 1);
-  const bool keep = key > kth;   // keys are distinct; 0 never passes
-  uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
-  if (bal == 0u) return false;
-  if (__popc(bal) > 4) {
-    list = warp_merge_top32(list, keep ? key : 0ull);
-    return true;
-  }
-  while (bal) {
-    const int src = __ffs(bal) - 1;
-    bal &= bal - 1u;
-    const uint64_t x = __shfl_sync(0xFFFFFFFFu, key, src);
-    const int pos = __popc(__ballot_sync(0xFFFFFFFFu, list > x));   // < k: x beats the k-th
-    const uint64_t up = __shfl_up_sync(0xFFFFFFFFu, list, 1);
-    list = lane < pos ? list : (lane == pos ? x : up);
-  }
-  return true;
-}
-
-// The merger warp: per row of the span, drains the row's key ring into the
-// CTA's best-32 list (publishing its k-th value as the row's threshold) until
-// every consumer lane is done with the row, then combines the consumer warps'
-// (max, sum) and finishes the row or leaves the CTA's partial.
-template <int DT>
-__device__ __forceinline__ void merge_span_rows(const RowsParams& P, RowSmem& S, long long r_first,
-                                                long long r_last) {
-  using E = Elem<DT>;
-  constexpr int EPV = E::kPerVec;
-  const int lane = threadIdx.x & 31;
-  const int k = P.k;
-  for (long long r = r_first; r <= r_last; ++r) {
-    const int rowseq = int(r - r_first);
-    const int rslot = rowseq % kRowSlots;
-    const uint32_t parity = uint32_t(rowseq / kRowSlots) & 1u;
-    volatile uint32_t* vid = S.vid[rslot];
-    uint32_t head = 0;
-    uint64_t list = 0;
-    long long t0 = clock64();
-    for (;;) {
-      // read "done" before the tail: once done, the tail read after it is final
-      const bool done = __shfl_sync(0xFFFFFFFFu, mbar_test_wait(&S.row_full[rslot], parity) ? 1 : 0, 0) != 0;
-      const uint32_t tail = __shfl_sync(0xFFFFFFFFu, *reinterpret_cast<volatile uint32_t*>(&S.tail[rslot]), 0);
-      if (tail != head) {
-        const uint32_t n = (tail - head) < 32u ? (tail - head) : 32u;
-        uint32_t tag = 0;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (uint32_t(lane) < n) {
-          const uint32_t i = (head + uint32_t(lane)) & uint32_t(kRingVecs - 1);
-          tag = vid[i];
-          if (tag == 0u) {
-            const long long t1 = clock64();
-            while ((tag = vid[i]) == 0u) {
-              if (aborted(S)) break;
-              if (clock64() - t1 > P.wait_limit) {
-                raise_abort(S, P.ctrl);
-                break;
-              }
-            }
-          }
-          __threadfence_block();   // the vector was stored before its tag
-          v = lds_v4_volatile(S.vdata[rslot] + i);
-          vid[i] = 0u;
-        }
-        if (__any_sync(0xFFFFFFFFu, aborted(S))) return;
-        head += n;
-        __threadfence_block();
-        if (lane == 0) *reinterpret_cast<volatile uint32_t*>(&S.head[rslot]) = head;
-        // expand the vectors: element e of lane's vector is id (tag & 0xFFFFFF) - 1 + e;
-        // elements below the row's published threshold (seed or k-th so far)
-        // cannot reach the row's best k and are dropped before any merging
-        const uint32_t id0 = (tag & 0xFFFFFFu) - 1u;
-        const uint32_t tau_o = __shfl_sync(0xFFFFFFFFu, *reinterpret_cast<volatile uint32_t*>(&S.tau[rslot]), 0);
-        // survivors: above the threshold and above the list's current k-th key
-        const uint64_t kth0 = __shfl_sync(0xFFFFFFFFu, list, k - 1);
-        uint64_t cand[EPV];
-        uint32_t cnt = 0;
+  int nk = 0;   // keys staged
+  for (int p0 = 0; p0 < nseg; p0 += 64) {
+    const int np = min(64, nseg - p0);
+    uint32_t c0 = 0, c1 = 0;
+    if (lane < np) c0 = min(__ldcg(slot_of(P, r, p0 + lane).count_p()), uint32_t(P.cp));
+    if (lane + 32 < np) c1 = min(__ldcg(slot_of(P, r, p0 + lane + 32).count_p()), uint32_t(P.cp));
+    uint32_t s0 = c0, s1 = c1;   // inclusive scans of the counts
 #pragma unroll
-        for (int p = 0; p < EPV / 2; ++p) {
-          const float2 z = E::pair(v, p);
-          const bool q0 = ((tag >> (24 + 2 * p)) & 1u) && ord_f32(z.x) >= tau_o;
-          const bool q1 = ((tag >> (25 + 2 * p)) & 1u) && ord_f32(z.y) >= tau_o;
-          cand[2 * p] = q0 ? elem_key(z.x, id0 + 2 * p) : 0ull;
-          cand[2 * p + 1] = q1 ? elem_key(z.y, id0 + 2 * p + 1) : 0ull;
-          if (cand[2 * p] <= kth0) cand[2 * p] = 0ull;
-          if (cand[2 * p + 1] <= kth0) cand[2 * p + 1] = 0ull;
-          cnt += (cand[2 * p] != 0ull) + (cand[2 * p + 1] != 0ull);
-        }
-        // compact them into shared memory (prefix sum of counts <= 8 by ballots)
-        const uint32_t c0 = __ballot_sync(0xFFFFFFFFu, cnt & 1u), c1 = __ballot_sync(0xFFFFFFFFu, cnt & 2u);
-        const uint32_t c2 = __ballot_sync(0xFFFFFFFFu, cnt & 4u), c3 = __ballot_sync(0xFFFFFFFFu, cnt & 8u);
-        const int total = __popc(c0) + 2 * __popc(c1) + 4 * __popc(c2) + 8 * __popc(c3);
-        const bool changed = total > 0;
-        if (changed) {
-          const uint32_t below = (1u << lane) - 1u;
-          int at = __popc(c0 & below) + 2 * __popc(c1 & below) + 4 * __popc(c2 & below) + 8 * __popc(c3 & below);
-#pragma unroll
-          for (int e = 0; e < EPV; ++e)
-            if (cand[e] != 0ull) S.mkeys[at++] = cand[e];
-          __syncwarp();
-          if (total <= 4) {
-            // a few: insert one at a time (a vote finds the position)
-            for (int t = 0; t < total; ++t) {
-              const uint64_t x = S.mkeys[t];
-              const int pos = __popc(__ballot_sync(0xFFFFFFFFu, list > x));
-              const uint64_t up = __shfl_up_sync(0xFFFFFFFFu, list, 1);
-              list = lane < pos ? list : (lane == pos ? x : up);
-            }
-          } else {
-            for (int b0 = 0; b0 < total; b0 += 32)
-              list = warp_merge_top32(list, b0 + lane < total ? S.mkeys[b0 + lane] : 0ull);
-          }
-          __syncwarp();
-        }
-        if (changed) {
-          const uint64_t kth = __shfl_sync(0xFFFFFFFFu, list, k - 1);
-          if (kth != 0 && lane == 0) atomicMax(&S.tau[rslot], uint32_t(kth >> 32));
-        }
-        t0 = clock64();
-        continue;
-      }
-      if (done) break;
-      __nanosleep(1000);   // an idle merger must not take issue slots from the consumers
-      if (__any_sync(0xFFFFFFFFu, aborted(S))) return;
-      if (__any_sync(0xFFFFFFFFu, clock64() - t0 > P.wait_limit)) {
-        raise_abort(S, P.ctrl);
-        return;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t0 = __shfl_up_sync(kFull, s0, o), t1 = __shfl_up_sync(kFull, s1, o);
+      if (lane >= o) {
+        s0 += t0;
+        s1 += t1;
       }
     }
-    // every lane acquires the completed phase (it cannot move on before the
-    // slot is handed back)
-    (void)mbar_test_wait(&S.row_full[rslot], parity);
-    // the consumer warps' (max, sum) of the row
-    const float2 pw = lane < kConsumers ? S.part[rslot][lane] : make_float2(-FLT_MAX, 0.f);
-    float M = pw.x;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-    float Sf = pw.y * ex2_approx((pw.x - M) * P.c);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) Sf += __shfl_xor_sync(0xFFFFFFFFu, Sf, o);
-    const double Ssum = double(Sf);
-    // hand the slot back (its ring is all zeros again)
-    if (lane == 0) {
-      S.tail[rslot] = 0u;
-      S.head[rslot] = 0u;
-      S.tau[rslot] = 0u;
-    }
+    s1 += __shfl_sync(kFull, s0, 31);
+    pend[w][lane] = s0;
+    pend[w][lane + 32] = s1;
+    const int total = int(__shfl_sync(kFull, s1, 31));
     __syncwarp();
-    __threadfence_block();
-    mbar_arrive(&S.row_free[rslot]);
-
-    const unsigned long long rb0 = (unsigned long long)r * P.stride * P.es;
-    const long long cfirst = (long long)(rb0 / P.span);
-    const long long clast = (long long)((rb0 + (unsigned long long)P.V * P.es - 1) / P.span);
-    if (cfirst == clast) {
-      finish_row(P, r, M, Ssum, list);
-      continue;
-    }
-    const int nseg = int(clast - cfirst + 1);
-    uint8_t* part = P.partials + ((size_t)r * P.pmax + (blockIdx.x - cfirst)) * P.pstride;
-    if (lane == 0) {
-      reinterpret_cast<float*>(part)[0] = M;
-      reinterpret_cast<double*>(part)[1] = Ssum;
-    }
-    if (lane < k) reinterpret_cast<unsigned long long*>(part + 16)[lane] = list;
-    __threadfence();
-    __syncwarp();
-    uint32_t old = 0;
-    if (lane == 0) old = atomicAdd(P.row_cnt + r, 1u);
-    old = __shfl_sync(0xFFFFFFFFu, old, 0);
-    if (int(old) == nseg - 1) {
-      __threadfence();
-      merge_row(P, r, nseg);
-      if (lane == 0) P.row_cnt[r] = 0u;   // every CTA of the row has arrived: ready for the next call
-    }
-  }
-}
-
-// -------------------------------------------------------------------- kernel
-template <int DT, int NSUB>
-__global__ void __launch_bounds__(kRowThreads, 1)
-row_stream_kernel(const RowsParams P) {
-  constexpr int SH = Elem<DT>::kShift;
-  constexpr uint32_t SB = uint32_t(kConsumers * NSUB * kSlice);   // stage bytes
-  constexpr int NST = kMaxStages / NSUB;                          // stages in the ring
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  RowSmem& S = *reinterpret_cast<RowSmem*>(smem_raw);
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;          // 0 producer, 1..kConsumers consumers, then the merger
-
-  const unsigned long long B0 = (unsigned long long)blockIdx.x * P.span;
-  const unsigned long long B1 = (B0 + P.span < P.total) ? B0 + P.span : P.total;
-  const unsigned long long e0 = B0 / P.es, e1 = B1 / P.es;
-  // the rows whose valid elements meet the span (none when it holds padding only)
-  long long r_first = (long long)(e0 / P.stride);
-  if (e0 - (unsigned long long)r_first * P.stride >= (unsigned long long)P.V) ++r_first;
-  const long long r_last = (long long)((e1 - 1) / P.stride);
-
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    // rows of this call, for clearing the counters after a failed call
-    P.ctrl[2] = uint32_t((unsigned long long)P.R);
-    P.ctrl[3] = uint32_t((unsigned long long)P.R >> 32);
-  }
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kMaxStages; ++i) {
-      mbar_init(&S.full[i], 1);
-      mbar_init(&S.empty[i], kConsumers);
-    }
-    for (int i = 0; i < kRowSlots; ++i) {
-      mbar_init(&S.row_full[i], kConsumers * 32);
-      mbar_init(&S.row_free[i], 32);
-    }
-    mbar_init(&S.seed_bar[0], kConsumers * 32);
-    mbar_init(&S.seed_bar[1], kConsumers * 32);
-    fence_mbar_init();
-  }
-  {
-    uint32_t* vz = &S.vid[0][0];
-    for (int i = threadIdx.x; i < kRowSlots * kRingVecs; i += blockDim.x) vz[i] = 0u;
-    if (threadIdx.x < kRowSlots) {
-      S.tail[threadIdx.x] = 0u;
-      S.head[threadIdx.x] = 0u;
-      S.tau[threadIdx.x] = 0u;
-    }
-    if (threadIdx.x == 0) S.abort = 0u;
-  }
-  __syncthreads();
-
-  // ---------------------------------------------------------------- producer
-  if (warp == 0) {
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      int slot = 0;
-      uint32_t round = 0;   // fills of `slot` so far
-      int issued = 0;
-      bool ok = true;
-      for (long long r = r_first; r <= r_last && ok; ++r) {
-        const Seg g = segment(P, e0, e1, r);
-        for (unsigned long long off = g.a; off < g.b; off += SB) {
-          if (round > 0 && !wait_phase(S, &S.empty[slot], (round - 1) & 1u, P.wait_limit, P.ctrl)) {
-            ok = false;
-            break;
-          }
-          const uint32_t bytes = uint32_t((g.b - off) < (unsigned long long)SB ? (g.b - off) : SB);
-          mbar_expect_tx(&S.full[slot], bytes);
-          bulk_g2s(S.ring + size_t(slot) * SB, P.logits + off, bytes, &S.full[slot], pol);
-          ++issued;
-          if (++slot == NST) {
-            slot = 0;
-            ++round;
-          }
-        }
-      }
-      // the CTA may not retire while a copy still writes its shared memory;
-      // these waits are bounded by the clock alone
-      for (int j = 0; j < NST && j < issued; ++j) {
-        // the last fill of each slot used so far
-        const int sl = (slot + NST - 1 - j) % NST;
-        const uint32_t rd = (sl < slot) ? round : round - 1;
-        if (!mbar_wait_bounded(&S.full[sl], rd & 1u, kDrainLimit)) {
-          set_dev_error(P.ctrl, DART_DEVERR_WAIT_TIMEOUT);
-          break;
-        }
-      }
-    }
-    return;
-  }
-
-  // ------------------------------------------------------------------ merger
-  if (warp == kMergerWarp) {
-    merge_span_rows<DT>(P, S, r_first, r_last);
-    return;
-  }
-
-  // --------------------------------------------------------------- consumers
-  const int w = warp - 1;
-  const long long lim = P.wait_limit;
-  int slot = 0;         // ring stage of the next stage
-  uint32_t round = 0;   // fills of `slot` before this one
-  int nseed = 0;   // seeds taken so far (rows with an aligned interior), the same in every consumer warp
-  for (long long r = r_first; r <= r_last; ++r) {
-    const int rowseq = int(r - r_first);
-    const int rslot = rowseq % kRowSlots;
-    if (rowseq >= kRowSlots &&
-        !__all_sync(0xFFFFFFFFu, wait_phase(S, &S.row_free[rslot], uint32_t(rowseq / kRowSlots - 1) & 1u, lim, P.ctrl)))
-      return;
-    const Seg g = segment(P, e0, e1, r);
-    const unsigned long long rs = (unsigned long long)r * P.stride;
-    RowCtx rc;
-    rc.m = -FLT_MAX;
-    rc.mc = scaled_max(rc.m, P.c);
-    rc.s = 0.f;
-    rc.tau_ord = 0u;
-    rc.tau = -INFINITY;
-    rc.tau_slot = &S.tau[rslot];
-    VecRing vr;
-    vr.tail = &S.tail[rslot];
-    vr.head = &S.head[rslot];
-    vr.vdata = S.vdata[rslot];
-    vr.vid = S.vid[rslot];
-    vr.S = &S;
-    vr.ctrl = P.ctrl;
-    vr.limit = lim;
-
-    // head: [s0, a) (or the whole segment when nothing is aligned), warp 0 only
-    if (w == 0) {
-      const unsigned long long hb0 = g.s0 * P.es;
-      const unsigned long long hb1 = (g.a < g.b) ? g.a : g.s1 * P.es;
-      if (hb1 > hb0) {
-        refresh_tau(rc);
-        const float2 ms = reduce_scalars<DT>(P.logits, hb0, hb1, P.es, uint32_t(g.s0 - rs), P.c, rc.m, rc.s, rc.tau, vr);
-        rc.m = ms.x;
-        rc.mc = scaled_max(rc.m, P.c);
-        rc.s = ms.y;
-      }
-    }
-    // aligned interior: this warp's slice of every stage
-    const uint32_t ilen = uint32_t(g.b - g.a);
-    const uint32_t id_a = uint32_t((g.a >> SH) - rs);
-    constexpr uint32_t kMine = uint32_t(NSUB * kSlice);   // bytes of a full stage per warp
-    const uint32_t s0 = uint32_t(w) * kMine;
-    for (uint32_t o = 0; o < ilen; o += SB) {
-      if (!__all_sync(0xFFFFFFFFu, wait_phase(S, &S.full[slot], round & 1u, lim, P.ctrl))) return;
-      const uint4* src = reinterpret_cast<const uint4*>(S.ring + size_t(slot) * SB + s0);
-      const uint32_t rem = ilen - o;
-      const int nvec = s0 < rem ? int(min(rem - s0, kMine) / 16) : 0;
-      if (o == 0) {
-        const uint32_t kth = seed_stage<DT>(src, nvec, &S, nseed, w, P.k, lim, P.ctrl);
-        if (__any_sync(0xFFFFFFFFu, aborted(S))) return;
-        raise_tau(rc, kth);
-        if (lane == 0 && kth != 0u) atomicMax(rc.tau_slot, kth);
-        ++nseed;
-      }
-      refresh_tau(rc);
-      if (rem >= SB) {
+    for (int j0 = 0; j0 < total; j0 += 256) {
+      uint4 v[8];
+      uint32_t tag[8];
 #pragma unroll
-        for (int j = 0; j < NSUB; ++j) {
-          const uint4* sj = src + j * (kSlice / 16);
-          reduce_slice<DT, true>(rc, sj, kSlice / 16, P.c, id_a + ((o + s0 + uint32_t(j * kSlice)) >> SH), vr);
+      for (int t = 0; t < 8; ++t) {
+        const int j = j0 + t * 32 + lane;
+        tag[t] = 0;
+        v[t] = make_uint4(0u, 0u, 0u, 0u);
+        if (j < total) {
+          int lo = 0, hi = np - 1;   // first piece whose running end exceeds j
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (pend[w][mid] > uint32_t(j)) hi = mid;
+            else lo = mid + 1;
+          }
+          const int i = j - (lo > 0 ? int(pend[w][lo - 1]) : 0);
+          const SlotView sv = slot_of(P, r, p0 + lo);
+          v[t] = __ldcg(sv.vecs() + i);
+          tag[t] = __ldcg(sv.tags() + i);
         }
-      } else if (nvec > 0) {
-        reduce_tail_stage<DT, NSUB>(&rc, src, nvec, id_a + ((o + s0) >> SH), SH, P.c, vr);
+      }
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        uint32_t cm = vec_hits<DT>(v[t], tag[t], tau);
+        int added;
+        const int pre = warp_prefix4(uint32_t(__popc(cm)), &added);
+        if (added == 0) continue;
+        if (nk + added > kKeyStage) {   // rare: make room (added <= kKeyStage)
+          list = merge_staged(list, keys[w], nk);
+          nk = 0;
+        }
+        int q = nk + pre;
+        const uint32_t id0 = tag[t] & 0xFFFFFFu;
+        while (cm) {
+          const int e = __ffs(cm) - 1;
+          cm &= cm - 1u;
+          keys[w][q++] = elem_key(Elem<DT>::elem(v[t], e), id0 + uint32_t(e));
+        }
+        nk += added;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.empty[slot]);
-      if (++slot == NST) {
-        slot = 0;
-        ++round;
-      }
     }
-    // tail: [b, s1), warp 0 only
-    if (w == 0 && g.a < g.b && g.s1 * P.es > g.b) {
-      refresh_tau(rc);
-      const float2 ms = reduce_scalars<DT>(P.logits, g.b, g.s1 * P.es, P.es, uint32_t((g.b >> SH) - rs), P.c, rc.m,
-                                           rc.s, rc.tau, vr);
-      rc.m = ms.x;
-      rc.mc = scaled_max(rc.m, P.c);
-      rc.s = ms.y;
-    }
-    // the warp's (max, sum) of the row
-    float m = rc.m, s = exact_sum(rc.m, rc.mc, rc.s, P.c);
-#pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) {
-      const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o2);
-      const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o2);
-      const float M = fmaxf(m, m2);
-      s = s * ex2_approx((m - M) * P.c) + s2 * ex2_approx((m2 - M) * P.c);
-      m = M;
-    }
-    if (lane == 0) S.part[rslot][w] = make_float2(m, s);
     __syncwarp();
-    mbar_arrive(&S.row_full[rslot]);
   }
+  list = merge_staged(list, keys[w], nk);
+  finish_row(P, r, M, S, list);
 }
 
 // ------------------------------------------------------------------ launch
@@ -954,7 +889,7 @@ void set_rows_wait_limit(long long cycles) {
 }
 
 cudaError_t launch_rows(const void* logits, long long R, int V, long long stride, int dtype, float T, int k,
-                        void* ws, const WsLayout& L, int sms,
+                        void* ws, const WsLayout& L, int /*sms*/,
                         int32_t* out_ids, float* out_logp, float* out_lse, cudaStream_t stream) {
   RowsParams P;
   const int es = dtype == DART_F32 ? 4 : 2;
@@ -964,28 +899,22 @@ cudaError_t launch_rows(const void* logits, long long R, int V, long long stride
   P.stride = (unsigned long long)stride;
   P.k = k;
   P.es = es;
-  P.T = double(T);
   P.invT = 1.0 / double(T);
   P.c = float(1.4426950408889634 / double(T));
   // the stream ends at the last valid element (the last row's padding may be absent)
   P.total = R > 0 ? ((unsigned long long)(R - 1) * P.stride + (unsigned long long)V) * (unsigned long long)es : 0ull;
-  // one span per SM, whole 16-byte units, at least kMinSpanBytes
-  const unsigned long long want = (P.total + (unsigned long long)sms - 1) / (unsigned long long)sms;
-  unsigned long long span = (want + 15) & ~15ull;
-  if (span < kMinSpanBytes) span = kMinSpanBytes;
-  if (span >= (1ull << 31)) return cudaErrorInvalidValue;   // 32-bit offsets inside a span
-  P.span = span;
-  P.grid = int((P.total + span - 1) / span);
-  // long rows take 48 KiB stages (less loop overhead per byte); rows shorter
-  // than about five of those take 24 KiB stages (less idle tail per row)
-  const unsigned long long row_bytes = (unsigned long long)V * (unsigned long long)es;
-  P.nsub = row_bytes >= 262144ull ? 2 : 1;
+  // spans of the fixed nominal grid; padded rows only make them longer, so
+  // a row never has more pieces than the layout's slots
+  P.wspan = row_pass_span(P.total);
+  if (P.wspan < L.wspan) return cudaErrorInvalidValue;
+  const unsigned long long warps = (P.total + P.wspan - 1) / P.wspan;
+  const unsigned long long grid = (warps + kRowWarps - 1) / kRowWarps;
   P.pmax = L.pmax;
-  P.pstride = L.pstride;
+  P.cp = L.cp;
+  P.slot_bytes = L.slot_bytes;
   uint8_t* w = static_cast<uint8_t*>(ws);
   P.ctrl = reinterpret_cast<uint32_t*>(w + L.ctrl);
-  P.row_cnt = reinterpret_cast<uint32_t*>(w + L.row_cnt);
-  P.partials = w + L.partials;
+  P.slots = w + L.slots;
   P.row_off = reinterpret_cast<double*>(w + L.row_off);
   P.row_ids = reinterpret_cast<int32_t*>(w + L.row_ids);
   P.row_base = reinterpret_cast<double*>(w + L.row_base);
@@ -995,20 +924,19 @@ cudaError_t launch_rows(const void* logits, long long R, int V, long long stride
   P.wait_limit = rows_wait_limit();
   if (P.total == 0) return cudaSuccess;
   const size_t smem = rows_smem_bytes();
+  const unsigned mgrid = unsigned((R + kMergeWarps - 1) / kMergeWarps);
   cudaError_t e = cudaSuccess;
-  auto go = [&](auto kernel) {
+  auto go = [&](auto kernel, auto merge) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e == cudaSuccess) kernel<<<P.grid, kRowThreads, smem, stream>>>(P);
+    if (e != cudaSuccess) return;
+    kernel<<<unsigned(grid), kRowThreads, smem, stream>>>(P);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return;
+    merge<<<mgrid, kMergeWarps * 32, 0, stream>>>(P);
   };
-  if (P.nsub == 2) {
-    if (dtype == DART_F32) go(row_stream_kernel<DART_F32, 2>);
-    else if (dtype == DART_F16) go(row_stream_kernel<DART_F16, 2>);
-    else go(row_stream_kernel<DART_BF16, 2>);
-  } else {
-    if (dtype == DART_F32) go(row_stream_kernel<DART_F32, 1>);
-    else if (dtype == DART_F16) go(row_stream_kernel<DART_F16, 1>);
-    else go(row_stream_kernel<DART_BF16, 1>);
-  }
+  if (dtype == DART_F32) go(row_stream_kernel<DART_F32>, row_merge_kernel<DART_F32>);
+  else if (dtype == DART_F16) go(row_stream_kernel<DART_F16>, row_merge_kernel<DART_F16>);
+  else go(row_stream_kernel<DART_BF16>, row_merge_kernel<DART_BF16>);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

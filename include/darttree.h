@@ -300,6 +300,22 @@ void dart_set_wait_limit(int64_t cycles);
  * DART_OK or an error code. */
 int dart_probe_ex2(int blocks, int threads, int iters, float* out, void* stream);
 
+/* Streaming-read probe: reads `bytes` (rounded down to a multiple of 16) of
+ * device memory at `src` (16-byte aligned) once, split into equal contiguous
+ * spans, one per warp, over `ctas` CTAs of `warps_per_cta` warps, and writes
+ * one float per lane to out (device, ctas * warps_per_cta * 32 floats) so
+ * that nothing is optimised away.  mode bit 0: 0 = 16-byte loads straight
+ * into registers (eight per lane in flight; warps_per_cta <= 16), 1 = each
+ * warp's own ring of `stages` (2..16) 4 KiB shared-memory stages filled by
+ * bulk copies (warps_per_cta * stages * 4 KiB must fit in shared memory).
+ * mode bit 1: reduce the data as bf16 logits (running maximum, one
+ * exponential per element) instead of xor-folding it.  A bulk wait that runs
+ * out (about two seconds) sets bit 0 of *device_err (device uint32).  Time it
+ * on `stream` to get the bandwidth a row pass of that shape can reach.
+ * Returns DART_OK or an error code. */
+int dart_probe_stream(const void* src, uint64_t bytes, int mode, int ctas, int warps_per_cta,
+                      int stages, float* out, uint32_t* device_err, void* stream);
+
 /* Static text for a status code. */
 const char* dart_status_string(int status);
 

@@ -1,8 +1,9 @@
 """The row pass's bounded waits, made to run out on purpose (needs a GB300).
 
-No fault is involved: with every wait limited to 64 SM cycles the merger warp
-gives up at its first idle poll, the CTA ends its other waits, lets its bulk
-copies land and returns with DART_DEVERR_WAIT_TIMEOUT in the workspace.  The
+No fault is involved: with every wait limited to 64 SM cycles a warp's wait
+for its first bulk-copy stage (which cannot land that fast) gives up, the warp
+lets its copies in flight land and returns with DART_DEVERR_WAIT_TIMEOUT in
+the workspace.  The
 context stays usable: dart_device_error reports the bit and clears the
 workspace, and the next call with the default limit is exact again.
 """

@@ -58,6 +58,7 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-per-config", action="store_true", help="skip the other configs' records")
     p.add_argument("--probe-sfu", action="store_true",
                    help="only measure the exponential unit's throughput (one JSON line)")
     p.add_argument("--probe-stream", action="store_true",
@@ -414,22 +415,12 @@ def run_reference(args):
     return 0
 
 
-def run_ours(args):
+def measure(L, D, torch, case, dev, stream, steps, warmup, world, with_select=False):
+    """One config: whole steps (row pass + row merge + tree kernel), the row
+    pass alone (the dominant kernel, for the roofline), the row merge alone;
+    CUDA events on `stream`, L2 flushed before every timed launch."""
     import ctypes as C
-
-    import torch
-    import draft_tree_construction_gb300 as D
-
-    rank, world, local = dist_setup()
-    dist_init(world, local)
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    D.build()
-    L = D.lib()
-
-    case = synth.make_config(args.config, seed=args.seed + rank)
     B, d, V, k = case.B, case.d, case.V, case.k
-    logit_bytes = case.logit_bytes
     if case.dtype == "bf16":
         host = torch.from_numpy(case.logits.view(np.int16).copy()).view(torch.bfloat16)
     else:
@@ -439,20 +430,18 @@ def run_ours(args):
     ctx = torch.from_numpy(np.ascontiguousarray(case.ctx)).to(dev) if tab is not None else None
     builder = D.TreeBuilder(B, d, V, z.dtype, case.T, k, case.W, case.lam, case.beta,
                             table=tab, ctx=ctx, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    # L2 flush between timed steps: a read-only sweep of 256 MB (twice the L2)
-    # evicts the logits, the n-gram table and the workspace without leaving
-    # dirty lines to be written back inside the next timed window
+    # L2 flush between timed launches: a read-only sweep of 256 MB (twice the
+    # L2) evicts the logits, the n-gram table and the workspace without
+    # leaving dirty lines to be written back inside the next timed window
     flush_buf = torch.ones(64 << 20, dtype=torch.float32, device=dev)
 
     def flush():
         flush_buf.sum()
 
-    def timed(fn, steps):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(steps)]
-        hold_gpu(stream, steps)
-        for i in range(steps):
+    def timed(fn, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        hold_gpu(stream, n)
+        for i in range(n):
             flush()
             evs[i][0].record(stream)
             fn(i)
@@ -460,38 +449,44 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         return [a.elapsed_time(b) for a, b in evs]
 
-    clk = clocks_start(dev.index or 0)
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         flush()
         builder(z)
     torch.cuda.synchronize(dev)
     assert D.device_error(builder.ws) == 0, "device error during warm-up"
-
-    # ---- timed region: whole steps (memset + streaming kernel + tree kernel)
     barrier(world)
     torch.cuda.synchronize(dev)
-    t_timed = time.time()
-    step_times = timed(lambda i: builder(z), args.steps)
+    t0 = time.time()
+    step_times = timed(lambda i: builder(z), steps)
+    t1 = time.time()
     barrier(world)
-    step_ms = max_over_ranks(statistics.mean(step_times), world)
-
-    # ---- the streaming kernel alone (same launch configuration), for the roofline
     code = D.DTYPE_CODES()[z.dtype]
     ws = builder.ws
+    sp = C.c_void_p(stream.cuda_stream)
 
-    def rows_only(i):
-        rc = L.dart_row_topk(C.c_void_p(z.data_ptr()), B * d, V, code, float(case.T), k,
-                             None, None, None, C.c_void_p(ws.data_ptr()), ws.numel(),
-                             C.c_void_p(stream.cuda_stream))
-        assert rc == 0
+    def row_pass(i):
+        assert L.dart_row_pass(C.c_void_p(z.data_ptr()), B * d, V, V, code, float(case.T), k,
+                               C.c_void_p(ws.data_ptr()), ws.numel(), sp) == 0
 
-    k1_times = timed(rows_only, args.steps)
-    k1_ms = max_over_ranks(statistics.mean(k1_times), world)
+    def row_finish(i):
+        assert L.dart_row_finish(B * d, V, V, code, float(case.T), k, None, None, None,
+                                 C.c_void_p(ws.data_ptr()), ws.numel(), sp) == 0
 
-    # ---- the verification tree chosen best-first from the step's candidate
-    # trees, budget 16 (one of the verification budgets PCTree quotes)
-    select = None
-    if builder.out.get("scores") is not None:
+    pass_times = timed(row_pass, steps)
+    merge_times = timed(row_finish, steps)
+    assert D.device_error(builder.ws) == 0, "device error during the timed steps"
+    res = {
+        "step_ms": max_over_ranks(statistics.mean(step_times), world),
+        "row_pass_ms": max_over_ranks(statistics.mean(pass_times), world),
+        "row_merge_ms": max_over_ranks(statistics.mean(merge_times), world),
+        "step_p10_p50_p90": [float(np.percentile(step_times, q)) for q in (10, 50, 90)],
+        "row_pass_p10_p50_p90": [float(np.percentile(pass_times, q)) for q in (10, 50, 90)],
+        "window": (t0, t1), "host": host, "z": z, "builder": builder,
+    }
+    res["tree_ms_by_difference"] = res["step_ms"] - res["row_pass_ms"] - res["row_merge_ms"]
+    if with_select and builder.out.get("scores") is not None:
+        # the verification tree chosen best-first from the step's candidate
+        # trees, budget 16 (one of the verification budgets PCTree quotes)
         o = builder.out
         budget = min(16, o["parents"].shape[1])
         sel_err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -500,13 +495,48 @@ def run_ours(args):
             D.tree_select(o["tokens"], o["parents"], o["pos"], o["scores"], budget, device_err=sel_err,
                           stream=stream)
 
-        sel_times = timed(select_only, min(args.steps, 200))
+        sel_times = timed(select_only, min(steps, 200))
         sel_ms = max_over_ranks(statistics.mean(sel_times), world)
         torch.cuda.synchronize(dev)
-        select = {"budget": budget, "us_per_call": sel_ms * 1e3, "trees_per_s": B * world / (sel_ms / 1e3),
-                  "kernel": "select_kernel (best-first verification tree)", "calls": len(sel_times),
-                  "device_error": int(sel_err.item())}
-    clocks = clocks_stop(clk, (t_timed, time.time()))
+        res["select"] = {"budget": budget, "us_per_call": sel_ms * 1e3, "trees_per_s": B * world / (sel_ms / 1e3),
+                         "kernel": "select_kernel (best-first verification tree)", "calls": len(sel_times),
+                         "device_error": int(sel_err.item())}
+    return res
+
+
+def stream_ceiling(L, torch, nbytes, dev, stream, steps):
+    """The bulk-copy ring of the row pass (twelve warps x three 4 KiB stages
+    per SM) with no arithmetic, on a buffer of the logits' size: the
+    bandwidth any row pass of this shape can reach at this size."""
+    buf = torch.empty(nbytes // 2, dtype=torch.bfloat16, device=dev).normal_()
+    flush_buf = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    gbs, ms = stream_probe(L, buf, 1, sms, 12, 3, stream, steps=steps, flush=lambda: flush_buf.sum())
+    del buf
+    return {"gbs": gbs, "us": ms * 1e3, "shape": "12 warps x 3 bulk-copy stages of 4 KiB per SM, no arithmetic"}
+
+
+def run_ours(args):
+    import torch
+    import draft_tree_construction_gb300 as D
+
+    rank, world, local = dist_setup()
+    dist_init(world, local)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    D.build()
+    L = D.lib()
+    stream = torch.cuda.current_stream(dev)
+    peaks, peaks_src = measured_peaks()
+
+    case = synth.make_config(args.config, seed=args.seed + rank)
+    B, d, V, k = case.B, case.d, case.V, case.k
+    logit_bytes = case.logit_bytes
+    clk = clocks_start(dev.index or 0)
+    m = measure(L, D, torch, case, dev, stream, args.steps, args.warmup, world, with_select=True)
+    clocks = clocks_stop(clk, m["window"])
+    step_ms, k1_ms = m["step_ms"], m["row_pass_ms"]
+    builder, z, host = m["builder"], m["z"], m["host"]
 
     # ---- end to end: pinned host logits in, pinned host outputs back, every step
     e2e = None
@@ -517,37 +547,68 @@ def run_ours(args):
         d2h = sum(v.numel() * v.element_size() for v in outs.values())
         h2d = pinned.numel() * pinned.element_size()
 
-        def e2e_step(i):
+        def e2e_step():
             z.copy_(pinned, non_blocking=True)
             builder(z)
             for key, v in outs.items():
                 v.copy_(builder.out[key], non_blocking=True)
 
-        for i in range(2):
-            e2e_step(i)
+        for _ in range(2):
+            e2e_step()
         torch.cuda.synchronize(dev)
         barrier(world)
-        e2e_times = timed(e2e_step, args.steps)
-        e2e_ms = max_over_ranks(statistics.mean(e2e_times), world)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        hold_gpu(stream, args.steps, us_per_step=900.0)
+        for a, b in evs:
+            a.record(stream)
+            e2e_step()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs), world)
+        numa = None
+        try:
+            numa = open(f"/sys/bus/pci/devices/{torch.cuda.get_device_properties(dev).pci_bus_id.lower()}/numa_node").read().strip()
+        except (OSError, AttributeError):
+            pass
         e2e = {"value": B * world / (e2e_ms / 1e3), "unit": "trees/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
-    assert D.device_error(builder.ws) == 0, "device error during the timed steps"
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "gpu_numa_node": numa}
 
-    peaks, peaks_src = measured_peaks()
     achieved = logit_bytes / (k1_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": k1_traffic(args.config),
-                "kernel": "row_stream_kernel (log-softmax + top-k stream)",
+                "kernel": "row_stream_kernel (log-softmax + top-k stream, dart_row_pass)",
                 "peak_source": f"{peaks_src} hbm_gbs",
                 "k1_ms": k1_ms, "frac_of_8tbs_nominal": achieved / 8000.0}
 
+    ceiling = None
+    per_config = None
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        S, dt, threads, ng = oracle_sample(case, args.cpu_seconds)
-        S1, dt1 = oracle_single_core(case, args.cpu_seconds / 3.0, ng)
-        cpu = {"value": S / dt, "unit": "trees/s", "cores": threads, "kind": "oracle",
-               "sample": f"first {S} of {B} trees of the same batch, full vocabulary and table",
-               "value_1_core": S1 / dt1, "sample_1_core": f"first {S1} of {B} trees, one thread"}
+    if rank == 0 and world == 1:
+        ceiling = stream_ceiling(L, torch, logit_bytes, dev, stream, min(args.steps, 50))
+        ceiling["frac"] = ceiling["gbs"] / peaks["hbm_gbs"]
+        ceiling["row_pass_over_ceiling"] = achieved / ceiling["gbs"]
+        if not args.no_per_config:
+            per_config = {}
+            for c2 in (1, 3, 4):
+                if c2 == args.config:
+                    continue
+                cc = synth.make_config(c2, seed=args.seed)
+                mm = measure(L, D, torch, cc, dev, stream, max(20, min(args.steps, 200)), args.warmup, world)
+                ach = cc.logit_bytes / (mm["row_pass_ms"] / 1e3) / 1e9
+                per_config[str(c2)] = {
+                    "workload": workload_name(c2), "ms_per_step": mm["step_ms"],
+                    "trees_per_s": cc.B / (mm["step_ms"] / 1e3), "row_pass_ms": mm["row_pass_ms"],
+                    "row_pass_frac": ach / peaks["hbm_gbs"], "row_merge_ms": mm["row_merge_ms"],
+                    "tree_ms_by_difference": mm["tree_ms_by_difference"],
+                    "logit_bytes": cc.logit_bytes}
+                del mm
+        if not args.no_cpu_baseline:
+            S, dt, threads, ng = oracle_sample(case, args.cpu_seconds)
+            S1, dt1 = oracle_single_core(case, args.cpu_seconds / 3.0, ng)
+            cpu = {"value": S / dt, "unit": "trees/s", "cores": threads, "kind": "oracle",
+                   "sample": f"first {S} of {B} trees of the same batch, full vocabulary and table",
+                   "value_1_core": S1 / dt1, "sample_1_core": f"first {S1} of {B} trees, one thread"}
 
     if rank == 0:
         value = B * world / (step_ms / 1e3)
@@ -558,16 +619,20 @@ def run_ours(args):
             "data": "synthetic",
             "config": {"workload": workload_name(args.config), "logit_dtype": case.dtype,
                        "trees_per_gpu": B, "logit_bytes_per_step": logit_bytes,
-                       "l2": "flushed before every timed step (read-only sweep of 256 MB)",
-                       "step_ms_p10_p50_p90": [float(np.percentile(step_times, q)) for q in (10, 50, 90)],
-                       "k1_ms_p10_p50_p90": [float(np.percentile(k1_times, q)) for q in (10, 50, 90)],
+                       "l2": "flushed before every timed launch (read-only sweep of 256 MB)",
+                       "step_ms_p10_p50_p90": m["step_p10_p50_p90"],
+                       "row_pass_ms_p10_p50_p90": m["row_pass_p10_p50_p90"],
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "hbm_gbs_whole_step": logit_bytes / (step_ms / 1e3) / 1e9,
             "roofline": roofline,
+            "stream_ceiling": ceiling,
+            "step_breakdown_ms": {"row_pass": k1_ms, "row_merge": m["row_merge_ms"],
+                                  "tree_by_difference": m["tree_ms_by_difference"]},
+            "per_config": per_config,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 2 * args.steps,
-            "verification_tree_select": select,
+            "gpu_launches": 3 * args.steps,
+            "verification_tree_select": m.get("select"),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -76,6 +76,10 @@ def _declare(L):
     L.dart_tree_build_strided.argtypes = [P, i32, i32, i32, i64, i32, f32, i32, i32, f32, f32, T, P,
                                           P, P, P, P, P, P, sz, P]
     L.dart_tree_build_strided.restype = i32
+    L.dart_row_pass.argtypes = [P, i32, i32, i64, i32, f32, i32, P, sz, P]
+    L.dart_row_pass.restype = i32
+    L.dart_row_finish.argtypes = [i32, i32, i64, i32, f32, i32, P, P, P, P, sz, P]
+    L.dart_row_finish.restype = i32
     L.dart_mask_pack.argtypes = [P, i32, i32, P, P, P]
     L.dart_mask_pack.restype = i32
     L.dart_tree_select.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, P, P, P, P]

@@ -46,13 +46,6 @@ int check_tree_shape(int B, int d, int k, int W, float lambda, float beta) {
   return DART_OK;
 }
 
-int device_sms(int* sms) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return DART_ERR_CUDA;
-  if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DART_ERR_CUDA;
-  return DART_OK;
-}
-
 TreeArgs tree_args(int B, int d, int k, int W, float lambda, float beta,
                    const dart_ngram_table_t* t, const int32_t* ctx,
                    int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
@@ -78,6 +71,25 @@ TreeArgs tree_args(int B, int d, int k, int W, float lambda, float beta,
   a.out_scores = out_scores;
   a.ctrl = nullptr;
   return a;
+}
+
+// The whole path on a workspace: the row pass, then the tree kernel.
+int launch_path(const void* logits, int B, int d, int V, int64_t row_stride, int dtype, float T, int k, int W,
+                float lambda, float beta, const dart_ngram_table_t* ngram_table, const int32_t* ctx_tokens,
+                int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos, uint32_t* out_mask,
+                float* out_scores, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
+  const long long R = (long long)B * d;
+  if (launch_rows(logits, R, V, row_stride, dtype, T, k, ws, L, nullptr, nullptr, nullptr, s) != cudaSuccess)
+    return DART_ERR_CUDA;
+  TreeArgs a = tree_args(B, d, k, W, lambda, beta, ngram_table, ctx_tokens, out_tokens, out_parents,
+                         out_pos, out_mask, out_scores);
+  a.ids = reinterpret_cast<const int32_t*>(ws + L.row_ids);
+  a.base = reinterpret_cast<const double*>(ws + L.row_base);
+  a.off = reinterpret_cast<const double*>(ws + L.row_off);
+  a.invT = 1.0 / double(T);
+  a.ctrl = reinterpret_cast<uint32_t*>(ws + L.ctrl);
+  if (launch_tree(a, s) != cudaSuccess) return DART_ERR_CUDA;
+  return DART_OK;
 }
 
 }  // namespace
@@ -157,21 +169,10 @@ int dart_tree_build_strided(const void* logits, int B, int d, int V, int64_t row
   const long long R = (long long)B * d;
   if (!ws_layout(R, V, elem_bytes(dtype), k, &L)) return DART_ERR_INVALID_ARG;
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return DART_ERR_WORKSPACE;
-  int sms = 0;
-  if ((rc = device_sms(&sms))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);   // counters are zero between calls
-  if (launch_rows(logits, R, V, row_stride, dtype, T, k, ws, L, sms, nullptr, nullptr, nullptr, s) != cudaSuccess)
-    return DART_ERR_CUDA;
-  TreeArgs a = tree_args(B, d, k, W, lambda, beta, ngram_table, ctx_tokens, out_tokens, out_parents,
-                         out_pos, out_mask, out_scores);
-  a.ids = reinterpret_cast<const int32_t*>(ws + L.row_ids);
-  a.base = reinterpret_cast<const double*>(ws + L.row_base);
-  a.off = reinterpret_cast<const double*>(ws + L.row_off);
-  a.invT = 1.0 / double(T);
-  a.ctrl = reinterpret_cast<uint32_t*>(ws + L.ctrl);
-  if (launch_tree(a, s) != cudaSuccess) return DART_ERR_CUDA;
-  return DART_OK;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return launch_path(logits, B, d, V, row_stride, dtype, T, k, W, lambda, beta, ngram_table, ctx_tokens,
+                     out_tokens, out_parents, out_pos, out_mask, out_scores, ws, L, s);
 }
 
 int dart_tree_build_noalloc(const void* logits, int B, int d, int V, int dtype,
@@ -193,24 +194,13 @@ int dart_tree_build_noalloc(const void* logits, int B, int d, int V, int dtype,
   if (L.total > kStaticScratchBytes) return DART_ERR_WORKSPACE;   // sizes beyond the fixed scratch
   void* scratch = nullptr;
   if ((rc = static_scratch(&scratch))) return rc;
-  int sms = 0;
-  if ((rc = device_sms(&sms))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(scratch);
   // errors are not reported on this path: clear the counters (and the error
   // word) of a call that may have given up, on this stream
   if (cudaMemsetAsync(ws, 0, L.clear_bytes, s) != cudaSuccess) return DART_ERR_CUDA;
-  if (launch_rows(logits, R, V, V, dtype, T, k, ws, L, sms, nullptr, nullptr, nullptr, s) != cudaSuccess)
-    return DART_ERR_CUDA;
-  TreeArgs a = tree_args(B, d, k, W, lambda, beta, ngram_table, ctx_tokens, out_tokens, out_parents,
-                         out_pos, out_mask, out_scores);
-  a.ids = reinterpret_cast<const int32_t*>(ws + L.row_ids);
-  a.base = reinterpret_cast<const double*>(ws + L.row_base);
-  a.off = reinterpret_cast<const double*>(ws + L.row_off);
-  a.invT = 1.0 / double(T);
-  a.ctrl = reinterpret_cast<uint32_t*>(ws + L.ctrl);
-  if (launch_tree(a, s) != cudaSuccess) return DART_ERR_CUDA;
-  return DART_OK;
+  return launch_path(logits, B, d, V, V, dtype, T, k, W, lambda, beta, ngram_table, ctx_tokens, out_tokens,
+                     out_parents, out_pos, out_mask, out_scores, ws, L, s);
 }
 
 int dart_tree_from_topk(const int32_t* cand_ids, const double* cand_logp,
@@ -251,12 +241,46 @@ int dart_row_topk_strided(const void* logits, int rows, int V, int64_t row_strid
   WsLayout L;
   if (!ws_layout(rows, V, elem_bytes(dtype), k, &L)) return DART_ERR_INVALID_ARG;
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return DART_ERR_WORKSPACE;
-  int sms = 0;
-  int rc = device_sms(&sms);
-  if (rc) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);   // counters are zero between calls
-  if (launch_rows(logits, rows, V, row_stride, dtype, T, k, workspace, L, sms, out_ids, out_logp, out_lse, s) !=
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_rows(logits, rows, V, row_stride, dtype, T, k, workspace, L, out_ids, out_logp, out_lse, s) !=
       cudaSuccess)
+    return DART_ERR_CUDA;
+  return DART_OK;
+}
+
+namespace {
+int check_rows(const void* logits, bool need_logits, int rows, int V, int64_t row_stride, int dtype, float T, int k,
+               const void* workspace, size_t workspace_bytes, WsLayout* L) {
+  if (rows < 0 || V < 2 || V > kMaxV || !valid_dtype(dtype) || k < 1 || k > kMaxK || k > V)
+    return DART_ERR_INVALID_ARG;
+  if (row_stride < V || row_stride > kMaxRowStride) return DART_ERR_INVALID_ARG;
+  if (!finite(T) || !(T > 0.f)) return DART_ERR_INVALID_ARG;
+  if (rows == 0) return DART_OK;
+  if (need_logits && (!logits || !aligned(logits, 16))) return DART_ERR_INVALID_ARG;
+  if (!ws_layout(rows, V, elem_bytes(dtype), k, L)) return DART_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < L->total) return DART_ERR_WORKSPACE;
+  return DART_OK;
+}
+}  // namespace
+
+int dart_row_pass(const void* logits, int rows, int V, int64_t row_stride, int dtype, float T, int k,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+  WsLayout L;
+  const int rc = check_rows(logits, true, rows, V, row_stride, dtype, T, k, workspace, workspace_bytes, &L);
+  if (rc || rows == 0) return rc;
+  if (launch_row_pass(logits, rows, V, row_stride, dtype, T, k, workspace, L, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return DART_ERR_CUDA;
+  return DART_OK;
+}
+
+int dart_row_finish(int rows, int V, int64_t row_stride, int dtype, float T, int k, int32_t* out_ids,
+                    float* out_logp, float* out_lse, void* workspace, size_t workspace_bytes, void* stream) {
+  WsLayout L;
+  const int rc = check_rows(nullptr, false, rows, V, row_stride, dtype, T, k, workspace, workspace_bytes, &L);
+  if (rc || rows == 0) return rc;
+  if (launch_row_merge(rows, V, row_stride, dtype, T, k, workspace, L, out_ids, out_logp, out_lse,
+                       static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return DART_ERR_CUDA;
   return DART_OK;
 }

@@ -109,9 +109,11 @@ constexpr uint64_t kMinTableSlots = 8;
 // [ctrl 256 B]                    <- ctrl word 0 holds error bits until read,
 //                                    words 2..3 the rows of the last call
 // [row_off R x f64][row_ids R*k x i32][row_base R*k x f64][piece slots]
-// row_off = the row's log-sum-exp of z / T; row_base = the candidates' logits;
-// a piece slot holds one warp's share of a row: its (max, scaled sum), its
-// lower bound of the row's k-th value and its candidate vectors.
+// row_off = the row's log-sum-exp of z / T; row_base = the candidates' logits.
+// A piece slot holds one warp's share of a row: {f32 max; u32 count; f64 sum
+// of 2^((z - max) c); u32 bound (an ordered float: a lower bound of the row's
+// k-th value); pad}, then cp candidate vectors of 16 bytes, then cp tags
+// ((element mask << 24) | row index of the vector's first element).
 //
 // The row pass cuts the logits into one contiguous span per warp of a fixed
 // nominal grid (152 SMs x 12 warps), so that the layout depends on the sizes
@@ -119,7 +121,7 @@ constexpr uint64_t kMinTableSlots = 8;
 constexpr int kCtrlBytes = 256;
 constexpr size_t kMinSpanBytes = 8192;      // smallest contiguous span of logits per warp of the row pass
 constexpr unsigned long long kRowPassWarps = 152ull * 12ull;
-constexpr int kSlotHeader = 32;             // {f32 max; u32 count; f64 sum; u32 bound; pad}
+constexpr int kSlotHeader = 32;
 
 // Bytes per warp of the row pass for a stream of `total` bytes.
 __host__ __device__ inline unsigned long long row_pass_span(unsigned long long total) {
@@ -127,9 +129,12 @@ __host__ __device__ inline unsigned long long row_pass_span(unsigned long long t
   span = (span + 15) & ~15ull;
   return span < kMinSpanBytes ? kMinSpanBytes : span;
 }
-// Candidate vectors one piece slot holds (about 2.5 times what a piece of
-// the streamed workloads typically keeps).
-__host__ __device__ inline int slot_capacity(int k) { return 8 + 12 * k; }
+// Candidate vectors a piece keeps (about 2.5 times what a piece of the
+// streamed workloads typically needs; more are compacted to the k best).
+__host__ __device__ inline int slot_capacity(int k) {
+  const int c = 8 + 12 * k;
+  return c < 200 ? c : 200;
+}
 
 struct WsLayout {
   size_t ctrl, clear_bytes;

@@ -9,8 +9,17 @@ namespace dart {
 long long rows_wait_limit();
 void set_rows_wait_limit(long long cycles);
 
+// The streaming pass over R rows (per-piece results in the workspace).
+cudaError_t launch_row_pass(const void* logits, long long R, int V, long long stride, int dtype, float T, int k,
+                            void* ws, const WsLayout& L, cudaStream_t stream);
+// The row merge: each row's results (row_off / row_ids / row_base in the
+// workspace, and the optional outputs) from the pass's per-piece results.
+cudaError_t launch_row_merge(long long R, int V, long long stride, int dtype, float T, int k, void* ws,
+                             const WsLayout& L, int32_t* out_ids, float* out_logp, float* out_lse,
+                             cudaStream_t stream);
+// Both.
 cudaError_t launch_rows(const void* logits, long long R, int V, long long stride, int dtype, float T, int k,
-                        void* ws, const WsLayout& L, int sms,
+                        void* ws, const WsLayout& L,
                         int32_t* out_ids, float* out_logp, float* out_lse, cudaStream_t stream);
 
 struct TreeArgs {

@@ -1,6 +1,5 @@
 // dart_rows.cu -- K1: one streaming pass over the logits computing, per row,
-// the temperature log-sum-exp and the k best candidates, and the row merge
-// that turns the pass's per-piece results into each row's answer.
+// the temperature log-sum-exp and the k best candidates.
 //
 // DART, Figure 3 caption: each of the d logit vectors of a sequence supplies
 // the candidates of one depth.  Here every row z[b][j][:] is read exactly once
@@ -12,31 +11,32 @@
 // span through its own ring of three 4 KiB shared-memory stages, filled by
 // bulk copies (cp.async.bulk, L2 evict-first) that its lane 0 issues three
 // stages ahead of the stage being reduced.  A span may cover the end of one
-// row and the start of the next; each (warp, row) overlap is a piece, with a
-// slot of its own in the workspace.
+// row and the start of the next; each (warp, row) overlap is a piece.
 //
 // Per stage a lane holds eight 16-byte vectors.  One packed maximum per
 // vector (bf16x2 / f16x2 max on 16-bit types) feeds one running-max update
 // per stage; each element then costs one fused multiply-add, one ex2.approx
 // and one add.
 //
-// Top-k.  The streaming warps keep no list.  Each lane's running maximum over
-// its elements of the piece is already at hand, and the lanes hold disjoint
-// elements, so the k-th largest of the 32 lane maxima is a lower bound tau of
-// the row's k-th value (k elements of the row reach it).  It only rises; it
-// is recomputed when k lanes have risen above it (one redux.sync min per lane
-// dropped), and warps of one CTA that work on the same row share it through
-// a word in shared memory (atomic max).  A stage's vectors whose maximum
-// reaches tau are copied, 16 bytes and an id with an element mask, into the
-// piece's slot: a vote and a few stores, no chain of shuffles.  Should a slot
-// fill up (inputs with very many near-equal values), the warp replaces its
-// candidates by their k best, which also lifts tau.
+// Top-k.  The streaming warps keep no sorted list.  Each lane's running
+// maximum over its elements of the piece is already at hand, and the lanes
+// hold disjoint elements, so the k-th largest of the 32 lane maxima is a lower
+// bound tau of the row's k-th value (k elements of the row reach it).  It only
+// rises; it is recomputed when k lanes have risen above it (one redux.sync
+// min per lane dropped), and warps of one CTA that work on the same row share
+// it through a word in shared memory (atomic max).  A stage's vectors whose
+// maximum reaches tau are copied, 16 bytes and an id with an element mask,
+// into the warp's candidate buffer in shared memory: a vote and a few stores,
+// no chain of shuffles.  Should the buffer fill up (inputs with very many
+// near-equal values), the warp replaces its candidates by their k best.
 //
-// Row merge.  A second, small kernel takes one warp per row: it merges the
-// pieces' (max, sum) in piece order, takes the largest of their bounds, keeps
-// the candidate elements that reach it and merges them into the row's k best
-// (warp bitonic merges), and writes the row's results.  Nothing in the
-// streaming kernel waits on another warp or on global memory.
+// Piece and row ends.  At a piece's end the warp writes its (max, sum), its
+// bound and its candidates to the piece's slot in the workspace (plain
+// stores, nothing waits).  The row merge, a second kernel with one CTA per
+// row, then merges the pieces' (max, sum) in piece order, takes the row's
+// bound (the largest of the pieces' bounds and, with k or more pieces, the
+// k-th largest piece maximum), keeps the candidate elements that reach it and
+// ranks them (each key counts the keys above it) to get the row's k best.
 //
 // Every wait (a stage landing) is bounded: on a timeout the warp records the
 // error bit, lets its copies in flight land and returns; the call's results
@@ -53,17 +53,17 @@ constexpr int kRowStages = 3;                     // bulk-copy stages in flight 
 constexpr int kStageBytes = 4096;                 // one stage: eight 16-byte vectors per lane
 constexpr int kStageVecs = kStageBytes / 16;
 constexpr int kVecPerLane = kStageVecs / 32;
-constexpr int kTauSlots = 64;                     // rows per CTA that can share a bound
-constexpr int kKeyStage = 32 * 8;                 // keys one expansion round can produce
+constexpr int kRowSlots = 64;                     // rows per CTA with a shared bound
+constexpr int kCandCap = 200;                     // candidate vectors a warp can buffer (slot_capacity <= this)
+constexpr int kKeyStage = 288;                    // keys a warp stages: one round of 32 x 8 plus k
 constexpr int kRowThreads = kRowWarps * 32;
-constexpr int kMergeWarps = 4;                    // rows per CTA of the row merge
 // Copies in flight always land before their warp retires: that drain is
 // bounded by about two seconds of SM clock whatever limit the other waits have.
 constexpr long long kDrainLimit = 4000000000LL;
 constexpr long long kDefaultWaitLimit = 4000000000LL;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 static_assert(kVecPerLane == 8, "stage_reduce reduces exactly eight vectors per lane");
-static_assert(kRowPassWarps % kRowWarps == 0, "whole CTAs");
+static_assert(kKeyStage >= 32 * 8 + kMaxK, "a stage must take one round of keys after keeping k");
 
 struct RowsParams {
   const uint8_t* logits;
@@ -87,33 +87,22 @@ struct RowsParams {
   long long wait_limit;
 };
 
-struct __align__(128) RowSmem {
-  uint8_t ring[kRowWarps][kRowStages][kStageBytes];
-  uint64_t keys[kRowWarps][kKeyStage];    // a warp's keys while it compacts a full slot
-  uint64_t full[kRowWarps][kRowStages];   // bytes of a stage have landed
-  uint32_t tau[kTauSlots];                // ordered form of each row's best published bound
+// A warp's candidates: vectors of logits and their tags (element mask << 24
+// | row index of the vector's first element; the mask says which elements
+// are real logits).
+struct WarpCands {
+  uint4 vecs[kCandCap];
+  uint32_t tags[kCandCap];
+  uint64_t keys[kKeyStage];   // keys while the warp ranks them
+  uint64_t best[kMaxK];
 };
 
-// A piece slot: header, then cp vectors of 16 bytes, then cp tags.  A tag is
-// (element mask << 24) | (row index of the vector's first element); the mask
-// says which of the vector's elements are real (a scalar head or tail, or a
-// kept candidate, is a vector with one real element).
-struct SlotView {
-  uint8_t* base;
-  int cp;
-  __device__ float* max_p() const { return reinterpret_cast<float*>(base); }
-  __device__ uint32_t* count_p() const { return reinterpret_cast<uint32_t*>(base + 4); }
-  __device__ double* sum_p() const { return reinterpret_cast<double*>(base + 8); }
-  __device__ uint32_t* bound_p() const { return reinterpret_cast<uint32_t*>(base + 16); }
-  __device__ uint4* vecs() const { return reinterpret_cast<uint4*>(base + kSlotHeader); }
-  __device__ uint32_t* tags() const { return reinterpret_cast<uint32_t*>(base + kSlotHeader + 16 * (size_t)cp); }
+struct __align__(128) RowSmem {
+  uint8_t ring[kRowWarps][kRowStages][kStageBytes];
+  WarpCands cand[kRowWarps];
+  uint64_t full[kRowWarps][kRowStages];   // bytes of a stage have landed
+  uint32_t tau[kRowSlots];                // ordered form of each row's best published bound
 };
-__device__ __forceinline__ SlotView slot_of(const RowsParams& P, long long r, long long p) {
-  SlotView v;
-  v.base = P.slots + ((size_t)r * P.pmax + (size_t)p) * P.slot_bytes;
-  v.cp = P.cp;
-  return v;
-}
 
 // ------------------------------------------------------------- element types
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
@@ -265,8 +254,7 @@ __device__ __forceinline__ uint32_t kth_above(uint32_t v, uint32_t above, int k)
   return __reduce_min_sync(kFull, cand ? v : 0xFFFFFFFFu);
 }
 
-// Keys (ordered value, inverted id) of the real elements of a vector that
-// reach tau; element e of a vector tagged (mask << 24) | id0 has id id0 + e.
+// Real elements of a tagged vector that reach tau (bit e = element e).
 template <int DT>
 __device__ __forceinline__ uint32_t vec_hits(const uint4& v, uint32_t tag, float tau) {
   uint32_t cm = 0;
@@ -276,89 +264,125 @@ __device__ __forceinline__ uint32_t vec_hits(const uint4& v, uint32_t tag, float
   return cm;
 }
 
-// Merges the keys of up to 32 vectors (one per lane, the elements in cm)
-// into the warp's best-32 list through the warp's key stage in shared memory.
-template <int DT>
-__device__ __forceinline__ uint64_t merge_vec_keys(uint64_t list, uint64_t* stage, const uint4& v, uint32_t tag,
-                                                   uint32_t cm) {
+// Keeps the k best of a warp's n staged keys (distinct) in keys[0..min(n,k)),
+// best first: each key counts the keys above it.  Returns min(n, k).
+__device__ __forceinline__ int keep_best(WarpCands& C, int n, int k) {
   const int lane = threadIdx.x & 31;
-  int nkeys;
-  int at = warp_prefix4(uint32_t(__popc(cm)), &nkeys);
-  const uint32_t id0 = tag & 0xFFFFFFu;
+  __syncwarp();
+  for (int i = lane; i < n; i += 32) {
+    const uint64_t key = C.keys[i];
+    int rank = 0;
+    for (int q = 0; q < n; ++q) rank += C.keys[q] > key ? 1 : 0;
+    if (rank < k) C.best[rank] = key;
+  }
+  __syncwarp();
+  const int kept = n < k ? n : k;
+  for (int i = lane; i < kept; i += 32) C.keys[i] = C.best[i];
+  __syncwarp();
+  return kept;
+}
+
+// Stages the keys of the elements in cm (element e of vector v has id
+// id0 + e; one vector per lane), keeping only the k best whenever the stage
+// could overflow.  Every lane takes part.
+template <int DT>
+__device__ __forceinline__ void stage_keys(WarpCands& C, int& n, int k, const uint4& v, uint32_t cm, uint32_t id0) {
+  int added;
+  const int pre = warp_prefix4(uint32_t(__popc(cm)), &added);
+  if (added == 0) return;
+  if (n + added > kKeyStage) n = keep_best(C, n, k);
+  int at = n + pre;
   while (cm) {
     const int e = __ffs(cm) - 1;
     cm &= cm - 1u;
-    stage[at++] = elem_key(Elem<DT>::elem(v, e), id0 + uint32_t(e));
+    C.keys[at++] = elem_key(Elem<DT>::elem(v, e), id0 + uint32_t(e));
   }
+  n += added;
   __syncwarp();
-  for (int q0 = 0; q0 < nkeys; q0 += 32) {
-    const uint64_t x = q0 + lane < nkeys ? stage[q0 + lane] : 0ull;
-    if (__any_sync(kFull, x != 0ull)) list = warp_merge_top32(list, x);
-  }
-  __syncwarp();
-  return list;
 }
 
-// A full slot: its candidates are replaced by their k best (tau rises to the
-// k-th of them when there are k).  Rare: only inputs with very many
-// near-equal values get here.
+// The k best keys of the warp's cnt candidates (elements reaching tau), best
+// first in C.keys; returns their number.
 template <int DT>
-__device__ __forceinline__ void compact_slot(const SlotView& sv, int& cnt, uint32_t& tau_o, uint64_t* stage, int k) {
+__device__ __forceinline__ int cands_best(WarpCands& C, int cnt, float tau, int k) {
   const int lane = threadIdx.x & 31;
-  __threadfence_block();   // the lanes' candidate stores before the reads below
   __syncwarp();
-  const float tau = tau_value(tau_o);
-  uint64_t list = 0;
+  int n = 0;
   for (int b0 = 0; b0 < cnt; b0 += 32) {
     const int i = b0 + lane;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     uint32_t tag = 0;
     if (i < cnt) {
-      v = __ldcg(sv.vecs() + i);
-      tag = __ldcg(sv.tags() + i);
+      v = C.vecs[i];
+      tag = C.tags[i];
     }
-    list = merge_vec_keys<DT>(list, stage, v, tag, i < cnt ? vec_hits<DT>(v, tag, tau) : 0u);
+    stage_keys<DT>(C, n, k, v, i < cnt ? vec_hits<DT>(v, tag, tau) : 0u, tag & 0xFFFFFFu);
   }
-  const bool keep = lane < k && list != 0ull;
-  cnt = __popc(__ballot_sync(kFull, keep));
-  if (keep) {
-    sv.vecs()[lane] = single_vec<DT>(key_value(list));
-    sv.tags()[lane] = (1u << 24) | key_id(list);
+  return keep_best(C, n, k);
+}
+
+// A full buffer: its candidates are replaced by their k best (tau rises to
+// the k-th of them when there are k).  Rare: only inputs with very many
+// near-equal values get here.
+template <int DT>
+__device__ __forceinline__ void compact_cands(WarpCands& C, int& cnt, uint32_t& tau_o, int k) {
+  const int lane = threadIdx.x & 31;
+  const int kept = cands_best<DT>(C, cnt, tau_value(tau_o), k);
+  if (lane < kept) {
+    const uint64_t key = C.keys[lane];
+    C.vecs[lane] = single_vec<DT>(key_value(key));
+    C.tags[lane] = (1u << 24) | key_id(key);
   }
-  if (cnt == k) {
-    const uint32_t o = uint32_t(__shfl_sync(kFull, list, k - 1) >> 32);
+  cnt = kept;
+  if (kept == k) {
+    const uint32_t o = uint32_t(C.keys[k - 1] >> 32);
     if (o > tau_o) tau_o = o;
   }
   __syncwarp();
 }
 
 // Appends the lanes' candidate vectors (vector u of the lane when bit u of
-// hm is set; its tag in tags[u]) to the slot, compacting whenever it is full.
+// hm is set), compacting whenever the buffer is full.
 template <int DT>
-__device__ __forceinline__ void slot_append(const SlotView& sv, int& cnt, uint32_t& tau_o, uint64_t* stage, int k,
-                                            const uint4 (&r)[kVecPerLane], uint32_t hm, uint32_t id0) {
+__device__ __forceinline__ void cands_append(WarpCands& C, int cap, int& cnt, uint32_t& tau_o, int k,
+                                             const uint4 (&r)[kVecPerLane], uint32_t hm, uint32_t id0) {
   constexpr int EPV = Elem<DT>::kPerVec;
   constexpr uint32_t kMask = ((1u << EPV) - 1u) << 24;
   const int lane = threadIdx.x & 31;
   int total;
   const int first = warp_prefix4(uint32_t(__popc(hm)), &total);
+  if (cnt + total <= cap) {
+    int pos = cnt + first;
+#pragma unroll
+    for (int u = 0; u < kVecPerLane; ++u) {
+      if ((hm >> u) & 1u) {
+        C.vecs[pos] = r[u];
+        C.tags[pos] = kMask | (id0 + uint32_t((u * 32 + lane) * EPV));
+        ++pos;
+      }
+    }
+    cnt += total;
+    __syncwarp();
+    return;
+  }
   int done = 0;
   while (done < total) {
-    if (cnt == sv.cp) compact_slot<DT>(sv, cnt, tau_o, stage, k);
-    const int take = min(sv.cp - cnt, total - done);
+    if (cnt == cap) compact_cands<DT>(C, cnt, tau_o, k);
+    const int take = min(cap - cnt, total - done);
     int q = first;
 #pragma unroll
     for (int u = 0; u < kVecPerLane; ++u) {
       if ((hm >> u) & 1u) {
         if (q >= done && q < done + take) {
-          sv.vecs()[cnt + q - done] = r[u];
-          sv.tags()[cnt + q - done] = kMask | (id0 + uint32_t((u * 32 + lane) * EPV));
+          C.vecs[cnt + q - done] = r[u];
+          C.tags[cnt + q - done] = kMask | (id0 + uint32_t((u * 32 + lane) * EPV));
         }
         ++q;
       }
     }
     cnt += take;
     done += take;
+    __syncwarp();
   }
 }
 
@@ -366,7 +390,7 @@ __device__ __forceinline__ void slot_append(const SlotView& sv, int& cnt, uint32
 // -inf, whose terms are exactly 0).  id0 = row index of the stage's first
 // element.  SEED: the stage opens a piece (its lanes' maxima are all new).
 template <int DT, bool SEED>
-__device__ __forceinline__ void stage_reduce(Acc& a, uint32_t& tau_o, int& cnt, const SlotView& sv, uint64_t* kstage,
+__device__ __forceinline__ void stage_reduce(Acc& a, uint32_t& tau_o, int& cnt, WarpCands& C, int cap,
                                              const uint4* src, int nv, uint32_t id0, float c, int k,
                                              uint32_t* tau_slot) {
   using E = Elem<DT>;
@@ -434,32 +458,16 @@ __device__ __forceinline__ void stage_reduce(Acc& a, uint32_t& tau_o, int& cnt, 
       for (int u = 0; u < U; ++u)
         if (u * 32 + lane >= nv) hm &= ~(1u << u);
     }
-    int total;
-    int pos = warp_prefix4(uint32_t(__popc(hm)), &total);
-    if (cnt + total <= sv.cp) {
-      constexpr uint32_t kMask = ((1u << EPV) - 1u) << 24;
-      pos += cnt;
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if ((hm >> u) & 1u) {
-          sv.vecs()[pos] = r[u];
-          sv.tags()[pos] = kMask | (id0 + uint32_t((u * 32 + lane) * EPV));
-          ++pos;
-        }
-      }
-      cnt += total;
-    } else {
-      slot_append<DT>(sv, cnt, tau_o, kstage, k, r, hm, id0);
-    }
+    cands_append<DT>(C, cap, cnt, tau_o, k, r, hm, id0);
   }
 }
 
 // Unaligned elements [b0, b1) of a piece (its head or tail), one per lane;
 // a candidate becomes a one-element vector.
 template <int DT>
-__device__ __forceinline__ void piece_scalars(Acc& a, uint32_t& tau_o, int& cnt, const SlotView& sv,
-                                              uint64_t* kstage, const uint8_t* logits, unsigned long long b0,
-                                              unsigned long long b1, int es, uint32_t id0, float c, int k) {
+__device__ __forceinline__ void piece_scalars(Acc& a, uint32_t& tau_o, int& cnt, WarpCands& C, int cap,
+                                              const uint8_t* logits, unsigned long long b0, unsigned long long b1,
+                                              int es, uint32_t id0, float c, int k) {
   const int lane = threadIdx.x & 31;
   const int n = int((b1 - b0) / es);
   for (int base = 0; base < n; base += 32) {
@@ -474,26 +482,13 @@ __device__ __forceinline__ void piece_scalars(Acc& a, uint32_t& tau_o, int& cnt,
     int total;
     const int at = warp_prefix4(hit ? 1u : 0u, &total);
     if (total == 0) continue;
-    if (cnt + total > sv.cp) compact_slot<DT>(sv, cnt, tau_o, kstage, k);
-    if (cnt + total > sv.cp) {
-      // still no room for 32 (k close to the slot size): one at a time
-      for (int j = 0; j < 32; ++j) {
-        const bool mine = hit && at == j;
-        if (!__any_sync(kFull, mine)) continue;
-        if (cnt == sv.cp) compact_slot<DT>(sv, cnt, tau_o, kstage, k);
-        if (mine) {
-          sv.vecs()[cnt] = single_vec<DT>(z);
-          sv.tags()[cnt] = (1u << 24) | (id0 + uint32_t(i));
-        }
-        ++cnt;
-      }
-      continue;
-    }
+    if (cnt + total > cap) compact_cands<DT>(C, cnt, tau_o, k);
     if (hit) {
-      sv.vecs()[cnt + at] = single_vec<DT>(z);
-      sv.tags()[cnt + at] = (1u << 24) | (id0 + uint32_t(i));
+      C.vecs[cnt + at] = single_vec<DT>(z);
+      C.tags[cnt + at] = (1u << 24) | (id0 + uint32_t(i));
     }
     cnt += total;
+    __syncwarp();
   }
 }
 
@@ -518,32 +513,59 @@ __device__ __forceinline__ Seg segment(const RowsParams& P, unsigned long long e
   return g;
 }
 
-// First and last warp whose span meets row r.
-__device__ __forceinline__ void row_warps(const RowsParams& P, long long r, long long* wa, long long* wb) {
-  const unsigned long long rb0 = (unsigned long long)r * P.stride * P.es;
-  *wa = (long long)(rb0 / P.wspan);
-  *wb = (long long)((rb0 + (unsigned long long)P.V * P.es - 1) / P.wspan);
+// ------------------------------------------------------------------ row end
+// A piece slot: {f32 max; u32 count; f64 sum; u32 bound; pad}, then cp
+// vectors, then cp tags.
+__device__ __forceinline__ uint8_t* slot_of(const RowsParams& P, long long r, long long p) {
+  return P.slots + ((size_t)r * P.pmax + (size_t)p) * P.slot_bytes;
+}
+__device__ __forceinline__ uint4* slot_vecs(const RowsParams& P, uint8_t* q) {
+  return reinterpret_cast<uint4*>(q + kSlotHeader);
+}
+__device__ __forceinline__ uint32_t* slot_tags(const RowsParams& P, uint8_t* q) {
+  return reinterpret_cast<uint32_t*>(q + kSlotHeader + 16 * (size_t)P.cp);
 }
 
-// The end of a piece: the warp's (max, sum), count and bound into its slot.
-__device__ __forceinline__ void piece_end(const RowsParams& P, const SlotView& sv, const Acc& a, int cnt,
-                                          uint32_t tau_o) {
+// First warp whose span meets row r; returns the row's number of pieces.
+__device__ __forceinline__ int row_pieces(const RowsParams& P, long long r, long long* wa) {
+  const unsigned long long rb0 = (unsigned long long)r * P.stride * P.es;
+  const long long a = (long long)(rb0 / P.wspan);
+  const long long b = (long long)((rb0 + (unsigned long long)P.V * P.es - 1) / P.wspan);
+  *wa = a;
+  return int(b - a + 1);
+}
+
+// The end of a piece of row r: the warp's (max, sum), bound and candidates
+// into the piece's slot.  Plain stores; nothing waits.
+__device__ __forceinline__ void piece_end(const RowsParams& P, const WarpCands& C, const Acc& a, int cnt,
+                                          uint32_t tau_o, long long r, long long gwarp) {
   const int lane = threadIdx.x & 31;
   float m = a.m, s = exact_sum(a, P.c);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float m2 = __shfl_xor_sync(kFull, m, o);
     const float s2 = __shfl_xor_sync(kFull, s, o);
-    const float M = fmaxf(m, m2);
-    s = s * ex2_approx((m - M) * P.c) + s2 * ex2_approx((m2 - M) * P.c);
-    m = M;
+    const float Mx = fmaxf(m, m2);
+    s = s * ex2_approx((m - Mx) * P.c) + s2 * ex2_approx((m2 - Mx) * P.c);
+    m = Mx;
   }
+  long long wa;
+  (void)row_pieces(P, r, &wa);
+  uint8_t* q = slot_of(P, r, gwarp - wa);
   if (lane == 0) {
-    *sv.max_p() = m;
-    *sv.count_p() = uint32_t(cnt);
-    *sv.sum_p() = double(s);
-    *sv.bound_p() = tau_o;
+    *reinterpret_cast<float*>(q) = m;
+    *reinterpret_cast<uint32_t*>(q + 4) = uint32_t(cnt);
+    *reinterpret_cast<double*>(q + 8) = double(s);
+    *reinterpret_cast<uint32_t*>(q + 16) = tau_o;
   }
+  __syncwarp();
+  uint4* vv = slot_vecs(P, q);
+  uint32_t* tt = slot_tags(P, q);
+  for (int i = lane; i < cnt; i += 32) {
+    vv[i] = C.vecs[i];
+    tt[i] = C.tags[i];
+  }
+  __syncwarp();
 }
 
 // Next stage of a warp's span after byte `off` of row r (a stage starts at
@@ -602,11 +624,11 @@ row_stream_kernel(const __grid_constant__ RowsParams P) {
   const long long gwarp = (long long)blockIdx.x * kRowWarps + w;
 
   if (blockIdx.x == 0 && threadIdx.x == 0) {
-    // rows of this call, for the error readout
+    // rows of this call, for clearing the counters after a failed call
     P.ctrl[2] = uint32_t((unsigned long long)P.R);
     P.ctrl[3] = uint32_t((unsigned long long)P.R >> 32);
   }
-  for (int i = threadIdx.x; i < kTauSlots; i += blockDim.x) S.tau[i] = 0u;
+  for (int i = threadIdx.x; i < kRowSlots; i += blockDim.x) S.tau[i] = 0u;
   if (lane == 0) {
     for (int s = 0; s < kRowStages; ++s) mbar_init(&S.full[w][s], 1);
     fence_mbar_init();
@@ -628,7 +650,7 @@ row_stream_kernel(const __grid_constant__ RowsParams P) {
   const uint64_t pol = policy_evict_first();
   uint8_t* ring = &S.ring[w][0][0];
   uint64_t* full = &S.full[w][0];
-  uint64_t* kstage = S.keys[w];
+  WarpCands& C = S.cand[w];
   // lane 0 issues the stages; every lane follows the same sequence to consume them
   Cursor iss;
   iss.r = r_first;
@@ -657,10 +679,7 @@ row_stream_kernel(const __grid_constant__ RowsParams P) {
     if (g.s1 <= g.s0) continue;
     const unsigned long long rs = (unsigned long long)r * P.stride;
     const long long slot_i = r - cta_r0;
-    uint32_t* tau_slot = (slot_i >= 0 && slot_i < kTauSlots) ? &S.tau[slot_i] : nullptr;
-    long long wa, wb;
-    row_warps(P, r, &wa, &wb);
-    const SlotView sv = slot_of(P, r, gwarp - wa);
+    uint32_t* tau_slot = (slot_i >= 0 && slot_i < kRowSlots) ? &S.tau[slot_i] : nullptr;
     Acc a;
     a.m = -FLT_MAX;
     a.mc = scaled_max(a.m, P.c);
@@ -671,7 +690,8 @@ row_stream_kernel(const __grid_constant__ RowsParams P) {
     {
       const unsigned long long hb0 = g.s0 * P.es;
       const unsigned long long hb1 = (g.a < g.b) ? g.a : g.s1 * P.es;
-      if (hb1 > hb0) piece_scalars<DT>(a, tau_o, cnt, sv, kstage, P.logits, hb0, hb1, P.es, uint32_t(g.s0 - rs), P.c, P.k);
+      if (hb1 > hb0)
+        piece_scalars<DT>(a, tau_o, cnt, C, P.cp, P.logits, hb0, hb1, P.es, uint32_t(g.s0 - rs), P.c, P.k);
     }
     // aligned interior, stage by stage (offsets within the interior fit 32 bits)
     const uint32_t ilen = uint32_t(g.b - g.a);
@@ -685,8 +705,8 @@ row_stream_kernel(const __grid_constant__ RowsParams P) {
       const uint32_t rem = ilen - o;
       const int nv = int((rem < uint32_t(kStageBytes) ? rem : uint32_t(kStageBytes)) >> 4);
       const uint32_t id0 = id_a + (o >> SH);
-      if (o == 0) stage_reduce<DT, true>(a, tau_o, cnt, sv, kstage, src, nv, id0, P.c, P.k, tau_slot);
-      else stage_reduce<DT, false>(a, tau_o, cnt, sv, kstage, src, nv, id0, P.c, P.k, tau_slot);
+      if (o == 0) stage_reduce<DT, true>(a, tau_o, cnt, C, P.cp, src, nv, id0, P.c, P.k, tau_slot);
+      else stage_reduce<DT, false>(a, tau_o, cnt, C, P.cp, src, nv, id0, P.c, P.k, tau_slot);
       __syncwarp();
       ++consumed;
       if (++cslot == kRowStages) {
@@ -699,9 +719,9 @@ row_stream_kernel(const __grid_constant__ RowsParams P) {
     if (!ok) break;
     // tail: [b, s1)
     if (g.a < g.b && g.s1 * P.es > g.b)
-      piece_scalars<DT>(a, tau_o, cnt, sv, kstage, P.logits, g.b, g.s1 * P.es, P.es, uint32_t((g.b >> SH) - rs), P.c,
+      piece_scalars<DT>(a, tau_o, cnt, C, P.cp, P.logits, g.b, g.s1 * P.es, P.es, uint32_t((g.b >> SH) - rs), P.c,
                         P.k);
-    piece_end(P, sv, a, cnt, tau_o);
+    piece_end(P, C, a, cnt, tau_o, r, gwarp);
   }
   if (!ok) {
     set_dev_error(lane == 0 ? P.ctrl : nullptr, DART_DEVERR_WAIT_TIMEOUT);
@@ -717,21 +737,27 @@ row_stream_kernel(const __grid_constant__ RowsParams P) {
 }
 
 // ---------------------------------------------------------------- row merge
+constexpr int kMergeThreads = 256;
+constexpr int kMergePieces = 64;     // pieces a row merges from shared memory (more: the loop below)
+constexpr int kMergeKeys = 1024;     // candidate keys a row keeps in shared memory (more: one warp merges)
+
 // Writes a row's results from its maximum M, its sum S of 2^((z - M) c) and
-// its best keys (lanes 0..k-1 hold them, descending).
-__device__ __forceinline__ void finish_row(const RowsParams& P, long long r, float M, double S, uint64_t list) {
+// its best keys (keys[0..kept), descending); one warp.
+__device__ __forceinline__ void finish_row(const RowsParams& P, long long r, float M, double S, const uint64_t* keys,
+                                           int kept) {
   const int lane = threadIdx.x & 31;
   const int k = P.k;
-  const float zmax = key_value(__shfl_sync(kFull, list, 0));
-  if (lane == 0 && zmax != M) set_dev_error(P.ctrl, DART_DEVERR_ROW_MAX);
+  const float zmax = kept > 0 ? key_value(keys[0]) : -INFINITY;
+  if (lane == 0 && (kept < k || zmax != M)) set_dev_error(P.ctrl, DART_DEVERR_ROW_MAX);
   // log S = e ln 2 + log f with S = f 2^e, f in [0.5, 1): one float log of
   // the mantissa keeps the slow double unit to a multiply and an add
   int e2;
   const double f = frexp(S, &e2);
   const double logS = double(e2) * 0.6931471805599453 + double(logf(float(f)));
   if (lane < k) {
-    const float z = key_value(list);
-    const int32_t id = int32_t(key_id(list));
+    const uint64_t key = lane < kept ? keys[lane] : 0ull;
+    const float z = key_value(key);
+    const int32_t id = int32_t(key_id(key));
     P.row_ids[(size_t)r * k + lane] = id;
     P.row_base[(size_t)r * k + lane] = double(z);
     if (P.out_ids) P.out_ids[(size_t)r * k + lane] = id;
@@ -744,137 +770,191 @@ __device__ __forceinline__ void finish_row(const RowsParams& P, long long r, flo
   }
 }
 
-// Merges the first n keys of a warp's key stage into its best-32 list.
-__device__ __forceinline__ uint64_t merge_staged(uint64_t list, const uint64_t* stage, int n) {
-  const int lane = threadIdx.x & 31;
-  for (int q0 = 0; q0 < n; q0 += 32) {
-    const uint64_t x = q0 + lane < n ? stage[q0 + lane] : 0ull;
-    if (__any_sync(kFull, x != 0ull)) list = warp_merge_top32(list, x);
-  }
-  __syncwarp();
-  return list;
-}
+struct MergeSmem {
+  float m[kMergePieces];
+  double s[kMergePieces];
+  uint32_t end[kMergePieces];   // running end of the pieces' candidates
+  uint32_t bound;
+  uint32_t nkeys;
+  float M;
+  double S;
+  uint64_t keys[kMergeKeys];
+  uint64_t best[kMaxK];
+};
 
-// One warp per row: the pieces' (max, sum) merged in piece order, the
-// largest of their bounds, and the row's k best among the candidates that
-// reach it.  All candidate loads of a round (eight per lane) are issued
-// together; the passing elements' keys are staged in shared memory and
-// merged once at the end (earlier only if the stage fills).
+// One CTA per row: every piece's header in one round of loads, the row's
+// bound, every candidate in one round (one per thread), the keys of the
+// elements reaching the bound appended in shared memory, and the row's k best
+// by ranking (each key counts the keys above it).  A row with more than
+// kMergePieces pieces, or more than kMergeKeys such keys, is merged by one
+// warp instead (inputs far from the streamed shapes).
 template <int DT>
-__global__ void __launch_bounds__(kMergeWarps * 32, 1)
+__global__ void __launch_bounds__(kMergeThreads)
 row_merge_kernel(const __grid_constant__ RowsParams P) {
-  __shared__ uint64_t keys[kMergeWarps][kKeyStage];
-  __shared__ uint32_t pend[kMergeWarps][64];   // running end of each piece's candidates (pieces <= 64 per round)
-  const int lane = threadIdx.x & 31;
-  const int w = threadIdx.x >> 5;
-  const long long r = (long long)blockIdx.x * kMergeWarps + w;
-  if (r >= P.R) return;
-  long long wa, wb;
-  row_warps(P, r, &wa, &wb);
-  const int nseg = int(wb - wa + 1);
-  // headers: every piece's max, sum and bound in one round of loads
-  float M = -FLT_MAX;
-  uint32_t bound = 0;
-  float mp[2] = {-FLT_MAX, -FLT_MAX};
-  double sp[2] = {0.0, 0.0};
+  __shared__ MergeSmem M;
+  __shared__ uint64_t wstage[kKeyStage];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long r = blockIdx.x;
+  long long wa;
+  const int nseg = row_pieces(P, r, &wa);
+  const int k = P.k;
+  if (nseg <= kMergePieces) {
+    if (tid < nseg) {
+      uint8_t* q = slot_of(P, r, tid);
+      M.m[tid] = __ldcg(reinterpret_cast<const float*>(q));
+      M.s[tid] = __ldcg(reinterpret_cast<const double*>(q + 8));
+      M.end[tid] = min(__ldcg(reinterpret_cast<const uint32_t*>(q + 4)), uint32_t(P.cp));
+    }
+    if (tid == 0) M.nkeys = 0u;
+    __syncthreads();
+    if (warp == 0) {
+      // the bound: the largest piece bound, and the k-th largest piece maximum
+      uint32_t b = 0;
+      for (int p = lane; p < nseg; p += 32) b = max(b, __ldcg(reinterpret_cast<const uint32_t*>(slot_of(P, r, p) + 16)));
+      if (nseg >= k) {
+        for (int p = lane; p < nseg; p += 32) {
+          const uint32_t x = ord_f32(M.m[p]);
+          int above = 0, atleast = 0;
+          for (int q2 = 0; q2 < nseg; ++q2) {
+            const uint32_t y = ord_f32(M.m[q2]);
+            above += y > x ? 1 : 0;
+            atleast += y >= x ? 1 : 0;
+          }
+          if (above < k && atleast >= k) b = max(b, x);
+        }
+      }
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int p = lane + 32 * h;
-    if (p < nseg) {
-      const SlotView sv = slot_of(P, r, p);
-      mp[h] = __ldcg(sv.max_p());
-      sp[h] = __ldcg(sv.sum_p());
-      bound = max(bound, __ldcg(sv.bound_p()));
+      for (int o = 16; o > 0; o >>= 1) b = max(b, __shfl_xor_sync(kFull, b, o));
+      if (lane == 0) {
+        // max, the sum in piece order, running ends of the candidates
+        float mx = -FLT_MAX;
+        for (int p = 0; p < nseg; ++p) mx = fmaxf(mx, M.m[p]);
+        double sum = 0.0;
+        uint32_t run = 0;
+        for (int p = 0; p < nseg; ++p) {
+          sum += M.s[p] * double(ex2_approx((M.m[p] - mx) * P.c));
+          run += M.end[p];
+          M.end[p] = run;
+        }
+        M.M = mx;
+        M.S = sum;
+        M.bound = b;
+      }
+    }
+    __syncthreads();
+    // candidates, one per thread and round
+    const uint32_t total = nseg > 0 ? M.end[nseg - 1] : 0u;
+    const float tau = tau_value(M.bound);
+    for (uint32_t e = tid; e < total; e += kMergeThreads) {
+      int lo = 0, hi = nseg - 1;   // first piece whose running end exceeds e
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (M.end[mid] > e) hi = mid;
+        else lo = mid + 1;
+      }
+      const uint32_t i = e - (lo > 0 ? M.end[lo - 1] : 0u);
+      uint8_t* q = slot_of(P, r, lo);
+      const uint4 v = __ldcg(slot_vecs(P, q) + i);
+      const uint32_t tag = __ldcg(slot_tags(P, q) + i);
+      uint32_t cm = vec_hits<DT>(v, tag, tau);
+      if (cm) {
+        uint32_t at = atomicAdd(&M.nkeys, uint32_t(__popc(cm)));
+        while (cm) {
+          const int el = __ffs(cm) - 1;
+          cm &= cm - 1u;
+          if (at < uint32_t(kMergeKeys)) M.keys[at] = elem_key(Elem<DT>::elem(v, el), (tag & 0xFFFFFFu) + uint32_t(el));
+          ++at;
+        }
+      }
+    }
+    __syncthreads();
+    const uint32_t n = M.nkeys;
+    if (n <= uint32_t(kMergeKeys)) {
+      for (uint32_t i = tid; i < n; i += kMergeThreads) {
+        const uint64_t key = M.keys[i];
+        int rank = 0;
+        for (uint32_t q2 = 0; q2 < n; ++q2) rank += M.keys[q2] > key ? 1 : 0;
+        if (rank < k) M.best[rank] = key;
+      }
+      __syncthreads();
+      if (warp == 0) finish_row(P, r, M.M, M.S, M.best, int(n < uint32_t(k) ? n : uint32_t(k)));
+      return;
     }
   }
-  for (int p = lane + 64; p < nseg; p += 32) {   // rows cut into more than 64 pieces
-    const SlotView sv = slot_of(P, r, p);
-    const float m2 = __ldcg(sv.max_p());
-    const double s2 = __ldcg(sv.sum_p());
-    const float M2 = fmaxf(mp[1], m2);
-    sp[1] = sp[1] * double(ex2_approx((mp[1] - M2) * P.c)) + s2 * double(ex2_approx((m2 - M2) * P.c));
-    mp[1] = M2;
-    bound = max(bound, __ldcg(sv.bound_p()));
+  // one warp, any number of pieces and keys: merged in rounds through the
+  // warp's key stage, the k best kept whenever it could overflow
+  if (warp != 0) return;
+  float mp = -FLT_MAX;
+  double sp = 0.0;
+  uint32_t b = 0;
+  for (int p = lane; p < nseg; p += 32) {
+    uint8_t* q = slot_of(P, r, p);
+    const float m2 = __ldcg(reinterpret_cast<const float*>(q));
+    const double s2 = __ldcg(reinterpret_cast<const double*>(q + 8));
+    const float M2 = fmaxf(mp, m2);
+    sp = sp * double(ex2_approx((mp - M2) * P.c)) + s2 * double(ex2_approx((m2 - M2) * P.c));
+    mp = M2;
+    b = max(b, __ldcg(reinterpret_cast<const uint32_t*>(q + 16)));
   }
-  M = fmaxf(mp[0], mp[1]);
+  float Mx = mp;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-    bound = max(bound, __shfl_xor_sync(kFull, bound, o));
+    Mx = fmaxf(Mx, __shfl_xor_sync(kFull, Mx, o));
+    b = max(b, __shfl_xor_sync(kFull, b, o));
   }
-  double S = sp[0] * double(ex2_approx((mp[0] - M) * P.c)) + sp[1] * double(ex2_approx((mp[1] - M) * P.c));
+  double Sx = sp * double(ex2_approx((mp - Mx) * P.c));
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(kFull, S, o);
-  const float tau = tau_value(bound);
-  // candidates, up to 64 pieces at a time: piece p's are entries
-  // [pend[p-1], pend[p]) of the round's flattened list
-  uint64_t list = 0;
-  int nk = 0;   // keys staged
-  for (int p0 = 0; p0 < nseg; p0 += 64) {
-    const int np = min(64, nseg - p0);
-    uint32_t c0 = 0, c1 = 0;
-    if (lane < np) c0 = min(__ldcg(slot_of(P, r, p0 + lane).count_p()), uint32_t(P.cp));
-    if (lane + 32 < np) c1 = min(__ldcg(slot_of(P, r, p0 + lane + 32).count_p()), uint32_t(P.cp));
-    uint32_t s0 = c0, s1 = c1;   // inclusive scans of the counts
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t t0 = __shfl_up_sync(kFull, s0, o), t1 = __shfl_up_sync(kFull, s1, o);
-      if (lane >= o) {
-        s0 += t0;
-        s1 += t1;
+  for (int o = 16; o > 0; o >>= 1) Sx += __shfl_xor_sync(kFull, Sx, o);
+  const float tau = tau_value(b);
+  int nk = 0;
+  for (int p = 0; p < nseg; ++p) {
+    uint8_t* q = slot_of(P, r, p);
+    const int cnt = int(min(__ldcg(reinterpret_cast<const uint32_t*>(q + 4)), uint32_t(P.cp)));
+    for (int i0 = 0; i0 < cnt; i0 += 32) {
+      const int i = i0 + lane;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      uint32_t tag = 0;
+      if (i < cnt) {
+        v = __ldcg(slot_vecs(P, q) + i);
+        tag = __ldcg(slot_tags(P, q) + i);
       }
-    }
-    s1 += __shfl_sync(kFull, s0, 31);
-    pend[w][lane] = s0;
-    pend[w][lane + 32] = s1;
-    const int total = int(__shfl_sync(kFull, s1, 31));
-    __syncwarp();
-    for (int j0 = 0; j0 < total; j0 += 256) {
-      uint4 v[8];
-      uint32_t tag[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int j = j0 + t * 32 + lane;
-        tag[t] = 0;
-        v[t] = make_uint4(0u, 0u, 0u, 0u);
-        if (j < total) {
-          int lo = 0, hi = np - 1;   // first piece whose running end exceeds j
-          while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (pend[w][mid] > uint32_t(j)) hi = mid;
-            else lo = mid + 1;
-          }
-          const int i = j - (lo > 0 ? int(pend[w][lo - 1]) : 0);
-          const SlotView sv = slot_of(P, r, p0 + lo);
-          v[t] = __ldcg(sv.vecs() + i);
-          tag[t] = __ldcg(sv.tags() + i);
+      uint32_t cm = i < cnt ? vec_hits<DT>(v, tag, tau) : 0u;
+      int added;
+      const int pre = warp_prefix4(uint32_t(__popc(cm)), &added);
+      if (added == 0) continue;
+      if (nk + added > kKeyStage) {
+        // keep the k best of the stage (ranking), best first
+        __syncwarp();
+        for (int x = lane; x < nk; x += 32) {
+          const uint64_t key = wstage[x];
+          int rank = 0;
+          for (int y = 0; y < nk; ++y) rank += wstage[y] > key ? 1 : 0;
+          if (rank < k) M.best[rank] = key;
         }
+        __syncwarp();
+        nk = nk < k ? nk : k;
+        for (int x = lane; x < nk; x += 32) wstage[x] = M.best[x];
+        __syncwarp();
       }
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        uint32_t cm = vec_hits<DT>(v[t], tag[t], tau);
-        int added;
-        const int pre = warp_prefix4(uint32_t(__popc(cm)), &added);
-        if (added == 0) continue;
-        if (nk + added > kKeyStage) {   // rare: make room (added <= kKeyStage)
-          list = merge_staged(list, keys[w], nk);
-          nk = 0;
-        }
-        int q = nk + pre;
-        const uint32_t id0 = tag[t] & 0xFFFFFFu;
-        while (cm) {
-          const int e = __ffs(cm) - 1;
-          cm &= cm - 1u;
-          keys[w][q++] = elem_key(Elem<DT>::elem(v[t], e), id0 + uint32_t(e));
-        }
-        nk += added;
+      int at = nk + pre;
+      while (cm) {
+        const int el = __ffs(cm) - 1;
+        cm &= cm - 1u;
+        wstage[at++] = elem_key(Elem<DT>::elem(v, el), (tag & 0xFFFFFFu) + uint32_t(el));
       }
+      nk += added;
       __syncwarp();
     }
-    __syncwarp();
   }
-  list = merge_staged(list, keys[w], nk);
-  finish_row(P, r, M, S, list);
+  __syncwarp();
+  for (int x = lane; x < nk; x += 32) {
+    const uint64_t key = wstage[x];
+    int rank = 0;
+    for (int y = 0; y < nk; ++y) rank += wstage[y] > key ? 1 : 0;
+    if (rank < k) M.best[rank] = key;
+  }
+  __syncwarp();
+  finish_row(P, r, Mx, Sx, M.best, nk < k ? nk : k);
 }
 
 // ------------------------------------------------------------------ launch
@@ -888,10 +968,9 @@ void set_rows_wait_limit(long long cycles) {
   g_wait_limit.store(cycles > 0 ? cycles : kDefaultWaitLimit, std::memory_order_relaxed);
 }
 
-cudaError_t launch_rows(const void* logits, long long R, int V, long long stride, int dtype, float T, int k,
-                        void* ws, const WsLayout& L, int /*sms*/,
-                        int32_t* out_ids, float* out_logp, float* out_lse, cudaStream_t stream) {
-  RowsParams P;
+static bool rows_params(RowsParams* Pp, const void* logits, long long R, int V, long long stride, int dtype, float T,
+                        int k, void* ws, const WsLayout& L, int32_t* out_ids, float* out_logp, float* out_lse) {
+  RowsParams& P = *Pp;
   const int es = dtype == DART_F32 ? 4 : 2;
   P.logits = static_cast<const uint8_t*>(logits);
   P.R = R;
@@ -906,9 +985,7 @@ cudaError_t launch_rows(const void* logits, long long R, int V, long long stride
   // spans of the fixed nominal grid; padded rows only make them longer, so
   // a row never has more pieces than the layout's slots
   P.wspan = row_pass_span(P.total);
-  if (P.wspan < L.wspan) return cudaErrorInvalidValue;
-  const unsigned long long warps = (P.total + P.wspan - 1) / P.wspan;
-  const unsigned long long grid = (warps + kRowWarps - 1) / kRowWarps;
+  if (P.wspan < L.wspan) return false;
   P.pmax = L.pmax;
   P.cp = L.cp;
   P.slot_bytes = L.slot_bytes;
@@ -922,23 +999,49 @@ cudaError_t launch_rows(const void* logits, long long R, int V, long long stride
   P.out_logp = out_logp;
   P.out_lse = out_lse;
   P.wait_limit = rows_wait_limit();
+  return true;
+}
+
+cudaError_t launch_row_pass(const void* logits, long long R, int V, long long stride, int dtype, float T, int k,
+                            void* ws, const WsLayout& L, cudaStream_t stream) {
+  RowsParams P;
+  if (!rows_params(&P, logits, R, V, stride, dtype, T, k, ws, L, nullptr, nullptr, nullptr))
+    return cudaErrorInvalidValue;
   if (P.total == 0) return cudaSuccess;
+  const unsigned long long warps = (P.total + P.wspan - 1) / P.wspan;
+  const unsigned long long grid = (warps + kRowWarps - 1) / kRowWarps;
   const size_t smem = rows_smem_bytes();
-  const unsigned mgrid = unsigned((R + kMergeWarps - 1) / kMergeWarps);
   cudaError_t e = cudaSuccess;
-  auto go = [&](auto kernel, auto merge) {
+  auto go = [&](auto kernel) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return;
-    kernel<<<unsigned(grid), kRowThreads, smem, stream>>>(P);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return;
-    merge<<<mgrid, kMergeWarps * 32, 0, stream>>>(P);
+    if (e == cudaSuccess) kernel<<<unsigned(grid), kRowThreads, smem, stream>>>(P);
   };
-  if (dtype == DART_F32) go(row_stream_kernel<DART_F32>, row_merge_kernel<DART_F32>);
-  else if (dtype == DART_F16) go(row_stream_kernel<DART_F16>, row_merge_kernel<DART_F16>);
-  else go(row_stream_kernel<DART_BF16>, row_merge_kernel<DART_BF16>);
+  if (dtype == DART_F32) go(row_stream_kernel<DART_F32>);
+  else if (dtype == DART_F16) go(row_stream_kernel<DART_F16>);
+  else go(row_stream_kernel<DART_BF16>);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+cudaError_t launch_row_merge(long long R, int V, long long stride, int dtype, float T, int k, void* ws,
+                             const WsLayout& L, int32_t* out_ids, float* out_logp, float* out_lse,
+                             cudaStream_t stream) {
+  RowsParams P;
+  if (!rows_params(&P, nullptr, R, V, stride, dtype, T, k, ws, L, out_ids, out_logp, out_lse))
+    return cudaErrorInvalidValue;
+  if (R == 0) return cudaSuccess;
+  if (dtype == DART_F32) row_merge_kernel<DART_F32><<<unsigned(R), kMergeThreads, 0, stream>>>(P);
+  else if (dtype == DART_F16) row_merge_kernel<DART_F16><<<unsigned(R), kMergeThreads, 0, stream>>>(P);
+  else row_merge_kernel<DART_BF16><<<unsigned(R), kMergeThreads, 0, stream>>>(P);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rows(const void* logits, long long R, int V, long long stride, int dtype, float T, int k,
+                        void* ws, const WsLayout& L,
+                        int32_t* out_ids, float* out_logp, float* out_lse, cudaStream_t stream) {
+  cudaError_t e = launch_row_pass(logits, R, V, stride, dtype, T, k, ws, L, stream);
+  if (e != cudaSuccess) return e;
+  return launch_row_merge(R, V, stride, dtype, T, k, ws, L, out_ids, out_logp, out_lse, stream);
 }
 
 }  // namespace dart

@@ -134,9 +134,8 @@ size_t dart_tree_workspace_bytes(int B, int d, int V, int dtype, int k);
  *  out_scores  device float [B][N] or NULL: each node's path score
  *  workspace   device, >= dart_tree_workspace_bytes(B,d,V,dtype,k) bytes,
  *              256-byte aligned, zero-filled before its first use (the
- *              library keeps its counters at zero from call to call, so no
- *              per-call clearing is launched; after a nonzero device error,
- *              dart_device_error clears it again)
+ *              library keeps no state in it between calls beyond the
+ *              device error word, so no per-call clearing is launched)
  * Returns DART_OK or an error code; see the conventions above. */
 int dart_tree_build(const void* logits, int B, int d, int V, int dtype,
                     float T, int k, int W, float lambda, float beta,
@@ -215,6 +214,20 @@ int dart_row_topk(const void* logits, int rows, int V, int dtype, float T, int k
 int dart_row_topk_strided(const void* logits, int rows, int V, int64_t row_stride, int dtype, float T, int k,
                           int32_t* out_ids, float* out_logp, float* out_lse,
                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* The row stage in two launches, for callers that overlap other work with
+ * the streaming pass or time it alone.  dart_row_pass reads the logits once
+ * and leaves each row's per-piece maxima, sums, bounds and candidates in the
+ * workspace; dart_row_finish merges them into the results dart_row_topk
+ * writes (out_ids, out_logp, out_lse: as there, each may be NULL; the rows'
+ * candidate ids, logits and log-sum-exp also stay in the workspace).
+ * Arguments as for dart_row_topk_strided (dart_row_finish takes no logits);
+ * pass the same sizes and workspace to both, in order on one stream.
+ * dart_row_topk_strided is dart_row_pass followed by dart_row_finish. */
+int dart_row_pass(const void* logits, int rows, int V, int64_t row_stride, int dtype, float T, int k,
+                  void* workspace, size_t workspace_bytes, void* stream);
+int dart_row_finish(int rows, int V, int64_t row_stride, int dtype, float T, int k, int32_t* out_ids,
+                    float* out_logp, float* out_lse, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Ancestor-or-self masks from a parent array (DART, Figure 3 caption: the
  * tree-attention input).  parents device int32 [B][N], each entry -1 or a

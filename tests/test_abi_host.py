@@ -275,3 +275,17 @@ def test_binding_rejects_host_tensors_and_bad_shapes():
     t = torch.zeros((2, 5), dtype=torch.int32)
     with pytest.raises(D.DartError):
         D.tree_select(t, t, t, torch.zeros((2, 5)), 3)         # host memory
+
+
+def test_noalloc_rejects_sizes_beyond_its_buffer(L):
+    # 65,536 rows with k = 32 need far more workspace than the fixed 16 MiB
+    # scratch; the call refuses before any CUDA call, so the fake pointers are
+    # never touched
+    B, d, V, k, W = 8192, 8, 4096, 32, 64
+    need = L.dart_tree_workspace_bytes(B, d, V, 2, k)
+    assert need > (16 << 20)
+    assert L.dart_tree_num_nodes(d, k, W) <= 1024
+    fake = C.c_void_p(0x10000000)
+    rc = L.dart_tree_build_noalloc(fake, B, d, V, 2, 1.0, k, W, 0.25, -14.0, None, None,
+                                   fake, fake, fake, fake, None, None)
+    assert rc == WORKSPACE

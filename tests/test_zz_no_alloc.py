@@ -20,9 +20,6 @@ pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
 
-WORKSPACE_TOO_SMALL = 3
-
-
 @pytest.fixture(scope="module")
 def D():
     import draft_tree_construction_gb300 as D
@@ -65,16 +62,3 @@ def test_noalloc_matches_tree_build_on_consecutive_calls(D):
             assert torch.equal(got[key], ref[key]), key
         err = (got["scores"].double() - ref["scores"].double()).abs().max().item()
         assert err <= parity.SCORE_TOL
-
-
-def test_noalloc_rejects_sizes_beyond_its_buffer(D):
-    # 4096 rows of a 1M-token vocabulary need far more than the 16 MiB buffer;
-    # the call must refuse before touching the (never allocated) logits
-    B, d, V = 512, 8, 1 << 20
-    assert D.workspace_bytes(B, d, V, 2, 16) > (16 << 20)
-    N = D.num_nodes(d, 16, 32)
-    fake = C.c_void_p(0x10000000)
-    rc = D.lib().dart_tree_build_noalloc(fake, B, d, V, 2, 1.0, 16, 32, 0.25, -14.0, None, None,
-                                         fake, fake, fake, fake, None, None)
-    assert rc == WORKSPACE_TOO_SMALL
-    assert N > 0

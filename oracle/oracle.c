@@ -19,7 +19,11 @@
  *      tree-attention verification (DART, Figure 3 caption; DARTree,
  *      Verification).
  * Readings where the pages are silent: the root is the last committed token
- * and is not a node; the n-gram context is the last n-1 tokens of (committed
+ * and is not a node; T = 0 (greedy decoding, DART Figure 2 caption) names
+ * the target's sampling, not a log-softmax: candidates come from the raw
+ * logits whatever T is, and the tree is scored with the draft's own
+ * log-probabilities, log_softmax(z), exactly as at T = 1, so that the first
+ * child of each depth extends the argmax chain when lambda = 0; the n-gram context is the last n-1 tokens of (committed
  * context ++ path); candidates are ranked on the raw logits, lower id first on
  * equal values; children are ranked by score, then lower parent index, then
  * lower token id, and nodes of a depth are numbered in that order.
@@ -92,9 +96,13 @@ static void one_row(const void* logits, int dtype, int64_t r, int V, double T, i
     }
 }
 
+/* The temperature the scores use: T itself, or 1 for greedy T = 0. */
+static double score_temperature(double T) { return T == 0.0 ? 1.0 : T; }
+
 int oracle_rows(const void* logits, int dtype, int64_t rows, int V, double T, int k,
                 int32_t* ids, double* logp, double* lse, int threads) {
-    if (!logits || rows < 0 || V < 1 || k < 1 || k > V || !(T > 0.0) || !ids || !logp) return 1;
+    if (!logits || rows < 0 || V < 1 || k < 1 || k > V || !(T >= 0.0) || !ids || !logp) return 1;
+    T = score_temperature(T);
     int fail = 0;
 #ifdef _OPENMP
     if (threads <= 0) threads = omp_get_max_threads();
@@ -362,7 +370,8 @@ int oracle_tree_build(const void* logits, int dtype, int B, int d, int V, double
                       int32_t* tokens, int32_t* parents, int32_t* pos, uint32_t* mask,
                       double* scores, double* min_pos_gap,
                       int32_t* row_ids, double* row_logp, double* row_lse, int threads) {
-    if (B < 0 || d < 1 || k < 1 || k > V) return 1;
+    if (B < 0 || d < 1 || k < 1 || k > V || !(T >= 0.0)) return 1;
+    T = score_temperature(T);
     size_t R = (size_t)B * d;
     int32_t* ids = row_ids ? row_ids : (int32_t*)malloc(sizeof(int32_t) * (R * k + 1));
     double* lp = row_logp ? row_logp : (double*)malloc(sizeof(double) * (R * k + 1));

@@ -32,7 +32,8 @@ extern "C" {
 /* dtype codes of the stored logits: 0 = f32, 1 = f16, 2 = bf16 (bit patterns). */
 
 /* Per row r < rows of logits[rows][V]: lse[r], the k best token ids (value
- * descending, lower id first on equal values) and their log-probabilities. */
+ * descending, lower id first on equal values) and their log-probabilities
+ * log_softmax(z / T).  T >= 0; T = 0 (greedy) scores as T = 1. */
 int oracle_rows(const void* logits, int dtype, int64_t rows, int V, double T, int k,
                 int32_t* ids, double* logp, double* lse, int threads);
 
@@ -67,7 +68,7 @@ int oracle_tree_from_lists(int B, int d, int k, int W,
                            int threads);
 
 /* Rows, then the tree, as one call (base = the candidates' logits, invT =
- * 1 / T, off = each row's log-sum-exp).  row_ids/row_logp/row_lse may be NULL. */
+ * 1 / T, off = each row's log-sum-exp; T = 0 scores as T = 1).  row_ids/row_logp/row_lse may be NULL. */
 int oracle_tree_build(const void* logits, int dtype, int B, int d, int V, double T,
                       int k, int W, double lam, double beta,
                       const oracle_ngram* tab, int n, const int32_t* ctx,

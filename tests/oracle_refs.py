@@ -129,14 +129,16 @@ def mask_row_to_set(words) -> set:
     return s
 
 
-def whole_path_brute_force_ok(lib=None, seed=3) -> bool:
-    """Rows + tree through oracle.tree_build at T != 1 with nothing pruned, against
-    scipy's log_softmax and an exhaustive enumeration of the paths."""
+def whole_path_brute_force_ok(lib=None, seed=3, T=0.7) -> bool:
+    """Rows + tree through oracle.tree_build with nothing pruned, against scipy's
+    log_softmax and an exhaustive enumeration of the paths.  T = 0 (greedy)
+    is scored with the draft's own log-probabilities, log_softmax(z)."""
     import scipy.special
     import oracle
     import synth
-    case = synth.make_case(B=2, d=3, V=40, dtype="bf16", T=0.7, k=3, W=27, n=2, M=600, lam=0.5,
+    case = synth.make_case(B=2, d=3, V=40, dtype="bf16", T=T, k=3, W=27, n=2, M=600, lam=0.5,
                            beta=-9.0, recipe=("normal", 3.0), seed=seed)
+    T_score = 1.0 if case.T == 0 else case.T    # the temperature as the case stores it
     try:
         out = oracle.tree_build(case, lib=lib)
     except ValueError:
@@ -144,7 +146,7 @@ def whole_path_brute_force_ok(lib=None, seed=3) -> bool:
     z = decode_np(case.logits, "bf16")
     table = dict_ngram(case.ng_keys, case.ng_vals)
     for b in range(case.B):
-        lsm = [scipy.special.log_softmax(z[b, j] / case.T) for j in range(case.d)]
+        lsm = [scipy.special.log_softmax(z[b, j] / T_score) for j in range(case.d)]
         ids = [topk_lexsort(z[b, j], case.k).tolist() for j in range(case.d)]
         logp = [[lsm[j][t] for t in ids[j]] for j in range(case.d)]
         ref = brute_force_paths(ids, logp, lam=case.lam, beta=case.beta, table=table, n=case.n,

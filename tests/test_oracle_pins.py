@@ -89,6 +89,47 @@ def test_rows_ties_constant_and_special_values():
     np.testing.assert_allclose(logp[2][0], logp[2][1], atol=0)
 
 
+def test_greedy_rows_closed_form():
+    """T = 0 (greedy decoding, DART Figure 2 caption): candidates come from the
+    raw logits and the scores are log_softmax(z).  Logits ln 4, ln 2, 0, 0
+    give probabilities 1/2, 1/4, 1/8, 1/8, so the log-probabilities are -ln 2,
+    -2 ln 2, -3 ln 2, -3 ln 2 and the log-sum-exp is ln 8."""
+    ln2 = math.log(2.0)
+    z = np.array([[0.0, 2 * ln2, 0.0, ln2], [3.0, 3.0, 3.0, 3.0]], dtype=np.float64)
+    ids, logp, lse = oracle.rows(z.astype(np.float32), "f32", 4, 0.0, 4)
+    assert ids[0].tolist() == [1, 3, 0, 2]
+    zf = z.astype(np.float32).astype(np.float64)   # the stored logits, rounded to float32
+    want = zf[0] - math.log(np.exp(zf[0]).sum())
+    np.testing.assert_allclose(logp[0], want[[1, 3, 0, 2]], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(logp[0], [-ln2, -2 * ln2, -3 * ln2, -3 * ln2], rtol=0, atol=1e-7)
+    np.testing.assert_allclose(lse[0], 3 * ln2, rtol=0, atol=1e-7)
+    assert ids[1].tolist() == [0, 1, 2, 3]           # a constant row: uniform, ids in order
+    np.testing.assert_allclose(logp[1], -math.log(4.0), rtol=0, atol=1e-15)
+    with pytest.raises(ValueError):
+        oracle.rows(z.astype(np.float32), "f32", 4, -1.0, 2)
+
+
+def test_greedy_tree_against_brute_force():
+    """The whole path at T = 0 against scipy and an enumeration of every path."""
+    for seed in (6, 7):
+        assert R.whole_path_brute_force_ok(seed=seed, T=0.0)
+
+
+def test_greedy_first_nodes_form_the_argmax_chain():
+    """With lambda = 0 the best child of a depth extends the best node of the
+    previous one by that depth's argmax, so node 0 of every depth lies on the
+    argmax chain (ties excluded by continuous logits)."""
+    case = synth.make_case(B=3, d=5, V=300, dtype="f32", T=0.0, k=4, W=6, n=0, M=0, lam=0.0,
+                           beta=0.0, recipe=("normal", 3.0), seed=21)
+    out = oracle.tree_build(case)
+    z = case.logits.reshape(case.B, case.d, case.V).astype(np.float64)
+    for b in range(case.B):
+        pos, par, tok = out["pos"][b], out["parents"][b], out["tokens"][b]
+        first = [int(np.flatnonzero(pos == j + 1)[0]) for j in range(case.d)]
+        assert [int(tok[x]) for x in first] == [int(np.argmax(z[b, j])) for j in range(case.d)]
+        assert [int(par[x]) for x in first] == [-1] + first[:-1]
+
+
 def test_decode_all_16bit_patterns():
     pat = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
     np.seterr(invalid="ignore")

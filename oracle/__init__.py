@@ -54,6 +54,9 @@ def _declare(lib):
     lib.oracle_tree_from_lists.argtypes = [i32, i32, i32, i32, P, P, dbl, P, dbl, dbl, P, i32, P,
                                            P, P, P, P, P, P, i32]
     lib.oracle_tree_from_lists.restype = i32
+    lib.oracle_tree_from_pairs.argtypes = [i32, i32, i32, i32, P, P, dbl, P, dbl, P,
+                                           P, P, P, P, P, P, i32]
+    lib.oracle_tree_from_pairs.restype = i32
     lib.oracle_tree_build.argtypes = [P, i32, i32, i32, i32, dbl, i32, i32, dbl, dbl, P, i32, P,
                                       P, P, P, P, P, P, P, P, P, i32]
     lib.oracle_tree_build.restype = i32
@@ -155,6 +158,36 @@ def tree_from_lists(ids, base, *, B, d, k, W, lam, beta, ngram: NGram | None, ct
                                     _p(tok), _p(par), _p(pos), _p(mask), _p(sc), _p(gap), threads)
     if rc:
         raise ValueError(f"oracle_tree_from_lists failed ({rc})")
+    return dict(tokens=tok, parents=par, pos=pos, mask=mask, scores=sc, min_pos_gap=gap)
+
+
+def tree_from_pairs(ids, base, pair, *, B, d, k, W, lam, invT: float = 1.0, off=None,
+                    threads: int = 0, lib=None):
+    """The tree stage with caller-supplied pair scores pair [B, d, k, k] as the
+    continuity term: a child with column c of row j adds pair[b, j, c', c],
+    c' its parent's column in row j-1 (0 at j = 0, the root)."""
+    lib = lib or load()
+    N = lib.oracle_num_nodes(d, k, W)
+    if N < 0:
+        raise ValueError("invalid d/k/W")
+    MW = (N + 31) // 32
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    base = np.ascontiguousarray(base, dtype=np.float64)
+    pr = np.ascontiguousarray(pair, dtype=np.float32)
+    if pr.shape != (B, d, k, k):
+        raise ValueError("pair must be [B, d, k, k]")
+    offa = None if off is None else np.ascontiguousarray(off, dtype=np.float64)
+    tok = np.zeros((B, N), dtype=np.int32)
+    par = np.zeros((B, N), dtype=np.int32)
+    pos = np.zeros((B, N), dtype=np.int32)
+    mask = np.zeros((B, N, MW), dtype=np.uint32)
+    sc = np.zeros((B, N), dtype=np.float64)
+    gap = np.zeros((B, d), dtype=np.float64)
+    rc = lib.oracle_tree_from_pairs(B, d, k, W, _p(ids), _p(base), float(invT), _p(offa), float(lam),
+                                    _p(pr), _p(tok), _p(par), _p(pos), _p(mask), _p(sc), _p(gap),
+                                    threads)
+    if rc:
+        raise ValueError(f"oracle_tree_from_pairs failed ({rc})")
     return dict(tokens=tok, parents=par, pos=pos, mask=mask, scores=sc, min_pos_gap=gap)
 
 

@@ -208,7 +208,7 @@ int oracle_num_nodes(int d, int k, int W) {
     return (int)total;
 }
 
-typedef struct { double key, Z, G; int32_t i; int32_t tok; } cand_t;
+typedef struct { double key, Z, G; int32_t i; int32_t tok; int32_t col; } cand_t;
 
 static int cmp_cand(const void* pa, const void* pb) {
     const cand_t* a = (const cand_t*)pa;
@@ -251,7 +251,7 @@ int oracle_mask_from_parents(int B, int N, const int32_t* parents, uint32_t* mas
 static int one_tree(int b, int d, int k, int W, int N,
                     const int32_t* ids, const double* base, double invT, const double* off,
                     double lam, double beta, const oracle_ngram* tab, int n,
-                    const int32_t* ctx,
+                    const float* pair, const int32_t* ctx,
                     int32_t* tokens, int32_t* parents, int32_t* pos, double* scores,
                     double* min_pos_gap) {
     int L = (n > 1 ? n - 1 : 0) + d;             /* longest sequence */
@@ -259,6 +259,8 @@ static int one_tree(int b, int d, int k, int W, int N,
     double* fZ = (double*)malloc(sizeof(double) * Wmax);
     double* fG = (double*)malloc(sizeof(double) * Wmax);
     int* fnode = (int*)malloc(sizeof(int) * Wmax);
+    int* fcol = (int*)malloc(sizeof(int) * Wmax);     /* each frontier node's column in its row */
+    int* ncol = (int*)malloc(sizeof(int) * Wmax);
     int32_t* fseq = (int32_t*)malloc(sizeof(int32_t) * (size_t)Wmax * (L > 0 ? L : 1));
     double* nZ = (double*)malloc(sizeof(double) * Wmax);
     double* nG = (double*)malloc(sizeof(double) * Wmax);
@@ -266,7 +268,7 @@ static int one_tree(int b, int d, int k, int W, int N,
     int32_t* nseq = (int32_t*)malloc(sizeof(int32_t) * (size_t)Wmax * (L > 0 ? L : 1));
     cand_t* cand = (cand_t*)malloc(sizeof(cand_t) * (size_t)Wmax * k);
     int rc = 0;
-    if (!fZ || !fG || !fnode || !fseq || !nZ || !nG || !nnode || !nseq || !cand) rc = 1;
+    if (!fZ || !fG || !fnode || !fcol || !ncol || !fseq || !nZ || !nG || !nnode || !nseq || !cand) rc = 1;
     int nc = n > 1 ? n - 1 : 0;                  /* committed context length */
     int F = 1, len = nc, next = 0;
     double Lsum = 0.0;
@@ -274,6 +276,7 @@ static int one_tree(int b, int d, int k, int W, int N,
         fZ[0] = 0.0;
         fG[0] = 0.0;
         fnode[0] = -1;
+        fcol[0] = 0;                             /* the root counts as column 0 */
         for (int c = 0; c < nc; ++c) fseq[c] = ctx[(size_t)b * nc + c];
     }
     for (int j = 0; j < d && !rc; ++j) {
@@ -293,12 +296,16 @@ static int one_tree(int b, int d, int k, int W, int N,
                     float g = 0.0f;
                     double gg = ngram_get(tab, key, &g) ? (double)g : beta;
                     G = G + gg;
+                } else if (pair) {
+                    /* caller-supplied continuity score of (parent's column, c) */
+                    G = G + (double)pair[(((size_t)b * d + j) * k + fcol[i]) * k + c];
                 }
                 cand[m].Z = Z;
                 cand[m].G = G;
                 cand[m].key = Z * invT + lam * G;
                 cand[m].i = i;
                 cand[m].tok = C[c];
+                cand[m].col = c;
                 ++m;
             }
         }
@@ -323,6 +330,7 @@ static int one_tree(int b, int d, int k, int W, int N,
             nZ[r] = e->Z;
             nG[r] = e->G;
             nnode[r] = node;
+            ncol[r] = e->col;
             memcpy(nseq + (size_t)r * L, fseq + (size_t)e->i * L, sizeof(int32_t) * (size_t)len);
             nseq[(size_t)r * L + len] = e->tok;
         }
@@ -333,10 +341,11 @@ static int one_tree(int b, int d, int k, int W, int N,
             memcpy(fZ, nZ, sizeof(double) * F);
             memcpy(fG, nG, sizeof(double) * F);
             memcpy(fnode, nnode, sizeof(int) * F);
+            memcpy(fcol, ncol, sizeof(int) * F);
             memcpy(fseq, nseq, sizeof(int32_t) * (size_t)F * L);
         }
     }
-    free(fZ); free(fG); free(fnode); free(fseq); free(nZ); free(nG); free(nnode); free(nseq); free(cand);
+    free(fZ); free(fG); free(fnode); free(fcol); free(ncol); free(fseq); free(nZ); free(nG); free(nnode); free(nseq); free(cand);
     if (rc) return rc;
     return next == N ? 0 : 3;
 }
@@ -357,7 +366,34 @@ int oracle_tree_from_lists(int B, int d, int k, int W,
 #pragma omp parallel for num_threads(threads) schedule(dynamic, 1) reduction(| : fail)
 #endif
     for (int b = 0; b < B; ++b)
-        fail |= one_tree(b, d, k, W, N, ids, base, invT, off, lam, beta, tab, tab ? n : 0, ctx,
+        fail |= one_tree(b, d, k, W, N, ids, base, invT, off, lam, beta, tab, tab ? n : 0, NULL, ctx,
+                         tokens, parents, pos, scores, min_pos_gap);
+    if (fail) return fail;
+    if (mask) return oracle_mask_from_parents(B, N, parents, mask);
+    return 0;
+}
+
+/* The tree with a caller-supplied continuity scorer in place of the n-gram
+ * model (DARTree, Method / Tree Construction: the children of a depth are
+ * scored by the head H in one batch; an order-2 head restricted to the
+ * candidate sets is a table of candidate-pair scores).  The term a child with
+ * column c of row j adds to G is pair[b][j][c'][c], c' the parent's column in
+ * row j-1, and c' = 0 (the root) at j = 0. */
+int oracle_tree_from_pairs(int B, int d, int k, int W,
+                           const int32_t* ids, const double* base, double invT, const double* off,
+                           double lam, const float* pair,
+                           int32_t* tokens, int32_t* parents, int32_t* pos,
+                           uint32_t* mask, double* scores, double* min_pos_gap,
+                           int threads) {
+    int N = oracle_num_nodes(d, k, W);
+    if (B < 0 || N < 0 || !ids || !base || !pair || !tokens || !parents || !pos) return 1;
+    int fail = 0;
+#ifdef _OPENMP
+    if (threads <= 0) threads = omp_get_max_threads();
+#pragma omp parallel for num_threads(threads) schedule(dynamic, 1) reduction(| : fail)
+#endif
+    for (int b = 0; b < B; ++b)
+        fail |= one_tree(b, d, k, W, N, ids, base, invT, off, lam, 0.0, NULL, 0, pair, NULL,
                          tokens, parents, pos, scores, min_pos_gap);
     if (fail) return fail;
     if (mask) return oracle_mask_from_parents(B, N, parents, mask);

@@ -67,6 +67,17 @@ int oracle_tree_from_lists(int B, int d, int k, int W,
                            uint32_t* mask, double* scores, double* min_pos_gap,
                            int threads);
 
+/* oracle_tree_from_lists with caller-supplied pair scores pair[B][d][k][k]
+ * in place of the n-gram model: a child with column c of row j adds
+ * pair[b][j][c'][c] to G, c' its parent's column in row j-1 (0 at j = 0, the
+ * root).  Ranking, tie rule and outputs as in oracle_tree_from_lists. */
+int oracle_tree_from_pairs(int B, int d, int k, int W,
+                           const int32_t* ids, const double* base, double invT, const double* off,
+                           double lam, const float* pair,
+                           int32_t* tokens, int32_t* parents, int32_t* pos,
+                           uint32_t* mask, double* scores, double* min_pos_gap,
+                           int threads);
+
 /* Rows, then the tree, as one call (base = the candidates' logits, invT =
  * 1 / T, off = each row's log-sum-exp; T = 0 scores as T = 1).  row_ids/row_logp/row_lse may be NULL. */
 int oracle_tree_build(const void* logits, int dtype, int B, int d, int V, double T,

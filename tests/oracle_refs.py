@@ -163,6 +163,106 @@ def whole_path_brute_force_ok(lib=None, seed=3, T=0.7) -> bool:
     return True
 
 
+def pair_brute_force_paths(logp, pair, *, lam):
+    """Every root-to-depth-j path of one tree scored with pair scores by direct
+    enumeration: sum_j logp[j][c_j] + lam * sum_j pair[j][c_{j-1}][c_j], with
+    c_{-1} = 0 (the root).  logp [d][k], pair [d][k][k]; keys are column tuples."""
+    d, k = len(logp), len(logp[0])
+    out = {}
+    for depth in range(1, d + 1):
+        for cols in itertools.product(range(k), repeat=depth):
+            s = 0.0
+            for j in range(depth):
+                prev = cols[j - 1] if j > 0 else 0
+                s = s + logp[j][cols[j]] + lam * float(pair[j][prev][cols[j]])
+            out[cols] = s
+    return out
+
+
+def pair_trees_ok(lib=None, seeds=(31, 32)) -> bool:
+    """Pins of oracle.tree_from_pairs.
+
+    1. Nothing pruned (W = k^d): every path and its score against an
+       enumeration.
+    2. Pruned trees: pair scores that restate a bigram model on the candidate
+       sets (pair[j][c'][c] = table(token of c' in row j-1, or the context's
+       last token at j = 0; token of c in row j), beta when absent) give the
+       n-gram tree exactly -- which needs the parent's column carried through
+       every cut.
+    3. lambda = 0 gives the tree with no continuity term."""
+    import oracle
+    import synth
+    rng = np.random.default_rng(seeds[0])
+    for seed in seeds:
+        B, d, k = 2, 3, 3
+        ids = np.stack([np.stack([rng.permutation(50)[:k] for _ in range(d)]) for _ in range(B)]).astype(np.int32)
+        logp = -rng.exponential(2.0, size=(B, d, k))
+        pair = (-rng.exponential(1.5, size=(B, d, k, k))).astype(np.float32)
+        out = oracle.tree_from_pairs(ids, logp, pair, B=B, d=d, k=k, W=k ** d, lam=0.7, lib=lib)
+        for b in range(B):
+            ref = pair_brute_force_paths(logp[b], pair[b], lam=0.7)
+            try:
+                paths = node_paths(out["tokens"][b].tolist(), out["parents"][b].tolist(), ids[b].tolist())
+            except (ValueError, IndexError):
+                return False
+            if sorted(paths) != sorted(ref.keys()):
+                return False
+            for x, q in enumerate(paths):
+                if abs(out["scores"][b, x] - ref[q]) > 1e-12:
+                    return False
+        # 2: a bigram model restated as pair scores, with pruning
+        case = synth.make_case(B=3, d=5, V=60, dtype="f32", T=1.0, k=4, W=5, n=2, M=900, lam=0.4,
+                               beta=-7.0, recipe=("normal", 3.0), seed=seed)
+        ng = oracle.NGram(2, case.ng_keys, case.ng_vals, lib=lib)
+        rid, rlp, _ = oracle.rows(case.logits, "f32", case.V, 1.0, case.k, lib=lib)
+        rid = rid.reshape(case.B, case.d, case.k)
+        rlp = rlp.reshape(case.B, case.d, case.k)
+        table = dict_ngram(case.ng_keys, case.ng_vals)
+        pr = np.zeros((case.B, case.d, case.k, case.k), dtype=np.float32)
+        for b in range(case.B):
+            for j in range(case.d):
+                for cp in range(case.k):
+                    prev = int(case.ctx[b][-1]) if j == 0 else int(rid[b, j - 1, cp])
+                    for c in range(case.k):
+                        g = table.get((prev, int(rid[b, j, c])))
+                        pr[b, j, cp, c] = case.beta if g is None else g
+        want = oracle.tree_from_lists(rid, rlp, B=case.B, d=case.d, k=case.k, W=case.W, lam=case.lam,
+                                      beta=case.beta, ngram=ng, ctx=case.ctx, lib=lib)
+        got = oracle.tree_from_pairs(rid, rlp, pr, B=case.B, d=case.d, k=case.k, W=case.W,
+                                     lam=case.lam, lib=lib)
+        for key in ("tokens", "parents", "pos", "mask"):
+            if not np.array_equal(got[key], want[key]):
+                return False
+        if np.abs(got["scores"] - want["scores"]).max() > 1e-12:
+            return False
+        # 3: lambda = 0
+        plain = oracle.tree_from_lists(rid, rlp, B=case.B, d=case.d, k=case.k, W=case.W, lam=0.0,
+                                       beta=0.0, ngram=None, ctx=None, lib=lib)
+        zero = oracle.tree_from_pairs(rid, rlp, pr, B=case.B, d=case.d, k=case.k, W=case.W, lam=0.0,
+                                      lib=lib)
+        for key in ("tokens", "parents", "pos", "mask", "scores"):
+            if not np.array_equal(zero[key], plain[key]):
+                return False
+    return True
+
+
+def greedy_ok(lib=None) -> bool:
+    """T = 0 rows against the closed form of logits ln 4, ln 2, 0, 0 and the
+    whole path at T = 0 against the enumeration."""
+    import math
+    import oracle
+    ln2 = math.log(2.0)
+    z = np.array([[0.0, 2 * ln2, 0.0, ln2]], dtype=np.float32)
+    ids, logp, lse = oracle.rows(z, "f32", 4, 0.0, 4, lib=lib)
+    if ids[0].tolist() != [1, 3, 0, 2]:
+        return False
+    if np.abs(logp[0] - np.array([-ln2, -2 * ln2, -3 * ln2, -3 * ln2])).max() > 1e-7:
+        return False
+    if abs(lse[0] - 3 * ln2) > 1e-7:
+        return False
+    return whole_path_brute_force_ok(lib=lib, seed=6, T=0.0)
+
+
 def best_sum_subset(scores, M: int):
     """Brute force: the size-M set of nodes with the largest score sum (sets
     compared by their sorted score lists when sums are equal).  For scores that

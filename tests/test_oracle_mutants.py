@@ -55,6 +55,12 @@ MUTANTS = {
     "select_worst_first": ("if (s[a] != s[b]) return s[a] > s[b];", "if (s[a] != s[b]) return s[a] < s[b];"),
     "select_ties_high_index": ("    return a < b;\n}", "    return a > b;\n}"),
     "select_all_available": ("if (par[i] < 0) avail[na++] = i;", "avail[na++] = i;"),
+    "greedy_as_small_temperature": ("return T == 0.0 ? 1.0 : T;", "return T == 0.0 ? 1e-3 : T;"),
+    "pair_uses_child_column": ("pair[(((size_t)b * d + j) * k + fcol[i]) * k + c]",
+                               "pair[(((size_t)b * d + j) * k + c) * k + c]"),
+    "pair_column_not_carried": ("ncol[r] = e->col;", "ncol[r] = 0;"),
+    "pair_depth_ignored": ("pair[(((size_t)b * d + j) * k + fcol[i]) * k + c]",
+                           "pair[(((size_t)b * d + 0) * k + fcol[i]) * k + c]"),
     "select_parent_not_renumbered": ("new_parents[(size_t)b * Mp + j] = par[i] < 0 ? -1 : newpos[par[i]];",
                                      "new_parents[(size_t)b * Mp + j] = par[i];"),
 }
@@ -212,7 +218,16 @@ def _pin_select(lib):
     return True
 
 
-PINS = [_pin_worked_examples, _pin_rows, _pin_brute_force, _pin_k_best, _pin_whole_path_temperature, _pin_select]
+def _pin_pairs(lib):
+    return R.pair_trees_ok(lib=lib)
+
+
+def _pin_greedy(lib):
+    return R.greedy_ok(lib=lib)
+
+
+PINS = [_pin_worked_examples, _pin_rows, _pin_brute_force, _pin_k_best, _pin_whole_path_temperature, _pin_select,
+        _pin_pairs, _pin_greedy]
 
 
 def _all_pins_pass(lib) -> bool:

@@ -130,6 +130,12 @@ def test_greedy_first_nodes_form_the_argmax_chain():
         assert [int(par[x]) for x in first] == [-1] + first[:-1]
 
 
+def test_pair_scored_trees():
+    """Caller-supplied pair scores in place of the n-gram model (DARTree,
+    Method / Tree Construction: children scored by a head in one batch)."""
+    assert R.pair_trees_ok()
+
+
 def test_decode_all_16bit_patterns():
     pat = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
     np.seterr(invalid="ignore")

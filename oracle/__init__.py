@@ -57,6 +57,8 @@ def _declare(lib):
     lib.oracle_tree_from_pairs.argtypes = [i32, i32, i32, i32, P, P, dbl, P, dbl, P,
                                            P, P, P, P, P, P, i32]
     lib.oracle_tree_from_pairs.restype = i32
+    lib.oracle_tree_trace.argtypes = [i32, i32, i32, P, P, dbl, P, dbl, dbl, P, i32, P, P, i64, P]
+    lib.oracle_tree_trace.restype = i32
     lib.oracle_tree_build.argtypes = [P, i32, i32, i32, i32, dbl, i32, i32, dbl, dbl, P, i32, P,
                                       P, P, P, P, P, P, P, P, P, i32]
     lib.oracle_tree_build.restype = i32
@@ -189,6 +191,36 @@ def tree_from_pairs(ids, base, pair, *, B, d, k, W, lam, invT: float = 1.0, off=
     if rc:
         raise ValueError(f"oracle_tree_from_pairs failed ({rc})")
     return dict(tokens=tok, parents=par, pos=pos, mask=mask, scores=sc, min_pos_gap=gap)
+
+
+TRACE_DTYPE = np.dtype([("depth", "<i4"), ("parent", "<i4"), ("parent_rank", "<i4"), ("token", "<i4"),
+                        ("column", "<i4"), ("found", "<i4"), ("node", "<i4"), ("pad", "<i4"),
+                        ("g", "<f8"), ("Z", "<f8"), ("G", "<f8"), ("key", "<f8")])
+
+
+def tree_trace(ids, base, *, d, k, W, lam, beta, ngram: NGram | None, ctx, invT: float = 1.0, off=None,
+               lib=None) -> np.ndarray:
+    """One tree (ids/base [d, k], ctx [n-1]) with every expanded child: a
+    structured array (TRACE_DTYPE), per depth the whole sorted candidate table."""
+    lib = lib or load()
+    ids = np.ascontiguousarray(ids, dtype=np.int32).reshape(d, k)
+    base = np.ascontiguousarray(base, dtype=np.float64).reshape(d, k)
+    offa = None if off is None else np.ascontiguousarray(off, dtype=np.float64).reshape(d)
+    cap = 0
+    width = 1
+    for _ in range(d):
+        cap += width * k
+        width = min(width * k, W)
+    out = np.zeros(cap, dtype=TRACE_DTYPE)
+    n = ngram.n if ngram is not None else 0
+    c = None if ctx is None else np.ascontiguousarray(ctx, dtype=np.int32)
+    length = C.c_int64(0)
+    rc = lib.oracle_tree_trace(d, k, W, _p(ids), _p(base), float(invT), _p(offa), float(lam), float(beta),
+                               ngram.h if ngram is not None else None, n, _p(c), _p(out), cap,
+                               C.byref(length))
+    if rc:
+        raise ValueError(f"oracle_tree_trace failed ({rc})")
+    return out[:length.value]
 
 
 def tree_build(case, ngram: NGram | None = None, threads: int = 0, use_table: bool = True, lib=None):

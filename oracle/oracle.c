@@ -208,7 +208,7 @@ int oracle_num_nodes(int d, int k, int W) {
     return (int)total;
 }
 
-typedef struct { double key, Z, G; int32_t i; int32_t tok; int32_t col; } cand_t;
+typedef struct { double key, Z, G, g; int32_t i; int32_t tok; int32_t col; int32_t found; } cand_t;
 
 static int cmp_cand(const void* pa, const void* pb) {
     const cand_t* a = (const cand_t*)pa;
@@ -253,7 +253,7 @@ static int one_tree(int b, int d, int k, int W, int N,
                     double lam, double beta, const oracle_ngram* tab, int n,
                     const float* pair, const int32_t* ctx,
                     int32_t* tokens, int32_t* parents, int32_t* pos, double* scores,
-                    double* min_pos_gap) {
+                    double* min_pos_gap, oracle_trace_entry* trace) {
     int L = (n > 1 ? n - 1 : 0) + d;             /* longest sequence */
     int Wmax = W;
     double* fZ = (double*)malloc(sizeof(double) * Wmax);
@@ -289,16 +289,22 @@ static int one_tree(int b, int d, int k, int W, int N,
             for (int c = 0; c < k; ++c) {
                 double Z = fZ[i] + P[c];
                 double G = fG[i];
+                double term = 0.0;
+                int found = 0;
                 if (tab) {
                     int32_t key[4];
                     for (int q = 0; q < n - 1; ++q) key[q] = seq[len - (n - 1) + q];
                     key[n - 1] = C[c];
                     float g = 0.0f;
-                    double gg = ngram_get(tab, key, &g) ? (double)g : beta;
+                    found = ngram_get(tab, key, &g);
+                    double gg = found ? (double)g : beta;
                     G = G + gg;
+                    term = gg;
                 } else if (pair) {
                     /* caller-supplied continuity score of (parent's column, c) */
-                    G = G + (double)pair[(((size_t)b * d + j) * k + fcol[i]) * k + c];
+                    term = (double)pair[(((size_t)b * d + j) * k + fcol[i]) * k + c];
+                    G = G + term;
+                    found = 1;
                 }
                 cand[m].Z = Z;
                 cand[m].G = G;
@@ -306,11 +312,29 @@ static int one_tree(int b, int d, int k, int W, int N,
                 cand[m].i = i;
                 cand[m].tok = C[c];
                 cand[m].col = c;
+                cand[m].g = term;
+                cand[m].found = found;
                 ++m;
             }
         }
         qsort(cand, (size_t)m, sizeof(cand_t), cmp_cand);
         int keep = m < W ? m : W;
+        if (trace) {
+            for (int r = 0; r < m; ++r, ++trace) {
+                trace->depth = j + 1;
+                trace->parent = fnode[cand[r].i];
+                trace->parent_rank = cand[r].i;
+                trace->token = cand[r].tok;
+                trace->column = cand[r].col;
+                trace->found = cand[r].found;
+                trace->node = r < keep ? next + r : -1;
+                trace->pad = 0;
+                trace->g = cand[r].g;
+                trace->Z = cand[r].Z;
+                trace->G = cand[r].G;
+                trace->key = cand[r].key;
+            }
+        }
         if (min_pos_gap) {
             double g = 1e300;
             for (int r = 0; r < keep && r + 1 < m; ++r) {
@@ -367,7 +391,7 @@ int oracle_tree_from_lists(int B, int d, int k, int W,
 #endif
     for (int b = 0; b < B; ++b)
         fail |= one_tree(b, d, k, W, N, ids, base, invT, off, lam, beta, tab, tab ? n : 0, NULL, ctx,
-                         tokens, parents, pos, scores, min_pos_gap);
+                         tokens, parents, pos, scores, min_pos_gap, NULL);
     if (fail) return fail;
     if (mask) return oracle_mask_from_parents(B, N, parents, mask);
     return 0;
@@ -394,10 +418,34 @@ int oracle_tree_from_pairs(int B, int d, int k, int W,
 #endif
     for (int b = 0; b < B; ++b)
         fail |= one_tree(b, d, k, W, N, ids, base, invT, off, lam, 0.0, NULL, 0, pair, NULL,
-                         tokens, parents, pos, scores, min_pos_gap);
+                         tokens, parents, pos, scores, min_pos_gap, NULL);
     if (fail) return fail;
     if (mask) return oracle_mask_from_parents(B, N, parents, mask);
     return 0;
+}
+
+/* One tree with every expanded child recorded (see oracle.h). */
+int oracle_tree_trace(int d, int k, int W, const int32_t* ids, const double* base, double invT,
+                      const double* off, double lam, double beta, const oracle_ngram* tab, int n,
+                      const int32_t* ctx, oracle_trace_entry* trace, int64_t trace_cap,
+                      int64_t* trace_len) {
+    int N = oracle_num_nodes(d, k, W);
+    if (N < 0 || !ids || !base || !trace || !trace_len) return 1;
+    if (tab && (n != tab->n || n < 2 || !ctx)) return 1;
+    int64_t need = 0, width = 1;
+    for (int j = 0; j < d; ++j) {
+        need += width * k;
+        width = width * k < W ? width * k : W;
+    }
+    if (need > trace_cap) return 1;
+    int32_t* tok = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
+    int32_t* par = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
+    int32_t* pos = (int32_t*)malloc(sizeof(int32_t) * (size_t)N);
+    int rc = (!tok || !par || !pos) ? 1 : one_tree(0, d, k, W, N, ids, base, invT, off, lam, beta, tab,
+                                                   tab ? n : 0, NULL, ctx, tok, par, pos, NULL, NULL, trace);
+    free(tok); free(par); free(pos);
+    *trace_len = rc ? 0 : need;
+    return rc;
 }
 
 int oracle_tree_build(const void* logits, int dtype, int B, int d, int V, double T,

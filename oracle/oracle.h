@@ -78,6 +78,24 @@ int oracle_tree_from_pairs(int B, int d, int k, int W,
                            uint32_t* mask, double* scores, double* min_pos_gap,
                            int threads);
 
+/* One expanded child of a traced tree: its depth, parent node (-1 = root) and
+ * the parent's rank in the frontier, token and column in its row, whether
+ * the n-gram was found, the node index it became (-1 if cut), the continuity
+ * term g it added (the n-gram value, or beta when absent), and its Z, G and
+ * ranking key. */
+typedef struct {
+    int32_t depth, parent, parent_rank, token, column, found, node, pad;
+    double g, Z, G, key;
+} oracle_trace_entry;
+
+/* One tree (ids/base [d][k], ctx [n-1]) with every expanded child recorded:
+ * per depth, the whole sorted candidate table (kept children first, in node
+ * order).  At most trace_cap entries; *trace_len receives the count. */
+int oracle_tree_trace(int d, int k, int W, const int32_t* ids, const double* base, double invT,
+                      const double* off, double lam, double beta, const oracle_ngram* tab, int n,
+                      const int32_t* ctx, oracle_trace_entry* trace, int64_t trace_cap,
+                      int64_t* trace_len);
+
 /* Rows, then the tree, as one call (base = the candidates' logits, invT =
  * 1 / T, off = each row's log-sum-exp; T = 0 scores as T = 1).  row_ids/row_logp/row_lse may be NULL. */
 int oracle_tree_build(const void* logits, int dtype, int B, int d, int V, double T,

@@ -347,6 +347,9 @@ def run_probe_stream(args):
     stream = torch.cuda.current_stream(dev)
     peaks, src = measured_peaks()
     shapes = []
+    # the row pass's shape in one, two and three waves of CTAs
+    for waves in (1, 2, 3):
+        shapes.append((1, waves, 12, 3))
     for math_ in (0, 2):
         for warps in (8, 12, 16):
             shapes.append((math_, 1, warps, 0))

@@ -26,12 +26,14 @@ from ._build import LIB as _LIB_PATH, build as _build_lib
 
 __all__ = [
     "DartError", "build", "lib", "NGramTable", "num_nodes", "mask_words", "workspace_bytes",
-    "tree_build", "tree_build_noalloc", "tree_from_topk", "row_topk", "mask_pack", "tree_select", "set_wait_limit", "device_error", "TreeBuilder",
+    "tree_build", "tree_build_noalloc", "tree_from_topk", "tree_from_rows", "row_topk", "mask_pack", "tree_select", "set_wait_limit", "device_error", "noalloc_device_error",
+    "TreeBuilder",
     "DTYPE_CODES",
 ]
 
 DART_OK = 0
-DEVERR = {1: "bulk-copy wait timeout", 2: "row max mismatch", 4: "tree selection", 8: "bad parent"}
+DEVERR = {1: "bulk-copy wait timeout", 2: "row max mismatch", 4: "tree selection", 8: "bad parent",
+          16: "score rises from a parent"}
 
 
 class DartError(RuntimeError):
@@ -69,6 +71,11 @@ def _declare(L):
     L.dart_tree_build_noalloc.restype = i32
     L.dart_tree_from_topk.argtypes = [P, P, i32, i32, i32, i32, f32, f32, T, P, P, P, P, P, P, P]
     L.dart_tree_from_topk.restype = i32
+    L.dart_tree_from_topk_pairs.argtypes = [P, P, P, i32, i32, i32, i32, f32, P, P, P, P, P, P]
+    L.dart_tree_from_topk_pairs.restype = i32
+    L.dart_tree_from_rows_pairs.argtypes = [i32, i32, i32, i32, f32, i32, i32, f32, P, P, P, P, P, P,
+                                            P, sz, P]
+    L.dart_tree_from_rows_pairs.restype = i32
     L.dart_row_topk.argtypes = [P, i32, i32, i32, f32, i32, P, P, P, P, sz, P]
     L.dart_row_topk.restype = i32
     L.dart_row_topk_strided.argtypes = [P, i32, i32, i64, i32, f32, i32, P, P, P, P, sz, P]
@@ -98,6 +105,8 @@ def _declare(L):
     L.dart_set_wait_limit.restype = None
     L.dart_device_error.argtypes = [P, C.POINTER(C.c_uint32), P]
     L.dart_device_error.restype = i32
+    L.dart_noalloc_device_error.argtypes = [C.POINTER(C.c_uint32), P]
+    L.dart_noalloc_device_error.restype = i32
     L.dart_status_string.argtypes = [i32]
     L.dart_status_string.restype = C.c_char_p
     return L
@@ -132,25 +141,103 @@ def DTYPE_CODES():
     return {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 
+def _mask_dtypes():
+    torch = _torch()
+    return tuple(t for t in (torch.int32, getattr(torch, "uint32", None)) if t is not None)
+
+
 def _ptr(t):
     return None if t is None else C.c_void_p(t.data_ptr())
 
 
-def _stream_ptr(stream):
+def _device_of(*named):
+    """The one CUDA device that every given tensor lives on.
+
+    named: (name, tensor-or-None) pairs.  Raises DartError for a tensor that
+    is not on a CUDA device, or for tensors on two devices: the library takes
+    device pointers of the current device, so each call runs with this device
+    current (see _on_device)."""
+    dev = None
+    for name, t in named:
+        if t is None:
+            continue
+        if not getattr(t, "is_cuda", False):
+            raise DartError(f"{name} must be a CUDA tensor")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise DartError(f"{name} is on {t.device}, but the other arguments are on {dev}")
+    return dev
+
+
+def _on_device(dev):
+    """Context manager that makes `dev` the current CUDA device for one call."""
+    return _torch().cuda.device(dev)
+
+
+def _stream_ptr(stream, dev=None):
     torch = _torch()
-    s = stream if stream is not None else torch.cuda.current_stream()
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    if dev is not None and getattr(s, "device", dev) != dev:
+        raise DartError(f"stream is on {s.device}, but the tensors are on {dev}")
     return C.c_void_p(s.cuda_stream)
 
 
-def _need_cuda(t, name, dtype=None, contiguous=True):
+def _check_tensor(t, name, dtype=None, shape=None, contiguous=True):
+    """dtype (one dtype or a tuple), exact shape and contiguity of a tensor."""
     if t is None:
         return
-    if not t.is_cuda:
-        raise DartError(f"{name} must be a CUDA tensor")
-    if dtype is not None and t.dtype != dtype:
-        raise DartError(f"{name} must be {dtype}, got {t.dtype}")
+    if dtype is not None:
+        allowed = dtype if isinstance(dtype, tuple) else (dtype,)
+        if t.dtype not in allowed:
+            want = " or ".join(str(a) for a in allowed)
+            raise DartError(f"{name} must be {want}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise DartError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     if contiguous and not t.is_contiguous():
         raise DartError(f"{name} must be contiguous")
+
+
+def _need_cuda(t, name, dtype=None, contiguous=True, shape=None):
+    if t is None:
+        return
+    _device_of((name, t))
+    _check_tensor(t, name, dtype, shape, contiguous)
+
+
+def _check_outputs(o, B, N, MW):
+    """Caller-supplied output tensors of a tree: tokens, parents, pos int32
+    [B, N]; mask int32 (or uint32) [B, N, MW]; scores float32 [B, N] or
+    absent / None.  All contiguous."""
+    torch = _torch()
+    if not isinstance(o, dict):
+        raise DartError("out must be a dict of tensors")
+    for key in ("tokens", "parents", "pos", "mask"):
+        if o.get(key) is None:
+            raise DartError(f"out['{key}'] is missing")
+    for key in ("tokens", "parents", "pos"):
+        _check_tensor(o[key], f"out['{key}']", torch.int32, (B, N))
+    _check_tensor(o["mask"], "out['mask']", _mask_dtypes(), (B, N, MW))
+    _check_tensor(o.get("scores"), "out['scores']", torch.float32, (B, N))
+
+
+def _check_ctx(table, ctx, B):
+    """The committed context a table needs: int32 [B, n-1], contiguous."""
+    if table is None:
+        return
+    if ctx is None:
+        raise DartError("ctx is required with an n-gram table")
+    _check_tensor(ctx, "ctx", _torch().int32, (B, table.n - 1))
+
+
+def _check_workspace(ws, need):
+    _check_tensor(ws, "workspace", contiguous=True)
+    if ws.numel() * ws.element_size() < need:
+        raise DartError(f"workspace holds {ws.numel() * ws.element_size()} bytes, {need} needed")
+
+
+def _out_names(o):
+    return [(f"out['{k}']", o.get(k)) for k in ("tokens", "parents", "pos", "mask", "scores")]
 
 
 def num_nodes(d: int, k: int, W: int) -> int:
@@ -197,12 +284,16 @@ class NGramTable:
     def lookup(self, keys, stream=None):
         """keys: CUDA int32 [Q, n] -> (vals float32 [Q], found bool [Q])."""
         torch = _torch()
-        _need_cuda(keys, "keys", torch.int32)
+        dev = _device_of(("keys", keys), ("table", self.slots))
+        _check_tensor(keys, "keys", torch.int32)
+        if keys.dim() != 2 or keys.shape[1] != self.n:
+            raise DartError(f"keys must be [Q, {self.n}], got {tuple(keys.shape)}")
         Q = keys.shape[0]
-        vals = torch.empty(Q, dtype=torch.float32, device=keys.device)
-        found = torch.empty(Q, dtype=torch.int32, device=keys.device)
-        _check(lib().dart_ngram_lookup(C.byref(self.desc), _ptr(keys), Q, _ptr(vals), _ptr(found),
-                                       _stream_ptr(stream)), "dart_ngram_lookup")
+        vals = torch.empty(Q, dtype=torch.float32, device=dev)
+        found = torch.empty(Q, dtype=torch.int32, device=dev)
+        with _on_device(dev):
+            _check(lib().dart_ngram_lookup(C.byref(self.desc), _ptr(keys), Q, _ptr(vals), _ptr(found),
+                                           _stream_ptr(stream, dev)), "dart_ngram_lookup")
         return vals, found.bool()
 
 
@@ -247,6 +338,31 @@ def _row_stride(logits) -> int:
     return int(step)
 
 
+def _table_args(table, ctx):
+    if table is None:
+        return None, None
+    return C.byref(table.desc), _ptr(ctx)
+
+
+def _tree_inputs(logits, k, W, table, ctx, out, extra=()):
+    """Shared checks of tree_build / tree_build_noalloc: returns (dev, B, d, V, N, MW)."""
+    codes = DTYPE_CODES()
+    dev = _device_of(("logits", logits), ("ctx", ctx if table is not None else None),
+                     ("table", table.slots if table is not None else None),
+                     *(_out_names(out) if out is not None else ()), *extra)
+    if logits.dtype not in codes or logits.dim() != 3:
+        raise DartError("logits must be [B, d, V] float32, float16 or bfloat16")
+    B, d, V = logits.shape
+    N = num_nodes(d, k, W)
+    if N < 0:
+        raise DartError("invalid d/k/W")
+    MW = mask_words(N)
+    _check_ctx(table, ctx, B)
+    if out is not None:
+        _check_outputs(out, B, N, MW)
+    return dev, B, d, V, N, MW
+
+
 def tree_build(logits, T: float, k: int, W: int, lam: float, beta: float,
                table: NGramTable | None = None, ctx=None, *, out: dict | None = None,
                workspace=None, stream=None, scores: bool = True) -> dict:
@@ -254,30 +370,27 @@ def tree_build(logits, T: float, k: int, W: int, lam: float, beta: float,
 
     The rows may be a view of a padded vocabulary (z[..., :V] of [B, d, V_pad]):
     only the V valid logits of each row are read.  mask is returned as int32
-    storage holding the uint32 bit pattern."""
+    storage holding the uint32 bit pattern.  T = 0 is greedy decoding: the
+    tree is then scored with log_softmax(z), as at T = 1.  Every tensor
+    (logits, ctx, the table, out, workspace) must be on one CUDA device; the
+    call runs with that device current."""
     torch = _torch()
-    codes = DTYPE_CODES()
-    _need_cuda(logits, "logits", contiguous=False)
-    if logits.dtype not in codes or logits.dim() != 3:
-        raise DartError("logits must be [B, d, V] float32, float16 or bfloat16")
-    B, d, V = logits.shape
+    dev, B, d, V, N, MW = _tree_inputs(logits, k, W, table, ctx, out, (("workspace", workspace),))
     stride = _row_stride(logits)
-    N = num_nodes(d, k, W)
-    if N < 0:
-        raise DartError("invalid d/k/W")
-    MW = mask_words(N)
-    o = out if out is not None else _outputs(B, N, MW, logits.device, scores)
-    need = workspace_bytes(B, d, V, codes[logits.dtype], k)
-    ws = workspace if workspace is not None else torch.zeros(max(need, 1), dtype=torch.uint8,
-                                                             device=logits.device)
-    if table is not None:
-        _need_cuda(ctx, "ctx", torch.int32)
-    rc = lib().dart_tree_build_strided(_ptr(logits), B, d, V, stride, codes[logits.dtype], float(T), k, W,
-                               float(lam), float(beta),
-                               C.byref(table.desc) if table is not None else None,
-                               _ptr(ctx) if table is not None else None,
-                               _ptr(o["tokens"]), _ptr(o["parents"]), _ptr(o["pos"]), _ptr(o["mask"]),
-                               _ptr(o.get("scores")), _ptr(ws), ws.numel(), _stream_ptr(stream))
+    code = DTYPE_CODES()[logits.dtype]
+    need = workspace_bytes(B, d, V, code, k)
+    with _on_device(dev):
+        o = out if out is not None else _outputs(B, N, MW, dev, scores)
+        if workspace is not None:
+            _check_workspace(workspace, need)
+            ws = workspace
+        else:
+            ws = torch.zeros(max(need, 1), dtype=torch.uint8, device=dev)
+        rc = lib().dart_tree_build_strided(_ptr(logits), B, d, V, stride, code, float(T), k, W,
+                                           float(lam), float(beta), *_table_args(table, ctx),
+                                           _ptr(o["tokens"]), _ptr(o["parents"]), _ptr(o["pos"]),
+                                           _ptr(o["mask"]), _ptr(o.get("scores")), _ptr(ws),
+                                           ws.numel() * ws.element_size(), _stream_ptr(stream, dev))
     _check(rc, "dart_tree_build_strided")
     o["workspace"] = ws
     return o
@@ -285,52 +398,122 @@ def tree_build(logits, T: float, k: int, W: int, lam: float, beta: float,
 
 def tree_build_noalloc(logits, T: float, k: int, W: int, lam: float, beta: float,
                        table: NGramTable | None = None, ctx=None, *, out: dict | None = None,
-                       stream=None, scores: bool = True) -> dict:
+                       stream=None, scores: bool = True, check_errors: bool = False) -> dict:
     """tree_build for callers that cannot allocate device scratch: the library's
     fixed 16 MiB buffer stands in for the workspace (see dart_tree_build_noalloc
-    in include/darttree.h for its limits and sharing rules)."""
-    torch = _torch()
-    codes = DTYPE_CODES()
-    _need_cuda(logits, "logits")
-    if logits.dtype not in codes or logits.dim() != 3:
-        raise DartError("logits must be [B, d, V] float32, float16 or bfloat16")
-    B, d, V = logits.shape
-    N = num_nodes(d, k, W)
-    if N < 0:
-        raise DartError("invalid d/k/W")
-    o = out if out is not None else _outputs(B, N, mask_words(N), logits.device, scores)
-    if table is not None:
-        _need_cuda(ctx, "ctx", torch.int32)
-    rc = lib().dart_tree_build_noalloc(_ptr(logits), B, d, V, codes[logits.dtype], float(T), k, W,
-                                       float(lam), float(beta),
-                                       C.byref(table.desc) if table is not None else None,
-                                       _ptr(ctx) if table is not None else None,
-                                       _ptr(o["tokens"]), _ptr(o["parents"]), _ptr(o["pos"]),
-                                       _ptr(o["mask"]), _ptr(o.get("scores")), _stream_ptr(stream))
-    _check(rc, "dart_tree_build_noalloc")
+    in include/darttree.h for its limits and sharing rules).  logits must be
+    contiguous.  With check_errors, the call then waits for the stream and
+    raises DartError if the buffer's device error word is set."""
+    dev, B, d, V, N, MW = _tree_inputs(logits, k, W, table, ctx, out)
+    _check_tensor(logits, "logits")
+    code = DTYPE_CODES()[logits.dtype]
+    with _on_device(dev):
+        o = out if out is not None else _outputs(B, N, MW, dev, scores)
+        sp = _stream_ptr(stream, dev)
+        rc = lib().dart_tree_build_noalloc(_ptr(logits), B, d, V, code, float(T), k, W,
+                                           float(lam), float(beta), *_table_args(table, ctx),
+                                           _ptr(o["tokens"]), _ptr(o["parents"]), _ptr(o["pos"]),
+                                           _ptr(o["mask"]), _ptr(o.get("scores")), sp)
+        _check(rc, "dart_tree_build_noalloc")
+        if check_errors:
+            flags = _noalloc_error(sp)
+            if flags:
+                raise DartError(f"dart_tree_build_noalloc: device error bits {flags:#x} "
+                                f"({_deverr_names(flags)})")
     return o
 
 
-def tree_from_topk(ids, logp, W: int, lam: float, beta: float, table: NGramTable | None = None,
-                   ctx=None, *, out: dict | None = None, stream=None, scores: bool = True) -> dict:
-    """ids: CUDA int32 [B, d, k]; logp: CUDA float64 [B, d, k] -> dict of CUDA outputs."""
+def _noalloc_error(stream_ptr) -> int:
+    flags = C.c_uint32(0)
+    _check(lib().dart_noalloc_device_error(C.byref(flags), stream_ptr), "dart_noalloc_device_error")
+    return int(flags.value)
+
+
+def noalloc_device_error(device=None, stream=None) -> int:
+    """Waits for the stream, then returns (and clears) the device error bits
+    that dart_tree_build_noalloc calls on `device` (default: the current one)
+    left in the library's internal buffer."""
     torch = _torch()
-    _need_cuda(ids, "ids", torch.int32)
-    _need_cuda(logp, "logp", torch.float64)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with _on_device(dev):
+        return _noalloc_error(_stream_ptr(stream, dev))
+
+
+def _deverr_names(flags: int) -> str:
+    return ", ".join(v for b, v in DEVERR.items() if flags & b) or "unknown"
+
+
+def tree_from_topk(ids, logp, W: int, lam: float, beta: float = 0.0, table: NGramTable | None = None,
+                   ctx=None, *, pairs=None, out: dict | None = None, stream=None,
+                   scores: bool = True) -> dict:
+    """ids: CUDA int32 [B, d, k]; logp: CUDA float64 [B, d, k] -> dict of CUDA outputs.
+
+    The continuity term is the n-gram table (with ctx), or `pairs`: CUDA
+    float32 [B, d, k, k] caller scores of (parent's list position in row j-1,
+    child's list position in row j), the root counting as position 0 for row
+    0 (dart_tree_from_topk_pairs), or nothing."""
+    torch = _torch()
+    if pairs is not None and table is not None:
+        raise DartError("give either an n-gram table or pair scores, not both")
+    dev = _device_of(("ids", ids), ("logp", logp), ("ctx", ctx if table is not None else None),
+                     ("table", table.slots if table is not None else None), ("pairs", pairs),
+                     *(_out_names(out) if out is not None else ()))
+    if ids.dim() != 3:
+        raise DartError("ids must be [B, d, k]")
+    _check_tensor(ids, "ids", torch.int32)
+    _check_tensor(logp, "logp", torch.float64, tuple(ids.shape))
     B, d, k = ids.shape
+    _check_tensor(pairs, "pairs", torch.float32, (B, d, k, k))
     N = num_nodes(d, k, W)
     if N < 0:
         raise DartError("invalid d/k/W")
     MW = mask_words(N)
-    o = out if out is not None else _outputs(B, N, MW, ids.device, scores)
-    if table is not None:
-        _need_cuda(ctx, "ctx", torch.int32)
-    rc = lib().dart_tree_from_topk(_ptr(ids), _ptr(logp), B, d, k, W, float(lam), float(beta),
-                                   C.byref(table.desc) if table is not None else None,
-                                   _ptr(ctx) if table is not None else None,
-                                   _ptr(o["tokens"]), _ptr(o["parents"]), _ptr(o["pos"]),
-                                   _ptr(o["mask"]), _ptr(o.get("scores")), _stream_ptr(stream))
-    _check(rc, "dart_tree_from_topk")
+    _check_ctx(table, ctx, B)
+    if out is not None:
+        _check_outputs(out, B, N, MW)
+    with _on_device(dev):
+        o = out if out is not None else _outputs(B, N, MW, dev, scores)
+        outs = (_ptr(o["tokens"]), _ptr(o["parents"]), _ptr(o["pos"]), _ptr(o["mask"]), _ptr(o.get("scores")))
+        if pairs is not None:
+            rc = lib().dart_tree_from_topk_pairs(_ptr(ids), _ptr(logp), _ptr(pairs), B, d, k, W, float(lam),
+                                                 *outs, _stream_ptr(stream, dev))
+            what = "dart_tree_from_topk_pairs"
+        else:
+            rc = lib().dart_tree_from_topk(_ptr(ids), _ptr(logp), B, d, k, W, float(lam), float(beta),
+                                           *_table_args(table, ctx), *outs, _stream_ptr(stream, dev))
+            what = "dart_tree_from_topk"
+    _check(rc, what)
+    return o
+
+
+def tree_from_rows(workspace, pairs, *, B: int, d: int, V: int, dtype, T: float, k: int, W: int,
+                   lam: float, out: dict | None = None, stream=None, scores: bool = True) -> dict:
+    """The tree stage on the candidate lists that row_topk left in `workspace`
+    (rows = B * d, same V, dtype, T and k), with pair scores `pairs` (CUDA
+    float32 [B, d, k, k], see tree_from_topk) as the continuity term
+    (dart_tree_from_rows_pairs)."""
+    torch = _torch()
+    code = DTYPE_CODES()[dtype]
+    dev = _device_of(("workspace", workspace), ("pairs", pairs),
+                     *(_out_names(out) if out is not None else ()))
+    if pairs is None:
+        raise DartError("pairs is required")
+    _check_tensor(pairs, "pairs", torch.float32, (B, d, k, k))
+    _check_workspace(workspace, workspace_bytes(B, d, V, code, k))
+    N = num_nodes(d, k, W)
+    if N < 0:
+        raise DartError("invalid d/k/W")
+    MW = mask_words(N)
+    if out is not None:
+        _check_outputs(out, B, N, MW)
+    with _on_device(dev):
+        o = out if out is not None else _outputs(B, N, MW, dev, scores)
+        rc = lib().dart_tree_from_rows_pairs(B, d, V, code, float(T), k, W, float(lam), _ptr(pairs),
+                                             _ptr(o["tokens"]), _ptr(o["parents"]), _ptr(o["pos"]),
+                                             _ptr(o["mask"]), _ptr(o.get("scores")), _ptr(workspace),
+                                             workspace.numel() * workspace.element_size(),
+                                             _stream_ptr(stream, dev))
+    _check(rc, "dart_tree_from_rows_pairs")
     return o
 
 
@@ -340,31 +523,49 @@ def row_topk(logits, T: float, k: int, *, workspace=None, stream=None):
     The rows may be a view of a padded vocabulary (z[:, :V] of [R, V_pad])."""
     torch = _torch()
     codes = DTYPE_CODES()
-    _need_cuda(logits, "logits", contiguous=False)
+    dev = _device_of(("logits", logits), ("workspace", workspace))
     if logits.dtype not in codes or logits.dim() != 2:
         raise DartError("logits must be [R, V] float32, float16 or bfloat16")
     R, V = logits.shape
     stride = _row_stride(logits)
-    ids = torch.empty((R, k), dtype=torch.int32, device=logits.device)
-    logp = torch.empty((R, k), dtype=torch.float32, device=logits.device)
-    lse = torch.empty((R,), dtype=torch.float32, device=logits.device)
     need = workspace_bytes(R, 1, V, codes[logits.dtype], k)
-    ws = workspace if workspace is not None else torch.zeros(max(need, 1), dtype=torch.uint8,
-                                                             device=logits.device)
-    _check(lib().dart_row_topk_strided(_ptr(logits), R, V, stride, codes[logits.dtype], float(T), k, _ptr(ids),
-                                       _ptr(logp), _ptr(lse), _ptr(ws), ws.numel(), _stream_ptr(stream)),
-           "dart_row_topk_strided")
+    with _on_device(dev):
+        ids = torch.empty((R, k), dtype=torch.int32, device=dev)
+        logp = torch.empty((R, k), dtype=torch.float32, device=dev)
+        lse = torch.empty((R,), dtype=torch.float32, device=dev)
+        if workspace is not None:
+            _check_workspace(workspace, need)
+            ws = workspace
+        else:
+            ws = torch.zeros(max(need, 1), dtype=torch.uint8, device=dev)
+        rc = lib().dart_row_topk_strided(_ptr(logits), R, V, stride, codes[logits.dtype], float(T), k,
+                                         _ptr(ids), _ptr(logp), _ptr(lse), _ptr(ws),
+                                         ws.numel() * ws.element_size(), _stream_ptr(stream, dev))
+    _check(rc, "dart_row_topk_strided")
     return ids, logp, lse, ws
+
+
+def _check_error_word(device_err):
+    if device_err is not None:
+        _check_tensor(device_err, "device_err", (_torch().int32,) + _mask_dtypes()[1:])
+        if device_err.numel() < 1:
+            raise DartError("device_err must hold at least one element")
 
 
 def mask_pack(parents, *, device_err=None, stream=None):
     """parents: CUDA int32 [B, N] -> mask int32 [B, N, ceil(N/32)] (uint32 bits)."""
     torch = _torch()
-    _need_cuda(parents, "parents", torch.int32)
+    dev = _device_of(("parents", parents), ("device_err", device_err))
+    if parents.dim() != 2:
+        raise DartError("parents must be [B, N]")
+    _check_tensor(parents, "parents", torch.int32)
+    _check_error_word(device_err)
     B, N = parents.shape
-    out = torch.empty((B, N, (N + 31) // 32), dtype=torch.int32, device=parents.device)
-    _check(lib().dart_mask_pack(_ptr(parents), B, N, _ptr(out), _ptr(device_err), _stream_ptr(stream)),
-           "dart_mask_pack")
+    with _on_device(dev):
+        out = torch.empty((B, N, (N + 31) // 32), dtype=torch.int32, device=dev)
+        rc = lib().dart_mask_pack(_ptr(parents), B, N, _ptr(out), _ptr(device_err),
+                                  _stream_ptr(stream, dev))
+    _check(rc, "dart_mask_pack")
     return out
 
 
@@ -376,27 +577,30 @@ def tree_select(tokens, parents, pos, scores, M: int, *, device_err=None, stream
     mask (int32 [B, M', ceil(M'/32)], uint32 bits) and scores (float32 [B, M']),
     M' = min(M, N)."""
     torch = _torch()
-    for t, name in ((tokens, "tokens"), (parents, "parents"), (pos, "pos")):
-        _need_cuda(t, name, torch.int32)
-    _need_cuda(scores, "scores", torch.float32)
-    _need_cuda(device_err, "device_err", torch.int32)
-    if parents.dim() != 2 or any(t.shape != parents.shape for t in (tokens, pos, scores)):
+    dev = _device_of(("tokens", tokens), ("parents", parents), ("pos", pos), ("scores", scores),
+                     ("device_err", device_err))
+    if parents.dim() != 2:
         raise DartError("tokens, parents, pos and scores must all be [B, N]")
+    for t, name in ((tokens, "tokens"), (parents, "parents"), (pos, "pos")):
+        _check_tensor(t, name, torch.int32, tuple(parents.shape))
+    _check_tensor(scores, "scores", torch.float32, tuple(parents.shape))
+    _check_error_word(device_err)
     if int(M) < 0:
         raise DartError("the budget M must be >= 0")
     B, N = parents.shape
     Mp = min(int(M), N)
-    dev = parents.device
-    out = dict(index=torch.empty((B, Mp), dtype=torch.int32, device=dev),
-               tokens=torch.empty((B, Mp), dtype=torch.int32, device=dev),
-               parents=torch.empty((B, Mp), dtype=torch.int32, device=dev),
-               pos=torch.empty((B, Mp), dtype=torch.int32, device=dev),
-               mask=torch.empty((B, Mp, (Mp + 31) // 32), dtype=torch.int32, device=dev),
-               scores=torch.empty((B, Mp), dtype=torch.float32, device=dev))
-    _check(lib().dart_tree_select(_ptr(tokens), _ptr(parents), _ptr(pos), _ptr(scores), B, N, int(M),
-                                  _ptr(out["index"]), _ptr(out["tokens"]), _ptr(out["parents"]),
-                                  _ptr(out["pos"]), _ptr(out["mask"]), _ptr(out["scores"]),
-                                  _ptr(device_err), _stream_ptr(stream)), "dart_tree_select")
+    with _on_device(dev):
+        out = dict(index=torch.empty((B, Mp), dtype=torch.int32, device=dev),
+                   tokens=torch.empty((B, Mp), dtype=torch.int32, device=dev),
+                   parents=torch.empty((B, Mp), dtype=torch.int32, device=dev),
+                   pos=torch.empty((B, Mp), dtype=torch.int32, device=dev),
+                   mask=torch.empty((B, Mp, (Mp + 31) // 32), dtype=torch.int32, device=dev),
+                   scores=torch.empty((B, Mp), dtype=torch.float32, device=dev))
+        rc = lib().dart_tree_select(_ptr(tokens), _ptr(parents), _ptr(pos), _ptr(scores), B, N, int(M),
+                                    _ptr(out["index"]), _ptr(out["tokens"]), _ptr(out["parents"]),
+                                    _ptr(out["pos"]), _ptr(out["mask"]), _ptr(out["scores"]),
+                                    _ptr(device_err), _stream_ptr(stream, dev))
+    _check(rc, "dart_tree_select")
     return out
 
 
@@ -408,10 +612,12 @@ def set_wait_limit(cycles: int) -> None:
 
 
 def device_error(workspace, stream=None) -> int:
-    """Synchronises the stream and returns the workspace's device error bits."""
+    """Synchronises the stream and returns (and clears) the workspace's device error bits."""
+    dev = _device_of(("workspace", workspace))
     flags = C.c_uint32(0)
-    _check(lib().dart_device_error(_ptr(workspace), C.byref(flags), _stream_ptr(stream)),
-           "dart_device_error")
+    with _on_device(dev):
+        _check(lib().dart_device_error(_ptr(workspace), C.byref(flags), _stream_ptr(stream, dev)),
+               "dart_device_error")
     return int(flags.value)
 
 
@@ -425,22 +631,34 @@ class TreeBuilder:
         self.dtype = dtype
         self.code = DTYPE_CODES()[dtype]
         self.T, self.k, self.W, self.lam, self.beta = float(T), k, W, float(lam), float(beta)
-        self.table, self.ctx = table, ctx
         self.N = num_nodes(d, k, W)
+        if self.N < 0:
+            raise DartError("invalid d/k/W")
         self.MW = mask_words(self.N)
-        self.out = _outputs(B, self.N, self.MW, device, scores)
-        self.ws = torch.zeros(max(workspace_bytes(B, d, V, self.code, k), 1), dtype=torch.uint8,
-                              device=device)
+        self.device = torch.device(device)
+        if self.device.type == "cuda" and self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
+        _device_of(("ctx", ctx if table is not None else None),
+                   ("table", table.slots if table is not None else None))
+        _check_ctx(table, ctx, B)
+        self.table, self.ctx = table, ctx
+        with _on_device(self.device):
+            self.out = _outputs(B, self.N, self.MW, self.device, scores)
+            self.ws = torch.zeros(max(workspace_bytes(B, d, V, self.code, k), 1), dtype=torch.uint8,
+                                  device=self.device)
+        _device_of(("workspace", self.ws), ("ctx", ctx if table is not None else None))
 
     def __call__(self, logits, stream=None):
         B, d, V = self.shape
-        rc = lib().dart_tree_build(_ptr(logits), B, d, V, self.code, self.T, self.k, self.W,
-                                   self.lam, self.beta,
-                                   C.byref(self.table.desc) if self.table is not None else None,
-                                   _ptr(self.ctx) if self.table is not None else None,
-                                   _ptr(self.out["tokens"]), _ptr(self.out["parents"]),
-                                   _ptr(self.out["pos"]), _ptr(self.out["mask"]),
-                                   _ptr(self.out.get("scores")), _ptr(self.ws), self.ws.numel(),
-                                   _stream_ptr(stream))
+        if _device_of(("logits", logits)) != self.device:
+            raise DartError(f"logits is on {logits.device}, the builder on {self.device}")
+        _check_tensor(logits, "logits", self.dtype, self.shape)
+        with _on_device(self.device):
+            rc = lib().dart_tree_build(_ptr(logits), B, d, V, self.code, self.T, self.k, self.W,
+                                       self.lam, self.beta, *_table_args(self.table, self.ctx),
+                                       _ptr(self.out["tokens"]), _ptr(self.out["parents"]),
+                                       _ptr(self.out["pos"]), _ptr(self.out["mask"]),
+                                       _ptr(self.out.get("scores")), _ptr(self.ws),
+                                       self.ws.numel(), _stream_ptr(stream, self.device))
         _check(rc, "dart_tree_build")
         return self.out

@@ -16,6 +16,17 @@ int elem_bytes(int dtype) { return dtype == DART_F32 ? 4 : 2; }
 bool valid_dtype(int dtype) { return dtype == DART_F32 || dtype == DART_F16 || dtype == DART_BF16; }
 bool pow2(uint64_t x) { return x >= 2 && (x & (x - 1)) == 0; }
 
+// Temperature check.  T = 0 is greedy decoding (DART, Figure 2 caption reports
+// results at T = 0 and T = 1): it names how the target samples, and
+// log_softmax(z / 0) is undefined, so the candidates (chosen on the raw
+// logits whatever T is) are scored with the draft's own log-probabilities,
+// the T = 1 values.  A negative or non-finite T is an argument error.
+bool score_temperature(float* T) {
+  if (!finite(*T) || *T < 0.f) return false;
+  if (*T == 0.f) *T = 1.f;
+  return true;
+}
+
 int num_nodes(int d, int k, int W) {
   if (d < 1 || k < 1 || W < 1) return -1;
   long long total = 0, width = 1;
@@ -64,6 +75,7 @@ TreeArgs tree_args(int B, int d, int k, int W, float lambda, float beta,
   a.ctx = ctx;
   a.slots = t ? t->slots : nullptr;
   a.capacity = t ? t->capacity : 0;
+  a.pair = nullptr;
   a.out_tokens = out_tokens;
   a.out_parents = out_parents;
   a.out_pos = out_pos;
@@ -103,24 +115,77 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 
 namespace {
 
-constexpr int kMaxScratchDevices = 64;
-std::mutex g_scratch_mutex;
-void* g_scratch_addr[kMaxScratchDevices] = {};
+// The CUDA runtime gives a __device__ variable one address per context, and a
+// context replaced by cudaDeviceReset (or a driver-API caller's own context)
+// may place it elsewhere, so the cache is keyed by the current context's
+// unique id.  cuCtxGetCurrent and cuCtxGetId come through the runtime's
+// driver entry-point query, which keeps the library free of a link-time
+// dependency on the driver library.
+using CtxGetCurrentFn = int (*)(void** ctx);
+using CtxGetIdFn = int (*)(void* ctx, unsigned long long* id);
 
-// Device address of g_static_scratch on the current device.  In host code the
-// array's name only stands in for the symbol, so the address is looked up once
-// per device (with that device current) and cached.
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  void* addr;
+};
+constexpr int kMaxScratchContexts = 64;
+std::mutex g_scratch_mutex;
+ScratchEntry g_scratch_cache[kMaxScratchContexts] = {};
+int g_scratch_used = 0;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+bool driver_entry(const char* name, void** fn) {
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  return cudaGetDriverEntryPointByVersion(name, fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+         q == cudaDriverEntryPointSuccess && *fn;
+}
+
+// Device address of g_static_scratch in the current context.  The first call
+// in a context binds the runtime's primary context if none is current yet and
+// looks the address up; later calls in that context use the cached address.
 int static_scratch(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return DART_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxScratchDevices) return DART_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return DART_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+  if (!g_ctx_get_current || !g_ctx_get_id) {
+    void* a = nullptr;
+    void* b = nullptr;
+    if (!driver_entry("cuCtxGetCurrent", &a) || !driver_entry("cuCtxGetId", &b)) return DART_ERR_CUDA;
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(b);
   }
-  *out = g_scratch_addr[dev];
+  void* ctx = nullptr;
+  void* addr = nullptr;
+  if (g_ctx_get_current(&ctx) != 0) return DART_ERR_CUDA;
+  if (!ctx) {
+    // no context current on this thread yet: the lookup binds the device's primary context
+    if (cudaGetSymbolAddress(&addr, g_static_scratch) != cudaSuccess || !addr) return DART_ERR_CUDA;
+    if (g_ctx_get_current(&ctx) != 0 || !ctx) return DART_ERR_CUDA;
+  }
+  unsigned long long id = 0;
+  if (g_ctx_get_id(ctx, &id) != 0) return DART_ERR_CUDA;
+  for (int i = 0; i < g_scratch_used; ++i)
+    if (g_scratch_cache[i].ctx_id == id) {
+      *out = g_scratch_cache[i].addr;
+      return DART_OK;
+    }
+  if (!addr && (cudaGetSymbolAddress(&addr, g_static_scratch) != cudaSuccess || !addr)) return DART_ERR_CUDA;
+  // a full cache forgets its oldest entry (contexts that old are usually gone)
+  if (g_scratch_used == kMaxScratchContexts) {
+    for (int i = 1; i < kMaxScratchContexts; ++i) g_scratch_cache[i - 1] = g_scratch_cache[i];
+    --g_scratch_used;
+  }
+  g_scratch_cache[g_scratch_used++] = ScratchEntry{id, addr};
+  *out = addr;
+  return DART_OK;
+}
+
+// Copies the control block's error word (word 0) to *out_flags and clears the
+// block when the word is nonzero.  The caller has synchronised the stream.
+int read_error_word(void* ctrl, uint32_t* out_flags) {
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, ctrl, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return DART_ERR_CUDA;
+  *out_flags = word;
+  if (word != 0u && cudaMemset(ctrl, 0, kCtrlBytes) != cudaSuccess) return DART_ERR_CUDA;
   return DART_OK;
 }
 
@@ -160,7 +225,7 @@ int dart_tree_build_strided(const void* logits, int B, int d, int V, int64_t row
   if (rc) return rc;
   if (V < 2 || V > kMaxV || k > V || !valid_dtype(dtype)) return DART_ERR_INVALID_ARG;
   if (row_stride < V || row_stride > kMaxRowStride) return DART_ERR_INVALID_ARG;
-  if (!finite(T) || !(T > 0.f)) return DART_ERR_INVALID_ARG;
+  if (!score_temperature(&T)) return DART_ERR_INVALID_ARG;
   if ((rc = check_table(ngram_table, ctx_tokens, B))) return rc;
   if (B == 0) return DART_OK;
   if (!logits || !aligned(logits, 16)) return DART_ERR_INVALID_ARG;
@@ -183,7 +248,7 @@ int dart_tree_build_noalloc(const void* logits, int B, int d, int V, int dtype,
   int rc = check_tree_shape(B, d, k, W, lambda, beta);
   if (rc) return rc;
   if (V < 2 || V > kMaxV || k > V || !valid_dtype(dtype)) return DART_ERR_INVALID_ARG;
-  if (!finite(T) || !(T > 0.f)) return DART_ERR_INVALID_ARG;
+  if (!score_temperature(&T)) return DART_ERR_INVALID_ARG;
   if ((rc = check_table(ngram_table, ctx_tokens, B))) return rc;
   if (B == 0) return DART_OK;
   if (!logits || !aligned(logits, 16)) return DART_ERR_INVALID_ARG;
@@ -194,11 +259,11 @@ int dart_tree_build_noalloc(const void* logits, int B, int d, int V, int dtype,
   if (L.total > kStaticScratchBytes) return DART_ERR_WORKSPACE;   // sizes beyond the fixed scratch
   void* scratch = nullptr;
   if ((rc = static_scratch(&scratch))) return rc;
+  // Nothing in the buffer has to start at zero for a call except the device
+  // error word, which starts at zero when the module loads and is cleared by
+  // dart_noalloc_device_error; every other byte a call reads it wrote itself.
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(scratch);
-  // errors are not reported on this path: clear the counters (and the error
-  // word) of a call that may have given up, on this stream
-  if (cudaMemsetAsync(ws, 0, L.clear_bytes, s) != cudaSuccess) return DART_ERR_CUDA;
   return launch_path(logits, B, d, V, V, dtype, T, k, W, lambda, beta, ngram_table, ctx_tokens, out_tokens,
                      out_parents, out_pos, out_mask, out_scores, ws, L, s);
 }
@@ -222,6 +287,50 @@ int dart_tree_from_topk(const int32_t* cand_ids, const double* cand_logp,
   return DART_OK;
 }
 
+int dart_tree_from_topk_pairs(const int32_t* cand_ids, const double* cand_logp, const float* pair_scores,
+                              int B, int d, int k, int W, float lambda,
+                              int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
+                              uint32_t* out_mask, float* out_scores, void* stream) {
+  int rc = check_tree_shape(B, d, k, W, lambda, 0.f);
+  if (rc) return rc;
+  if (B == 0) return DART_OK;
+  if (!cand_ids || !cand_logp || !pair_scores || !out_tokens || !out_parents || !out_pos || !out_mask)
+    return DART_ERR_INVALID_ARG;
+  TreeArgs a = tree_args(B, d, k, W, lambda, 0.f, nullptr, nullptr, out_tokens, out_parents, out_pos,
+                         out_mask, out_scores);
+  a.ids = cand_ids;
+  a.base = cand_logp;
+  a.pair = pair_scores;
+  if (launch_tree(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return DART_ERR_CUDA;
+  return DART_OK;
+}
+
+int dart_tree_from_rows_pairs(int B, int d, int V, int dtype, float T, int k, int W, float lambda,
+                              const float* pair_scores, int32_t* out_tokens, int32_t* out_parents,
+                              int32_t* out_pos, uint32_t* out_mask, float* out_scores,
+                              const void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_tree_shape(B, d, k, W, lambda, 0.f);
+  if (rc) return rc;
+  if (V < 2 || V > kMaxV || k > V || !valid_dtype(dtype)) return DART_ERR_INVALID_ARG;
+  if (!score_temperature(&T)) return DART_ERR_INVALID_ARG;
+  if (B == 0) return DART_OK;
+  if (!pair_scores || !out_tokens || !out_parents || !out_pos || !out_mask) return DART_ERR_INVALID_ARG;
+  WsLayout L;
+  if (!ws_layout((long long)B * d, V, elem_bytes(dtype), k, &L)) return DART_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return DART_ERR_WORKSPACE;
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  TreeArgs a = tree_args(B, d, k, W, lambda, 0.f, nullptr, nullptr, out_tokens, out_parents, out_pos,
+                         out_mask, out_scores);
+  a.ids = reinterpret_cast<const int32_t*>(ws + L.row_ids);
+  a.base = reinterpret_cast<const double*>(ws + L.row_base);
+  a.off = reinterpret_cast<const double*>(ws + L.row_off);
+  a.invT = 1.0 / double(T);
+  a.pair = pair_scores;
+  a.ctrl = reinterpret_cast<uint32_t*>(const_cast<uint8_t*>(ws) + L.ctrl);
+  if (launch_tree(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return DART_ERR_CUDA;
+  return DART_OK;
+}
+
 int dart_row_topk(const void* logits, int rows, int V, int dtype, float T, int k,
                   int32_t* out_ids, float* out_logp, float* out_lse,
                   void* workspace, size_t workspace_bytes, void* stream) {
@@ -235,7 +344,7 @@ int dart_row_topk_strided(const void* logits, int rows, int V, int64_t row_strid
   if (rows < 0 || V < 2 || V > kMaxV || !valid_dtype(dtype) || k < 1 || k > kMaxK || k > V)
     return DART_ERR_INVALID_ARG;
   if (row_stride < V || row_stride > kMaxRowStride) return DART_ERR_INVALID_ARG;
-  if (!finite(T) || !(T > 0.f)) return DART_ERR_INVALID_ARG;
+  if (!score_temperature(&T)) return DART_ERR_INVALID_ARG;
   if (rows == 0) return DART_OK;
   if (!logits || !aligned(logits, 16)) return DART_ERR_INVALID_ARG;
   WsLayout L;
@@ -254,7 +363,7 @@ int check_rows(const void* logits, bool need_logits, int rows, int V, int64_t ro
   if (rows < 0 || V < 2 || V > kMaxV || !valid_dtype(dtype) || k < 1 || k > kMaxK || k > V)
     return DART_ERR_INVALID_ARG;
   if (row_stride < V || row_stride > kMaxRowStride) return DART_ERR_INVALID_ARG;
-  if (!finite(T) || !(T > 0.f)) return DART_ERR_INVALID_ARG;
+  if (!score_temperature(&T)) return DART_ERR_INVALID_ARG;
   if (rows == 0) return DART_OK;
   if (need_logits && (!logits || !aligned(logits, 16))) return DART_ERR_INVALID_ARG;
   if (!ws_layout(rows, V, elem_bytes(dtype), k, L)) return DART_ERR_INVALID_ARG;
@@ -389,17 +498,16 @@ int dart_device_error(const void* workspace, uint32_t* out_flags, void* stream) 
   if (!workspace || !out_flags) return DART_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return DART_ERR_CUDA;
-  // word 0: error bits; words 2..3: rows of the last row-stream call (written by the kernel)
-  uint32_t head[4] = {0, 0, 0, 0};
-  if (cudaMemcpy(head, workspace, sizeof(head), cudaMemcpyDeviceToHost) != cudaSuccess) return DART_ERR_CUDA;
-  *out_flags = head[0];
-  if (head[0] != 0u) {
-    const unsigned long long rows = (unsigned long long)head[2] | ((unsigned long long)head[3] << 32);
-    WsLayout L;
-    const size_t clear = ws_layout((long long)rows, 2, 1, 1, &L) ? L.clear_bytes : size_t(kCtrlBytes);
-    if (cudaMemset(const_cast<void*>(workspace), 0, clear) != cudaSuccess) return DART_ERR_CUDA;
-  }
-  return DART_OK;
+  return read_error_word(const_cast<void*>(workspace), out_flags);
+}
+
+int dart_noalloc_device_error(uint32_t* out_flags, void* stream) {
+  if (!out_flags) return DART_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  int rc = static_scratch(&scratch);
+  if (rc) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DART_ERR_CUDA;
+  return read_error_word(scratch, out_flags);
 }
 
 const char* dart_status_string(int status) {

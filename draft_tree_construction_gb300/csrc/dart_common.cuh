@@ -137,7 +137,7 @@ __host__ __device__ inline int slot_capacity(int k) {
 }
 
 struct WsLayout {
-  size_t ctrl, clear_bytes;
+  size_t ctrl;               // control block: word 0 holds the device error bits
   size_t row_off, row_ids, row_base, slots, total;
   unsigned long long wspan;  // bytes per warp when rows are V apart (the smallest span)
   int pmax;                  // piece slots per row
@@ -158,7 +158,6 @@ inline bool ws_layout(long long R, int V, int es, int k, WsLayout* L) {
   L->slot_bytes = align_up(kSlotHeader + 20 * size_t(L->cp), 16);
   size_t o = 0;
   L->ctrl = o;      o += kCtrlBytes;
-  L->clear_bytes = o;
   L->row_off = o;   o = align_up(o + 8 * size_t(R), 256);
   L->row_ids = o;   o = align_up(o + 4 * size_t(R) * k, 256);
   L->row_base = o;  o = align_up(o + 8 * size_t(R) * k, 256);

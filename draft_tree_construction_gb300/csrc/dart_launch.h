@@ -23,7 +23,7 @@ cudaError_t launch_rows(const void* logits, long long R, int V, long long stride
                         int32_t* out_ids, float* out_logp, float* out_lse, cudaStream_t stream);
 
 struct TreeArgs {
-  int B, d, k, W, N, MW, n;    // n = 0: no continuity term
+  int B, d, k, W, N, MW, n;    // n = 0: no n-gram term
   double lam, beta;
   const int32_t* ids;          // [B][d][k] candidate tokens
   const double* base;          // [B][d][k] candidate base values (logits, or log-probabilities)
@@ -32,6 +32,7 @@ struct TreeArgs {
   const int32_t* ctx;          // [B][n-1]
   const void* slots;
   unsigned long long capacity;
+  const float* pair;           // [B][d][k][k] caller pair scores (with n = 0), or nullptr
   int32_t* out_tokens;
   int32_t* out_parents;
   int32_t* out_pos;

@@ -623,11 +623,6 @@ row_stream_kernel(const __grid_constant__ RowsParams P) {
   const int w = threadIdx.x >> 5;
   const long long gwarp = (long long)blockIdx.x * kRowWarps + w;
 
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    // rows of this call, for clearing the counters after a failed call
-    P.ctrl[2] = uint32_t((unsigned long long)P.R);
-    P.ctrl[3] = uint32_t((unsigned long long)P.R >> 32);
-  }
   for (int i = threadIdx.x; i < kRowSlots; i += blockDim.x) S.tau[i] = 0u;
   if (lane == 0) {
     for (int s = 0; s < kRowStages; ++s) mbar_init(&S.full[w][s], 1);
@@ -737,7 +732,7 @@ row_stream_kernel(const __grid_constant__ RowsParams P) {
 }
 
 // ---------------------------------------------------------------- row merge
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 128;
 constexpr int kMergePieces = 64;     // pieces a row merges from shared memory (more: the loop below)
 constexpr int kMergeKeys = 1024;     // candidate keys a row keeps in shared memory (more: one warp merges)
 
@@ -773,7 +768,8 @@ __device__ __forceinline__ void finish_row(const RowsParams& P, long long r, flo
 struct MergeSmem {
   float m[kMergePieces];
   double s[kMergePieces];
-  uint32_t end[kMergePieces];   // running end of the pieces' candidates
+  uint32_t end[kMergePieces];   // the pieces' candidate counts
+  uint32_t pb[kMergePieces];    // the pieces' bounds
   uint32_t bound;
   uint32_t nkeys;
   float M;
@@ -782,88 +778,119 @@ struct MergeSmem {
   uint64_t best[kMaxK];
 };
 
-// One CTA per row: every piece's header in one round of loads, the row's
-// bound, every candidate in one round (one per thread), the keys of the
-// elements reaching the bound appended in shared memory, and the row's k best
+// One CTA per row: every piece's header and every candidate slot entry are
+// loaded in one round (entries past a piece's count are dropped after), the
+// row's bound follows from the headers, the keys of the candidate elements
+// that reach it are appended in shared memory, and the row's k best are found
 // by ranking (each key counts the keys above it).  A row with more than
-// kMergePieces pieces, or more than kMergeKeys such keys, is merged by one
-// warp instead (inputs far from the streamed shapes).
+// kMergePieces pieces, more entries than one round holds, or more than
+// kMergeKeys such keys, is merged by one warp instead (inputs far from the
+// streamed shapes).
 template <int DT>
 __global__ void __launch_bounds__(kMergeThreads)
 row_merge_kernel(const __grid_constant__ RowsParams P) {
   __shared__ MergeSmem M;
   __shared__ uint64_t wstage[kKeyStage];
+  constexpr int kPer = 8;   // slot entries per thread in the one round
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const long long r = blockIdx.x;
   long long wa;
   const int nseg = row_pieces(P, r, &wa);
   const int k = P.k;
   if (nseg <= kMergePieces) {
+    // one round: headers (threads < nseg) and slot entries e = tid + u * T
     if (tid < nseg) {
       uint8_t* q = slot_of(P, r, tid);
       M.m[tid] = __ldcg(reinterpret_cast<const float*>(q));
       M.s[tid] = __ldcg(reinterpret_cast<const double*>(q + 8));
       M.end[tid] = min(__ldcg(reinterpret_cast<const uint32_t*>(q + 4)), uint32_t(P.cp));
+      M.pb[tid] = __ldcg(reinterpret_cast<const uint32_t*>(q + 16));
+    }
+    uint4 v[kPer];
+    uint32_t tag[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int e = tid + u * kMergeThreads;
+      v[u] = make_uint4(0u, 0u, 0u, 0u);
+      tag[u] = 0u;
+      if (e < nseg * P.cp) {
+        const int p = e / P.cp, i = e - p * P.cp;
+        uint8_t* q = slot_of(P, r, p);
+        v[u] = __ldcg(slot_vecs(P, q) + i);
+        tag[u] = __ldcg(slot_tags(P, q) + i);
+      }
     }
     if (tid == 0) M.nkeys = 0u;
     __syncthreads();
     if (warp == 0) {
-      // the bound: the largest piece bound, and the k-th largest piece maximum
-      uint32_t b = 0;
-      for (int p = lane; p < nseg; p += 32) b = max(b, __ldcg(reinterpret_cast<const uint32_t*>(slot_of(P, r, p) + 16)));
+      // max, sum (a fixed shuffle tree) and the bound: the largest piece
+      // bound, and the k-th largest piece maximum; pieces lane and lane + 32
+      const bool h0 = lane < nseg, h1 = lane + 32 < nseg;
+      const float m0 = h0 ? M.m[lane] : -FLT_MAX, m1 = h1 ? M.m[lane + 32] : -FLT_MAX;
+      uint32_t b = max(h0 ? M.pb[lane] : 0u, h1 ? M.pb[lane + 32] : 0u);
+      float mx = fmaxf(m0, m1);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+      double sum = (h0 ? M.s[lane] * double(ex2_approx((m0 - mx) * P.c)) : 0.0) +
+                   (h1 ? M.s[lane + 32] * double(ex2_approx((m1 - mx) * P.c)) : 0.0);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
       if (nseg >= k) {
-        for (int p = lane; p < nseg; p += 32) {
-          const uint32_t x = ord_f32(M.m[p]);
+        const uint32_t o0 = h0 ? ord_f32(m0) : 0u, o1 = h1 ? ord_f32(m1) : 0u;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t x = h == 0 ? o0 : o1;
           int above = 0, atleast = 0;
-          for (int q2 = 0; q2 < nseg; ++q2) {
-            const uint32_t y = ord_f32(M.m[q2]);
-            above += y > x ? 1 : 0;
-            atleast += y >= x ? 1 : 0;
+          for (int src = 0; src < 32; ++src) {
+            const uint32_t y0 = __shfl_sync(kFull, o0, src), y1 = __shfl_sync(kFull, o1, src);
+            above += (y0 > x ? 1 : 0) + (y1 > x ? 1 : 0);
+            atleast += (y0 >= x ? 1 : 0) + (y1 >= x ? 1 : 0);
           }
-          if (above < k && atleast >= k) b = max(b, x);
+          if (x != 0u && above < k && atleast >= k) b = max(b, x);
         }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) b = max(b, __shfl_xor_sync(kFull, b, o));
       if (lane == 0) {
-        // max, the sum in piece order, running ends of the candidates
-        float mx = -FLT_MAX;
-        for (int p = 0; p < nseg; ++p) mx = fmaxf(mx, M.m[p]);
-        double sum = 0.0;
-        uint32_t run = 0;
-        for (int p = 0; p < nseg; ++p) {
-          sum += M.s[p] * double(ex2_approx((M.m[p] - mx) * P.c));
-          run += M.end[p];
-          M.end[p] = run;
-        }
         M.M = mx;
         M.S = sum;
         M.bound = b;
       }
     }
     __syncthreads();
-    // candidates, one per thread and round
-    const uint32_t total = nseg > 0 ? M.end[nseg - 1] : 0u;
     const float tau = tau_value(M.bound);
-    for (uint32_t e = tid; e < total; e += kMergeThreads) {
-      int lo = 0, hi = nseg - 1;   // first piece whose running end exceeds e
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (M.end[mid] > e) hi = mid;
-        else lo = mid + 1;
+    const int entries = nseg * P.cp;
+    for (int base = 0; base < entries; base += kMergeThreads * kPer) {
+      if (base > 0) {   // rows of many pieces: further rounds of entries
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int e = base + tid + u * kMergeThreads;
+          v[u] = make_uint4(0u, 0u, 0u, 0u);
+          tag[u] = 0u;
+          if (e < entries) {
+            const int p = e / P.cp, i = e - p * P.cp;
+            uint8_t* q = slot_of(P, r, p);
+            v[u] = __ldcg(slot_vecs(P, q) + i);
+            tag[u] = __ldcg(slot_tags(P, q) + i);
+          }
+        }
       }
-      const uint32_t i = e - (lo > 0 ? M.end[lo - 1] : 0u);
-      uint8_t* q = slot_of(P, r, lo);
-      const uint4 v = __ldcg(slot_vecs(P, q) + i);
-      const uint32_t tag = __ldcg(slot_tags(P, q) + i);
-      uint32_t cm = vec_hits<DT>(v, tag, tau);
-      if (cm) {
-        uint32_t at = atomicAdd(&M.nkeys, uint32_t(__popc(cm)));
-        while (cm) {
-          const int el = __ffs(cm) - 1;
-          cm &= cm - 1u;
-          if (at < uint32_t(kMergeKeys)) M.keys[at] = elem_key(Elem<DT>::elem(v, el), (tag & 0xFFFFFFu) + uint32_t(el));
-          ++at;
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int e = base + tid + u * kMergeThreads;
+        if (e >= entries) continue;
+        const int p = e / P.cp, i = e - p * P.cp;
+        if (uint32_t(i) >= M.end[p]) continue;   // past the piece's count
+        uint32_t cm = vec_hits<DT>(v[u], tag[u], tau);
+        if (cm) {
+          uint32_t at = atomicAdd(&M.nkeys, uint32_t(__popc(cm)));
+          while (cm) {
+            const int el = __ffs(cm) - 1;
+            cm &= cm - 1u;
+            if (at < uint32_t(kMergeKeys))
+              M.keys[at] = elem_key(Elem<DT>::elem(v[u], el), (tag[u] & 0xFFFFFFu) + uint32_t(el));
+            ++at;
+          }
         }
       }
     }

@@ -161,7 +161,8 @@ struct RowBuf {
 };
 
 // One CTA per tree.  A frontier node carries Z (sum of its candidates' base
-// values) and G (sum of its n-gram terms); a child's ranking key is
+// values) and G (sum of its continuity terms: n-gram values, or the caller's
+// pair scores of (parent column, child column)); a child's ranking key is
 // Z * invT + lam * G, accumulated in double exactly as the oracle does it, so
 // equal keys (ties the inputs hold exactly) stay equal.  The reported score
 // subtracts the rows' offsets (their log-sum-exp), which every node of one
@@ -224,6 +225,8 @@ tree_kernel(const TreeArgs A) {
   const unsigned long long nbuckets = A.capacity / 4;
   const int nctx = n > 1 ? n - 1 : 0;
   const double invT = A.invT, lam = A.lam;
+  // caller pair scores of this tree: [d][k][k], the parent's column first
+  const float* pair = A.pair ? A.pair + (size_t)b * dk * k : nullptr;
 
   // child key of frontier entry (Zp, Gp, context ctx) with candidate c of row R
   auto child = [&](double Zp, double Gp, int x0, int x1, int x2, const RowBuf& Rw, int c, double* Gout) {
@@ -238,6 +241,8 @@ tree_kernel(const TreeArgs A) {
       float g = 0.f;
       const double gg = probe(slots, nbuckets, pack_ngram(t, n), &g) ? double(g) : A.beta;
       G = __dadd_rn(G, gg);
+    } else if (pair) {
+      G = __dadd_rn(G, double(__ldg(pair + c)));   // row 0: the root is column 0
     }
     *Gout = G;
     return __dadd_rn(__dmul_rn(Z, invT), __dmul_rn(lam, G));
@@ -259,8 +264,10 @@ tree_kernel(const TreeArgs A) {
     const int j = e / k, c = e - j * k;
     const int* ids = rows_id + j * k;
     const int t = ids[c];
+    // equal ids (which valid inputs never hold) fall to their list order, so
+    // the ranks stay a permutation and every child keeps a distinct tie key
     int r = 0;
-    for (int c2 = 0; c2 < k; ++c2) r += ids[c2] < t;
+    for (int c2 = 0; c2 < k; ++c2) r += (ids[c2] < t || (ids[c2] == t && c2 < c)) ? 1 : 0;
     rows_rank[e] = r;
     rows_inv[j * k + r] = c;
   }
@@ -452,6 +459,8 @@ tree_kernel(const TreeArgs A) {
         // start the lookup of child (x, c2) before the rest of the work
         Probe pr;
         Key96 ckey{0u, 0u, 0u};
+        float pg = 0.f;
+        if (!last && pair) pg = __ldg(pair + ((size_t)(j + 1) * k + c) * k + c2);
         if (!last && n > 0) {
           const int ctok = Rn.rid[c2];
           int32_t t[4] = {ctx[0], ctx[1], ctx[2], 0};
@@ -490,6 +499,8 @@ tree_kernel(const TreeArgs A) {
           if (n > 0) {
             float g = 0.f;
             G = __dadd_rn(G, probe_match(pr, ckey, &g) ? double(g) : A.beta);
+          } else if (pair) {
+            G = __dadd_rn(G, double(pg));
           }
           cG_next[q] = G;
           ks2 = ord_f64(__dadd_rn(ZinvT, __dmul_rn(lam, G)));

@@ -21,6 +21,11 @@
  *           (descending), then lower parent index, then lower token id
  *   The root (last committed token) is not a node.  Nodes are numbered depth
  *   by depth in that order; a depth-1 node has parent -1.
+ *   T = 0 is greedy decoding (DART, Figure 2 caption, reports results at T = 0
+ *   and T = 1): it says how the target samples, and log_softmax(z / 0) is
+ *   undefined, so p_j is then log_softmax(z_j), the draft's own
+ *   log-probabilities (the T = 1 values).  C_j does not depend on T; with
+ *   lambda = 0 node 0 of every depth lies on the argmax chain.
  * All children of one depth share the sum of their rows' log-sum-exp terms,
  * so the ranking uses key = (sum of the path's logits) * (1/T) + lambda *
  * (sum of its g terms), both sums accumulated in double along the path; a
@@ -30,7 +35,8 @@
  * Conventions for every entry point:
  *  - All buffers belong to the caller.  The library allocates no memory and
  *    keeps no state between calls; calls on different streams with different
- *    workspaces may run concurrently.
+ *    workspaces may run concurrently.  (dart_tree_build_noalloc is the one
+ *    exception: it uses a buffer inside the library, described there.)
  *  - Pointers documented as "device" must point to memory of the current CUDA
  *    device; "host" pointers to ordinary host memory.  `stream` is a
  *    cudaStream_t (NULL = the legacy default stream).
@@ -117,8 +123,8 @@ size_t dart_tree_workspace_bytes(int B, int d, int V, int dtype, int k);
  *              not supported (results unspecified).
  *  B           sequences, >= 0 (0 = nothing to do, returns DART_OK)
  *  d           depths, 1..32          V  vocabulary, 2..2^24-1
- *  T           temperature, finite and > 0 (T = 0, greedy, is not a
- *              log-softmax and is rejected)
+ *  T           temperature, finite and >= 0; T = 0 (greedy) scores with
+ *              log_softmax(z), as T = 1 does (see the readings above)
  *  k           candidates per position, 1..min(32, V)
  *  W           frontier width, 1..64; N = dart_tree_num_nodes(d,k,W) <= 1024
  *  lambda,beta finite; lambda scales the n-gram log-probability, beta is the
@@ -171,14 +177,16 @@ int dart_tree_build_strided(const void* logits, int B, int d, int V, int64_t row
  * library holds until the process exits.  Sizes whose
  * dart_tree_workspace_bytes(B, d, V, dtype, k) exceeds 16 MiB are rejected
  * with DART_ERR_WORKSPACE before anything is launched.  The call allocates
- * nothing; since its error bits are not reported, it clears the buffer's
- * counters on `stream` before each use.
- * The first call on each device looks up the buffer's device address (with
- * that device current) and caches it; make that first call before any
- * stream capture.  All calls on a device share the one buffer, which keeps
- * the last call's contents: calls that overlap on the GPU (other streams,
- * other host threads) race and must be serialised by the caller.  Device
- * error bits are kept in that buffer and are not reported. */
+ * nothing and launches no clearing: no byte of the buffer has to start at
+ * zero except its device error word, which is zero when the library loads
+ * and is read (and cleared) with dart_noalloc_device_error.
+ * The first call in each CUDA context (the current device's primary context,
+ * bound if none is current) looks up the buffer's device address and caches
+ * it under the context's unique id, so a context that cudaDeviceReset
+ * replaced gets a fresh lookup; make that first call before any stream
+ * capture.  All calls in a context share the one buffer, which keeps the last
+ * call's contents: calls that overlap on the GPU (other streams, other host
+ * threads) race and must be serialised by the caller. */
 int dart_tree_build_noalloc(const void* logits, int B, int d, int V, int dtype,
                             float T, int k, int W, float lambda, float beta,
                             const dart_ngram_table_t* ngram_table, const int32_t* ctx_tokens,
@@ -188,7 +196,8 @@ int dart_tree_build_noalloc(const void* logits, int B, int d, int V, int dtype,
 /* The tree stage alone, from candidate lists a caller already has (for
  * example a drafter that emits its own top-k):
  *  cand_ids   device int32 [B][d][k], token ids in [0, 2^24-1), distinct
- *             within a row (any order)
+ *             within a row (any order; a row with a repeated id still
+ *             gives a well-formed tree, its tie order unspecified)
  *  cand_logp  device double [B][d][k], the candidates' log-probabilities
  * Children are ranked by (sum of logp along the path) + lambda * (sum of g),
  * both sums in double, and that value is the reported score.  Other
@@ -199,10 +208,40 @@ int dart_tree_from_topk(const int32_t* cand_ids, const double* cand_logp,
                         int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
                         uint32_t* out_mask, float* out_scores, void* stream);
 
+/* The tree stage with a caller-supplied continuity scorer in place of the
+ * n-gram table (DARTree, Method / Tree Construction: the children of a depth
+ * are scored by a head in one batch; an order-2 head, restricted to the
+ * candidate sets, is a table of candidate-pair scores):
+ *  pair_scores device float [B][d][k][k]: a child with list position c in
+ *              row j adds pair_scores[b][j][c'][c] to its continuity sum,
+ *              c' the list position of its parent's token in row j-1; for
+ *              row 0 the parent is the root and c' = 0 (the rest of row 0's
+ *              k x k block is not read).  Values finite.
+ * Children are ranked by (path's log-probability sum) + lambda * (sum of its
+ * pair scores), ties as in dart_tree_build.  Other arguments and outputs as
+ * in dart_tree_from_topk (no table, no context, no beta). */
+int dart_tree_from_topk_pairs(const int32_t* cand_ids, const double* cand_logp, const float* pair_scores,
+                              int B, int d, int k, int W, float lambda,
+                              int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
+                              uint32_t* out_mask, float* out_scores, void* stream);
+
+/* The same tree stage on the candidate lists that dart_row_topk (or
+ * dart_row_pass followed by dart_row_finish) left in `workspace` for rows =
+ * B * d rows of [B][d][V] logits: call it with the same V, dtype, T and k, on
+ * the same stream, after the caller has scored the pairs of those candidates
+ * (their ids are dart_row_topk's out_ids).  The ranking key is that of
+ * dart_tree_build with the pair scores as the continuity term, so the scores
+ * are log-probabilities at temperature T plus lambda times the pair sum.  The
+ * workspace is only read, apart from its device error word. */
+int dart_tree_from_rows_pairs(int B, int d, int V, int dtype, float T, int k, int W, float lambda,
+                              const float* pair_scores, int32_t* out_tokens, int32_t* out_parents,
+                              int32_t* out_pos, uint32_t* out_mask, float* out_scores,
+                              const void* workspace, size_t workspace_bytes, void* stream);
+
 /* The row stage alone: for each of `rows` rows of logits[rows][V] (device,
  * 16-byte aligned): the k best ids (value descending, lower id first),
  * their log-probabilities log_softmax(z / T)[id] and the row's
- * log-sum-exp of z / T.  out_ids device int32 [rows][k], out_logp device
+ * log-sum-exp of z / T (T = 0: of z, as for dart_tree_build).  out_ids device int32 [rows][k], out_logp device
  * float [rows][k], out_lse device float [rows] (each may be NULL).
  * workspace as for dart_tree_build with B = rows, d = 1. */
 int dart_row_topk(const void* logits, int rows, int V, int dtype, float T, int k,
@@ -292,10 +331,17 @@ int dart_ngram_lookup(const dart_ngram_table_t* table, const int32_t* keys, int6
 
 /* Waits for `stream`, then copies the workspace's device error word to
  * *out_flags (host).  The word collects the DART_DEVERR_* bits of every call
- * since the last nonzero read; a nonzero read clears it together with the
- * workspace's counters (a call that gave up may leave them set), so the
- * workspace is ready for the next call.  Returns DART_OK, or DART_ERR_CUDA. */
+ * since the last nonzero read; a nonzero read clears it.  Returns DART_OK, or
+ * DART_ERR_CUDA. */
 int dart_device_error(const void* workspace, uint32_t* out_flags, void* stream);
+
+/* dart_device_error for dart_tree_build_noalloc's internal buffer in the
+ * current context: waits for `stream`, copies the buffer's error word to
+ * *out_flags (host) and clears it when nonzero.  The word collects the bits
+ * of every dart_tree_build_noalloc call in this context since the last
+ * nonzero read.  Returns DART_OK, DART_ERR_INVALID_ARG (out_flags NULL) or
+ * DART_ERR_CUDA.  The pages have no counterpart. */
+int dart_noalloc_device_error(uint32_t* out_flags, void* stream);
 
 /* Sets the number of SM clock cycles any one wait of the row pass (a bulk
  * copy landing, a slot freeing, a barrier of the CTA) may take before the pass

@@ -290,3 +290,29 @@ def make_candidate_trees(*, B: int, d: int, k: int, W: int, seed: int = 0, tie_f
             start += n_j
             prev = idx
     return dict(tokens=tokens, parents=parents, pos=pos, scores=scores)
+
+
+def head_pair_scores(ids: np.ndarray, roots: np.ndarray, *, rank: int = 8, seed: int = 0) -> np.ndarray:
+    """Pair scores [B, d, k, k] of a random low-rank order-2 head, restricted to
+    the candidate lists ids [B, d, k]: token t has seeded embeddings u(t) and
+    v(t) in R^rank, and the score of child position c after parent position c'
+    is the log-softmax over the k children of u(parent token) . v(child
+    token) / sqrt(rank).  The parent of row 0 is the tree's root token
+    roots[b]; rows j > 0 take row j-1's candidates as parents.  float32."""
+    ids = np.asarray(ids, dtype=np.int64)
+    B, d, k = ids.shape
+    toks = np.unique(np.concatenate([ids.reshape(-1), np.asarray(roots, dtype=np.int64).reshape(-1)]))
+    rng = np.random.default_rng(seed)
+    U = rng.standard_normal((toks.size, rank))
+    Vv = rng.standard_normal((toks.size, rank))
+    row = {int(t): i for i, t in enumerate(toks.tolist())}
+    out = np.zeros((B, d, k, k), dtype=np.float32)
+    for b in range(B):
+        for j in range(d):
+            parents = [int(roots[b])] * k if j == 0 else ids[b, j - 1].tolist()
+            child = np.array([row[int(t)] for t in ids[b, j].tolist()])
+            for cp, pt in enumerate(parents):
+                logits = Vv[child] @ U[row[pt]] / np.sqrt(rank)
+                m = logits.max()
+                out[b, j, cp] = (logits - m - np.log(np.exp(logits - m).sum())).astype(np.float32)
+    return out

@@ -81,7 +81,7 @@ def _build(L, **over):
     (dict(d=0), INVALID), (dict(d=33), INVALID), (dict(V=1), INVALID), (dict(V=1 << 24), INVALID),
     (dict(k=0), INVALID), (dict(k=33), INVALID), (dict(k=5, V=4), INVALID), (dict(W=0), INVALID),
     (dict(W=65), INVALID), (dict(d=32, k=32, W=64), INVALID),       # N > 1024
-    (dict(T=0.0), INVALID), (dict(T=-1.0), INVALID), (dict(T=float("nan")), INVALID),
+    (dict(T=-1e-30), INVALID), (dict(T=-1.0), INVALID), (dict(T=float("nan")), INVALID),
     (dict(T=float("inf")), INVALID), (dict(lam=float("nan")), INVALID),
     (dict(beta=float("-inf")), INVALID), (dict(dtype=3), INVALID), (dict(B=-1), INVALID),
     (dict(logits=0), INVALID), (dict(logits=FAKE + 8), INVALID), (dict(tok=0), INVALID),
@@ -112,7 +112,10 @@ def test_table_argument_checks(L, tab, ctx, code):
 def test_other_entry_points_check_arguments(L):
     P = C.c_void_p
     assert L.dart_row_topk(P(FAKE), 4, 1, 2, 1.0, 1, None, None, None, None, 0, None) == INVALID
-    assert L.dart_row_topk(P(FAKE), 4, 100, 2, 0.0, 4, None, None, None, None, 0, None) == INVALID
+    assert L.dart_row_topk(P(FAKE), 4, 100, 2, -0.5, 4, None, None, None, None, 0, None) == INVALID
+    # T = 0 (greedy) passes the argument checks: the missing workspace is what fails
+    assert L.dart_row_topk(P(FAKE), 4, 100, 2, 0.0, 4, None, None, None, None, 0, None) == WORKSPACE
+    assert L.dart_noalloc_device_error(None, None) == INVALID
     assert L.dart_row_topk(P(FAKE), 4, 100, 2, 1.0, 4, None, None, None, None, 0, None) == WORKSPACE
     assert L.dart_row_topk(None, 0, 100, 2, 1.0, 4, None, None, None, None, 0, None) == OK
     assert L.dart_tree_from_topk(None, None, 2, 4, 4, 4, 0.5, -1.0, None, None, None, None, None, None,

@@ -85,6 +85,7 @@ struct RowsParams {
   float* out_logp;    // optional [R][k]
   float* out_lse;     // optional [R]
   long long wait_limit;
+  int spread;         // warps dealt round-robin over the CTAs (inputs too small to fill every SM)
 };
 
 // A warp's candidates: vectors of logits and their tags (element mask << 24
@@ -621,7 +622,9 @@ row_stream_kernel(const __grid_constant__ RowsParams P) {
   RowSmem& S = *reinterpret_cast<RowSmem*>(smem_raw);
   const int lane = threadIdx.x & 31;
   const int w = threadIdx.x >> 5;
-  const long long gwarp = (long long)blockIdx.x * kRowWarps + w;
+  // spans are numbered CTA by CTA; a small input deals them round-robin so
+  // that every SM streams a share
+  const long long gwarp = P.spread ? (long long)w * gridDim.x + blockIdx.x : (long long)blockIdx.x * kRowWarps + w;
 
   for (int i = threadIdx.x; i < kRowSlots; i += blockDim.x) S.tau[i] = 0u;
   if (lane == 0) {
@@ -674,7 +677,7 @@ row_stream_kernel(const __grid_constant__ RowsParams P) {
     if (g.s1 <= g.s0) continue;
     const unsigned long long rs = (unsigned long long)r * P.stride;
     const long long slot_i = r - cta_r0;
-    uint32_t* tau_slot = (slot_i >= 0 && slot_i < kRowSlots) ? &S.tau[slot_i] : nullptr;
+    uint32_t* tau_slot = (!P.spread && slot_i >= 0 && slot_i < kRowSlots) ? &S.tau[slot_i] : nullptr;
     Acc a;
     a.m = -FLT_MAX;
     a.mc = scaled_max(a.m, P.c);
@@ -765,6 +768,179 @@ __device__ __forceinline__ void finish_row(const RowsParams& P, long long r, flo
   }
 }
 
+// A whole row merged by one warp (rows beyond what one CTA merges from shared
+// memory).  The headers come first: the pieces' (max, sum)
+// combine into the row's (a fixed shuffle tree over the pieces' running
+// pairs), and the bound is the largest piece bound or, with k or more pieces
+// (up to 64), the k-th largest piece maximum if that is higher.  Only pieces
+// whose maximum reaches the bound can hold one of the k best; their entries
+// are gathered (eight per lane per round trip) and the keys of the elements
+// that reach the bound go through the warp's key stage, the k best kept
+// whenever it could overflow.  `lists` holds 2 * kMergeSel + 1 ints.
+constexpr int kMergeSel = 256;   // selected pieces per gathering round
+
+template <int DT>
+__device__ __forceinline__ void stage_keys_of(uint64_t* wstage, uint64_t* best, int& nk, int k, const uint4& vv,
+                                              uint32_t tag, uint32_t cm) {
+  const int lane = threadIdx.x & 31;
+  int added;
+  const int pre = warp_prefix4(uint32_t(__popc(cm)), &added);
+  if (added == 0) return;
+  if (nk + added > kKeyStage) {
+    // keep the k best of the stage (ranking), best first
+    __syncwarp();
+    for (int x = lane; x < nk; x += 32) {
+      const uint64_t key = wstage[x];
+      int rank = 0;
+      for (int y = 0; y < nk; ++y) rank += wstage[y] > key ? 1 : 0;
+      if (rank < k) best[rank] = key;
+    }
+    __syncwarp();
+    nk = nk < k ? nk : k;
+    for (int x = lane; x < nk; x += 32) wstage[x] = best[x];
+    __syncwarp();
+  }
+  int at = nk + pre;
+  while (cm) {
+    const int el = __ffs(cm) - 1;
+    cm &= cm - 1u;
+    wstage[at++] = elem_key(Elem<DT>::elem(vv, el), (tag & 0xFFFFFFu) + uint32_t(el));
+  }
+  nk += added;
+  __syncwarp();
+}
+
+template <int DT>
+__device__ __noinline__ void merge_row_warp(const RowsParams& P, long long r, uint64_t* wstage, uint64_t* best,
+                                            int* lists) {
+  const long long v = r;
+  const int lane = threadIdx.x & 31;
+  const int k = P.k;
+  long long wa;
+  const int nseg = row_pieces(P, v, &wa);
+  // headers: running (max, sum) per lane over its pieces, the largest bound;
+  // pieces lane and lane + 32 keep their maxima for the k-th largest
+  float mp = -FLT_MAX;
+  double sp = 0.0;
+  uint32_t b = 0;
+  uint32_t om[2] = {0u, 0u};
+  for (int p0 = 0; p0 < nseg; p0 += 32) {
+    const int p = p0 + lane;
+    if (p < nseg) {
+      const uint8_t* q = slot_of(P, v, p);
+      const float m2 = __ldcg(reinterpret_cast<const float*>(q));
+      const double s2 = __ldcg(reinterpret_cast<const double*>(q + 8));
+      const uint32_t b2 = __ldcg(reinterpret_cast<const uint32_t*>(q + 16));
+      const float M2 = fmaxf(mp, m2);
+      sp = sp * double(ex2_approx((mp - M2) * P.c)) + s2 * double(ex2_approx((m2 - M2) * P.c));
+      mp = M2;
+      b = max(b, b2);
+      if (p0 < 64) om[p0 >> 5] = ord_f32(m2);
+    }
+  }
+  float Mx = mp;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Mx = fmaxf(Mx, __shfl_xor_sync(kFull, Mx, o));
+    b = max(b, __shfl_xor_sync(kFull, b, o));
+  }
+  double Sx = sp * double(ex2_approx((mp - Mx) * P.c));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) Sx += __shfl_xor_sync(kFull, Sx, o);
+  if (nseg >= k && nseg <= 64) {
+    // the k-th largest piece maximum: k pieces each hold an element that high
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t x = om[h];
+      int above = 0, atleast = 0;
+      for (int src = 0; src < 32; ++src) {
+        const uint32_t y0 = __shfl_sync(kFull, om[0], src), y1 = __shfl_sync(kFull, om[1], src);
+        above += (y0 > x ? 1 : 0) + (y1 > x ? 1 : 0);
+        atleast += (y0 >= x ? 1 : 0) + (y1 >= x ? 1 : 0);
+      }
+      if (x != 0u && above < k && atleast >= k) b = max(b, x);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) b = max(b, __shfl_xor_sync(kFull, b, o));
+  }
+  const float tau = tau_value(b);
+  const uint32_t otau = b;
+  int* sel = lists;                    // selected pieces
+  int* start = lists + kMergeSel;      // their first entry in the gathered range
+  int nk = 0;
+  int p0 = 0;
+  while (p0 < nseg) {
+    // select pieces whose maximum reaches the bound, up to kMergeSel of them
+    int ns = 0, E = 0;
+    for (; p0 < nseg && ns + 32 <= kMergeSel; p0 += 32) {
+      const int p = p0 + lane;
+      int cnt = 0;
+      bool take = false;
+      if (p < nseg) {
+        const uint8_t* q = slot_of(P, v, p);
+        cnt = int(min(__ldcg(reinterpret_cast<const uint32_t*>(q + 4)), uint32_t(P.cp)));
+        take = cnt > 0 && ord_f32(__ldcg(reinterpret_cast<const float*>(q))) >= otau;
+      }
+      const uint32_t tm = __ballot_sync(kFull, take);
+      // prefix of the taken pieces' counts (exclusive), lanes in order
+      int incl = take ? cnt : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int excl = incl - (take ? cnt : 0);
+      if (take) {
+        const int at = ns + __popc(tm & ((1u << lane) - 1u));
+        sel[at] = p;
+        start[at] = E + excl;
+      }
+      ns += __popc(tm);
+      E += __shfl_sync(kFull, incl, 31);
+    }
+    if (lane == 0) start[ns] = E;
+    __syncwarp();
+    // gather the selected pieces' entries, eight per lane per round trip
+    for (int e0 = 0; e0 < E; e0 += 256) {
+      uint4 vv[8];
+      uint32_t tg[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int e = e0 + u * 32 + lane;
+        vv[u] = make_uint4(0u, 0u, 0u, 0u);
+        tg[u] = 0u;
+        if (e < E) {
+          int lo = 0, hi = ns - 1;     // the selected piece holding entry e
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (start[mid] <= e) lo = mid;
+            else hi = mid - 1;
+          }
+          const uint8_t* q = slot_of(P, v, sel[lo]);
+          const int i = e - start[lo];
+          vv[u] = __ldcg(slot_vecs(P, const_cast<uint8_t*>(q)) + i);
+          tg[u] = __ldcg(slot_tags(P, const_cast<uint8_t*>(q)) + i);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int e = e0 + u * 32 + lane;
+        const uint32_t cm = e < E ? vec_hits<DT>(vv[u], tg[u], tau) : 0u;
+        stage_keys_of<DT>(wstage, best, nk, k, vv[u], tg[u], cm);
+      }
+    }
+    __syncwarp();
+  }
+  for (int x = lane; x < nk; x += 32) {
+    const uint64_t key = wstage[x];
+    int rank = 0;
+    for (int y = 0; y < nk; ++y) rank += wstage[y] > key ? 1 : 0;
+    if (rank < k) best[rank] = key;
+  }
+  __syncwarp();
+  finish_row(P, r, Mx, Sx, best, nk < k ? nk : k);
+}
+
 struct MergeSmem {
   float m[kMergePieces];
   double s[kMergePieces];
@@ -776,6 +952,10 @@ struct MergeSmem {
   double S;
   uint64_t keys[kMergeKeys];
   uint64_t best[kMaxK];
+  int sel[kMergePieces];          // pieces whose maximum reaches the bound (rows of many entries)
+  int start[kMergePieces + 1];    // their first entry in the gathered range
+  int E;                          // entries of the selected pieces
+  int nsel;                       // selected pieces
 };
 
 // One CTA per row: every piece's header and every candidate slot entry are
@@ -798,7 +978,10 @@ row_merge_kernel(const __grid_constant__ RowsParams P) {
   const int nseg = row_pieces(P, r, &wa);
   const int k = P.k;
   if (nseg <= kMergePieces) {
-    // one round: headers (threads < nseg) and slot entries e = tid + u * T
+    // one round: headers (threads < nseg) and slot entries e = tid + u * T,
+    // when one round holds them all; else the headers first, and then only
+    // the entries of pieces whose maximum reaches the row's bound
+    const bool one_round = nseg * P.cp <= kMergeThreads * kPer;
     if (tid < nseg) {
       uint8_t* q = slot_of(P, r, tid);
       M.m[tid] = __ldcg(reinterpret_cast<const float*>(q));
@@ -813,7 +996,7 @@ row_merge_kernel(const __grid_constant__ RowsParams P) {
       const int e = tid + u * kMergeThreads;
       v[u] = make_uint4(0u, 0u, 0u, 0u);
       tag[u] = 0u;
-      if (e < nseg * P.cp) {
+      if (one_round && e < nseg * P.cp) {
         const int p = e / P.cp, i = e - p * P.cp;
         uint8_t* q = slot_of(P, r, p);
         v[u] = __ldcg(slot_vecs(P, q) + i);
@@ -856,20 +1039,62 @@ row_merge_kernel(const __grid_constant__ RowsParams P) {
         M.S = sum;
         M.bound = b;
       }
+      if (!one_round) {
+        // the pieces that can hold one of the k best, in piece order, and
+        // where their entries start in the gathered range
+        const bool t0 = h0 && M.end[lane] > 0u && ord_f32(m0) >= b;
+        const bool t1 = h1 && M.end[lane + 32] > 0u && ord_f32(m1) >= b;
+        const int c0 = t0 ? int(M.end[lane]) : 0, c1 = t1 ? int(M.end[lane + 32]) : 0;
+        int i0 = c0, i1 = c1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y0 = __shfl_up_sync(kFull, i0, o), y1 = __shfl_up_sync(kFull, i1, o);
+          if (lane >= o) {
+            i0 += y0;
+            i1 += y1;
+          }
+        }
+        const int tot0 = __shfl_sync(kFull, i0, 31);
+        const uint32_t bm0 = __ballot_sync(kFull, t0), bm1 = __ballot_sync(kFull, t1);
+        const uint32_t below = (1u << lane) - 1u;
+        if (t0) {
+          const int at = __popc(bm0 & below);
+          M.sel[at] = lane;
+          M.start[at] = i0 - c0;
+        }
+        if (t1) {
+          const int at = __popc(bm0) + __popc(bm1 & below);
+          M.sel[at] = lane + 32;
+          M.start[at] = tot0 + i1 - c1;
+        }
+        const int tot1 = __shfl_sync(kFull, i1, 31);
+        if (lane == 0) {
+          const int ns = __popc(bm0) + __popc(bm1);
+          M.E = tot0 + tot1;
+          M.start[ns] = tot0 + tot1;
+          M.nsel = ns;
+        }
+      }
     }
     __syncthreads();
     const float tau = tau_value(M.bound);
-    const int entries = nseg * P.cp;
+    const int entries = one_round ? nseg * P.cp : M.E;
     for (int base = 0; base < entries; base += kMergeThreads * kPer) {
-      if (base > 0) {   // rows of many pieces: further rounds of entries
+      if (!one_round) {   // gathered entries of the selected pieces
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
           const int e = base + tid + u * kMergeThreads;
           v[u] = make_uint4(0u, 0u, 0u, 0u);
           tag[u] = 0u;
           if (e < entries) {
-            const int p = e / P.cp, i = e - p * P.cp;
-            uint8_t* q = slot_of(P, r, p);
+            int lo = 0, hi = M.nsel - 1;    // the selected piece holding entry e
+            while (lo < hi) {
+              const int mid = (lo + hi + 1) >> 1;
+              if (M.start[mid] <= e) lo = mid;
+              else hi = mid - 1;
+            }
+            uint8_t* q = slot_of(P, r, M.sel[lo]);
+            const int i = e - M.start[lo];
             v[u] = __ldcg(slot_vecs(P, q) + i);
             tag[u] = __ldcg(slot_tags(P, q) + i);
           }
@@ -879,8 +1104,10 @@ row_merge_kernel(const __grid_constant__ RowsParams P) {
       for (int u = 0; u < kPer; ++u) {
         const int e = base + tid + u * kMergeThreads;
         if (e >= entries) continue;
-        const int p = e / P.cp, i = e - p * P.cp;
-        if (uint32_t(i) >= M.end[p]) continue;   // past the piece's count
+        if (one_round) {
+          const int p = e / P.cp, i = e - p * P.cp;
+          if (uint32_t(i) >= M.end[p]) continue;   // past the piece's count
+        }
         uint32_t cm = vec_hits<DT>(v[u], tag[u], tau);
         if (cm) {
           uint32_t at = atomicAdd(&M.nkeys, uint32_t(__popc(cm)));
@@ -908,80 +1135,9 @@ row_merge_kernel(const __grid_constant__ RowsParams P) {
       return;
     }
   }
-  // one warp, any number of pieces and keys: merged in rounds through the
-  // warp's key stage, the k best kept whenever it could overflow
+  // one warp, any number of pieces and keys
   if (warp != 0) return;
-  float mp = -FLT_MAX;
-  double sp = 0.0;
-  uint32_t b = 0;
-  for (int p = lane; p < nseg; p += 32) {
-    uint8_t* q = slot_of(P, r, p);
-    const float m2 = __ldcg(reinterpret_cast<const float*>(q));
-    const double s2 = __ldcg(reinterpret_cast<const double*>(q + 8));
-    const float M2 = fmaxf(mp, m2);
-    sp = sp * double(ex2_approx((mp - M2) * P.c)) + s2 * double(ex2_approx((m2 - M2) * P.c));
-    mp = M2;
-    b = max(b, __ldcg(reinterpret_cast<const uint32_t*>(q + 16)));
-  }
-  float Mx = mp;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    Mx = fmaxf(Mx, __shfl_xor_sync(kFull, Mx, o));
-    b = max(b, __shfl_xor_sync(kFull, b, o));
-  }
-  double Sx = sp * double(ex2_approx((mp - Mx) * P.c));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) Sx += __shfl_xor_sync(kFull, Sx, o);
-  const float tau = tau_value(b);
-  int nk = 0;
-  for (int p = 0; p < nseg; ++p) {
-    uint8_t* q = slot_of(P, r, p);
-    const int cnt = int(min(__ldcg(reinterpret_cast<const uint32_t*>(q + 4)), uint32_t(P.cp)));
-    for (int i0 = 0; i0 < cnt; i0 += 32) {
-      const int i = i0 + lane;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      uint32_t tag = 0;
-      if (i < cnt) {
-        v = __ldcg(slot_vecs(P, q) + i);
-        tag = __ldcg(slot_tags(P, q) + i);
-      }
-      uint32_t cm = i < cnt ? vec_hits<DT>(v, tag, tau) : 0u;
-      int added;
-      const int pre = warp_prefix4(uint32_t(__popc(cm)), &added);
-      if (added == 0) continue;
-      if (nk + added > kKeyStage) {
-        // keep the k best of the stage (ranking), best first
-        __syncwarp();
-        for (int x = lane; x < nk; x += 32) {
-          const uint64_t key = wstage[x];
-          int rank = 0;
-          for (int y = 0; y < nk; ++y) rank += wstage[y] > key ? 1 : 0;
-          if (rank < k) M.best[rank] = key;
-        }
-        __syncwarp();
-        nk = nk < k ? nk : k;
-        for (int x = lane; x < nk; x += 32) wstage[x] = M.best[x];
-        __syncwarp();
-      }
-      int at = nk + pre;
-      while (cm) {
-        const int el = __ffs(cm) - 1;
-        cm &= cm - 1u;
-        wstage[at++] = elem_key(Elem<DT>::elem(v, el), (tag & 0xFFFFFFu) + uint32_t(el));
-      }
-      nk += added;
-      __syncwarp();
-    }
-  }
-  __syncwarp();
-  for (int x = lane; x < nk; x += 32) {
-    const uint64_t key = wstage[x];
-    int rank = 0;
-    for (int y = 0; y < nk; ++y) rank += wstage[y] > key ? 1 : 0;
-    if (rank < k) M.best[rank] = key;
-  }
-  __syncwarp();
-  finish_row(P, r, Mx, Sx, M.best, nk < k ? nk : k);
+  merge_row_warp<DT>(P, r, wstage, M.best, reinterpret_cast<int*>(M.keys));
 }
 
 // ------------------------------------------------------------------ launch
@@ -1026,6 +1182,7 @@ static bool rows_params(RowsParams* Pp, const void* logits, long long R, int V, 
   P.out_logp = out_logp;
   P.out_lse = out_lse;
   P.wait_limit = rows_wait_limit();
+  P.spread = 0;
   return true;
 }
 
@@ -1036,7 +1193,13 @@ cudaError_t launch_row_pass(const void* logits, long long R, int V, long long st
     return cudaErrorInvalidValue;
   if (P.total == 0) return cudaSuccess;
   const unsigned long long warps = (P.total + P.wspan - 1) / P.wspan;
-  const unsigned long long grid = (warps + kRowWarps - 1) / kRowWarps;
+  unsigned long long grid = (warps + kRowWarps - 1) / kRowWarps;
+  constexpr unsigned long long kSMs = kRowPassWarps / kRowWarps;   // the grid the spans are sized for
+  if (grid < kSMs) {
+    // fewer spans than CTAs x warps: one CTA per SM, the spans dealt round-robin
+    P.spread = 1;
+    grid = warps < kSMs ? warps : kSMs;
+  }
   const size_t smem = rows_smem_bytes();
   cudaError_t e = cudaSuccess;
   auto go = [&](auto kernel) {

@@ -126,12 +126,14 @@ __host__ __device__ inline int tree_pad(int W, int k) {
   const int run = tree_run_len(W);
   return (W * k + run - 1) / run * run;
 }
-// Threads per tree: one per child of a full frontier, 32..512.
+constexpr int kRankMax = 256;   // up to this many children a depth selects by ranking
+// Threads per tree: one per child of a full frontier, 32..512.  (Two per
+// child would halve the ranking loop, but at 122 registers a thread it
+// leaves one CTA per SM for 320 threads: two waves for 256 trees.)
 inline int tree_threads(int W, int k) {
   const int t = (W * k + 31) / 32 * 32;
   return t < 32 ? 32 : (t > kTreeThreads ? kTreeThreads : t);
 }
-constexpr int kRankMax = 256;   // up to this many children a depth selects by ranking
 
 inline size_t tree_smem_bytes(int d, int W, int k, int MW) {
   const size_t np = size_t(tree_pad(W, k));
@@ -225,6 +227,7 @@ tree_kernel(const TreeArgs A) {
   const unsigned long long nbuckets = A.capacity / 4;
   const int nctx = n > 1 ? n - 1 : 0;
   const double invT = A.invT, lam = A.lam;
+  const bool unit_T = invT == 1.0;   // Z * 1 is Z itself: the multiply is skipped, the bits are the same
   // caller pair scores of this tree: [d][k][k], the parent's column first
   const float* pair = A.pair ? A.pair + (size_t)b * dk * k : nullptr;
 
@@ -245,7 +248,7 @@ tree_kernel(const TreeArgs A) {
       G = __dadd_rn(G, double(__ldg(pair + c)));   // row 0: the root is column 0
     }
     *Gout = G;
-    return __dadd_rn(__dmul_rn(Z, invT), __dmul_rn(lam, G));
+    return __dadd_rn(unit_T ? Z : __dmul_rn(Z, invT), __dmul_rn(lam, G));
   };
 
   // ---- every row's candidates and offset, then their token ranks
@@ -270,6 +273,14 @@ tree_kernel(const TreeArgs A) {
     for (int c2 = 0; c2 < k; ++c2) r += (ids[c2] < t || (ids[c2] == t && c2 < c)) ? 1 : 0;
     rows_rank[e] = r;
     rows_inv[j * k + r] = c;
+  }
+  if (tid == 0) {
+    // each depth's sum of row offsets, accumulated in depth order
+    double acc = 0.0;
+    for (int j = 0; j < d; ++j) {
+      acc = __dadd_rn(acc, offs[j]);
+      offs[j] = acc;
+    }
   }
   __syncthreads();
 
@@ -312,13 +323,13 @@ tree_kernel(const TreeArgs A) {
     for (int f = 0; f < nctx; ++f) fctx_cur[f] = rootctx[f];
   }
   int nf = 1, node_base = 0;
-  double Lsum = 0.0;   // sum of the row offsets down to this depth (same in every thread)
+  double Lsum = 0.0;   // sum of the row offsets down to this depth
   __syncthreads();
 
   for (int j = 0; j < d; ++j) {
     const RowBuf Rc = row(j);                      // row j: candidates of the children selected now
     const RowBuf Rn = row(j + 1 < d ? j + 1 : j);  // row j+1: candidates of the next depth
-    Lsum = __dadd_rn(Lsum, offs[j]);
+    Lsum = offs[j];
     const int m = nf * k;
     const int nsel = m < W ? m : W;
     const uint64_t* src_s;     // the nsel survivors, best first
@@ -326,16 +337,24 @@ tree_kernel(const TreeArgs A) {
     uint64_t* ks_dst;          // keys of the next depth go here
     uint32_t* kt_dst;
     if (m <= kRankMax) {
-      // rank: the number of keys better than mine (keys are distinct)
-      if (tid < m) {
-        const uint64_t sq = keys[tid];
-        const uint32_t tq = ties[tid];
+      // rank: the number of keys better than mine (keys are distinct); at
+      // depths with at most half as many children as threads, each key is
+      // ranked by two threads against one half of the keys each
+      const int parts = int(blockDim.x) >= 2 * m ? 2 : 1;
+      if (warp * 32 < parts * m) {
+        const int q0 = parts == 2 ? (tid >> 1) : tid;
+        const int part = parts == 2 ? (tid & 1) : 0;
+        const bool live = q0 < m;
+        const uint64_t sq = live ? keys[q0] : 0ull;
+        const uint32_t tq = live ? ties[q0] : 0u;
         int rank = 0;
         // eight keys per step from 16-byte loads; the zero padding up to a
         // multiple of 32 never beats a real key
         const ulonglong2* k2 = reinterpret_cast<const ulonglong2*>(keys);
         const uint4* t4 = reinterpret_cast<const uint4*>(ties);
-        for (int q = 0; q < m; q += 8) {
+        const int half = parts == 2 ? (m + 15) / 16 * 8 : m;
+        const int lo = live ? part * half : 0, hi = live ? (part == 0 ? half : m) : 0;
+        for (int q = lo; q < hi; q += 8) {
           const ulonglong2 a0 = k2[(q >> 1) + 0], a1 = k2[(q >> 1) + 1];
           const ulonglong2 a2 = k2[(q >> 1) + 2], a3 = k2[(q >> 1) + 3];
           const uint4 b0 = t4[(q >> 2) + 0], b1 = t4[(q >> 2) + 1];
@@ -348,7 +367,8 @@ tree_kernel(const TreeArgs A) {
           rank += (a3.x > sq || (a3.x == sq && b1.z > tq)) ? 1 : 0;
           rank += (a3.y > sq || (a3.y == sq && b1.w > tq)) ? 1 : 0;
         }
-        if (rank < nsel) {
+        if (parts == 2) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, 1);
+        if (live && part == 0 && rank < nsel) {
           sel_s[rank] = sq;
           sel_t[rank] = tq;
         }
@@ -494,7 +514,8 @@ tree_kernel(const TreeArgs A) {
         }
         if (!last) {
           // key of child (x, c2): (Zp + base) * invT + lam * (Gp + g), as in child()
-          const double ZinvT = __dmul_rn(__dadd_rn(Zp, Rn.rb[c2]), invT);
+          const double Zc = __dadd_rn(Zp, Rn.rb[c2]);
+          const double ZinvT = unit_T ? Zc : __dmul_rn(Zc, invT);
           double G = Gp;
           if (n > 0) {
             float g = 0.f;

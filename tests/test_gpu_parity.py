@@ -234,6 +234,28 @@ def test_workspace_serves_repeated_calls(D):
     assert D.device_error(ws) == 0 and _control_clean(ws)
 
 
+def test_one_workspace_serves_calls_of_different_shapes(D):
+    """One buffer, passed with the same size to calls of different batch,
+    vocabulary and element type: the arrival counters sit where no call's
+    other data goes, so every call starts from clean counters."""
+    cases = [synth.make_config(2, seed=7, B=6, M=1 << 14),
+             synth.make_config(0, seed=7),
+             synth.make_config(2, seed=8, B=2, M=1 << 14),
+             synth.make_config(3, seed=7, B=12, M=1 << 14),
+             synth.make_config(4, seed=7, B=2, V=20011, M=1 << 14, dtype="f16"),
+             synth.make_config(2, seed=7, B=6, M=1 << 14)]
+    need = max(D.workspace_bytes(c.B, c.d, c.V, D.DTYPE_CODES()[parity.to_device(c).dtype], c.k) for c in cases)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    for case in cases:
+        z = parity.to_device(case)
+        tab, ctx = parity.gpu_table(case)
+        out = D.tree_build(z, case.T, case.k, case.W, case.lam, case.beta, table=tab, ctx=ctx, workspace=ws)
+        assert D.device_error(ws) == 0
+        got = {key: _np(v) for key, v in out.items() if key != "workspace" and v is not None}
+        ref = oracle.tree_build(case)
+        assert parity.compare_all(case, got, ref, ref["ngram"])["exact"] == case.B
+
+
 # ------------------------------------------------------- greedy decoding, T = 0
 
 @pytest.mark.parametrize("cfg,over", [

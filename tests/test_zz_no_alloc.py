@@ -77,11 +77,15 @@ def test_noalloc_binding_and_error_readout(D):
     """A wait limit of 64 SM cycles makes the row pass give up (no fault: the
     warps let their copies land and return); the bit shows up in the internal
     buffer's error word, is cleared by the read, and the next call is exact."""
-    case = synth.make_config(1, seed=3, V=151936, M=1 << 12)
+    case = synth.make_config(2, seed=3, B=8, M=1 << 12)
     z = parity.to_device(case)
     tab, ctx = parity.gpu_table(case)
+    # the logits come from HBM, not from L2, so no bulk copy can land within
+    # the first waits' 64 cycles
+    flush = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
     D.set_wait_limit(64)
     try:
+        flush.mul_(1.0)
         D.tree_build_noalloc(z, case.T, case.k, case.W, case.lam, case.beta, table=tab, ctx=ctx)
         flags = D.noalloc_device_error()
     finally:

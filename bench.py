@@ -504,6 +504,28 @@ def measure(L, D, torch, case, dev, stream, steps, warmup, world, with_select=Fa
         res["select"] = {"budget": budget, "us_per_call": sel_ms * 1e3, "trees_per_s": B * world / (sel_ms / 1e3),
                          "kernel": "select_kernel (best-first verification tree)", "calls": len(sel_times),
                          "device_error": int(sel_err.item())}
+        # the same verification tree chosen inside the tree kernel
+        # (dart_tree_build_verify): the whole step with it, against without
+        Mp = budget
+        vout = [torch.empty((B, Mp), dtype=torch.int32, device=dev) for _ in range(4)]
+        vmask = torch.empty((B, Mp, (Mp + 31) // 32), dtype=torch.int32, device=dev)
+        vsc = torch.empty((B, Mp), dtype=torch.float32, device=dev)
+        tab = builder.table
+        P = lambda t: C.c_void_p(t.data_ptr())
+
+        def build_verify(i):
+            assert L.dart_tree_build_verify(
+                P(z), B, d, V, V, code, float(case.T), k, case.W, float(case.lam), float(case.beta),
+                C.byref(tab.desc) if tab is not None else None, P(builder.ctx) if tab is not None else None,
+                P(o["tokens"]), P(o["parents"]), P(o["pos"]), P(o["mask"]), P(o["scores"]), Mp,
+                P(vout[0]), P(vout[1]), P(vout[2]), P(vout[3]), P(vmask), P(vsc), P(ws), ws.numel(), sp) == 0
+
+        ver_times = timed(build_verify, min(steps, 200))
+        ver_ms = max_over_ranks(statistics.mean(ver_times), world)
+        assert D.device_error(builder.ws) == 0, "device error in the verify steps"
+        res["select"]["fused_in_tree_kernel"] = {
+            "entry": "dart_tree_build_verify", "step_ms": ver_ms,
+            "extra_us_over_step": (ver_ms - res["step_ms"]) * 1e3, "calls": len(ver_times)}
     return res
 
 

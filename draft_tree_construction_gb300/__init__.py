@@ -66,6 +66,9 @@ def _declare(L):
     L.dart_tree_build.argtypes = [P, i32, i32, i32, i32, f32, i32, i32, f32, f32, T, P,
                                   P, P, P, P, P, P, sz, P]
     L.dart_tree_build.restype = i32
+    L.dart_tree_build_verify.argtypes = [P, i32, i32, i32, i64, i32, f32, i32, i32, f32, f32, T, P,
+                                         P, P, P, P, P, i32, P, P, P, P, P, P, P, sz, P]
+    L.dart_tree_build_verify.restype = i32
     L.dart_tree_build_noalloc.argtypes = [P, i32, i32, i32, i32, f32, i32, i32, f32, f32, T, P,
                                           P, P, P, P, P, P]
     L.dart_tree_build_noalloc.restype = i32
@@ -363,9 +366,19 @@ def _tree_inputs(logits, k, W, table, ctx, out, extra=()):
     return dev, B, d, V, N, MW
 
 
+def _verify_outputs(B, Mp, device, scores: bool):
+    torch = _torch()
+    return dict(index=torch.empty((B, Mp), dtype=torch.int32, device=device),
+                tokens=torch.empty((B, Mp), dtype=torch.int32, device=device),
+                parents=torch.empty((B, Mp), dtype=torch.int32, device=device),
+                pos=torch.empty((B, Mp), dtype=torch.int32, device=device),
+                mask=torch.empty((B, Mp, (Mp + 31) // 32), dtype=torch.int32, device=device),
+                scores=torch.empty((B, Mp), dtype=torch.float32, device=device) if scores else None)
+
+
 def tree_build(logits, T: float, k: int, W: int, lam: float, beta: float,
                table: NGramTable | None = None, ctx=None, *, out: dict | None = None,
-               workspace=None, stream=None, scores: bool = True) -> dict:
+               workspace=None, stream=None, scores: bool = True, verify_budget: int | None = None) -> dict:
     """logits: CUDA [B, d, V] float32/float16/bfloat16 -> dict of CUDA outputs.
 
     The rows may be a view of a padded vocabulary (z[..., :V] of [B, d, V_pad]):
@@ -373,12 +386,17 @@ def tree_build(logits, T: float, k: int, W: int, lam: float, beta: float,
     storage holding the uint32 bit pattern.  T = 0 is greedy decoding: the
     tree is then scored with log_softmax(z), as at T = 1.  Every tensor
     (logits, ctx, the table, out, workspace) must be on one CUDA device; the
-    call runs with that device current."""
+    call runs with that device current.  With verify_budget = M the same
+    kernels also choose each tree's best-first verification tree of min(M, N)
+    nodes (dart_tree_build_verify), returned under "verify" with the keys of
+    tree_select."""
     torch = _torch()
     dev, B, d, V, N, MW = _tree_inputs(logits, k, W, table, ctx, out, (("workspace", workspace),))
     stride = _row_stride(logits)
     code = DTYPE_CODES()[logits.dtype]
     need = workspace_bytes(B, d, V, code, k)
+    if verify_budget is not None and int(verify_budget) < 1:
+        raise DartError("verify_budget must be >= 1")
     with _on_device(dev):
         o = out if out is not None else _outputs(B, N, MW, dev, scores)
         if workspace is not None:
@@ -386,12 +404,23 @@ def tree_build(logits, T: float, k: int, W: int, lam: float, beta: float,
             ws = workspace
         else:
             ws = torch.zeros(max(need, 1), dtype=torch.uint8, device=dev)
-        rc = lib().dart_tree_build_strided(_ptr(logits), B, d, V, stride, code, float(T), k, W,
-                                           float(lam), float(beta), *_table_args(table, ctx),
-                                           _ptr(o["tokens"]), _ptr(o["parents"]), _ptr(o["pos"]),
-                                           _ptr(o["mask"]), _ptr(o.get("scores")), _ptr(ws),
-                                           ws.numel() * ws.element_size(), _stream_ptr(stream, dev))
-    _check(rc, "dart_tree_build_strided")
+        outs = (_ptr(o["tokens"]), _ptr(o["parents"]), _ptr(o["pos"]), _ptr(o["mask"]), _ptr(o.get("scores")))
+        if verify_budget is None:
+            rc = lib().dart_tree_build_strided(_ptr(logits), B, d, V, stride, code, float(T), k, W,
+                                               float(lam), float(beta), *_table_args(table, ctx), *outs,
+                                               _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream, dev))
+            what = "dart_tree_build_strided"
+        else:
+            M = int(verify_budget)
+            v = _verify_outputs(B, min(M, N), dev, scores)
+            rc = lib().dart_tree_build_verify(_ptr(logits), B, d, V, stride, code, float(T), k, W,
+                                              float(lam), float(beta), *_table_args(table, ctx), *outs, M,
+                                              _ptr(v["index"]), _ptr(v["tokens"]), _ptr(v["parents"]),
+                                              _ptr(v["pos"]), _ptr(v["mask"]), _ptr(v["scores"]),
+                                              _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream, dev))
+            what = "dart_tree_build_verify"
+            o["verify"] = v
+    _check(rc, what)
     o["workspace"] = ws
     return o
 

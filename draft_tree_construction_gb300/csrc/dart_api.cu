@@ -82,14 +82,30 @@ TreeArgs tree_args(int B, int d, int k, int W, float lambda, float beta,
   a.out_mask = out_mask;
   a.out_scores = out_scores;
   a.ctrl = nullptr;
+  a.M = 0;
+  a.v_index = a.v_tokens = a.v_parents = a.v_pos = nullptr;
+  a.v_mask = nullptr;
+  a.v_scores = nullptr;
   return a;
 }
+
+// The verification tree's outputs of dart_tree_build_verify.
+struct VerifyOut {
+  int M;
+  int32_t* index;
+  int32_t* tokens;
+  int32_t* parents;
+  int32_t* pos;
+  uint32_t* mask;
+  float* scores;
+};
 
 // The whole path on a workspace: the row pass, then the tree kernel.
 int launch_path(const void* logits, int B, int d, int V, int64_t row_stride, int dtype, float T, int k, int W,
                 float lambda, float beta, const dart_ngram_table_t* ngram_table, const int32_t* ctx_tokens,
                 int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos, uint32_t* out_mask,
-                float* out_scores, uint8_t* ws, const WsLayout& L, cudaStream_t s) {
+                float* out_scores, uint8_t* ws, const WsLayout& L, cudaStream_t s,
+                const VerifyOut* verify = nullptr) {
   const long long R = (long long)B * d;
   if (launch_rows(logits, R, V, row_stride, dtype, T, k, ws, L, nullptr, nullptr, nullptr, s) != cudaSuccess)
     return DART_ERR_CUDA;
@@ -100,6 +116,15 @@ int launch_path(const void* logits, int B, int d, int V, int64_t row_stride, int
   a.off = reinterpret_cast<const double*>(ws + L.row_off);
   a.invT = 1.0 / double(T);
   a.ctrl = reinterpret_cast<uint32_t*>(ws + L.ctrl);
+  if (verify) {
+    a.M = verify->M;
+    a.v_index = verify->index;
+    a.v_tokens = verify->tokens;
+    a.v_parents = verify->parents;
+    a.v_pos = verify->pos;
+    a.v_mask = verify->mask;
+    a.v_scores = verify->scores;
+  }
   if (launch_tree(a, s) != cudaSuccess) return DART_ERR_CUDA;
   return DART_OK;
 }
@@ -238,6 +263,35 @@ int dart_tree_build_strided(const void* logits, int B, int d, int V, int64_t row
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   return launch_path(logits, B, d, V, row_stride, dtype, T, k, W, lambda, beta, ngram_table, ctx_tokens,
                      out_tokens, out_parents, out_pos, out_mask, out_scores, ws, L, s);
+}
+
+int dart_tree_build_verify(const void* logits, int B, int d, int V, int64_t row_stride, int dtype,
+                           float T, int k, int W, float lambda, float beta,
+                           const dart_ngram_table_t* ngram_table, const int32_t* ctx_tokens,
+                           int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
+                           uint32_t* out_mask, float* out_scores, int M, int32_t* out_vindex,
+                           int32_t* out_vtokens, int32_t* out_vparents, int32_t* out_vpos,
+                           uint32_t* out_vmask, float* out_vscores,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_tree_shape(B, d, k, W, lambda, beta);
+  if (rc) return rc;
+  if (V < 2 || V > kMaxV || k > V || !valid_dtype(dtype)) return DART_ERR_INVALID_ARG;
+  if (row_stride < V || row_stride > kMaxRowStride) return DART_ERR_INVALID_ARG;
+  if (!score_temperature(&T)) return DART_ERR_INVALID_ARG;
+  if (M < 1) return DART_ERR_INVALID_ARG;
+  if ((rc = check_table(ngram_table, ctx_tokens, B))) return rc;
+  if (B == 0) return DART_OK;
+  if (!logits || !aligned(logits, 16)) return DART_ERR_INVALID_ARG;
+  if (!out_tokens || !out_parents || !out_pos || !out_mask) return DART_ERR_INVALID_ARG;
+  if (!out_vindex || !out_vtokens || !out_vparents || !out_vpos || !out_vmask) return DART_ERR_INVALID_ARG;
+  WsLayout L;
+  const long long R = (long long)B * d;
+  if (!ws_layout(R, V, elem_bytes(dtype), k, &L)) return DART_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return DART_ERR_WORKSPACE;
+  const VerifyOut verify{M, out_vindex, out_vtokens, out_vparents, out_vpos, out_vmask, out_vscores};
+  return launch_path(logits, B, d, V, row_stride, dtype, T, k, W, lambda, beta, ngram_table, ctx_tokens,
+                     out_tokens, out_parents, out_pos, out_mask, out_scores, static_cast<uint8_t*>(workspace), L,
+                     static_cast<cudaStream_t>(stream), &verify);
 }
 
 int dart_tree_build_noalloc(const void* logits, int B, int d, int V, int dtype,

@@ -39,6 +39,14 @@ struct TreeArgs {
   uint32_t* out_mask;
   float* out_scores;
   uint32_t* ctrl;              // device error word or nullptr
+  // the best-first verification tree of budget M (M = 0: none), [B][min(M, N)]
+  int M;
+  int32_t* v_index;
+  int32_t* v_tokens;
+  int32_t* v_parents;
+  int32_t* v_pos;
+  uint32_t* v_mask;            // [B][min(M, N)][ceil(min(M, N) / 32)]
+  float* v_scores;             // or nullptr
 };
 
 cudaError_t launch_tree(const TreeArgs& a, cudaStream_t stream);

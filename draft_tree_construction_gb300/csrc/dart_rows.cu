@@ -11,7 +11,9 @@
 // span through its own ring of three 4 KiB shared-memory stages, filled by
 // bulk copies (cp.async.bulk, L2 evict-first) that its lane 0 issues three
 // stages ahead of the stage being reduced.  A span may cover the end of one
-// row and the start of the next; each (warp, row) overlap is a piece.
+// row and the start of the next; each (warp, row) overlap is a piece.  Spans
+// are at least 8 KiB; an input with fewer spans than 152 x 12 warps deals
+// them round-robin over one CTA per SM, so that every SM streams a share.
 //
 // Per stage a lane holds eight 16-byte vectors.  One packed maximum per
 // vector (bf16x2 / f16x2 max on 16-bit types) feeds one running-max update
@@ -37,6 +39,9 @@
 // bound (the largest of the pieces' bounds and, with k or more pieces, the
 // k-th largest piece maximum), keeps the candidate elements that reach it and
 // ranks them (each key counts the keys above it) to get the row's k best.
+// When one round of loads holds every slot entry of the row, headers and
+// entries are read together; otherwise the headers come first and only the
+// pieces whose maximum reaches the bound have their entries gathered.
 //
 // Every wait (a stage landing) is bounded: on a timeout the warp records the
 // error bit, lets its copies in flight land and returns; the call's results

@@ -17,6 +17,8 @@
 
 namespace dart {
 
+#include "dart_select.cuh"
+
 constexpr int kTreeThreads = 512;
 constexpr uint32_t kTieMax = 0xFFFFFu;      // (parent rank << 5 | token rank) < 2^11
 
@@ -127,6 +129,7 @@ __host__ __device__ inline int tree_pad(int W, int k) {
   return (W * k + run - 1) / run * run;
 }
 constexpr int kRankMax = 256;   // up to this many children a depth selects by ranking
+constexpr int kGroup = 4;       // sorted runs one warp folds together per merge round
 // Threads per tree: one per child of a full frontier, 32..512.  (Two per
 // child would halve the ranking loop, but at 122 registers a thread it
 // leaves one CTA per SM for 320 threads: two waves for 256 trees.)
@@ -135,7 +138,7 @@ inline int tree_threads(int W, int k) {
   return t < 32 ? 32 : (t > kTreeThreads ? kTreeThreads : t);
 }
 
-inline size_t tree_smem_bytes(int d, int W, int k, int MW) {
+inline size_t tree_smem_bytes(int d, int W, int k, int MW, int N, bool select) {
   const size_t np = size_t(tree_pad(W, k));
   const size_t dk = size_t(d) * k;
   size_t b = 0;
@@ -150,6 +153,7 @@ inline size_t tree_smem_bytes(int d, int W, int k, int MW) {
   b += 2 * kMaxW * 3 * sizeof(int);               // frontier n-gram contexts
   b += 2 * size_t(kMaxW) * MW * sizeof(uint32_t); // frontier mask rows
   b += 3 * align_up(dk * sizeof(int), 16);        // ids, token ranks, inverse ranks of every row
+  if (select) b += select_shared_bytes(N);          // the verification tree's selection
   return b + 64;
 }
 
@@ -214,6 +218,20 @@ tree_kernel(const TreeArgs A) {
   int* rows_id = reinterpret_cast<int*>(take(size_t(dk) * sizeof(int)));
   int* rows_rank = reinterpret_cast<int*>(take(size_t(dk) * sizeof(int)));
   int* rows_inv = reinterpret_cast<int*>(take(size_t(dk) * sizeof(int)));
+  // the verification tree's selection (only with a budget)
+  SelectShared S{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  float* sel_score = nullptr;
+  int32_t* sel_par = nullptr;
+  if (A.M > 0) {
+    S.key = reinterpret_cast<uint64_t*>(take(size_t(N) * 8));
+    sel_score = reinterpret_cast<float*>(take(size_t(N) * 4));
+    sel_par = reinterpret_cast<int32_t*>(take(size_t(N) * 4));
+    S.fresh = reinterpret_cast<int32_t*>(take(size_t(N) * 4));
+    S.npar = reinterpret_cast<int32_t*>(take(size_t(N) * 4));
+    S.chunk = reinterpret_cast<uint32_t*>(take(size_t(kMaxN / 32) * 4));
+    S.score = sel_score;
+    S.parent = sel_par;
+  }
   auto row = [&](int j) {
     RowBuf r;
     r.rid = rows_id + j * k;
@@ -399,34 +417,34 @@ tree_kernel(const TreeArgs A) {
         }
       }
       __syncthreads();
-      // merge runs pairwise, keeping the best RUN keys of each pair
+      // merge runs in groups of kGroup: each warp folds a group's runs into
+      // one run in registers (the best RUN keys so far, merged with the next
+      // run reversed), so a round costs one barrier for kGroup runs
       uint64_t* ks_src = keys;
       uint32_t* kt_src = ties;
       ks_dst = (keys == ks_a) ? ks_b : ks_a;
       kt_dst = (ties == kt_a) ? kt_b : kt_a;
       while (nr > 1) {
-        const int nout = (nr + 1) >> 1;
+        const int nout = (nr + kGroup - 1) / kGroup;
         for (int t = warp; t < nout; t += nwarps) {
           CKey v[R];
-          if (2 * t + 1 < nr) {
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const int e = r * 32 + lane;
+            v[r].s = ks_src[(t * kGroup) * RUN + e];
+            v[r].t = kt_src[(t * kGroup) * RUN + e];
+          }
+          for (int f = 1; f < kGroup && t * kGroup + f < nr; ++f) {
+            const int run = t * kGroup + f;
 #pragma unroll
             for (int r = 0; r < R; ++r) {
               const int e = r * 32 + lane;
-              CKey x, y;
-              x.s = ks_src[(2 * t) * RUN + e];
-              x.t = kt_src[(2 * t) * RUN + e];
-              y.s = ks_src[(2 * t + 1) * RUN + (RUN - 1 - e)];
-              y.t = kt_src[(2 * t + 1) * RUN + (RUN - 1 - e)];
-              v[r] = ck_gt(y, x) ? y : x;
+              CKey y;
+              y.s = ks_src[run * RUN + (RUN - 1 - e)];
+              y.t = kt_src[run * RUN + (RUN - 1 - e)];
+              if (ck_gt(y, v[r])) v[r] = y;
             }
             run_merge_desc<R>(v);
-          } else {
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-              const int e = r * 32 + lane;
-              v[r].s = ks_src[(2 * t) * RUN + e];
-              v[r].t = kt_src[(2 * t) * RUN + e];
-            }
           }
 #pragma unroll
           for (int r = 0; r < R; ++r) {
@@ -504,7 +522,14 @@ tree_kernel(const TreeArgs A) {
           A.out_tokens[o] = tok;
           A.out_parents[o] = j == 0 ? -1 : fnode_cur[i];
           A.out_pos[o] = j + 1;
-          if (A.out_scores) A.out_scores[o] = float(__dsub_rn(unord_f64(ks), Lsum));
+          if (A.out_scores || A.M > 0) {
+            const float sc = float(__dsub_rn(unord_f64(ks), Lsum));
+            if (A.out_scores) A.out_scores[o] = sc;
+            if (A.M > 0) {
+              sel_score[node] = sc;
+              sel_par[node] = j == 0 ? -1 : fnode_cur[i];
+            }
+          }
           fZ_nxt[x] = Zp;
           fG_nxt[x] = Gp;
           fnode_nxt[x] = node;
@@ -546,11 +571,21 @@ tree_kernel(const TreeArgs A) {
     node_base += nsel;
     __syncthreads();
   }
+  if (A.M > 0) {
+    // the verification tree chosen best-first from the tree just built
+    __syncthreads();
+    const int Mp = A.M < N ? A.M : N;
+    const size_t ob = (size_t)b * Mp;
+    const size_t tb = (size_t)b * N;
+    select_best_first(N, Mp, S, A.out_tokens + tb, A.out_pos + tb, A.v_index + ob, A.v_tokens + ob,
+                      A.v_parents + ob, A.v_pos + ob, A.v_mask + ob * ((Mp + 31) / 32),
+                      A.v_scores ? A.v_scores + ob : nullptr, A.ctrl);
+  }
 }
 
 cudaError_t launch_tree(const TreeArgs& a, cudaStream_t stream) {
   if (a.B == 0) return cudaSuccess;
-  const size_t smem = tree_smem_bytes(a.d, a.W, a.k, a.MW);
+  const size_t smem = tree_smem_bytes(a.d, a.W, a.k, a.MW, a.N, a.M > 0);
   const int threads = tree_threads(a.W, a.k);
   cudaError_t e;
   if (a.W <= 32) {

@@ -165,6 +165,25 @@ int dart_tree_build_strided(const void* logits, int B, int d, int V, int64_t row
                             uint32_t* out_mask, float* out_scores,
                             void* workspace, size_t workspace_bytes, void* stream);
 
+/* dart_tree_build_strided that also emits the best-first verification tree
+ * of budget M >= 1 (dart_tree_select's result on the candidate trees, with
+ * the same reading and outputs), chosen by each tree's CTA right after it has
+ * built the tree, so no second launch reads the candidate trees back:
+ *  out_vindex, out_vtokens, out_vparents, out_vpos  device int32 [B][M'],
+ *  out_vmask device uint32 [B][M'][ceil(M'/32)], out_vscores device float
+ *  [B][M'] or NULL; M' = min(M, N).
+ * A node that outscores its parent sets DART_DEVERR_SCORE_RISES in the
+ * workspace's error word (as dart_tree_select does in its device_err).
+ * Every other argument as for dart_tree_build_strided. */
+int dart_tree_build_verify(const void* logits, int B, int d, int V, int64_t row_stride, int dtype,
+                           float T, int k, int W, float lambda, float beta,
+                           const dart_ngram_table_t* ngram_table, const int32_t* ctx_tokens,
+                           int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
+                           uint32_t* out_mask, float* out_scores, int M, int32_t* out_vindex,
+                           int32_t* out_vtokens, int32_t* out_vparents, int32_t* out_vpos,
+                           uint32_t* out_vmask, float* out_vscores,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
 /* dart_tree_build without a workspace argument, for callers that cannot
  * allocate device memory: an engine whose own pool allocator has reserved
  * the device's memory (a side cudaMalloc would fail or fragment it), a

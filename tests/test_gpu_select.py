@@ -110,3 +110,35 @@ def test_whole_path_then_select(D, cfg, over, M):
             assert sel[key][b].cpu().tolist() == ref[key][b].tolist(), (b, key)
         assert np.array_equal(sel["mask"][b].cpu().numpy().view(np.uint32), ref["mask"][b])
     assert checked >= max(1, B // 2)
+
+
+@pytest.mark.parametrize("cfg,over", [
+    (0, {}),
+    (2, dict(B=8, M=1 << 16)),
+    (3, dict(B=32, M=1 << 16)),
+    (4, dict(B=4, M=1 << 18)),
+    (2, dict(B=4, M=1 << 14, T=0.0)),
+])
+def test_tree_build_emits_the_verification_tree(D, cfg, over):
+    """dart_tree_build_verify: the tree kernel chooses each tree's verification
+    tree right after building it.  Its result must be the oracle's selection
+    on the candidate trees the same call returned (bit-exact), for budgets
+    from 1 to past N; the candidate trees must equal those of tree_build."""
+    case = synth.make_config(cfg, seed=31, **over)
+    z = parity.to_device(case)
+    tab, ctx = parity.gpu_table(case)
+    plain = D.tree_build(z, case.T, case.k, case.W, case.lam, case.beta, table=tab, ctx=ctx)
+    N = plain["parents"].shape[1]
+    for M in sorted({1, 7, 16, N // 2, N, N + 5}):
+        out = D.tree_build(z, case.T, case.k, case.W, case.lam, case.beta, table=tab, ctx=ctx, verify_budget=M)
+        assert D.device_error(out["workspace"]) == 0
+        for key in ("tokens", "parents", "pos", "mask", "scores"):
+            assert torch.equal(out[key], plain[key]), key
+        tree = {key: out[key].cpu().numpy() for key in ("tokens", "parents", "pos", "scores")}
+        want = oracle.select_tree(tree["tokens"], tree["parents"], tree["pos"], tree["scores"].astype(np.float64), M)
+        v = out["verify"]
+        for key in ("index", "tokens", "parents", "pos"):
+            assert np.array_equal(v[key].cpu().numpy(), want[key]), (M, key)
+        assert np.array_equal(v["mask"].cpu().numpy().view(np.uint32), want["mask"]), M
+        gathered = np.take_along_axis(tree["scores"], want["index"].astype(np.int64), axis=1)
+        assert np.array_equal(v["scores"].cpu().numpy(), gathered)

@@ -529,6 +529,42 @@ def measure(L, D, torch, case, dev, stream, steps, warmup, world, with_select=Fa
     return res
 
 
+def numa_placement(index: int) -> dict:
+    """NUMA node of the GPU (from its PCI device in sysfs) and the nodes of the
+    CPUs this process may run on (the pinned host buffers are first touched
+    there), so the host link's rate can be read against their placement."""
+    out = {"gpu_numa_node": None, "process_cpu_numa_nodes": None, "gpu_pci_bus_id": None}
+    try:
+        bus = subprocess.run(["nvidia-smi", "-i", str(index), "--query-gpu=pci.bus_id", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout.strip()
+        out["gpu_pci_bus_id"] = bus or None
+        if bus:
+            path = f"/sys/bus/pci/devices/{bus[-12:].lower()}/numa_node"
+            out["gpu_numa_node"] = int(open(path).read().strip())
+    except (OSError, ValueError, subprocess.SubprocessError):
+        pass
+    try:
+        cpus = os.sched_getaffinity(0)
+        nodes = []
+        base = "/sys/devices/system/node"
+        for name in sorted(os.listdir(base)):
+            if not name.startswith("node") or not name[4:].isdigit():
+                continue
+            ids = set()
+            for part in open(os.path.join(base, name, "cpulist")).read().strip().split(","):
+                if "-" in part:
+                    a, b = part.split("-")
+                    ids.update(range(int(a), int(b) + 1))
+                elif part:
+                    ids.add(int(part))
+            if ids & cpus:
+                nodes.append(int(name[4:]))
+        out["process_cpu_numa_nodes"] = nodes
+    except (OSError, ValueError):
+        pass
+    return out
+
+
 def stream_ceiling(L, torch, nbytes, dev, stream, steps):
     """The bulk-copy ring of the row pass (twelve warps x three 4 KiB stages
     per SM) with no arithmetic, on a buffer of the logits' size: the
@@ -591,13 +627,8 @@ def run_ours(args):
             b.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs), world)
-        numa = None
-        try:
-            numa = open(f"/sys/bus/pci/devices/{torch.cuda.get_device_properties(dev).pci_bus_id.lower()}/numa_node").read().strip()
-        except (OSError, AttributeError):
-            pass
         e2e = {"value": B * world / (e2e_ms / 1e3), "unit": "trees/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "gpu_numa_node": numa}
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, **numa_placement(dev.index or 0)}
 
     achieved = logit_bytes / (k1_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",

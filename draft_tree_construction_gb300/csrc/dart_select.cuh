@@ -45,10 +45,10 @@ __host__ __device__ inline size_t select_shared_bytes(int N) {
 // out_*: the tree's rows of the outputs (Mp entries, masks Mp x ceil(Mp/32)).
 // Every thread of the CTA takes part; the caller has filled S.score and
 // S.parent and passed a barrier.
-__device__ void select_best_first(int N, int Mp, const SelectShared& S, const int32_t* tokens,
-                                  const int32_t* pos, int32_t* out_index, int32_t* out_tokens,
-                                  int32_t* out_parents, int32_t* out_pos, uint32_t* out_mask,
-                                  float* out_scores, uint32_t* err) {
+static __device__ void select_best_first(int N, int Mp, const SelectShared& S, const int32_t* tokens,
+                                         const int32_t* pos, int32_t* out_index, int32_t* out_tokens,
+                                         int32_t* out_parents, int32_t* out_pos, uint32_t* out_mask,
+                                         float* out_scores, uint32_t* err) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthreads = blockDim.x, nwarps = nthreads >> 5;
   for (int i = tid; i < N; i += nthreads) {

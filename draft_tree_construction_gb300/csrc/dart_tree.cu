@@ -128,7 +128,7 @@ __host__ __device__ inline int tree_pad(int W, int k) {
   const int run = tree_run_len(W);
   return (W * k + run - 1) / run * run;
 }
-constexpr int kRankMax = 256;   // up to this many children a depth selects by ranking
+constexpr int kRankMax = 128;   // up to this many children a depth selects by ranking (more: sorted runs)
 constexpr int kGroup = 4;       // sorted runs one warp folds together per merge round
 // Threads per tree: one per child of a full frontier, 32..512.  (Two per
 // child would halve the ranking loop, but at 122 registers a thread it

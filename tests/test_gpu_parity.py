@@ -335,3 +335,33 @@ def test_ngram_lookup_matches_oracle(D):
     rv, rf = ng.lookup(q)
     np.testing.assert_array_equal(_np(found), rf)
     np.testing.assert_array_equal(_np(vals)[rf], rv[rf])
+
+
+def test_tree_builder_replays_in_a_cuda_graph(D):
+    """The whole path launches no allocation, copy or host synchronisation,
+    so a fixed-shape builder call can be captured in a CUDA graph (as a
+    decode loop does) and replayed on new logits with results identical to
+    eager calls."""
+    cases = [synth.make_config(2, seed=s, B=8, M=1 << 14) for s in (40, 41)]
+    za, zb = parity.to_device(cases[0]), parity.to_device(cases[1])
+    tab, ctx = parity.gpu_table(cases[0])
+    c = cases[0]
+    b = D.TreeBuilder(c.B, c.d, c.V, za.dtype, c.T, c.k, c.W, c.lam, c.beta, table=tab, ctx=ctx)
+    z = za.clone()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        b(z, stream=stream)                      # warm-up outside the capture
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        b(z, stream=torch.cuda.current_stream())
+    for src in (za, zb, za):
+        z.copy_(src)
+        graph.replay()
+        torch.cuda.synchronize()
+        got = {key: v.clone() for key, v in b.out.items() if v is not None}
+        eager = D.tree_build(src, c.T, c.k, c.W, c.lam, c.beta, table=tab, ctx=ctx)
+        for key in ("tokens", "parents", "pos", "mask", "scores"):
+            assert torch.equal(got[key], eager[key]), key
+    assert D.device_error(b.ws) == 0

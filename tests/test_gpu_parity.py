@@ -365,3 +365,18 @@ def test_tree_builder_replays_in_a_cuda_graph(D):
         for key in ("tokens", "parents", "pos", "mask", "scores"):
             assert torch.equal(got[key], eager[key]), key
     assert D.device_error(b.ws) == 0
+
+
+@pytest.mark.parametrize("shape", [
+    dict(B=2, d=32, V=300, k=32, W=32, n=4, M=2000),   # N = 1024 nodes (the limit), 32 mask words per row
+    dict(B=3, d=32, V=97, k=2, W=32, n=2, M=2000),     # 32 depths of two candidates, W reached at depth 5
+    dict(B=4, d=1, V=2, k=2, W=1, n=2, M=2),           # the smallest vocabulary, one depth, one survivor
+    dict(B=2, d=3, V=5, k=5, W=64, n=3, M=40),         # k = V: every token is a candidate, nothing pruned
+])
+def test_whole_path_at_the_size_limits(D, shape):
+    case = synth.make_case(dtype="bf16", T=0.9, lam=0.4, beta=-9.0, recipe=("normal", 3.0), seed=77, **shape)
+    assert D.num_nodes(case.d, case.k, case.W) <= 1024
+    got = _run_full(D, case)
+    ref = oracle.tree_build(case)
+    stats = parity.compare_all(case, got, ref, ref["ngram"])
+    assert stats["exact"] == case.B

@@ -111,6 +111,28 @@ struct __align__(128) RowSmem {
 };
 
 // ------------------------------------------------------------- element types
+// Two floats in one 64-bit register pair, for the packed f32x2 operations
+// (each lane of fma.rn.f32x2 / add.rn.f32x2 rounds as fma.rn.f32 / add.rn.f32).
+__device__ __forceinline__ uint64_t pack_f32x2(float x, float y) {
+  uint64_t v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(x), "f"(y));
+  return v;
+}
+__device__ __forceinline__ float2 unpack_f32x2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -434,22 +456,23 @@ __device__ __forceinline__ void stage_reduce(Acc& a, uint32_t& tau_o, int& cnt, 
     }
     tau_o = o;
   }
-  // one fused multiply-add, one exponential and one add per element, into
+  // one fused multiply-add, one exponential and one add per element, the
+  // multiply-adds and adds two elements to an instruction (f32x2), into
   // eight independent sums (element e of every vector goes to sum e)
-  const float nmc = -a.mc;
-  float acc[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+  const uint64_t c2 = pack_f32x2(c, c), nmc2 = pack_f32x2(-a.mc, -a.mc);
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
   for (int u = 0; u < U; ++u) {
 #pragma unroll
     for (int p = 0; p < EPV / 2; ++p) {
       const float2 z = E::pair(r[u], p);
-      acc[(2 * p) & 7] += ex2_approx(fmaf(z.x, c, nmc));
-      acc[(2 * p + 1) & 7] += ex2_approx(fmaf(z.y, c, nmc));
+      const float2 t = unpack_f32x2(fma_f32x2(pack_f32x2(z.x, z.y), c2, nmc2));
+      acc[p & 3] = add_f32x2(acc[p & 3], pack_f32x2(ex2_approx(t.x), ex2_approx(t.y)));
     }
   }
-  a.s += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+  const float2 s01 = unpack_f32x2(acc[0]), s23 = unpack_f32x2(acc[1]);
+  const float2 s45 = unpack_f32x2(acc[2]), s67 = unpack_f32x2(acc[3]);
+  a.s += ((s01.x + s01.y) + (s23.x + s23.y)) + ((s45.x + s45.y) + (s67.x + s67.y));
   // candidates: absent vectors hold -inf, which must not pass while tau is -inf
   const float tau = tau_value(tau_o);
   if (__ballot_sync(kFull, lane < nv && vm >= tau) != 0u) {
@@ -782,6 +805,24 @@ __device__ __forceinline__ void finish_row(const RowsParams& P, long long r, flo
 // are gathered (eight per lane per round trip) and the keys of the elements
 // that reach the bound go through the warp's key stage, the k best kept
 // whenever it could overflow.  `lists` holds 2 * kMergeSel + 1 ints.
+// The k-th largest of the warp's values (two per lane, ordered floats; 0 =
+// no value), or 0 when fewer than k are nonzero: k rounds of a warp maximum,
+// each removing one occurrence of the value it found.  Registers only.
+__device__ __forceinline__ uint32_t warp_kth_largest2(uint32_t v0, uint32_t v1, int k) {
+  const int lane = threadIdx.x & 31;
+  uint32_t m = 0;
+  for (int i = 0; i < k; ++i) {
+    m = __reduce_max_sync(kFull, v0 > v1 ? v0 : v1);
+    if (m == 0u) return 0u;
+    const uint32_t holder = __ballot_sync(kFull, v0 == m || v1 == m);
+    if (lane == __ffs(holder) - 1) {
+      if (v0 == m) v0 = 0u;
+      else v1 = 0u;
+    }
+  }
+  return m;
+}
+
 constexpr int kMergeSel = 256;   // selected pieces per gathering round
 
 template <int DT>
@@ -854,19 +895,7 @@ __device__ __noinline__ void merge_row_warp(const RowsParams& P, long long r, ui
   for (int o = 16; o > 0; o >>= 1) Sx += __shfl_xor_sync(kFull, Sx, o);
   if (nseg >= k && nseg <= 64) {
     // the k-th largest piece maximum: k pieces each hold an element that high
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t x = om[h];
-      int above = 0, atleast = 0;
-      for (int src = 0; src < 32; ++src) {
-        const uint32_t y0 = __shfl_sync(kFull, om[0], src), y1 = __shfl_sync(kFull, om[1], src);
-        above += (y0 > x ? 1 : 0) + (y1 > x ? 1 : 0);
-        atleast += (y0 >= x ? 1 : 0) + (y1 >= x ? 1 : 0);
-      }
-      if (x != 0u && above < k && atleast >= k) b = max(b, x);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) b = max(b, __shfl_xor_sync(kFull, b, o));
+    b = max(b, warp_kth_largest2(om[0], om[1], k));
   }
   const float tau = tau_value(b);
   const uint32_t otau = b;
@@ -1023,20 +1052,7 @@ row_merge_kernel(const __grid_constant__ RowsParams P) {
                    (h1 ? M.s[lane + 32] * double(ex2_approx((m1 - mx) * P.c)) : 0.0);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
-      if (nseg >= k) {
-        const uint32_t o0 = h0 ? ord_f32(m0) : 0u, o1 = h1 ? ord_f32(m1) : 0u;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t x = h == 0 ? o0 : o1;
-          int above = 0, atleast = 0;
-          for (int src = 0; src < 32; ++src) {
-            const uint32_t y0 = __shfl_sync(kFull, o0, src), y1 = __shfl_sync(kFull, o1, src);
-            above += (y0 > x ? 1 : 0) + (y1 > x ? 1 : 0);
-            atleast += (y0 >= x ? 1 : 0) + (y1 >= x ? 1 : 0);
-          }
-          if (x != 0u && above < k && atleast >= k) b = max(b, x);
-        }
-      }
+      if (nseg >= k) b = max(b, warp_kth_largest2(h0 ? ord_f32(m0) : 0u, h1 ? ord_f32(m1) : 0u, k));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) b = max(b, __shfl_xor_sync(kFull, b, o));
       if (lane == 0) {

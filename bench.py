@@ -356,13 +356,17 @@ def run_probe_stream(args):
         shapes.append((math_, 2, 8, 0))
         for warps, stages in ((8, 4), (8, 6), (12, 3), (12, 4), (16, 3), (6, 8)):
             shapes.append((math_ | 1, 1, warps, stages))
+        # the CTA's warps interleaved over one span
+        for warps, stages in ((8, 4), (12, 3), (16, 3)):
+            shapes.append((math_ | 5, 1, warps, stages))
     clk = clocks_start(0)
     t0 = time.time()
     rows = []
     for mode, per_sm, warps, stages in shapes:
         gbs, ms = stream_probe(L, buf, mode, sms * per_sm, warps, stages, stream, steps=args.steps,
                                flush=lambda: flush_buf.sum())
-        rows.append({"loader": "bulk ring" if mode & 1 else "direct", "math": bool(mode & 2),
+        rows.append({"loader": ("bulk ring, warps interleaved" if mode & 4 else "bulk ring") if mode & 1 else "direct",
+                     "math": bool(mode & 2),
                      "ctas_per_sm": per_sm, "warps_per_cta": warps, "stages": stages,
                      "gbs": gbs, "us": ms * 1e3, "frac_of_peak": gbs / peaks["hbm_gbs"]})
     clocks = clocks_stop(clk, (t0, time.time()))

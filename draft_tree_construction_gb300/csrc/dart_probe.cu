@@ -17,7 +17,9 @@
 // the previous eight are reduced) or through its own ring of 4 KiB
 // shared-memory stages filled by bulk copies (cp.async.bulk) that the warp
 // itself issues.  The results are the ceilings a row pass of either kind can
-// reach on this GPU.
+// reach on this GPU.  The bulk ring can also interleave its warps: the CTA
+// reads one contiguous span, warp w taking its 4 KiB steps w, w + warps,
+// w + 2 warps, ... (fewer, longer sequential streams for the memory system).
 #include "dart_common.cuh"
 
 #include <cfloat>
@@ -48,6 +50,7 @@ struct StreamProbe {
   unsigned long long nvec;   // 16-byte vectors in the buffer
   unsigned long long span;   // vectors per warp (a multiple of 256)
   int stages;                // bulk ring: stages per warp
+  int interleave;            // bulk ring: the CTA's warps share one span, step by step
   float* out;                // one value per warp
   uint32_t* err;             // a bulk wait ran out (bit 0)
 };
@@ -153,8 +156,13 @@ __global__ void __launch_bounds__(1024) stream_probe_bulk(const StreamProbe P) {
   const int wl = threadIdx.x >> 5;
   const int nw = blockDim.x >> 5;
   const unsigned long long gw = (unsigned long long)blockIdx.x * nw + wl;
-  const unsigned long long v0 = gw * P.span;
-  const unsigned long long v1 = min(P.nvec, v0 + P.span);
+  // contiguous: the warp's span [v0, v1), step st at v0 + 256 st; interleaved:
+  // the CTA's span [c0, c1), step st of the warp at c0 + 256 (st nw + wl)
+  const unsigned long long c0 = (unsigned long long)blockIdx.x * nw * P.span;
+  const unsigned long long c1 = min(P.nvec, c0 + nw * P.span);
+  const unsigned long long v0 = P.interleave ? c0 + 256ull * wl : gw * P.span;
+  const unsigned long long v1 = P.interleave ? c1 : min(P.nvec, v0 + P.span);
+  const unsigned long long vstep = P.interleave ? 256ull * nw : 256ull;
   uint8_t* ring = smem_raw + (size_t)wl * P.stages * kProbeStage;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + (size_t)nw * P.stages * kProbeStage) + (size_t)wl * P.stages;
   const uint64_t pol = policy_evict_first();
@@ -163,9 +171,9 @@ __global__ void __launch_bounds__(1024) stream_probe_bulk(const StreamProbe P) {
     fence_mbar_init();
   }
   __syncwarp();
-  const unsigned long long nstep = v0 < v1 ? (v1 - v0 + 255) / 256 : 0;
+  const unsigned long long nstep = v0 < v1 ? (v1 - v0 + vstep - 1) / vstep : 0;
   auto issue = [&](unsigned long long step) {
-    const unsigned long long v = v0 + step * 256;
+    const unsigned long long v = v0 + step * vstep;
     const uint32_t bytes = uint32_t(min(256ull, v1 - v) * 16ull);
     const int s = int(step % (unsigned long long)P.stages);
     mbar_expect_tx(&bars[s], bytes);
@@ -186,7 +194,7 @@ __global__ void __launch_bounds__(1024) stream_probe_bulk(const StreamProbe P) {
       if (lane == 0) atomicOr(P.err, 1u);
       break;
     }
-    const unsigned long long v = v0 + st * 256;
+    const unsigned long long v = v0 + st * vstep;
     const int valid_vecs = int(min(256ull, v1 - v));
     const uint4* src = reinterpret_cast<const uint4*>(ring + (size_t)s * kProbeStage);
     uint4 r[kProbeVec];
@@ -223,7 +231,8 @@ extern "C" int dart_probe_stream(const void* src, uint64_t bytes, int mode, int 
                                  int stages, float* out, uint32_t* device_err, void* stream) {
   using namespace dart;
   if (!src || (reinterpret_cast<uintptr_t>(src) & 15u) || !out || !device_err || ctas < 1 || warps_per_cta < 1 ||
-      warps_per_cta > 32 || mode < 0 || mode > 3 || (!(mode & 1) && warps_per_cta > 16))
+      warps_per_cta > 32 || mode < 0 || mode > 7 || (!(mode & 1) && warps_per_cta > 16) ||
+      ((mode & 4) && !(mode & 1)))
     return DART_ERR_INVALID_ARG;
   const bool bulk = (mode & 1) != 0, math = (mode & 2) != 0;
   if (bulk && (stages < 2 || stages > 16)) return DART_ERR_INVALID_ARG;
@@ -235,6 +244,7 @@ extern "C" int dart_probe_stream(const void* src, uint64_t bytes, int mode, int 
   const unsigned long long warps = (unsigned long long)ctas * warps_per_cta;
   P.span = ((P.nvec + warps - 1) / warps + 255) / 256 * 256;
   P.stages = stages;
+  P.interleave = (mode & 4) ? 1 : 0;
   P.out = out;
   P.err = device_err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -95,15 +95,15 @@ __device__ __forceinline__ void run_merge_desc(CKey (&v)[R]) {
 
 // A lookup reads the key's two buckets (eight slots, 128 bytes) at once: one
 // memory round trip whether the key is present or not.  probe_issue starts
-// the loads; probe_match, called once the caller has done other work,
-// compares.
+// the loads (32 bytes each: a bucket is 64-byte aligned); probe_match,
+// called once the caller has done other work, compares.
 struct Probe { uint4 s[8]; };
 __device__ __forceinline__ void probe_issue(const uint4* slots, unsigned long long nb, Key96 key, Probe& pr) {
   const Buckets bk = key_buckets(key, nb);
 #pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    pr.s[t] = ldg_nc_v4(slots + 4 * bk.b1 + t);
-    pr.s[4 + t] = ldg_nc_v4(slots + 4 * bk.b2 + t);
+  for (int t = 0; t < 4; t += 2) {
+    ldg_nc_v8(slots + 4 * bk.b1 + t, pr.s[t], pr.s[t + 1]);
+    ldg_nc_v8(slots + 4 * bk.b2 + t, pr.s[4 + t], pr.s[5 + t]);
   }
 }
 __device__ __forceinline__ bool probe_match(const Probe& pr, Key96 key, float* val) {

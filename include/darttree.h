@@ -387,7 +387,9 @@ int dart_probe_ex2(int blocks, int threads, int iters, float* out, void* stream)
  * warp's own ring of `stages` (2..16) 4 KiB shared-memory stages filled by
  * bulk copies (warps_per_cta * stages * 4 KiB must fit in shared memory).
  * mode bit 1: reduce the data as bf16 logits (running maximum, one
- * exponential per element) instead of xor-folding it.  A bulk wait that runs
+ * exponential per element) instead of xor-folding it. mode bit 2 (bulk ring
+ * only): the warps of a CTA share one contiguous span of warps_per_cta
+ * spans, warp w reading its 4 KiB steps w, w + warps_per_cta, ...  A bulk wait that runs
  * out (about two seconds) sets bit 0 of *device_err (device uint32).  Time it
  * on `stream` to get the bandwidth a row pass of that shape can reach.
  * Returns DART_OK or an error code. */

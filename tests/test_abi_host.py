@@ -136,6 +136,14 @@ def test_other_entry_points_check_arguments(L):
     assert L.dart_probe_ex2(0, 64, 8, P(FAKE), None) == INVALID       # no blocks
     assert L.dart_probe_ex2(4, 48, 8, P(FAKE), None) == INVALID       # threads not a multiple of 32
     assert L.dart_probe_ex2(4, 64, 8, None, None) == INVALID          # no output
+    ps = lambda src, mode, warps, stages: L.dart_probe_stream(src, 1 << 20, mode, 4, warps, stages, P(FAKE),
+                                                               P(FAKE), None)
+    assert ps(P(FAKE + 8), 1, 12, 3) == INVALID       # source not 16-byte aligned
+    assert ps(P(FAKE), 8, 12, 3) == INVALID           # unknown mode bit
+    assert ps(P(FAKE), 4, 12, 3) == INVALID           # interleaving is a bulk-ring mode
+    assert ps(P(FAKE), 0, 17, 0) == INVALID           # direct loads: at most 16 warps
+    assert ps(P(FAKE), 5, 12, 1) == INVALID           # a ring needs two stages
+    assert ps(P(FAKE), 5, 16, 4) == INVALID           # 16 x 4 stages of 4 KiB exceed shared memory
     sel = lambda B, N, M, ptr: L.dart_tree_select(ptr, ptr, ptr, ptr, B, N, M, ptr, ptr, ptr, ptr, ptr,
                                                   None, None, None)
     assert sel(2, 0, 4, P(FAKE)) == INVALID          # no nodes

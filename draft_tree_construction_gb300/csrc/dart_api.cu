@@ -42,8 +42,7 @@ int num_nodes(int d, int k, int W) {
 int check_table(const dart_ngram_table_t* t, const int32_t* ctx, int B) {
   if (!t) return DART_OK;
   if (t->n < 2 || t->n > 4 || t->reserved != 0) return DART_ERR_INVALID_ARG;
-  if (!pow2(t->capacity) || t->capacity < kMinTableSlots || t->capacity > kMaxTableSlots || !t->slots ||
-      !aligned(t->slots, 64))
+  if (!pow2(t->capacity) || t->capacity < kMinTableSlots || !t->slots || !aligned(t->slots, 64))
     return DART_ERR_INVALID_ARG;
   if (B > 0 && !ctx) return DART_ERR_INVALID_ARG;
   return DART_OK;
@@ -460,7 +459,7 @@ int dart_mask_pack(const int32_t* parents, int B, int N, uint32_t* out_mask, uin
 }
 
 uint64_t dart_ngram_capacity_for(uint64_t M) {
-  if (M > kMaxTableSlots / 2) return 0;
+  if (M > (1ull << 62)) return 0;
   uint64_t c = kMinTableSlots;
   while (c < 2 * M) c <<= 1;
   return c;
@@ -484,8 +483,7 @@ void put(uint32_t* slot, const Key96& k, uint32_t v) {
 
 int dart_ngram_table_pack_host(int n, const int32_t* keys, const float* vals, uint64_t M,
                                uint64_t capacity, void* host_slots, uint64_t* out_distinct) {
-  if (n < 1 || n > 4 || !pow2(capacity) || capacity < kMinTableSlots || capacity > kMaxTableSlots || !host_slots)
-    return DART_ERR_INVALID_ARG;
+  if (n < 1 || n > 4 || !pow2(capacity) || capacity < kMinTableSlots || !host_slots) return DART_ERR_INVALID_ARG;
   if (M > 0 && (!keys || !vals)) return DART_ERR_INVALID_ARG;
   uint32_t* s = static_cast<uint32_t*>(host_slots);
   for (uint64_t i = 0; i < capacity; ++i) put(s + 4 * i, Key96{kEmpty, kEmpty, kEmpty}, 0u);
@@ -538,7 +536,7 @@ int dart_ngram_table_pack_host(int n, const int32_t* keys, const float* vals, ui
 int dart_ngram_lookup(const dart_ngram_table_t* table, const int32_t* keys, int64_t Q,
                       float* vals, int32_t* found, void* stream) {
   if (!table || table->n < 1 || table->n > 4 || !pow2(table->capacity) || table->capacity < kMinTableSlots ||
-      table->capacity > kMaxTableSlots || !table->slots || !aligned(table->slots, 64) || Q < 0)
+      !table->slots || !aligned(table->slots, 64) || Q < 0)
     return DART_ERR_INVALID_ARG;
   if (Q == 0) return DART_OK;
   if (!keys || !vals || !found) return DART_ERR_INVALID_ARG;

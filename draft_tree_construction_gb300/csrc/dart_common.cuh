@@ -104,7 +104,6 @@ __host__ __device__ __forceinline__ Buckets key_buckets(Key96 k, uint64_t nb) {
   return b;
 }
 constexpr uint64_t kMinTableSlots = 8;
-constexpr uint64_t kMaxTableSlots = 1ull << 33;   // bucket indices fit 31 bits
 
 // ------------------------------------------------------- workspace layout
 // [ctrl 256 B]                    <- ctrl word 0 holds error bits until read,

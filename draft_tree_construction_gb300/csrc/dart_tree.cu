@@ -123,62 +123,6 @@ __device__ __forceinline__ bool probe(const uint4* slots, unsigned long long nb,
   return probe_match(pr, key, val);
 }
 
-// The lookups of a whole warp, made together: four lanes serve one key (two
-// per bucket, 32 bytes each), eight keys a round, four rounds.  One load
-// instruction then reads sixteen whole buckets instead of 32-byte slices of
-// 32 buckets, a quarter of the L1 requests of lane-by-lane lookups.  Every
-// lane of the warp calls both halves; a lane without a key passes has =
-// false (its buckets are not read, its result is a miss).  Bucket indices
-// travel as 32 bits (tables hold at most 2^33 slots).
-constexpr uint32_t kNoBucket = 0xFFFFFFFFu;
-struct WarpProbe { uint4 s[8]; };
-__device__ __forceinline__ void warp_probe_issue(const uint4* slots, unsigned long long nb, Key96 key, bool has,
-                                                 WarpProbe& pr) {
-  const int lane = threadIdx.x & 31;
-  const Buckets bk = key_buckets(key, nb);
-  const uint32_t b1 = has ? uint32_t(bk.b1) : kNoBucket, b2 = has ? uint32_t(bk.b2) : kNoBucket;
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int kl = 8 * r + (lane >> 2);   // the key this lane serves in round r
-    const uint32_t u1 = __shfl_sync(0xFFFFFFFFu, b1, kl), u2 = __shfl_sync(0xFFFFFFFFu, b2, kl);
-    const uint32_t bucket = (lane & 2) ? u2 : u1;
-    if (bucket != kNoBucket) {
-      ldg_nc_v8(slots + 4 * (unsigned long long)bucket + 2 * (lane & 1), pr.s[2 * r], pr.s[2 * r + 1]);
-    } else {
-      pr.s[2 * r] = make_uint4(kEmpty, kEmpty, kEmpty, 0u);
-      pr.s[2 * r + 1] = pr.s[2 * r];
-    }
-  }
-}
-__device__ __forceinline__ bool warp_probe_match(const WarpProbe& pr, Key96 key, bool has, float* val) {
-  const int lane = threadIdx.x & 31;
-  bool found = false;
-  uint32_t v = 0u;
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int kl = 8 * r + (lane >> 2);
-    const uint32_t w0 = __shfl_sync(0xFFFFFFFFu, key.w0, kl), w1 = __shfl_sync(0xFFFFFFFFu, key.w1, kl);
-    const uint32_t w2 = __shfl_sync(0xFFFFFFFFu, key.w2, kl);
-    const uint4& a = pr.s[2 * r];
-    const uint4& b = pr.s[2 * r + 1];
-    const bool ha = a.x == w0 && a.y == w1 && a.z == w2;
-    const bool hb = b.x == w0 && b.y == w1 && b.z == w2;
-    const uint32_t mine = hb ? b.w : a.w;
-    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ha || hb);
-    // lane 8r + j owns the key served by lanes 4j .. 4j + 3
-    const int j = lane - 8 * r;
-    const uint32_t bits = (j >= 0 && j < 8) ? (bal >> (4 * j)) & 0xFu : 0u;
-    const int src = bits ? 4 * j + __ffs(bits) - 1 : lane;
-    const uint32_t got = __shfl_sync(0xFFFFFFFFu, mine, src);
-    if (bits) {
-      found = true;
-      v = got;
-    }
-  }
-  if (found && has) *val = __uint_as_float(v);
-  return found && has;
-}
-
 __host__ __device__ inline int tree_run_len(int W) { return W <= 32 ? 32 : 64; }
 __host__ __device__ inline int tree_pad(int W, int k) {
   const int run = tree_run_len(W);
@@ -397,7 +341,6 @@ tree_kernel(const TreeArgs A) {
     for (int f = 0; f < nctx; ++f) fctx_cur[f] = rootctx[f];
   }
   int nf = 1, node_base = 0;
-  bool runs_sorted = false;   // the current keys are already sorted runs of RUN
   double Lsum = 0.0;   // sum of the row offsets down to this depth
   __syncthreads();
 
@@ -455,10 +398,9 @@ tree_kernel(const TreeArgs A) {
       kt_dst = (ties == kt_a) ? kt_b : kt_a;
     } else {
       const int npad = (m + RUN - 1) / RUN * RUN;
-      // sort runs of RUN keys, one warp per run (unless the depth before
-      // sorted them as it scored them)
+      // sort runs of RUN keys, one warp per run
       int nr = npad / RUN;
-      for (int run = runs_sorted ? nr : warp; run < nr; run += nwarps) {
+      for (int run = warp; run < nr; run += nwarps) {
         CKey v[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
@@ -474,7 +416,7 @@ tree_kernel(const TreeArgs A) {
           ties[e] = v[r].t;
         }
       }
-      if (!runs_sorted) __syncthreads();
+      __syncthreads();
       // merge runs in groups of kGroup: each warp folds a group's runs into
       // one run in registers (the best RUN keys so far, merged with the next
       // run reversed), so a round costs one barrier for kGroup runs
@@ -526,34 +468,24 @@ tree_kernel(const TreeArgs A) {
     const int m2 = nsel * kk;
     const int npad2 = last ? m2 : (m2 + RUN - 1) / RUN * RUN;
     double* cG_next = (cG == cG_a) ? cG_b : cG_a;
-    // below the last depth the lookups are made a warp at a time: npad2 is
-    // then a multiple of 32, so every lane of a warp runs the same iterations
-    const bool lookups = !last && n > 0;
-    // when the next depth sorts runs of 32 keys and every thread scores at
-    // most one child, each warp's 32 children are one run: sort it here, in
-    // registers, and spare the next depth a pass and a barrier
-    const bool sort_here = R == 1 && !last && m2 > kRankMax && npad2 <= int(blockDim.x);
     for (int q = tid; q < npad2; q += blockDim.x) {
       uint64_t ks2 = 0;
       uint32_t kt2 = 0;
-      const bool live = q < m2;
-      int x = 0, c2 = 0, i = 0, c = 0, tok = 0;
-      uint64_t ks = 0;
-      int ctx[3] = {0, 0, 0};
-      Key96 ckey{0u, 0u, 0u};
-      if (live) {
-        x = q / kk;             // survivor rank = node index within the depth
-        c2 = q - x * kk;        // its child column in row j+1
-        ks = src_s[x];
+      if (q < m2) {
+        const int x = q / kk;             // survivor rank = node index within the depth
+        const int c2 = q - x * kk;        // its child column in row j+1
+        const uint64_t ks = src_s[x];
         const uint32_t tie = kTieMax - src_t[x];
-        i = int(tie >> 5);
-        c = (i < nf) ? Rc.rinv[tie & 31u] : 0;
+        int i = int(tie >> 5);
+        int c = (i < nf) ? Rc.rinv[tie & 31u] : 0;
         if (ks == 0 || i >= nf) {
           set_dev_error(A.ctrl, DART_DEVERR_SELECT);
           i = 0;
           c = 0;
         }
-        tok = Rc.rid[c];
+        const int tok = Rc.rid[c];
+        const int node = node_base + x;
+        int ctx[3] = {0, 0, 0};
 #pragma unroll
         for (int f = 0; f + 1 < 3; ++f)
           if (f + 1 < nctx) ctx[f] = fctx_cur[i * 3 + f + 1];
@@ -562,25 +494,22 @@ tree_kernel(const TreeArgs A) {
           else if (nctx == 2) ctx[1] = tok;
           else ctx[2] = tok;
         }
-        if (lookups) {
+        // start the lookup of child (x, c2) before the rest of the work
+        Probe pr;
+        Key96 ckey{0u, 0u, 0u};
+        float pg = 0.f;
+        if (!last && pair) pg = __ldg(pair + ((size_t)(j + 1) * k + c) * k + c2);
+        if (!last && n > 0) {
           const int ctok = Rn.rid[c2];
           int32_t t[4] = {ctx[0], ctx[1], ctx[2], 0};
           if (nctx == 1) t[1] = ctok;
           else if (nctx == 2) t[2] = ctok;
           else t[3] = ctok;
           ckey = pack_ngram(t, n);
+          probe_issue(slots, nbuckets, ckey, pr);
         }
-      }
-      // start the lookups of the warp's children before the rest of the work
-      WarpProbe pr;
-      if (lookups) warp_probe_issue(slots, nbuckets, ckey, live, pr);
-      float pg = 0.f;
-      double Zp = 0.0, Gp = 0.0;
-      if (live) {
-        const int node = node_base + x;
-        if (!last && pair) pg = __ldg(pair + ((size_t)(j + 1) * k + c) * k + c2);
-        Zp = __dadd_rn(fZ_cur[i], Rc.rb[c]);
-        Gp = cG[i * k + c];
+        const double Zp = __dadd_rn(fZ_cur[i], Rc.rb[c]);
+        const double Gp = cG[i * k + c];
         // ancestor-mask words of the node, spread over its k child threads
         for (int w = c2; w < MW; w += kk) {
           uint32_t val = (j == 0) ? 0u : fmask_cur[i * MW + w];
@@ -608,17 +537,14 @@ tree_kernel(const TreeArgs A) {
           for (int f = 0; f < 3; ++f)
             if (f < nctx) fctx_nxt[x * 3 + f] = ctx[f];
         }
-      }
-      float g = 0.f;
-      const bool hit = lookups && warp_probe_match(pr, ckey, live, &g);
-      if (live) {
         if (!last) {
           // key of child (x, c2): (Zp + base) * invT + lam * (Gp + g), as in child()
           const double Zc = __dadd_rn(Zp, Rn.rb[c2]);
           const double ZinvT = unit_T ? Zc : __dmul_rn(Zc, invT);
           double G = Gp;
           if (n > 0) {
-            G = __dadd_rn(G, hit ? double(g) : A.beta);
+            float g = 0.f;
+            G = __dadd_rn(G, probe_match(pr, ckey, &g) ? double(g) : A.beta);
           } else if (pair) {
             G = __dadd_rn(G, double(pg));
           }
@@ -627,21 +553,12 @@ tree_kernel(const TreeArgs A) {
           kt2 = kTieMax - ((uint32_t(x) << 5) | uint32_t(Rn.rrank[c2]));
         }
       }
-      if (sort_here) {
-        CKey v[1];
-        v[0].s = ks2;
-        v[0].t = kt2;
-        run_sort<1>(v);
-        ks2 = v[0].s;
-        kt2 = v[0].t;
-      }
       if (!last) {
         ks_dst[q] = ks2;
         kt_dst[q] = kt2;
       }
     }
     if (last) break;
-    runs_sorted = sort_here;
     keys = ks_dst;
     ties = kt_dst;
     cG = cG_next;

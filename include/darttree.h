@@ -96,7 +96,7 @@ enum {
 typedef struct {
   int32_t n;            /* order, 2..4 */
   int32_t reserved;     /* must be 0 */
-  uint64_t capacity;    /* number of slots, a power of two in [8, 2^33] */
+  uint64_t capacity;    /* number of slots, a power of two >= 8 */
   const void* slots;    /* device, capacity * 16 bytes, 64-byte aligned */
 } dart_ngram_table_t;
 
@@ -326,14 +326,14 @@ int dart_tree_select(const int32_t* tokens, const int32_t* parents, const int32_
                      int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
                      uint32_t* out_mask, float* out_scores, uint32_t* device_err, void* stream);
 
-/* Smallest power of two >= max(2 * M, 8) (load factor at most 1/2); 0 when
- * that exceeds 2^33 slots (the largest table the lookups address). */
+/* Smallest power of two >= max(2 * M, 8) (load factor at most 1/2); 0 on
+ * overflow. */
 uint64_t dart_ngram_capacity_for(uint64_t M);
 
 /* Build the slots of an n-gram table on the host.
  *  keys host int32 [M][n] (t_0 oldest ... t_{n-1} predicted), each in
  *  [0, 2^24-1); vals host float [M]; host_slots host, capacity * 16 bytes;
- *  capacity a power of two in [8, 2^33].
+ *  capacity a power of two >= 8.
  * A repeated key keeps its first value; *out_distinct (may be NULL)
  * receives the number of distinct keys stored.  Keys whose two buckets are
  * full move earlier keys to their other bucket (cuckoo displacement, a fixed

@@ -110,9 +110,9 @@ constexpr uint64_t kMinTableSlots = 8;
 //                                    words 2..3 the rows of the last call
 // [row_off R x f64][row_ids R*k x i32][row_base R*k x f64][piece slots]
 // row_off = the row's log-sum-exp of z / T; row_base = the candidates' logits.
-// A piece slot holds one warp's share of a row: {f32 max; u32 count; f64 sum
-// of 2^((z - max) c); u32 bound (an ordered float: a lower bound of the row's
-// k-th value); pad}, then cp candidate vectors of 16 bytes, then cp tags
+// A piece slot holds one warp's share of a row: {f32 max; u32 count; f32 sum
+// of 2^((z - max) c); pad; u32 bound (an ordered float: a lower bound of the
+// row's k-th value); pad}, then cp candidate vectors of 16 bytes, then cp tags
 // ((element mask << 24) | row index of the vector's first element).
 //
 // The row pass cuts the logits into one contiguous span per warp of a fixed

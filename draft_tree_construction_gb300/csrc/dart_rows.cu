@@ -543,7 +543,7 @@ __device__ __forceinline__ Seg segment(const RowsParams& P, unsigned long long e
 }
 
 // ------------------------------------------------------------------ row end
-// A piece slot: {f32 max; u32 count; f64 sum; u32 bound; pad}, then cp
+// A piece slot: {f32 max; u32 count; f32 sum; pad; u32 bound; pad}, then cp
 // vectors, then cp tags.
 __device__ __forceinline__ uint8_t* slot_of(const RowsParams& P, long long r, long long p) {
   return P.slots + ((size_t)r * P.pmax + (size_t)p) * P.slot_bytes;
@@ -584,7 +584,7 @@ __device__ __forceinline__ void piece_end(const RowsParams& P, const WarpCands& 
   if (lane == 0) {
     *reinterpret_cast<float*>(q) = m;
     *reinterpret_cast<uint32_t*>(q + 4) = uint32_t(cnt);
-    *reinterpret_cast<double*>(q + 8) = double(s);
+    *reinterpret_cast<float*>(q + 8) = s;
     *reinterpret_cast<uint32_t*>(q + 16) = tau_o;
   }
   __syncwarp();
@@ -769,17 +769,17 @@ constexpr int kMergeKeys = 1024;     // candidate keys a row keeps in shared mem
 
 // Writes a row's results from its maximum M, its sum S of 2^((z - M) c) and
 // its best keys (keys[0..kept), descending); one warp.
-__device__ __forceinline__ void finish_row(const RowsParams& P, long long r, float M, double S, const uint64_t* keys,
+__device__ __forceinline__ void finish_row(const RowsParams& P, long long r, float M, float S, const uint64_t* keys,
                                            int kept) {
   const int lane = threadIdx.x & 31;
   const int k = P.k;
   const float zmax = kept > 0 ? key_value(keys[0]) : -INFINITY;
   if (lane == 0 && (kept < k || zmax != M)) set_dev_error(P.ctrl, DART_DEVERR_ROW_MAX);
-  // log S = e ln 2 + log f with S = f 2^e, f in [0.5, 1): one float log of
-  // the mantissa keeps the slow double unit to a multiply and an add
+  // log S = e ln 2 + log f with S = f 2^e, f in [0.5, 1): the float log of
+  // the mantissa is within about 1e-7 of its value
   int e2;
-  const double f = frexp(S, &e2);
-  const double logS = double(e2) * 0.6931471805599453 + double(logf(float(f)));
+  const float f = frexpf(S, &e2);
+  const double logS = fma(double(e2), 0.6931471805599453, double(logf(f)));
   if (lane < k) {
     const uint64_t key = lane < kept ? keys[lane] : 0ull;
     const float z = key_value(key);
@@ -866,8 +866,7 @@ __device__ __noinline__ void merge_row_warp(const RowsParams& P, long long r, ui
   const int nseg = row_pieces(P, v, &wa);
   // headers: running (max, sum) per lane over its pieces, the largest bound;
   // pieces lane and lane + 32 keep their maxima for the k-th largest
-  float mp = -FLT_MAX;
-  double sp = 0.0;
+  float mp = -FLT_MAX, sp = 0.f;
   uint32_t b = 0;
   uint32_t om[2] = {0u, 0u};
   for (int p0 = 0; p0 < nseg; p0 += 32) {
@@ -875,22 +874,19 @@ __device__ __noinline__ void merge_row_warp(const RowsParams& P, long long r, ui
     if (p < nseg) {
       const uint8_t* q = slot_of(P, v, p);
       const float m2 = __ldcg(reinterpret_cast<const float*>(q));
-      const double s2 = __ldcg(reinterpret_cast<const double*>(q + 8));
+      const float s2 = __ldcg(reinterpret_cast<const float*>(q + 8));
       const uint32_t b2 = __ldcg(reinterpret_cast<const uint32_t*>(q + 16));
       const float M2 = fmaxf(mp, m2);
-      sp = sp * double(ex2_approx((mp - M2) * P.c)) + s2 * double(ex2_approx((m2 - M2) * P.c));
+      sp = sp * ex2_approx((mp - M2) * P.c) + s2 * ex2_approx((m2 - M2) * P.c);
       mp = M2;
       b = max(b, b2);
       if (p0 < 64) om[p0 >> 5] = ord_f32(m2);
     }
   }
-  float Mx = mp;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    Mx = fmaxf(Mx, __shfl_xor_sync(kFull, Mx, o));
-    b = max(b, __shfl_xor_sync(kFull, b, o));
-  }
-  double Sx = sp * double(ex2_approx((mp - Mx) * P.c));
+  // mp > -FLT_MAX only for lanes with a piece, so the ordered maximum is a real one
+  const float Mx = unord_f32(__reduce_max_sync(kFull, ord_f32(mp)));
+  b = __reduce_max_sync(kFull, b);
+  float Sx = sp * ex2_approx((mp - Mx) * P.c);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) Sx += __shfl_xor_sync(kFull, Sx, o);
   if (nseg >= k && nseg <= 64) {
@@ -977,13 +973,13 @@ __device__ __noinline__ void merge_row_warp(const RowsParams& P, long long r, ui
 
 struct MergeSmem {
   float m[kMergePieces];
-  double s[kMergePieces];
+  float s[kMergePieces];
   uint32_t end[kMergePieces];   // the pieces' candidate counts
   uint32_t pb[kMergePieces];    // the pieces' bounds
   uint32_t bound;
   uint32_t nkeys;
   float M;
-  double S;
+  float S;
   uint64_t keys[kMergeKeys];
   uint64_t best[kMaxK];
   int sel[kMergePieces];          // pieces whose maximum reaches the bound (rows of many entries)
@@ -1019,7 +1015,7 @@ row_merge_kernel(const __grid_constant__ RowsParams P) {
     if (tid < nseg) {
       uint8_t* q = slot_of(P, r, tid);
       M.m[tid] = __ldcg(reinterpret_cast<const float*>(q));
-      M.s[tid] = __ldcg(reinterpret_cast<const double*>(q + 8));
+      M.s[tid] = __ldcg(reinterpret_cast<const float*>(q + 8));
       M.end[tid] = min(__ldcg(reinterpret_cast<const uint32_t*>(q + 4)), uint32_t(P.cp));
       M.pb[tid] = __ldcg(reinterpret_cast<const uint32_t*>(q + 16));
     }
@@ -1045,16 +1041,14 @@ row_merge_kernel(const __grid_constant__ RowsParams P) {
       const bool h0 = lane < nseg, h1 = lane + 32 < nseg;
       const float m0 = h0 ? M.m[lane] : -FLT_MAX, m1 = h1 ? M.m[lane + 32] : -FLT_MAX;
       uint32_t b = max(h0 ? M.pb[lane] : 0u, h1 ? M.pb[lane + 32] : 0u);
-      float mx = fmaxf(m0, m1);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-      double sum = (h0 ? M.s[lane] * double(ex2_approx((m0 - mx) * P.c)) : 0.0) +
-                   (h1 ? M.s[lane + 32] * double(ex2_approx((m1 - mx) * P.c)) : 0.0);
+      // (every row has a piece, so the ordered maximum is a real one)
+      const float mx = unord_f32(__reduce_max_sync(kFull, ord_f32(fmaxf(m0, m1))));
+      float sum = (h0 ? M.s[lane] * ex2_approx((m0 - mx) * P.c) : 0.f) +
+                  (h1 ? M.s[lane + 32] * ex2_approx((m1 - mx) * P.c) : 0.f);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
       if (nseg >= k) b = max(b, warp_kth_largest2(h0 ? ord_f32(m0) : 0u, h1 ? ord_f32(m1) : 0u, k));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) b = max(b, __shfl_xor_sync(kFull, b, o));
+      b = __reduce_max_sync(kFull, b);
       if (lane == 0) {
         M.M = mx;
         M.S = sum;

@@ -69,6 +69,7 @@ constexpr long long kDefaultWaitLimit = 4000000000LL;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 static_assert(kVecPerLane == 8, "stage_reduce reduces exactly eight vectors per lane");
 static_assert(kKeyStage >= 32 * 8 + kMaxK, "a stage must take one round of keys after keeping k");
+static_assert(kCandCap < 256, "piece counts must fit the row merge's 8-bit prefix sums");
 
 struct RowsParams {
   const uint8_t* logits;
@@ -253,6 +254,21 @@ __device__ __forceinline__ void raise_max(Acc& a, float v, float c) {
 // s against exact m c: s * 2^-(m c - mc).  0 stays 0.
 __device__ __forceinline__ float exact_sum(const Acc& a, float c) {
   return a.s > 0.f ? a.s * ex2_approx(-fmaf(a.m, c, -a.mc)) : 0.f;
+}
+
+// Exclusive prefix and total over the warp of a per-lane count in 0..255:
+// one ballot per bit, all independent.
+__device__ __forceinline__ int warp_prefix8(uint32_t cnt, int* total) {
+  const uint32_t below = (1u << (threadIdx.x & 31)) - 1u;
+  int pre = 0, tot = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t q = __ballot_sync(kFull, (cnt >> j) & 1u);
+    pre += __popc(q & below) << j;
+    tot += __popc(q) << j;
+  }
+  *total = tot;
+  return pre;
 }
 
 // Exclusive prefix and total over the warp of a per-lane count in 0..15.
@@ -1047,7 +1063,22 @@ row_merge_kernel(const __grid_constant__ RowsParams P) {
                   (h1 ? M.s[lane + 32] * ex2_approx((m1 - mx) * P.c) : 0.f);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
-      if (nseg >= k) b = max(b, warp_kth_largest2(h0 ? ord_f32(m0) : 0u, h1 ? ord_f32(m1) : 0u, k));
+      if (nseg >= k) {
+        // the k-th largest piece maximum: of the lane's two maxima, one with
+        // fewer than k pieces above it and at least k at or above it (the
+        // lane counts over all the maxima, broadcast reads of shared memory)
+        const uint32_t o0 = h0 ? ord_f32(m0) : 0u, o1 = h1 ? ord_f32(m1) : 0u;
+        int a0 = 0, t0 = 0, a1 = 0, t1 = 0;
+        for (int q = 0; q < nseg; ++q) {
+          const uint32_t y = ord_f32(M.m[q]);
+          a0 += y > o0 ? 1 : 0;
+          t0 += y >= o0 ? 1 : 0;
+          a1 += y > o1 ? 1 : 0;
+          t1 += y >= o1 ? 1 : 0;
+        }
+        if (h0 && a0 < k && t0 >= k) b = max(b, o0);
+        if (h1 && a1 < k && t1 >= k) b = max(b, o1);
+      }
       b = __reduce_max_sync(kFull, b);
       if (lane == 0) {
         M.M = mx;
@@ -1056,33 +1087,25 @@ row_merge_kernel(const __grid_constant__ RowsParams P) {
       }
       if (!one_round) {
         // the pieces that can hold one of the k best, in piece order, and
-        // where their entries start in the gathered range
+        // where their entries start in the gathered range: bit-sliced
+        // prefix sums of the counts (independent ballots, no scan chain)
         const bool t0 = h0 && M.end[lane] > 0u && ord_f32(m0) >= b;
         const bool t1 = h1 && M.end[lane + 32] > 0u && ord_f32(m1) >= b;
-        const int c0 = t0 ? int(M.end[lane]) : 0, c1 = t1 ? int(M.end[lane + 32]) : 0;
-        int i0 = c0, i1 = c1;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y0 = __shfl_up_sync(kFull, i0, o), y1 = __shfl_up_sync(kFull, i1, o);
-          if (lane >= o) {
-            i0 += y0;
-            i1 += y1;
-          }
-        }
-        const int tot0 = __shfl_sync(kFull, i0, 31);
+        int tot0, tot1;
+        const int i0 = warp_prefix8(t0 ? M.end[lane] : 0u, &tot0);
+        const int i1 = warp_prefix8(t1 ? M.end[lane + 32] : 0u, &tot1);
         const uint32_t bm0 = __ballot_sync(kFull, t0), bm1 = __ballot_sync(kFull, t1);
         const uint32_t below = (1u << lane) - 1u;
         if (t0) {
           const int at = __popc(bm0 & below);
           M.sel[at] = lane;
-          M.start[at] = i0 - c0;
+          M.start[at] = i0;
         }
         if (t1) {
           const int at = __popc(bm0) + __popc(bm1 & below);
           M.sel[at] = lane + 32;
-          M.start[at] = tot0 + i1 - c1;
+          M.start[at] = tot0 + i1;
         }
-        const int tot1 = __shfl_sync(kFull, i1, 31);
         if (lane == 0) {
           const int ns = __popc(bm0) + __popc(bm1);
           M.E = tot0 + tot1;

@@ -13,6 +13,7 @@
 // (ordered ranking key, then inverted (parent rank, token rank)), sorts 32- or
 // 64-key runs with warp bitonic networks and merges runs pairwise, keeping
 // only the best run length, until one run holds the survivors in order.
+#include <atomic>
 #include "dart_launch.h"
 
 namespace dart {
@@ -130,12 +131,31 @@ __host__ __device__ inline int tree_pad(int W, int k) {
 }
 constexpr int kRankMax = 128;   // up to this many children a depth selects by ranking (more: sorted runs)
 constexpr int kGroup = 4;       // sorted runs one warp folds together per merge round
-// Threads per tree: one per child of a full frontier, 32..512.  (Two per
-// child would halve the ranking loop, but at 122 registers a thread it
-// leaves one CTA per SM for 320 threads: two waves for 256 trees.)
-inline int tree_threads(int W, int k) {
-  const int t = (W * k + 31) / 32 * 32;
-  return t < 32 ? 32 : (t > kTreeThreads ? kTreeThreads : t);
+// Threads per tree: one per child of a full frontier, 32..512; two per child
+// when every depth selects by ranking and the trees fit one CTA per SM (then
+// two threads rank each key against half of the keys).  Doubling for more
+// trees than SMs would cost a second wave: at about 120 registers a thread
+// an SM holds one CTA of 320 threads.
+inline int tree_threads(int W, int k, int B, int sms) {
+  int t = (W * k + 31) / 32 * 32;
+  t = t < 32 ? 32 : (t > kTreeThreads ? kTreeThreads : t);
+  if (W * k <= kRankMax && 2 * t <= kTreeThreads && B <= sms) t *= 2;
+  return t;
+}
+
+// Multiprocessors of the current device (cached per device).
+static int device_sms() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < 64) cache[dev].store(sms, std::memory_order_relaxed);
+  return sms;
 }
 
 inline size_t tree_smem_bytes(int d, int W, int k, int MW, int N, bool select) {
@@ -271,15 +291,30 @@ tree_kernel(const TreeArgs A) {
 
   // ---- every row's candidates and offset, then their token ranks
   const size_t row0 = (size_t)b * dk;
-  for (int e = tid; e < dk; e += blockDim.x) {
-    rows_id[e] = A.ids[row0 + e];
-    rows_b[e] = A.base[row0 + e];
-  }
-  for (int j = tid; j < d; j += blockDim.x) offs[j] = A.off ? A.off[(size_t)b * d + j] : 0.0;
   int rootctx[3] = {0, 0, 0};
 #pragma unroll
   for (int f = 0; f < 3; ++f)
     if (f < nctx) rootctx[f] = A.ctx[(size_t)b * nctx + f];
+  int tok0 = 0;   // thread q < k: candidate q of row 0, the root's child q
+  for (int e = tid; e < dk; e += blockDim.x) {
+    const int id = A.ids[row0 + e];
+    rows_id[e] = id;
+    rows_b[e] = A.base[row0 + e];
+    if (e == tid) tok0 = id;
+  }
+  for (int j = tid; j < d; j += blockDim.x) offs[j] = A.off ? A.off[(size_t)b * d + j] : 0.0;
+  // the root's children's lookups start now and land while the ranks are made
+  Probe rp;
+  Key96 rkey{0u, 0u, 0u};
+  const bool root_probe = n > 0 && tid < k;
+  if (root_probe) {
+    int32_t t[4] = {rootctx[0], rootctx[1], rootctx[2], 0};
+    if (nctx == 1) t[1] = tok0;
+    else if (nctx == 2) t[2] = tok0;
+    else t[3] = tok0;
+    rkey = pack_ngram(t, n);
+    probe_issue(slots, nbuckets, rkey, rp);
+  }
   __syncthreads();
   for (int e = tid; e < dk; e += blockDim.x) {
     const int j = e / k, c = e - j * k;
@@ -313,8 +348,16 @@ tree_kernel(const TreeArgs A) {
       uint64_t ks = 0;
       uint32_t kt = 0;
       if (q < k) {
-        double G;
-        const double key = child(0.0, 0.0, rootctx[0], rootctx[1], rootctx[2], R0, q, &G);
+        double G, key;
+        if (root_probe && q == tid) {
+          // as child() for the root (Z = 0 + base, G = 0 + g), on the lookup started above
+          float g = 0.f;
+          const double Z = __dadd_rn(0.0, R0.rb[q]);
+          G = __dadd_rn(0.0, probe_match(rp, rkey, &g) ? double(g) : A.beta);
+          key = __dadd_rn(unit_T ? Z : __dmul_rn(Z, invT), __dmul_rn(lam, G));
+        } else {
+          key = child(0.0, 0.0, rootctx[0], rootctx[1], rootctx[2], R0, q, &G);
+        }
         cG[q] = G;
         ks = ord_f64(key);
         kt = kTieMax - uint32_t(R0.rrank[q]);             // parent rank 0
@@ -586,7 +629,7 @@ tree_kernel(const TreeArgs A) {
 cudaError_t launch_tree(const TreeArgs& a, cudaStream_t stream) {
   if (a.B == 0) return cudaSuccess;
   const size_t smem = tree_smem_bytes(a.d, a.W, a.k, a.MW, a.N, a.M > 0);
-  const int threads = tree_threads(a.W, a.k);
+  const int threads = tree_threads(a.W, a.k, a.B, device_sms());
   cudaError_t e;
   if (a.W <= 32) {
     e = cudaFuncSetAttribute(tree_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));

@@ -298,6 +298,25 @@ __device__ __forceinline__ uint32_t kth_above(uint32_t v, uint32_t above, int k)
   return __reduce_min_sync(kFull, cand ? v : 0xFFFFFFFFu);
 }
 
+// The same for a piece's first stage, where most lanes are above `above`:
+// a bitonic sort of the 32 values (fifteen exchange steps) instead of one
+// removal per excess lane.
+__device__ __forceinline__ uint32_t kth_sorted(uint32_t v, uint32_t above, int k) {
+  const int lane = threadIdx.x & 31;
+  uint32_t x = v > above ? v : 0u;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint32_t y = __shfl_xor_sync(kFull, x, stride);
+      const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+      x = keep_max ? max(x, y) : min(x, y);
+    }
+  }
+  const uint32_t kth = __shfl_sync(kFull, x, k - 1);   // descending: lane k-1 holds the k-th largest
+  return kth > above ? kth : above;
+}
+
 // Real elements of a tagged vector that reach tau (bit e = element e).
 template <int DT>
 __device__ __forceinline__ uint32_t vec_hits(const uint4& v, uint32_t tag, float tau) {
@@ -464,7 +483,8 @@ __device__ __forceinline__ void stage_reduce(Acc& a, uint32_t& tau_o, int& cnt, 
   {
     const uint32_t post = a.m > -FLT_MAX ? ord_f32(a.m) : 0u;
     uint32_t o = tau_o;
-    if (SEED || __popc(__ballot_sync(kFull, post > o)) >= k) o = kth_above(post, o, k);
+    if (SEED) o = kth_sorted(post, o, k);
+    else if (__popc(__ballot_sync(kFull, post > o)) >= k) o = kth_above(post, o, k);
     if (tau_slot) {
       if (o > tau_o && lane == 0) atomicMax(tau_slot, o);
       const uint32_t so = *reinterpret_cast<volatile uint32_t*>(tau_slot);

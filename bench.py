@@ -185,8 +185,9 @@ def kernel_source_hash() -> str:
 
 
 def k1_traffic(config: int):
-    """DRAM bytes per launch of the streaming kernel from the committed ncu summary,
-    or None when the kernel source changed since that capture."""
+    """DRAM bytes (read + write) of one launch of the streaming kernel on `config`
+    from the committed ncu capture of that config, or None when there is none or
+    the kernel source changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "row_stream_dram.json")
     try:
         with open(path) as f:
@@ -195,11 +196,10 @@ def k1_traffic(config: int):
         return None
     if rec.get("source_sha256") != kernel_source_hash():
         return None
-    per = rec.get("dram_bytes_per_logit_byte")
-    if per is None:
+    c = rec.get("configs", {}).get(str(config))
+    if not c:
         return None
-    c = synth.CONFIGS[config]
-    return per * c["B"] * c["d"] * c["V"] * synth.ELEM_BYTES[c["dtype"]]
+    return c["dram_bytes_read"] + c["dram_bytes_write"]
 
 
 # -------------------------------------------------------------- CPU oracle
@@ -659,7 +659,8 @@ def run_ours(args):
                 per_config[str(c2)] = {
                     "workload": workload_name(c2), "ms_per_step": mm["step_ms"],
                     "trees_per_s": cc.B / (mm["step_ms"] / 1e3), "row_pass_ms": mm["row_pass_ms"],
-                    "row_pass_frac": ach / peaks["hbm_gbs"], "row_merge_ms": mm["row_merge_ms"],
+                    "row_pass_frac": ach / peaks["hbm_gbs"], "row_pass_traffic": k1_traffic(c2),
+                    "row_merge_ms": mm["row_merge_ms"],
                     "tree_ms_by_difference": mm["tree_ms_by_difference"],
                     "logit_bytes": cc.logit_bytes}
                 del mm

@@ -7,6 +7,8 @@
 namespace dart {
 
 long long rows_wait_limit();
+// Multiprocessors of the current device (cached per device; 0 if unknown).
+int device_sms();
 void set_rows_wait_limit(long long cycles);
 
 // The streaming pass over R rows (per-piece results in the workspace).

@@ -47,6 +47,7 @@
 // error bit, lets its copies in flight land and returns; the call's results
 // are then invalid.
 #include "dart_common.cuh"
+#include "dart_launch.h"
 
 #include <atomic>
 #include <cfloat>
@@ -1032,8 +1033,8 @@ struct MergeSmem {
 // kMergePieces pieces, more entries than one round holds, or more than
 // kMergeKeys such keys, is merged by one warp instead (inputs far from the
 // streamed shapes).
-template <int DT>
-__global__ void __launch_bounds__(kMergeThreads)
+template <int DT, int MINB>
+__global__ void __launch_bounds__(kMergeThreads, MINB)
 row_merge_kernel(const __grid_constant__ RowsParams P) {
   __shared__ MergeSmem M;
   __shared__ uint64_t wstage[kKeyStage];
@@ -1278,9 +1279,15 @@ cudaError_t launch_row_merge(long long R, int V, long long stride, int dtype, fl
   if (!rows_params(&P, nullptr, R, V, stride, dtype, T, k, ws, L, out_ids, out_logp, out_lse))
     return cudaErrorInvalidValue;
   if (R == 0) return cudaSuccess;
-  if (dtype == DART_F32) row_merge_kernel<DART_F32><<<unsigned(R), kMergeThreads, 0, stream>>>(P);
-  else if (dtype == DART_F16) row_merge_kernel<DART_F16><<<unsigned(R), kMergeThreads, 0, stream>>>(P);
-  else row_merge_kernel<DART_BF16><<<unsigned(R), kMergeThreads, 0, stream>>>(P);
+  // more rows than four CTAs per SM: the build held to 64 registers, so that
+  // eight CTAs share an SM and the rows take fewer waves (a few spilled
+  // registers make it slower when the rows fit one wave anyway)
+  const int sms = device_sms();
+  const bool dense = sms > 0 && R > 4LL * sms;
+  auto go = [&](auto kernel) { kernel<<<unsigned(R), kMergeThreads, 0, stream>>>(P); };
+  if (dtype == DART_F32) dense ? go(row_merge_kernel<DART_F32, 8>) : go(row_merge_kernel<DART_F32, 1>);
+  else if (dtype == DART_F16) dense ? go(row_merge_kernel<DART_F16, 8>) : go(row_merge_kernel<DART_F16, 1>);
+  else dense ? go(row_merge_kernel<DART_BF16, 8>) : go(row_merge_kernel<DART_BF16, 1>);
   return cudaGetLastError();
 }
 

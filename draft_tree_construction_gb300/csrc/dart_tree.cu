@@ -143,8 +143,7 @@ inline int tree_threads(int W, int k, int B, int sms) {
   return t;
 }
 
-// Multiprocessors of the current device (cached per device).
-static int device_sms() {
+int device_sms() {
   static std::atomic<int> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;

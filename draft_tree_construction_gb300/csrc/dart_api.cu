@@ -469,8 +469,8 @@ namespace {
 bool slot_is(const uint32_t* slot, const Key96& k) { return slot[0] == k.w0 && slot[1] == k.w1 && slot[2] == k.w2; }
 bool slot_empty(const uint32_t* slot) { return slot[0] == kEmpty && slot[1] == kEmpty && slot[2] == kEmpty; }
 uint32_t* free_slot(uint32_t* s, uint64_t bucket) {
-  for (int t = 0; t < 4; ++t)
-    if (slot_empty(s + 4 * (4 * bucket + t))) return s + 4 * (4 * bucket + t);
+  for (int t = 0; t < kBucketSlots; ++t)
+    if (slot_empty(s + 4 * (kBucketSlots * bucket + t))) return s + 4 * (kBucketSlots * bucket + t);
   return nullptr;
 }
 void put(uint32_t* slot, const Key96& k, uint32_t v) {
@@ -487,7 +487,7 @@ int dart_ngram_table_pack_host(int n, const int32_t* keys, const float* vals, ui
   if (M > 0 && (!keys || !vals)) return DART_ERR_INVALID_ARG;
   uint32_t* s = static_cast<uint32_t*>(host_slots);
   for (uint64_t i = 0; i < capacity; ++i) put(s + 4 * i, Key96{kEmpty, kEmpty, kEmpty}, 0u);
-  const uint64_t nb = capacity / 4;
+  const uint64_t nb = capacity / kBucketSlots;
   uint64_t distinct = 0;
   int rc = DART_OK;
   for (uint64_t i = 0; i < M && rc == DART_OK; ++i) {
@@ -500,8 +500,8 @@ int dart_ngram_table_pack_host(int n, const int32_t* keys, const float* vals, ui
     memcpy(&val, &vals[i], 4);
     const Buckets bk = key_buckets(key, nb);
     bool present = false;
-    for (int tt = 0; tt < 8 && !present; ++tt)
-      present = slot_is(s + 4 * (4 * (tt < 4 ? bk.b1 : bk.b2) + (tt & 3)), key);
+    for (int tt = 0; tt < 2 * kBucketSlots && !present; ++tt)
+      present = slot_is(s + 4 * (kBucketSlots * (tt < kBucketSlots ? bk.b1 : bk.b2) + tt % kBucketSlots), key);
     if (present) continue;   // the first value of a key is kept
     if (distinct >= capacity / 2) {
       rc = DART_ERR_TABLE_FULL;
@@ -512,7 +512,7 @@ int dart_ngram_table_pack_host(int n, const int32_t* keys, const float* vals, ui
     // both buckets full: displace along the chain b -> the victim's other bucket
     uint64_t b = bk.b1;
     for (int kick = 0; !slot && kick < 500; ++kick) {
-      uint32_t* victim = s + 4 * (4 * b + uint64_t(kick & 3));
+      uint32_t* victim = s + 4 * (kBucketSlots * b + uint64_t(kick % kBucketSlots));
       const Key96 vk{victim[0], victim[1], victim[2]};
       const uint32_t vv = victim[3];
       put(victim, key, val);

@@ -93,7 +93,9 @@ __host__ __device__ __forceinline__ uint64_t hash_key(Key96 k) {
   return x;
 }
 
-// The two buckets (4 slots each) a key may live in; nb = capacity / 4 >= 2.
+// The two buckets (kBucketSlots slots, 32 bytes each) a key may live in;
+// nb = capacity / kBucketSlots >= 2.
+constexpr int kBucketSlots = 2;
 struct Buckets { uint64_t b1, b2; };
 __host__ __device__ __forceinline__ Buckets key_buckets(Key96 k, uint64_t nb) {
   const uint64_t h = hash_key(k);

@@ -94,23 +94,21 @@ __device__ __forceinline__ void run_merge_desc(CKey (&v)[R]) {
   }
 }
 
-// A lookup reads the key's two buckets (eight slots, 128 bytes) at once: one
-// memory round trip whether the key is present or not.  probe_issue starts
-// the loads (32 bytes each: a bucket is 64-byte aligned); probe_match,
-// called once the caller has done other work, compares.
-struct Probe { uint4 s[8]; };
+// A lookup reads the key's two buckets (four slots, 64 bytes) at once, one
+// 32-byte load each: one memory round trip whether the key is present or
+// not.  probe_issue starts the loads; probe_match, called once the caller has
+// done other work, compares.
+static_assert(kBucketSlots == 2, "a bucket is one 32-byte load");
+struct Probe { uint4 s[2 * kBucketSlots]; };
 __device__ __forceinline__ void probe_issue(const uint4* slots, unsigned long long nb, Key96 key, Probe& pr) {
   const Buckets bk = key_buckets(key, nb);
-#pragma unroll
-  for (int t = 0; t < 4; t += 2) {
-    ldg_nc_v8(slots + 4 * bk.b1 + t, pr.s[t], pr.s[t + 1]);
-    ldg_nc_v8(slots + 4 * bk.b2 + t, pr.s[4 + t], pr.s[5 + t]);
-  }
+  ldg_nc_v8(slots + kBucketSlots * bk.b1, pr.s[0], pr.s[1]);
+  ldg_nc_v8(slots + kBucketSlots * bk.b2, pr.s[2], pr.s[3]);
 }
 __device__ __forceinline__ bool probe_match(const Probe& pr, Key96 key, float* val) {
   bool hit = false;
 #pragma unroll
-  for (int t = 0; t < 8; ++t) {
+  for (int t = 0; t < 2 * kBucketSlots; ++t) {
     if (pr.s[t].x == key.w0 && pr.s[t].y == key.w1 && pr.s[t].z == key.w2) {
       *val = __uint_as_float(pr.s[t].w);
       hit = true;
@@ -261,7 +259,7 @@ tree_kernel(const TreeArgs A) {
   };
 
   const uint4* slots = static_cast<const uint4*>(A.slots);
-  const unsigned long long nbuckets = A.capacity / 4;
+  const unsigned long long nbuckets = A.capacity / kBucketSlots;
   const int nctx = n > 1 ? n - 1 : 0;
   const double invT = A.invT, lam = A.lam;
   const bool unit_T = invT == 1.0;   // Z * 1 is Z itself: the multiply is skipped, the bits are the same
@@ -698,7 +696,7 @@ cudaError_t launch_ngram_lookup(const void* slots, unsigned long long capacity, 
   const int threads = 256;
   const long long blocks = (Q + threads - 1) / threads;
   ngram_lookup_kernel<<<unsigned(blocks), threads, 0, stream>>>(
-      static_cast<const uint4*>(slots), capacity / 4, n, keys, Q, vals, found);
+      static_cast<const uint4*>(slots), capacity / kBucketSlots, n, keys, Q, vals, found);
   return cudaGetLastError();
 }
 

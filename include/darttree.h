@@ -82,16 +82,16 @@ enum {
 };
 
 /* An n-gram model in device memory: a two-choice bucketed hash table.
- * Each slot is 16 bytes {uint32 key[3]; float logprob}; four consecutive slots
- * form a 64-byte bucket, and the table holds capacity / 4 buckets.  A key packs
+ * Each slot is 16 bytes {uint32 key[3]; float logprob}; two consecutive slots
+ * form a 32-byte bucket, and the table holds capacity / 2 buckets.  A key packs
  * the n tokens (t_0 = oldest context token ... t_{n-1} = the predicted token)
  * as 24-bit fields, t_f at bits [24f, 24f+24) of the 96-bit value key[0] |
  * key[1] << 32 | key[2] << 64, unused fields zero.  An empty slot holds
  * 0xFFFFFFFF in all three key words.  With h =
  * splitmix64-finalizer((key[0] | key[1] << 32) ^ (key[2] * 0x9E3779B97F4A7C15))
- * and nb = capacity / 4, a key lives in bucket b1 = h & (nb - 1) or bucket
+ * and nb = capacity / 2, a key lives in bucket b1 = h & (nb - 1) or bucket
  * b2 = (h >> 32) & (nb - 1), where b2 = b1 ^ 1 when the two coincide; a lookup
- * reads both buckets (128 bytes) at once, so it always takes one memory round
+ * reads both buckets (64 bytes) at once, so it always takes one memory round
  * trip.  Build the slots with dart_ngram_table_pack_host. */
 typedef struct {
   int32_t n;            /* order, 2..4 */

@@ -177,10 +177,13 @@ def _key_words(tokens):
     return v & 0xFFFFFFFF, (v >> 32) & 0xFFFFFFFF, (v >> 64) & 0xFFFFFFFF
 
 
+BUCKET_SLOTS = 2   # two 16-byte slots to a 32-byte bucket, as the header describes it
+
+
 def _buckets(w, cap):
-    """The key's two 4-slot buckets, as the header describes them."""
+    """The key's two buckets, as the header describes them."""
     h = _splitmix_fold(*w)
-    nb = cap // 4
+    nb = cap // BUCKET_SLOTS
     b1, b2 = h & (nb - 1), (h >> 32) & (nb - 1)
     return b1, (b1 ^ 1 if b2 == b1 else b2)
 
@@ -188,8 +191,8 @@ def _buckets(w, cap):
 def _find(slots, cap, tokens):
     w = _key_words(tokens)
     for b in _buckets(w, cap):
-        for t in range(4):
-            s = slots[4 * b + t]
+        for t in range(BUCKET_SLOTS):
+            s = slots[BUCKET_SLOTS * b + t]
             if tuple(int(x) for x in s[:3]) == w:
                 return True, s[3:4].view(np.float32)[0]
     return False, None
@@ -237,8 +240,8 @@ def test_packer_at_half_load_displaces_and_keeps_every_key(L):
                                       M, cap, slots.ctypes.data_as(C.c_void_p), C.byref(distinct))
     assert rc == OK and distinct.value == M
     home = sum(1 for key in keys.tolist()
-               if any(tuple(int(x) for x in slots[4 * _buckets(_key_words(key), cap)[0] + t][:3])
-                      == _key_words(key) for t in range(4)))
+               if any(tuple(int(x) for x in slots[BUCKET_SLOTS * _buckets(_key_words(key), cap)[0] + t][:3])
+                      == _key_words(key) for t in range(BUCKET_SLOTS)))
     assert home < M                                              # some keys sit in their second bucket
     for key, v in zip(keys.tolist(), vals):
         ok, got = _find(slots, cap, key)

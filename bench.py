@@ -467,6 +467,12 @@ def measure(L, D, torch, case, dev, stream, steps, warmup, world, with_select=Fa
     step_times = timed(lambda i: builder(z), steps)
     t1 = time.time()
     barrier(world)
+    # the same steps with a direct dart_tree_build call each (three launches
+    # from the host instead of one graph replay): the reference for the
+    # per-kernel breakdown below, whose parts are direct launches too
+    builder.graph = False
+    direct_times = timed(lambda i: builder(z), steps)
+    builder.graph = True
     code = D.DTYPE_CODES()[z.dtype]
     ws = builder.ws
     sp = C.c_void_p(stream.cuda_stream)
@@ -486,11 +492,12 @@ def measure(L, D, torch, case, dev, stream, steps, warmup, world, with_select=Fa
         "step_ms": max_over_ranks(statistics.mean(step_times), world),
         "row_pass_ms": max_over_ranks(statistics.mean(pass_times), world),
         "row_merge_ms": max_over_ranks(statistics.mean(merge_times), world),
+        "direct_step_ms": max_over_ranks(statistics.mean(direct_times), world),
         "step_p10_p50_p90": [float(np.percentile(step_times, q)) for q in (10, 50, 90)],
         "row_pass_p10_p50_p90": [float(np.percentile(pass_times, q)) for q in (10, 50, 90)],
         "window": (t0, t1), "host": host, "z": z, "builder": builder,
     }
-    res["tree_ms_by_difference"] = res["step_ms"] - res["row_pass_ms"] - res["row_merge_ms"]
+    res["tree_ms_by_difference"] = res["direct_step_ms"] - res["row_pass_ms"] - res["row_merge_ms"]
     if with_select and builder.out.get("scores") is not None:
         # the verification tree chosen best-first from the step's candidate
         # trees, budget 16 (one of the verification budgets PCTree quotes)
@@ -658,6 +665,7 @@ def run_ours(args):
                 ach = cc.logit_bytes / (mm["row_pass_ms"] / 1e3) / 1e9
                 per_config[str(c2)] = {
                     "workload": workload_name(c2), "ms_per_step": mm["step_ms"],
+                    "direct_launches_ms_per_step": mm["direct_step_ms"],
                     "trees_per_s": cc.B / (mm["step_ms"] / 1e3), "row_pass_ms": mm["row_pass_ms"],
                     "row_pass_frac": ach / peaks["hbm_gbs"], "row_pass_traffic": k1_traffic(c2),
                     "row_merge_ms": mm["row_merge_ms"],
@@ -687,7 +695,9 @@ def run_ours(args):
             "hbm_gbs_whole_step": logit_bytes / (step_ms / 1e3) / 1e9,
             "roofline": roofline,
             "stream_ceiling": ceiling,
-            "step_breakdown_ms": {"row_pass": k1_ms, "row_merge": m["row_merge_ms"],
+            "step_breakdown_ms": {"launch": "one CUDA-graph replay of the three kernels a step (dart_tree_plan_launch)",
+                                  "direct_launches_step": m["direct_step_ms"],
+                                  "row_pass": k1_ms, "row_merge": m["row_merge_ms"],
                                   "tree_by_difference": m["tree_ms_by_difference"]},
             "per_config": per_config,
             "cpu_baseline": cpu,

@@ -86,6 +86,13 @@ def _declare(L):
     L.dart_tree_build_strided.argtypes = [P, i32, i32, i32, i64, i32, f32, i32, i32, f32, f32, T, P,
                                           P, P, P, P, P, P, sz, P]
     L.dart_tree_build_strided.restype = i32
+    L.dart_tree_plan_create.argtypes = [C.POINTER(P), P, i32, i32, i32, i64, i32, f32, i32, i32, f32, f32, T, P,
+                                        P, P, P, P, P, P, sz]
+    L.dart_tree_plan_create.restype = i32
+    L.dart_tree_plan_launch.argtypes = [P, P]
+    L.dart_tree_plan_launch.restype = i32
+    L.dart_tree_plan_destroy.argtypes = [P]
+    L.dart_tree_plan_destroy.restype = i32
     L.dart_row_pass.argtypes = [P, i32, i32, i64, i32, f32, i32, P, sz, P]
     L.dart_row_pass.restype = i32
     L.dart_row_finish.argtypes = [i32, i32, i64, i32, f32, i32, P, P, P, P, sz, P]
@@ -651,10 +658,15 @@ def device_error(workspace, stream=None) -> int:
 
 
 class TreeBuilder:
-    """Fixed-shape driver: preallocated outputs and workspace, one C call per step."""
+    """Fixed-shape driver: preallocated outputs and workspace, one C call per step.
+
+    With graph=True (the default) the first call on a logits buffer records
+    the path's launches once (dart_tree_plan_create) and every call on the same
+    buffer replays them (dart_tree_plan_launch); a call on another buffer
+    records a new plan.  graph=False calls dart_tree_build every time."""
 
     def __init__(self, B, d, V, dtype, T, k, W, lam, beta, table=None, ctx=None, device="cuda",
-                 scores=True):
+                 scores=True, graph=True):
         torch = _torch()
         self.shape = (B, d, V)
         self.dtype = dtype
@@ -676,12 +688,48 @@ class TreeBuilder:
             self.ws = torch.zeros(max(workspace_bytes(B, d, V, self.code, k), 1), dtype=torch.uint8,
                                   device=self.device)
         _device_of(("workspace", self.ws), ("ctx", ctx if table is not None else None))
+        self.graph = graph
+        self._plan = None          # (logits address, plan handle)
+
+    def _drop_plan(self):
+        if self._plan is not None:
+            _check(lib().dart_tree_plan_destroy(self._plan[1]), "dart_tree_plan_destroy")
+            self._plan = None
+
+    def __del__(self):
+        try:
+            if self._plan is not None:
+                _torch().cuda.synchronize(self.device)
+                self._drop_plan()
+        except Exception:
+            pass
 
     def __call__(self, logits, stream=None):
         B, d, V = self.shape
         if _device_of(("logits", logits)) != self.device:
             raise DartError(f"logits is on {logits.device}, the builder on {self.device}")
         _check_tensor(logits, "logits", self.dtype, self.shape)
+        # inside a caller's own graph capture the kernels are launched directly,
+        # so that the caller's graph records them
+        if self.graph and not _torch().cuda.is_current_stream_capturing():
+            with _on_device(self.device):
+                sp = _stream_ptr(stream, self.device)
+                if self._plan is None or self._plan[0] != logits.data_ptr():
+                    if self._plan is not None:
+                        _torch().cuda.synchronize(self.device)   # launches of the old plan are done
+                    self._drop_plan()
+                    plan = C.c_void_p()
+                    rc = lib().dart_tree_plan_create(C.byref(plan), _ptr(logits), B, d, V, V, self.code, self.T,
+                                                     self.k, self.W, self.lam, self.beta,
+                                                     *_table_args(self.table, self.ctx),
+                                                     _ptr(self.out["tokens"]), _ptr(self.out["parents"]),
+                                                     _ptr(self.out["pos"]), _ptr(self.out["mask"]),
+                                                     _ptr(self.out.get("scores")), _ptr(self.ws), self.ws.numel())
+                    _check(rc, "dart_tree_plan_create")
+                    self._plan = (logits.data_ptr(), plan)
+                rc = lib().dart_tree_plan_launch(self._plan[1], sp)
+            _check(rc, "dart_tree_plan_launch")
+            return self.out
         with _on_device(self.device):
             rc = lib().dart_tree_build(_ptr(logits), B, d, V, self.code, self.T, self.k, self.W,
                                        self.lam, self.beta, *_table_args(self.table, self.ctx),

@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include "dart_launch.h"
 
@@ -240,29 +241,158 @@ int dart_tree_build(const void* logits, int B, int d, int V, int dtype,
                                  workspace_bytes, stream);
 }
 
+namespace {
+// The argument checks of dart_tree_build_strided; on DART_OK with B > 0,
+// *L holds the workspace layout and *T the scoring temperature.
+int prepare_build(const void* logits, int B, int d, int V, int64_t row_stride, int dtype, float* T, int k, int W,
+                  float lambda, float beta, const dart_ngram_table_t* ngram_table, const int32_t* ctx_tokens,
+                  int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos, uint32_t* out_mask,
+                  void* workspace, size_t workspace_bytes, WsLayout* L) {
+  int rc = check_tree_shape(B, d, k, W, lambda, beta);
+  if (rc) return rc;
+  if (V < 2 || V > kMaxV || k > V || !valid_dtype(dtype)) return DART_ERR_INVALID_ARG;
+  if (row_stride < V || row_stride > kMaxRowStride) return DART_ERR_INVALID_ARG;
+  if (!score_temperature(T)) return DART_ERR_INVALID_ARG;
+  if ((rc = check_table(ngram_table, ctx_tokens, B))) return rc;
+  if (B == 0) return DART_OK;
+  if (!logits || !aligned(logits, 16)) return DART_ERR_INVALID_ARG;
+  if (!out_tokens || !out_parents || !out_pos || !out_mask) return DART_ERR_INVALID_ARG;
+  const long long R = (long long)B * d;
+  if (!ws_layout(R, V, elem_bytes(dtype), k, L)) return DART_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < L->total) return DART_ERR_WORKSPACE;
+  return DART_OK;
+}
+}  // namespace
+
 int dart_tree_build_strided(const void* logits, int B, int d, int V, int64_t row_stride, int dtype,
                             float T, int k, int W, float lambda, float beta,
                             const dart_ngram_table_t* ngram_table, const int32_t* ctx_tokens,
                             int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
                             uint32_t* out_mask, float* out_scores,
                             void* workspace, size_t workspace_bytes, void* stream) {
-  int rc = check_tree_shape(B, d, k, W, lambda, beta);
-  if (rc) return rc;
-  if (V < 2 || V > kMaxV || k > V || !valid_dtype(dtype)) return DART_ERR_INVALID_ARG;
-  if (row_stride < V || row_stride > kMaxRowStride) return DART_ERR_INVALID_ARG;
-  if (!score_temperature(&T)) return DART_ERR_INVALID_ARG;
-  if ((rc = check_table(ngram_table, ctx_tokens, B))) return rc;
-  if (B == 0) return DART_OK;
-  if (!logits || !aligned(logits, 16)) return DART_ERR_INVALID_ARG;
-  if (!out_tokens || !out_parents || !out_pos || !out_mask) return DART_ERR_INVALID_ARG;
   WsLayout L;
-  const long long R = (long long)B * d;
-  if (!ws_layout(R, V, elem_bytes(dtype), k, &L)) return DART_ERR_INVALID_ARG;
-  if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.total) return DART_ERR_WORKSPACE;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int rc = prepare_build(logits, B, d, V, row_stride, dtype, &T, k, W, lambda, beta, ngram_table, ctx_tokens,
+                               out_tokens, out_parents, out_pos, out_mask, workspace, workspace_bytes, &L);
+  if (rc || B == 0) return rc;
   return launch_path(logits, B, d, V, row_stride, dtype, T, k, W, lambda, beta, ngram_table, ctx_tokens,
-                     out_tokens, out_parents, out_pos, out_mask, out_scores, ws, L, s);
+                     out_tokens, out_parents, out_pos, out_mask, out_scores, static_cast<uint8_t*>(workspace), L,
+                     static_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------- plans
+struct dart_tree_plan_s {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+  int device;
+  // the call's arguments, for launches into a stream that is itself being
+  // captured (the kernels are then launched as dart_tree_build_strided would)
+  const void* logits;
+  int B, d, V, dtype, k, W;
+  int64_t row_stride;
+  float T, lambda, beta;
+  bool has_table;
+  dart_ngram_table_t table;
+  const int32_t* ctx;
+  int32_t *tokens, *parents, *pos;
+  uint32_t* mask;
+  float* scores;
+  uint8_t* ws;
+  WsLayout L;
+};
+
+int dart_tree_plan_create(dart_tree_plan_t* out_plan, const void* logits, int B, int d, int V, int64_t row_stride,
+                          int dtype, float T, int k, int W, float lambda, float beta,
+                          const dart_ngram_table_t* ngram_table, const int32_t* ctx_tokens,
+                          int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
+                          uint32_t* out_mask, float* out_scores, void* workspace, size_t workspace_bytes) {
+  if (!out_plan) return DART_ERR_INVALID_ARG;
+  *out_plan = nullptr;
+  WsLayout L;
+  int rc = prepare_build(logits, B, d, V, row_stride, dtype, &T, k, W, lambda, beta, ngram_table, ctx_tokens,
+                         out_tokens, out_parents, out_pos, out_mask, workspace, workspace_bytes, &L);
+  if (rc) return rc;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DART_ERR_CUDA;
+  cudaStream_t s = nullptr;
+  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return DART_ERR_CUDA;
+  // the launches are recorded on a stream of the plan's own, none of them runs
+  cudaGraph_t graph = nullptr;
+  if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaStreamDestroy(s);
+    return DART_ERR_CUDA;
+  }
+  if (B > 0)
+    rc = launch_path(logits, B, d, V, row_stride, dtype, T, k, W, lambda, beta, ngram_table, ctx_tokens,
+                     out_tokens, out_parents, out_pos, out_mask, out_scores, static_cast<uint8_t*>(workspace), L, s);
+  const cudaError_t ec = cudaStreamEndCapture(s, &graph);
+  cudaStreamDestroy(s);
+  if (rc == DART_OK && ec != cudaSuccess) rc = DART_ERR_CUDA;
+  cudaGraphExec_t exec = nullptr;
+  if (rc == DART_OK && cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) rc = DART_ERR_CUDA;
+  if (rc != DART_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    cudaGetLastError();
+    return rc;
+  }
+  dart_tree_plan_s* plan = new (std::nothrow) dart_tree_plan_s{};
+  if (plan) {
+    plan->graph = graph;
+    plan->exec = exec;
+    plan->device = dev;
+    plan->logits = logits;
+    plan->B = B;
+    plan->d = d;
+    plan->V = V;
+    plan->dtype = dtype;
+    plan->k = k;
+    plan->W = W;
+    plan->row_stride = row_stride;
+    plan->T = T;
+    plan->lambda = lambda;
+    plan->beta = beta;
+    plan->has_table = ngram_table != nullptr;
+    if (ngram_table) plan->table = *ngram_table;
+    plan->ctx = ctx_tokens;
+    plan->tokens = out_tokens;
+    plan->parents = out_parents;
+    plan->pos = out_pos;
+    plan->mask = out_mask;
+    plan->scores = out_scores;
+    plan->ws = static_cast<uint8_t*>(workspace);
+    plan->L = L;
+  }
+  if (!plan) {
+    cudaGraphExecDestroy(exec);
+    cudaGraphDestroy(graph);
+    return DART_ERR_INTERNAL;
+  }
+  *out_plan = plan;
+  return DART_OK;
+}
+
+int dart_tree_plan_launch(dart_tree_plan_t plan, void* stream) {
+  if (!plan) return DART_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DART_ERR_CUDA;
+  if (dev != plan->device) return DART_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return DART_ERR_CUDA;
+  if (cs != cudaStreamCaptureStatusNone) {
+    // a caller capturing its own graph: record the kernels themselves
+    if (plan->B == 0) return DART_OK;
+    return launch_path(plan->logits, plan->B, plan->d, plan->V, plan->row_stride, plan->dtype, plan->T, plan->k,
+                       plan->W, plan->lambda, plan->beta, plan->has_table ? &plan->table : nullptr, plan->ctx,
+                       plan->tokens, plan->parents, plan->pos, plan->mask, plan->scores, plan->ws, plan->L, s);
+  }
+  return cudaGraphLaunch(plan->exec, s) == cudaSuccess ? DART_OK : DART_ERR_CUDA;
+}
+
+int dart_tree_plan_destroy(dart_tree_plan_t plan) {
+  if (!plan) return DART_OK;
+  const bool ok = cudaGraphExecDestroy(plan->exec) == cudaSuccess && cudaGraphDestroy(plan->graph) == cudaSuccess;
+  delete plan;
+  return ok ? DART_OK : DART_ERR_CUDA;
 }
 
 int dart_tree_build_verify(const void* logits, int B, int d, int V, int64_t row_stride, int dtype,

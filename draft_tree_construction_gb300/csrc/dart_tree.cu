@@ -128,7 +128,7 @@ __host__ __device__ inline int tree_pad(int W, int k) {
   return (W * k + run - 1) / run * run;
 }
 constexpr int kRankMax = 128;   // up to this many children a depth selects by ranking (more: sorted runs)
-constexpr int kGroup = 4;       // sorted runs one warp folds together per merge round
+constexpr int kGroup = 2;       // sorted runs one warp folds together per merge round
 // Threads per tree: one per child of a full frontier, 32..512; two per child
 // when every depth selects by ranking and the trees fit one CTA per SM (then
 // two threads rank each key against half of the keys).  Doubling for more

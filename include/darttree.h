@@ -165,6 +165,35 @@ int dart_tree_build_strided(const void* logits, int B, int d, int V, int64_t row
                             uint32_t* out_mask, float* out_scores,
                             void* workspace, size_t workspace_bytes, void* stream);
 
+/* A dart_tree_build_strided call captured once as a CUDA graph and replayed,
+ * for decode loops that build trees of the same sizes into the same buffers
+ * every step (no counterpart in the pages: it changes how the kernels are
+ * launched, not what they compute).  dart_tree_plan_create takes
+ * dart_tree_build_strided's arguments without the stream, checks them as that
+ * call does (returning its error codes, nothing captured), records its
+ * launches on a stream of its own (nothing runs) and returns a host handle in
+ * *out_plan (NULL on error).  The device buffers must stay allocated at the
+ * same addresses while the plan lives; their contents may change between
+ * launches; the table descriptor and the scalars are read at creation.
+ * dart_tree_plan_launch(plan, stream) replays the captured kernels on `stream`
+ * (NULL = the default stream) on the device that was current at creation
+ * (another current device: DART_ERR_INVALID_ARG): results and device error
+ * bits are exactly those of dart_tree_build_strided with the same arguments.
+ * Into a stream that is itself being captured, it launches the kernels
+ * directly, so that the caller's graph records them.
+ * dart_tree_plan_destroy releases a plan (NULL: nothing to do); launches
+ * already queued must be complete or ordered before it (it does not wait).
+ * Returns DART_OK or an error code (DART_ERR_CUDA when graph capture or
+ * instantiation fails, DART_ERR_INTERNAL when the host is out of memory). */
+typedef struct dart_tree_plan_s* dart_tree_plan_t;
+int dart_tree_plan_create(dart_tree_plan_t* out_plan, const void* logits, int B, int d, int V, int64_t row_stride,
+                          int dtype, float T, int k, int W, float lambda, float beta,
+                          const dart_ngram_table_t* ngram_table, const int32_t* ctx_tokens,
+                          int32_t* out_tokens, int32_t* out_parents, int32_t* out_pos,
+                          uint32_t* out_mask, float* out_scores, void* workspace, size_t workspace_bytes);
+int dart_tree_plan_launch(dart_tree_plan_t plan, void* stream);
+int dart_tree_plan_destroy(dart_tree_plan_t plan);
+
 /* dart_tree_build_strided that also emits the best-first verification tree
  * of budget M >= 1 (dart_tree_select's result on the candidate trees, with
  * the same reading and outputs), chosen by each tree's CTA right after it has

@@ -153,6 +153,16 @@ def test_other_entry_points_check_arguments(L):
     assert sel(0, 16, 4, None) == OK                 # nothing to do: no launch
     assert sel(2, 16, 0, None) == OK
     assert L.dart_device_error(None, None, None) == INVALID
+    plan = C.c_void_p(12345)
+    assert L.dart_tree_plan_create(None, P(FAKE), 2, 3, 100, 100, 2, 1.0, 4, 4, 0.5, -1.0, None, None, P(FAKE),
+                                   P(FAKE), P(FAKE), P(FAKE), None, P(FAKE), 1 << 30) == INVALID
+    assert L.dart_tree_plan_create(C.byref(plan), P(FAKE), 2, 3, 100, 100, 2, 1.0, 4, 0, 0.5, -1.0, None, None,
+                                   P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, P(FAKE), 1 << 30) == INVALID
+    assert plan.value is None                          # W = 0 refused before anything is captured
+    assert L.dart_tree_plan_create(C.byref(plan), P(FAKE), 2, 3, 100, 100, 2, 1.0, 4, 4, 0.5, -1.0, None, None,
+                                   P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, P(FAKE), 16) == WORKSPACE
+    assert L.dart_tree_plan_launch(None, None) == INVALID
+    assert L.dart_tree_plan_destroy(None) == OK
     assert L.dart_status_string(1).decode() == "invalid argument"
 
 

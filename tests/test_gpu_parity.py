@@ -7,6 +7,7 @@ same order).  Whole path: bit-exact tokens / parents / depths / masks and
 scores within 1e-5 (the exemption for oracle near-ties is in parity.py; the
 full-size test requires every tree to match exactly).
 """
+import ctypes
 import dataclasses
 
 import numpy as np
@@ -364,6 +365,59 @@ def test_tree_builder_replays_in_a_cuda_graph(D):
         eager = D.tree_build(src, c.T, c.k, c.W, c.lam, c.beta, table=tab, ctx=ctx)
         for key in ("tokens", "parents", "pos", "mask", "scores"):
             assert torch.equal(got[key], eager[key]), key
+    assert D.device_error(b.ws) == 0
+
+
+@pytest.mark.parametrize("cfg,over", [(2, dict(B=8, M=1 << 14)), (4, dict(B=3, M=1 << 16)), (1, dict(V=20000))])
+def test_tree_plan_replays_the_whole_path(D, cfg, over):
+    """A plan records the path's launches once (dart_tree_plan_create); every
+    launch on new logits in the same buffer matches the oracle and, bit for
+    bit, a direct dart_tree_build call."""
+    cases = [synth.make_config(cfg, seed=s, **over) for s in (50, 51)]
+    c = cases[0]
+    za, zb = parity.to_device(cases[0]), parity.to_device(cases[1])
+    tab, ctx = parity.gpu_table(c)      # one table and context for both batches
+    b = D.TreeBuilder(c.B, c.d, c.V, za.dtype, c.T, c.k, c.W, c.lam, c.beta, table=tab, ctx=ctx, graph=True)
+    z = za.clone()
+    for i, src in enumerate((za, zb, za)):
+        z.copy_(src)
+        out = b(z)
+        torch.cuda.synchronize()
+        assert b._plan is not None and b._plan[0] == z.data_ptr()
+        eager = D.tree_build(src, c.T, c.k, c.W, c.lam, c.beta, table=tab, ctx=ctx)
+        for key in ("tokens", "parents", "pos", "mask", "scores"):
+            assert torch.equal(out[key], eager[key]), (i, key)
+        if i == 0:
+            got = {key: _np(v) for key, v in out.items() if v is not None}
+            ref = oracle.tree_build(c)
+            assert parity.compare_all(c, got, ref, ref["ngram"])["exact"] == c.B
+    assert D.device_error(b.ws) == 0
+
+
+def test_tree_plan_inside_a_callers_graph(D):
+    """Launched into a stream that the caller is capturing, a plan's kernels go
+    into the caller's graph, whose replays then give the same trees."""
+    c = synth.make_config(2, seed=60, B=4, M=1 << 14)
+    z = parity.to_device(c)
+    tab, ctx = parity.gpu_table(c)
+    b = D.TreeBuilder(c.B, c.d, c.V, z.dtype, c.T, c.k, c.W, c.lam, c.beta, table=tab, ctx=ctx, graph=True)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        b(z, stream=stream)                      # records the plan, outside any capture
+    stream.synchronize()
+    first = {key: v.clone() for key, v in b.out.items() if v is not None}
+    for v in b.out.values():
+        if v is not None:
+            v.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        rc = D.lib().dart_tree_plan_launch(b._plan[1], ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    graph.replay()
+    torch.cuda.synchronize()
+    for key, v in first.items():
+        assert torch.equal(b.out[key], v), key
     assert D.device_error(b.ws) == 0
 
 

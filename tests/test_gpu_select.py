@@ -65,8 +65,8 @@ def test_every_budget_small_trees(D):
         _compare(D, tree, M)
 
 
-def test_full_size_config4_shape(D):
-    # config 4's tree shape: B = 32 trees of N = 496 nodes, budget 256
+def test_32_trees_of_496_nodes(D):
+    # the largest benchmarked tree shape (d = 16, k = 16, W = 32): 32 trees of 496 nodes, budget 256
     tree = synth.make_candidate_trees(B=32, d=16, k=16, W=32, seed=4)
     _compare(D, tree, 256)
 

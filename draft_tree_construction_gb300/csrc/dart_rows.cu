@@ -188,6 +188,17 @@ template <> struct Elem<DART_BF16> {
   __device__ static float punpack(uint32_t m) {
     return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
   }
+  // tau (a bf16 value, or -inf) in both halves; 1 when a half of m reaches it
+  __device__ static uint32_t pack_tau(float tau) {
+    const uint32_t t = __float_as_uint(tau) >> 16;
+    return t | (t << 16);
+  }
+  __device__ static uint32_t any_ge(uint32_t m, uint32_t t2) {
+    uint32_t r;
+    asm("{\n .reg .pred p, q;\n setp.ge.bf16x2 p|q, %1, %2;\n or.pred p, p, q;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(r) : "r"(m), "r"(t2));
+    return r;
+  }
   __device__ static float scalar(const uint8_t* p) {
     const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(p));
     return __uint_as_float(uint32_t(h) << 16);
@@ -210,6 +221,16 @@ template <> struct Elem<DART_F16> {
   __device__ static float punpack(uint32_t m) {
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&m));
     return fmaxf(f.x, f.y);
+  }
+  __device__ static uint32_t pack_tau(float tau) {
+    const uint32_t t = uint32_t(__half_as_ushort(__float2half_rn(tau)));   // exact: tau is an f16 value or -inf
+    return t | (t << 16);
+  }
+  __device__ static uint32_t any_ge(uint32_t m, uint32_t t2) {
+    uint32_t r;
+    asm("{\n .reg .pred p, q;\n setp.ge.f16x2 p|q, %1, %2;\n or.pred p, p, q;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(r) : "r"(m), "r"(t2));
+    return r;
   }
   __device__ static float scalar(const uint8_t* p) {
     const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(p));
@@ -516,9 +537,17 @@ __device__ __forceinline__ void stage_reduce(Acc& a, uint32_t& tau_o, int& cnt, 
     // vectors past nv are -inf and tau is finite here unless no bound
     // exists yet, so the index test only matters in partial stages
     uint32_t hm = 0;
+    if constexpr (DT == DART_F32) {
 #pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (E::punpack(pm[u]) >= tau) hm |= 1u << u;
+      for (int u = 0; u < U; ++u)
+        if (E::punpack(pm[u]) >= tau) hm |= 1u << u;
+    } else {
+      // 16-bit elements: the bound is one of them (or -inf), so a packed
+      // compare of each vector's two-half maximum decides exactly
+      const uint32_t t2 = E::pack_tau(tau);
+#pragma unroll
+      for (int u = 0; u < U; ++u) hm |= E::any_ge(pm[u], t2) << u;
+    }
     if (!whole) {
 #pragma unroll
       for (int u = 0; u < U; ++u)

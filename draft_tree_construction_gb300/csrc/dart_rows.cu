@@ -427,15 +427,35 @@ __device__ __forceinline__ void compact_cands(WarpCands& C, int& cnt, uint32_t& 
 }
 
 // Appends the lanes' candidate vectors (vector u of the lane when bit u of
-// hm is set), compacting whenever the buffer is full.
+// hm is set; r holds them, and src, the stage buffer, holds vector u of the
+// lane at u * 32 + lane), compacting whenever the buffer is full.
 template <int DT>
 __device__ __forceinline__ void cands_append(WarpCands& C, int cap, int& cnt, uint32_t& tau_o, int k,
-                                             const uint4 (&r)[kVecPerLane], uint32_t hm, uint32_t id0) {
+                                             const uint4 (&r)[kVecPerLane], const uint4* src, uint32_t hm,
+                                             uint32_t id0) {
   constexpr int EPV = Elem<DT>::kPerVec;
   constexpr uint32_t kMask = ((1u << EPV) - 1u) << 24;
   const int lane = threadIdx.x & 31;
-  int total;
-  const int first = warp_prefix4(uint32_t(__popc(hm)), &total);
+  int total, first;
+  if (!__any_sync(kFull, (hm & (hm - 1u)) != 0u)) {
+    // the usual case, no lane with more than one vector: one ballot, and the
+    // vector copied from the stage buffer (still intact) by its index
+    const uint32_t b = __ballot_sync(kFull, hm != 0u);
+    total = __popc(b);
+    first = __popc(b & ((1u << lane) - 1u));
+    if (cnt + total <= cap) {
+      if (hm) {
+        const int u = __ffs(hm) - 1;
+        C.vecs[cnt + first] = src[u * 32 + lane];
+        C.tags[cnt + first] = kMask | (id0 + uint32_t((u * 32 + lane) * EPV));
+      }
+      cnt += total;
+      __syncwarp();
+      return;
+    }
+  } else {
+    first = warp_prefix4(uint32_t(__popc(hm)), &total);
+  }
   if (cnt + total <= cap) {
     int pos = cnt + first;
 #pragma unroll
@@ -553,7 +573,7 @@ __device__ __forceinline__ void stage_reduce(Acc& a, uint32_t& tau_o, int& cnt, 
       for (int u = 0; u < U; ++u)
         if (u * 32 + lane >= nv) hm &= ~(1u << u);
     }
-    cands_append<DT>(C, cap, cnt, tau_o, k, r, hm, id0);
+    cands_append<DT>(C, cap, cnt, tau_o, k, r, src, hm, id0);
   }
 }
 

@@ -767,8 +767,9 @@ row_stream_kernel(const __grid_constant__ RowsParams P) {
   Cursor iss;
   iss.r = r_first;
   cursor_seek(P, iss, e0, e1, r_last);
-  // stages issued / consumed so far; a stage's ring slot and phase follow
-  // from its number (slot = n mod kRowStages, phase parity = (n / kRowStages) & 1)
+  // stages issued (counted by lane 0, the only lane that reads it) and
+  // consumed so far; a stage's ring slot and phase follow from its number
+  // (slot = n mod kRowStages, phase parity = (n / kRowStages) & 1)
   uint32_t issued = 0, consumed = 0;
   int islot = 0, cslot = 0;
   uint32_t cpar = 0;
@@ -783,7 +784,6 @@ row_stream_kernel(const __grid_constant__ RowsParams P) {
   };
   if (lane == 0)
     for (int s = 0; s < kRowStages && iss.valid; ++s) issue();
-  issued = __shfl_sync(kFull, issued, 0);
 
   bool ok = true;
   for (long long r = r_first; r <= r_last && ok; ++r) {
@@ -826,7 +826,6 @@ row_stream_kernel(const __grid_constant__ RowsParams P) {
         cpar ^= 1u;
       }
       if (lane == 0 && iss.valid) issue();
-      issued = __shfl_sync(kFull, issued, 0);
     }
     if (!ok) break;
     // tail: [b, s1)
